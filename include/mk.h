@@ -1,0 +1,221 @@
+/*
+ * mk.h — C ABI of the GB300 persistent MoE decode step.
+ *
+ * One decode step of a BF16 parallel-layer MoE transformer runs as ONE
+ * persistent kernel: one thread block per SM stays resident for the whole
+ * step and walks a host-built per-SM task list ("Inside the megakernel serving
+ * engine for North Mini Code", §What is a Megakernel, Fig 2).  Dependencies
+ * between tiles are global-memory counters that producers increment and
+ * consumers spin on (§Barriers, Listing 2); attention and expert tiles whose
+ * count depends on the live sequence lengths and on routing sit in shared
+ * queues drained by claimer tasks (§The task scheduler, the dynamic part).
+ *
+ * The host side mirrors the pages' decode service loop (§The serving engine
+ * around the kernel: update_kv_page_tables, clear_scratch_and_barriers,
+ * select_schedule(max_live_context), launch_megakernel):
+ *   mk_create         validate the model, record the caller's weight and KV
+ *                     pool pointers, allocate counters / scratch / queues;
+ *   mk_schedule_step  snapshot one batch (tokens, page tables, lengths) into
+ *                     the step's device state and pick the split-KV schedule;
+ *   mk_decode_step    clear the counters and launch the persistent kernel;
+ *   mk_step_status    read the device error word after the stream has synced.
+ *
+ * Conventions for every call:
+ *   - Return 0 (MK_OK) or a negative MK_ERR_* code.  Nothing throws across
+ *     the ABI; mk_strerror() names a code.
+ *   - "device" pointers are CUDA global-memory addresses on the device that
+ *     was current at mk_create; "host" pointers are ordinary host memory.
+ *   - A handle is single-stream and not thread-safe: calls on one handle
+ *     must not overlap.  Different handles are independent.
+ *   - BF16 values are IEEE bfloat16 bit patterns; all layouts are row-major.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MK_ABI_VERSION 1
+
+enum mk_status {
+  MK_OK = 0,
+  MK_ERR_BAD_CONFIG = -1,      /* unsupported or inconsistent model / config      */
+  MK_ERR_OOM = -2,             /* device or pinned-host allocation failed         */
+  MK_ERR_BAD_PAGE = -3,        /* a page index needed this step is out of range   */
+  MK_ERR_BATCH_TOO_LARGE = -4, /* batch > config.max_batch or batch < 1           */
+  MK_ERR_NOT_SCHEDULED = -5,   /* mk_decode_step without a preceding schedule     */
+  MK_ERR_TIMEOUT = -6,         /* a device-side wait ran past config.timeout_ms   */
+  MK_ERR_CUDA = -7,            /* a CUDA runtime call failed (no GPU, launch ...) */
+  MK_ERR_BAD_ARG = -8,         /* NULL handle / pointer, bad length, bad token    */
+  MK_ERR_DEVICE = -9           /* the kernel reported an inconsistent task/queue  */
+};
+
+/* Wave orders of the host scheduler (§The task scheduler, the static part:
+ * named waves per layer, one chosen order, task k dealt to SM k mod nSM). */
+enum mk_wave_order {
+  MK_WAVES_DEFAULT = 0,    /* qkv, router(+top-k, route setup), attention, MoE up, MoE down, O-proj, norm */
+  MK_WAVES_ATTN_FIRST = 1, /* qkv, router, attention, O-proj, MoE up, MoE down, norm */
+  MK_WAVES_INTERLEAVED = 2 /* qkv, router, MoE up, attention, MoE down, O-proj, norm */
+};
+
+typedef struct {
+  /* model (§Tasks: the decode graph; the parallel transformer layer) */
+  int n_layers;       /* L                                                       */
+  int hidden;         /* H; multiple of 32 and one of the supported K (below)    */
+  int n_q_heads;      /* hq                                                      */
+  int n_kv_heads;     /* hkv; hq % hkv == 0 and hq / hkv <= 8 (GQA group)        */
+  int head_dim;       /* d: 64 or 128                                            */
+  int n_experts;      /* E <= 256                                                */
+  int top_k;          /* k <= 8                                                  */
+  int moe_inter;      /* I (expert intermediate size)                            */
+  int vocab;          /* V                                                       */
+  int page_size;      /* KV page size in tokens: 16                              */
+  double rope_theta;  /* RoPE base                                               */
+  float rms_eps;      /* RMSNorm epsilon                                         */
+  /* capacity */
+  int max_batch;          /* 1..16 sequences per step                            */
+  int max_pages_per_seq;  /* columns of the page table                           */
+  int num_kv_pages;       /* pages in each layer's K (and V) pool                */
+  int max_attn_items;     /* split-KV items per layer; 0 = 8192                  */
+  /* schedule */
+  int wave_order;         /* enum mk_wave_order                                  */
+  int n_attn_claimers;    /* ATTN claimer tasks per layer; 0 = one per SM        */
+  int n_moe_claimers;     /* claimers per MoE drain wave; 0 = one per SM         */
+  int kv_split_tokens;    /* split-KV chunk (multiple of 64); 0 = per step       */
+  int sm_cap;             /* use at most this many SMs; 0 = all                  */
+  int timeout_ms;         /* device spin limit per wait; 0 = 2000                */
+} mk_config;
+
+/*
+ * Weights and KV pools, all owned by the caller, all device pointers, all
+ * BF16.  They must stay valid until mk_destroy.  Per-layer arrays are HOST
+ * arrays of L device pointers (copied at mk_create).
+ *   embed, lm_head   [V][H]            (untied)
+ *   final_norm       [H]               RMSNorm gain before the LM head
+ *   attn_norm[l]     [H]               the layer's RMSNorm gain
+ *   w_qkv[l]         [(hq + 2 hkv) d][H]  rows: q heads, then k heads, then v heads
+ *   w_o[l]           [H][hq d]
+ *   w_router[l]      [E][H]
+ *   w_gate[l], w_up[l]  [E][I][H]
+ *   w_down[l]        [E][H][I]
+ *   k_pool[l], v_pool[l]  [num_kv_pages][hkv][page_size][d]  (written: the
+ *                    step stores its new K/V, post-RoPE, at position seq_len)
+ * Every pointer must be 16-byte aligned.
+ */
+typedef struct {
+  const void* embed;
+  const void* lm_head;
+  const void* final_norm;
+  const void* const* attn_norm;
+  const void* const* w_qkv;
+  const void* const* w_o;
+  const void* const* w_router;
+  const void* const* w_gate;
+  const void* const* w_up;
+  const void* const* w_down;
+  void* const* k_pool;
+  void* const* v_pool;
+} mk_weights;
+
+/* Device error word, read by mk_step_status. */
+typedef struct {
+  int code;        /* MK_OK, MK_ERR_TIMEOUT, MK_ERR_DEVICE                   */
+  int sm;          /* block that reported it                                 */
+  int task;        /* index in that block's task list (-1: not a list task)  */
+  int op;          /* opcode being executed                                  */
+  int barrier;     /* counter index waited on (-1: a shared-memory wait)     */
+  unsigned value;  /* counter value seen at the give-up time                 */
+  unsigned target; /* value that was waited for                              */
+} mk_error;
+
+typedef struct mk_handle mk_handle;
+
+/* Create a decoder on the current CUDA device.
+ * Validates cfg (MK_ERR_BAD_CONFIG), copies the per-layer pointer arrays,
+ * allocates the library-owned device state (counters, activations scratch,
+ * queues, task lists: MK_ERR_OOM on failure) and builds the per-layer waves.
+ * On success *out owns that state until mk_destroy. */
+int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out);
+
+/* Snapshot one decode batch (the park/resume rule of the pages' decode
+ * service: the kernel never sees a half-updated batch).  All arrays are HOST
+ * arrays and may be reused by the caller as soon as the call returns.
+ *   batch        1..max_batch
+ *   seq_ids      [batch] caller's ids (recorded, not interpreted); may be NULL
+ *   tokens       [batch] input token of each sequence, 0 <= t < V
+ *   page_tables  [batch][max_pages_per_seq] physical page of each 16-token
+ *                logical page; entries past the needed pages are ignored
+ *   seq_lens     [batch] tokens already cached; the step writes the new K/V
+ *                at position seq_lens[i], whose page must already be present
+ * Uploads the step state on `stream` (a cudaStream_t; NULL = default) and
+ * picks the split-KV chunk from the longest live context.  The caller
+ * increments seq_lens itself afterwards.  Errors: MK_ERR_BATCH_TOO_LARGE,
+ * MK_ERR_BAD_PAGE (an index >= num_kv_pages or < 0 among the pages the step
+ * reads, or seq_lens[i] + 1 > max_pages_per_seq * page_size), MK_ERR_BAD_ARG. */
+int mk_schedule_step(mk_handle* h, int batch, const int32_t* seq_ids, const int32_t* tokens,
+                     const int32_t* page_tables, const int32_t* seq_lens, void* stream);
+
+/* Run the scheduled step on `stream`: zero the counters and launch the
+ * persistent kernel (cooperative launch, one block per SM).  Writes the
+ * logits, fp32 [batch][V], to the DEVICE buffer `logits` and the new K/V into
+ * the pools.  Asynchronous: errors found by the kernel surface through
+ * mk_step_status once the stream has synchronised. */
+int mk_decode_step(mk_handle* h, float* logits, void* stream);
+
+/* After the stream of the last mk_decode_step has synchronised: copy the
+ * device error word into *out (may be NULL) and return its code. */
+int mk_step_status(mk_handle* h, mk_error* out);
+
+/* Routing of the last completed step, for checking: HOST arrays
+ * idx int32 [L][batch][top_k] (best first) and w fp32 [L][batch][top_k]
+ * (renormalised weights); either may be NULL.  Synchronous. */
+int mk_get_routing(mk_handle* h, int32_t* idx, float* w);
+
+/* Intermediate activations of the last completed step, for checking.
+ * which: MK_SCRATCH_* below; layer in [0, L] where the kind allows it
+ * (X and H take L for the final norm).  Copies min(bytes, size) bytes to the
+ * HOST buffer dst and returns the full size in *size_out (may be NULL). */
+enum mk_scratch {
+  MK_SCRATCH_H = 0,       /* fp32 [batch][H]  residual entering the layer     */
+  MK_SCRATCH_X = 1,       /* bf16 [batch][H]  normalised layer input          */
+  MK_SCRATCH_Q = 2,       /* bf16 [batch][hq][d]  query after RoPE            */
+  MK_SCRATCH_ATTN = 3,    /* bf16 [batch][hq*d]   attention output            */
+  MK_SCRATCH_ROUTER = 4,  /* fp32 [batch][E]  router logits                   */
+  MK_SCRATCH_OPROJ = 5,   /* fp32 [hkv][batch][H]  O-proj split-K partials    */
+  MK_SCRATCH_MOE = 6      /* fp32 [batch][top_k][H] weighted expert outputs   */
+};
+int mk_read_scratch(mk_handle* h, int which, int layer, void* dst, size_t bytes,
+                    size_t* size_out);
+
+/* Per-SM task lists of the schedule for `batch` (built on demand), for
+ * checking the host scheduler without a GPU: descriptors int32 [n][32] in
+ * SM-major order and offsets int32 [n_sm + 1].  With tasks == NULL only the
+ * sizes are returned.  Host-only; needs no device. */
+int mk_plan(const mk_config* cfg, int n_sm, int batch, int32_t* tasks, int32_t* offsets,
+            int* n_tasks_out, int* n_barriers_out);
+
+/* Testing aid for the device timeout path: add `delta` to the wait target of
+ * the norm task of `layer` in the cached schedules, so that its counter wait
+ * can never complete and runs out after config.timeout_ms (the kernel then
+ * stops every block and reports MK_ERR_TIMEOUT).  delta = 0 restores it. */
+int mk_debug_bump_wait(mk_handle* h, int layer, int delta);
+
+/* Library-owned device bytes (counters, scratch, queues, task lists). */
+size_t mk_device_bytes(const mk_handle* h);
+/* SMs the persistent grid uses. */
+int mk_num_sms(const mk_handle* h);
+/* Bytes mk_schedule_step uploads for `batch` sequences (host -> device). */
+size_t mk_step_upload_bytes(const mk_handle* h, int batch);
+
+void mk_destroy(mk_handle* h);
+const char* mk_strerror(int code);
+int mk_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */

@@ -1,0 +1,515 @@
+// C ABI of the persistent decode step (declared in include/mk.h).
+//
+// Mirrors the host loop of "Inside the megakernel serving engine for North
+// Mini Code", §The serving engine around the kernel: the page tables and
+// per-sequence state are snapshot into device memory (update_kv_page_tables),
+// the counters are zeroed (clear_scratch_and_barriers), the split-KV schedule
+// follows the longest live context (select_schedule(max_live_context)) and the
+// persistent kernel is launched (launch_megakernel).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <map>
+#include <new>
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_layout.h"
+#include "mk_sched.h"
+
+namespace mk {
+cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream);
+size_t step_smem_bytes();
+}  // namespace mk
+
+using namespace mk;
+
+namespace {
+
+struct DevPlan {
+  int32_t* tasks = nullptr;
+  int32_t* off = nullptr;
+  size_t n_tasks = 0;
+};
+
+struct Staging {
+  uint8_t* host = nullptr;   // pinned
+  cudaEvent_t done = nullptr;
+  bool pending = false;
+};
+
+}  // namespace
+
+struct mk_handle {
+  mk_config cfg;
+  int device = 0;
+  int n_sm = 0;
+  Params base;                // everything but the per-step fields
+  std::vector<void*> allocs;  // device allocations owned here
+  size_t dev_bytes = 0;
+  std::map<int, DevPlan> plans;   // per batch size
+  int bump_layer = -1, bump = 0;
+  // per-step device inputs
+  int32_t* d_tokens = nullptr;
+  int32_t* d_pos = nullptr;
+  int32_t* d_pt = nullptr;
+  float* d_rope = nullptr;
+  int32_t* d_items = nullptr;
+  size_t step_bytes_cap = 0;
+  Staging stage[2];
+  int stage_idx = 0;
+  // scheduled step
+  bool scheduled = false;
+  int batch = 0;
+  int n_items = 0;
+  int split = 0;
+  int last_batch = 0;
+  uint32_t* d_bars = nullptr;   // err words live at the start
+  size_t bar_words = 0;
+};
+
+namespace {
+
+constexpr int kErrWords = 32;
+
+template <class T>
+int dalloc(mk_handle* h, T** p, size_t count) {
+  void* q = nullptr;
+  const size_t bytes = std::max<size_t>(count * sizeof(T), 16);
+  if (cudaMalloc(&q, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_OOM;
+  }
+  h->allocs.push_back(q);
+  h->dev_bytes += bytes;
+  *p = (T*)q;
+  return MK_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int upload_ptrs(mk_handle* h, const void* const* src, int L, const void* const** dst) {
+  if (!src) return MK_ERR_BAD_ARG;
+  for (int l = 0; l < L; l++)
+    if (!src[l] || !aligned16(src[l])) return MK_ERR_BAD_ARG;
+  void** d = nullptr;
+  int rc = dalloc(h, &d, (size_t)L);
+  if (rc) return rc;
+  if (cudaMemcpy(d, src, sizeof(void*) * L, cudaMemcpyHostToDevice) != cudaSuccess) return MK_ERR_CUDA;
+  *dst = (const void* const*)d;
+  return MK_OK;
+}
+
+void free_plans(mk_handle* h) {
+  for (auto& kv : h->plans) {
+    cudaFree(kv.second.tasks);
+    cudaFree(kv.second.off);
+  }
+  h->plans.clear();
+}
+
+int ensure_plan(mk_handle* h, int batch, DevPlan** out) {
+  auto it = h->plans.find(batch);
+  if (it == h->plans.end()) {
+    Plan plan;
+    int rc = build_plan(h->cfg, h->n_sm, batch, &plan, h->bump_layer, h->bump);
+    if (rc) return rc;
+    DevPlan dp;
+    dp.n_tasks = plan.tasks.size() / kDescWords;
+    if (cudaMalloc(&dp.tasks, std::max<size_t>(plan.tasks.size() * 4, 16)) != cudaSuccess ||
+        cudaMalloc(&dp.off, plan.off.size() * 4) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(dp.tasks);
+      return MK_ERR_OOM;
+    }
+    if (cudaMemcpy(dp.tasks, plan.tasks.data(), plan.tasks.size() * 4, cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
+        cudaMemcpy(dp.off, plan.off.data(), plan.off.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+      return MK_ERR_CUDA;
+    it = h->plans.emplace(batch, dp).first;
+  }
+  *out = &it->second;
+  return MK_OK;
+}
+
+size_t step_upload_bytes(const mk_config& c, int batch, int n_items) {
+  return (size_t)batch * 4 * 2 + (size_t)batch * c.max_pages_per_seq * 4 +
+         (size_t)batch * (c.head_dim / 2) * 2 * 4 + (size_t)n_items * 8 * 4;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mk_abi_version(void) { return MK_ABI_VERSION; }
+
+const char* mk_strerror(int code) {
+  switch (code) {
+    case MK_OK: return "ok";
+    case MK_ERR_BAD_CONFIG: return "unsupported or inconsistent config";
+    case MK_ERR_OOM: return "allocation failed";
+    case MK_ERR_BAD_PAGE: return "page index out of range";
+    case MK_ERR_BATCH_TOO_LARGE: return "batch outside 1..max_batch";
+    case MK_ERR_NOT_SCHEDULED: return "decode step without a scheduled batch";
+    case MK_ERR_TIMEOUT: return "device wait timed out";
+    case MK_ERR_CUDA: return "CUDA runtime error";
+    case MK_ERR_BAD_ARG: return "bad argument";
+    case MK_ERR_DEVICE: return "kernel reported an inconsistent task or queue";
+  }
+  return "unknown error";
+}
+
+int mk_plan(const mk_config* cfg, int n_sm, int batch, int32_t* tasks, int32_t* offsets,
+            int* n_tasks_out, int* n_barriers_out) {
+  if (!cfg) return MK_ERR_BAD_ARG;
+  Plan plan;
+  int rc = build_plan(*cfg, n_sm, batch, &plan);
+  if (rc) return rc;
+  if (n_tasks_out) *n_tasks_out = (int)(plan.tasks.size() / kDescWords);
+  if (n_barriers_out) *n_barriers_out = plan.n_bars;
+  if (tasks) memcpy(tasks, plan.tasks.data(), plan.tasks.size() * 4);
+  if (offsets) memcpy(offsets, plan.off.data(), plan.off.size() * 4);
+  return MK_OK;
+}
+
+void mk_destroy(mk_handle* h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  free_plans(h);
+  for (void* p : h->allocs) cudaFree(p);
+  for (auto& s : h->stage) {
+    if (s.host) cudaFreeHost(s.host);
+    if (s.done) cudaEventDestroy(s.done);
+  }
+  delete h;
+}
+
+int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
+  if (!cfg || !w || !out) return MK_ERR_BAD_ARG;
+  *out = nullptr;
+  int rc = validate_config(*cfg);
+  if (rc) return rc;
+  if (!w->embed || !w->lm_head || !w->final_norm || !aligned16(w->embed) || !aligned16(w->lm_head) ||
+      !aligned16(w->final_norm))
+    return MK_ERR_BAD_ARG;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev < 1) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  mk_handle* h = new (std::nothrow) mk_handle();
+  if (!h) return MK_ERR_OOM;
+  h->cfg = *cfg;
+  mk_config& c = h->cfg;
+  if (c.max_attn_items == 0) c.max_attn_items = 8192;
+  if (c.timeout_ms == 0) c.timeout_ms = 2000;
+  cudaGetDevice(&h->device);
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, h->device) != cudaSuccess) { delete h; return MK_ERR_CUDA; }
+  int coop = 0;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device);
+  if (!coop || prop.sharedMemPerBlockOptin < step_smem_bytes()) { delete h; return MK_ERR_CUDA; }
+  h->n_sm = prop.multiProcessorCount;
+  if (c.sm_cap > 0) h->n_sm = std::min(h->n_sm, c.sm_cap);
+
+  const int L = c.n_layers, H = c.hidden, hq = c.n_q_heads, hkv = c.n_kv_heads, d = c.head_dim;
+  const int E = c.n_experts, K = c.top_k, I = c.moe_inter, Bm = c.max_batch;
+  const int grp = hq / hkv;
+  Params& p = h->base;
+  memset(&p, 0, sizeof(p));
+  p.L = L; p.H = H; p.hq = hq; p.hkv = hkv; p.d = d; p.E = E; p.topk = K; p.I = I;
+  p.V = c.vocab; p.P = c.page_size; p.grp = grp; p.qkv_rows = (hq + 2 * hkv) * d;
+  p.max_pages = c.max_pages_per_seq; p.num_pages = c.num_kv_pages; p.Bmax = Bm;
+  p.rms_eps = c.rms_eps;
+  p.attn_scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
+  p.embed = (const uint16_t*)w->embed;
+  p.lm_head = (const uint16_t*)w->lm_head;
+  p.final_norm = (const uint16_t*)w->final_norm;
+  p.timeout_ns = (unsigned long long)c.timeout_ms * 1000000ull;
+  p.bl = bar_layout(hkv, E, Bm);
+  p.bar_per_layer = p.bl.per_layer;
+
+#define TRY(x) do { int _r = (x); if (_r) { mk_destroy(h); return _r; } } while (0)
+  TRY(upload_ptrs(h, (const void* const*)w->attn_norm, L, (const void* const**)&p.attn_norm));
+  TRY(upload_ptrs(h, (const void* const*)w->w_qkv, L, (const void* const**)&p.w_qkv));
+  TRY(upload_ptrs(h, (const void* const*)w->w_o, L, (const void* const**)&p.w_o));
+  TRY(upload_ptrs(h, (const void* const*)w->w_router, L, (const void* const**)&p.w_router));
+  TRY(upload_ptrs(h, (const void* const*)w->w_gate, L, (const void* const**)&p.w_gate));
+  TRY(upload_ptrs(h, (const void* const*)w->w_up, L, (const void* const**)&p.w_up));
+  TRY(upload_ptrs(h, (const void* const*)w->w_down, L, (const void* const**)&p.w_down));
+  TRY(upload_ptrs(h, (const void* const*)w->k_pool, L, (const void* const**)&p.k_pool));
+  TRY(upload_ptrs(h, (const void* const*)w->v_pool, L, (const void* const**)&p.v_pool));
+
+  const size_t Ls = (size_t)L, Bs = (size_t)Bm;
+  p.max_up = std::min(E, Bm * K) * (I / kRowsUp);
+  p.max_down = std::min(E, Bm * K) * (H / kRowsDown);
+  p.max_attn_items = c.max_attn_items;
+  TRY(dalloc(h, &p.h, (Ls + 1) * Bs * H));
+  TRY(dalloc(h, &p.x, (Ls + 1) * Bs * H));
+  TRY(dalloc(h, &p.q, Ls * Bs * hq * d));
+  TRY(dalloc(h, &p.knew, Ls * Bs * hkv * d));
+  TRY(dalloc(h, &p.vnew, Ls * Bs * hkv * d));
+  TRY(dalloc(h, &p.rlog, Ls * Bs * E));
+  TRY(dalloc(h, &p.ridx, Ls * Bs * K));
+  TRY(dalloc(h, &p.rw, Ls * Bs * K));
+  TRY(dalloc(h, &p.ecnt, Ls * E));
+  TRY(dalloc(h, &p.eoff, Ls * (E + 1)));
+  TRY(dalloc(h, &p.elist, Ls * Bs * K));
+  TRY(dalloc(h, &p.upq, Ls * p.max_up));
+  TRY(dalloc(h, &p.downq, Ls * p.max_down));
+  TRY(dalloc(h, &p.qmeta, Ls * 4));
+  TRY(dalloc(h, &p.attn_part, (size_t)c.max_attn_items * grp * d));
+  TRY(dalloc(h, &p.attn_ml, (size_t)c.max_attn_items * grp * 2));
+  TRY(dalloc(h, &p.attn_out, Ls * Bs * hq * d));
+  TRY(dalloc(h, &p.oproj, Ls * hkv * Bs * H));
+  TRY(dalloc(h, &p.abuf, Ls * Bs * K * I));
+  TRY(dalloc(h, &p.ybuf, Ls * Bs * K * H));
+  h->bar_words = kErrWords + (size_t)(L + 1) * p.bl.per_layer;
+  TRY(dalloc(h, &h->d_bars, h->bar_words));
+  p.err = h->d_bars;
+  p.bars = h->d_bars + kErrWords;
+  TRY(dalloc(h, &h->d_tokens, Bs));
+  TRY(dalloc(h, &h->d_pos, Bs));
+  TRY(dalloc(h, &h->d_pt, Bs * c.max_pages_per_seq));
+  TRY(dalloc(h, &h->d_rope, Bs * (d / 2) * 2));
+  TRY(dalloc(h, &h->d_items, (size_t)c.max_attn_items * 8));
+  if (cudaMemset(h->d_bars, 0, h->bar_words * 4) != cudaSuccess) { mk_destroy(h); return MK_ERR_CUDA; }
+  h->step_bytes_cap = step_upload_bytes(c, Bm, c.max_attn_items);
+  for (auto& s : h->stage) {
+    if (cudaMallocHost(&s.host, h->step_bytes_cap) != cudaSuccess) { cudaGetLastError(); mk_destroy(h); return MK_ERR_OOM; }
+    if (cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess) { mk_destroy(h); return MK_ERR_CUDA; }
+  }
+#undef TRY
+  *out = h;
+  return MK_OK;
+}
+
+int mk_schedule_step(mk_handle* h, int batch, const int32_t* seq_ids, const int32_t* tokens,
+                     const int32_t* page_tables, const int32_t* seq_lens, void* stream) {
+  (void)seq_ids;
+  if (!h) return MK_ERR_BAD_ARG;
+  const mk_config& c = h->cfg;
+  h->scheduled = false;
+  if (batch < 1 || batch > c.max_batch) return MK_ERR_BATCH_TOO_LARGE;
+  if (!tokens || !page_tables || !seq_lens) return MK_ERR_BAD_ARG;
+  const int P = c.page_size, MP = c.max_pages_per_seq, hkv = c.n_kv_heads, d = c.head_dim;
+  long long total_keys = 0;
+  int max_ctx = 0;
+  for (int b = 0; b < batch; b++) {
+    if (tokens[b] < 0 || tokens[b] >= c.vocab) return MK_ERR_BAD_ARG;
+    if (seq_lens[b] < 0) return MK_ERR_BAD_ARG;
+    if ((long long)seq_lens[b] + 1 > (long long)MP * P) return MK_ERR_BAD_PAGE;
+    const int need = (seq_lens[b] + 1 + P - 1) / P;
+    for (int i = 0; i < need; i++) {
+      const int32_t pg = page_tables[(size_t)b * MP + i];
+      if (pg < 0 || pg >= c.num_kv_pages) return MK_ERR_BAD_PAGE;
+    }
+    total_keys += seq_lens[b] + 1;
+    max_ctx = std::max(max_ctx, seq_lens[b] + 1);
+  }
+  // select_schedule: split-KV chunk from the live contexts, about two items per SM
+  int S = c.kv_split_tokens;
+  if (S <= 0) {
+    long long want = (total_keys * hkv + 2LL * h->n_sm - 1) / (2LL * h->n_sm);
+    want = (want + 63) / 64 * 64;
+    S = (int)std::max<long long>(256, std::min<long long>(want, 1 << 22));
+  }
+  auto count_items = [&](int s) {
+    long long n = 0;
+    for (int b = 0; b < batch; b++) n += (long long)hkv * ((seq_lens[b] + 1 + s - 1) / s);
+    return n;
+  };
+  while (count_items(S) > c.max_attn_items) S *= 2;
+  const int n_items = (int)count_items(S);
+  (void)max_ctx;
+
+  DevPlan* plan = nullptr;
+  int rc = ensure_plan(h, batch, &plan);
+  if (rc) return rc;
+
+  // stage the step state in pinned memory, then one upload per array
+  Staging& st = h->stage[h->stage_idx];
+  h->stage_idx ^= 1;
+  if (st.pending) {
+    cudaEventSynchronize(st.done);
+    st.pending = false;
+  }
+  uint8_t* cur = st.host;
+  int32_t* s_tok = (int32_t*)cur; cur += (size_t)batch * 4;
+  int32_t* s_pos = (int32_t*)cur; cur += (size_t)batch * 4;
+  int32_t* s_pt = (int32_t*)cur; cur += (size_t)batch * MP * 4;
+  float* s_rope = (float*)cur; cur += (size_t)batch * (d / 2) * 2 * 4;
+  int32_t* s_items = (int32_t*)cur;
+  memcpy(s_tok, tokens, (size_t)batch * 4);
+  memcpy(s_pos, seq_lens, (size_t)batch * 4);
+  memcpy(s_pt, page_tables, (size_t)batch * MP * 4);
+  for (int b = 0; b < batch; b++) {
+    const double pos = (double)seq_lens[b];
+    for (int i = 0; i < d / 2; i++) {
+      const double ang = pos * pow(c.rope_theta, -2.0 * i / (double)d);
+      s_rope[((size_t)b * (d / 2) + i) * 2 + 0] = (float)cos(ang);
+      s_rope[((size_t)b * (d / 2) + i) * 2 + 1] = (float)sin(ang);
+    }
+  }
+  int k = 0;
+  for (int b = 0; b < batch; b++) {
+    const int keys = seq_lens[b] + 1;
+    const int ns = (keys + S - 1) / S;
+    for (int g = 0; g < hkv; g++) {
+      const int base = k;
+      for (int s = 0; s < ns; s++, k++) {
+        int32_t* it = s_items + (size_t)k * 8;
+        it[AI_B] = b; it[AI_G] = g; it[AI_S] = s; it[AI_NSPLIT] = ns;
+        it[AI_T0] = s * S; it[AI_T1] = std::min(keys, (s + 1) * S);
+        it[AI_BASE] = base; it[AI_POS] = seq_lens[b];
+      }
+    }
+  }
+  cudaStream_t sm = (cudaStream_t)stream;
+  bool ok = cudaMemcpyAsync(h->d_tokens, s_tok, (size_t)batch * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
+            cudaMemcpyAsync(h->d_pos, s_pos, (size_t)batch * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
+            cudaMemcpyAsync(h->d_pt, s_pt, (size_t)batch * MP * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
+            cudaMemcpyAsync(h->d_rope, s_rope, (size_t)batch * (d / 2) * 2 * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
+            cudaMemcpyAsync(h->d_items, s_items, (size_t)n_items * 8 * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
+            cudaEventRecord(st.done, sm) == cudaSuccess;
+  if (!ok) return MK_ERR_CUDA;
+  st.pending = true;
+  h->scheduled = true;
+  h->batch = batch;
+  h->n_items = n_items;
+  h->split = S;
+  return MK_OK;
+}
+
+int mk_decode_step(mk_handle* h, float* logits, void* stream) {
+  if (!h || !logits) return MK_ERR_BAD_ARG;
+  if (!h->scheduled) return MK_ERR_NOT_SCHEDULED;
+  DevPlan* plan = nullptr;
+  int rc = ensure_plan(h, h->batch, &plan);
+  if (rc) return rc;
+  cudaStream_t sm = (cudaStream_t)stream;
+  if (cudaMemsetAsync(h->d_bars, 0, h->bar_words * 4, sm) != cudaSuccess) return MK_ERR_CUDA;
+  Params p = h->base;
+  p.B = h->batch;
+  p.n_attn_items = h->n_items;
+  p.tokens = h->d_tokens;
+  p.pos = h->d_pos;
+  p.page_tables = h->d_pt;
+  p.rope = h->d_rope;
+  p.attn_items = h->d_items;
+  p.logits = logits;
+  p.tasks = plan->tasks;
+  p.task_off = plan->off;
+  if (launch_step(p, h->n_sm, sm) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  h->last_batch = h->batch;
+  return MK_OK;
+}
+
+int mk_step_status(mk_handle* h, mk_error* out) {
+  if (!h) return MK_ERR_BAD_ARG;
+  uint32_t e[kErrWords];
+  if (cudaMemcpy(e, h->d_bars, sizeof(e), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  int code = MK_OK;
+  if (e[E_CODE] == DEV_TIMEOUT || e[E_CODE] == DEV_SMEM_TIMEOUT) code = MK_ERR_TIMEOUT;
+  else if (e[E_CODE] != 0) code = MK_ERR_DEVICE;
+  if (out) {
+    out->code = code;
+    out->sm = (int)e[E_SM];
+    out->task = (int)e[E_TASK];
+    out->op = (int)e[E_OP];
+    out->barrier = (int)e[E_BAR];
+    out->value = e[E_VAL];
+    out->target = e[E_TGT];
+  }
+  return code;
+}
+
+int mk_get_routing(mk_handle* h, int32_t* idx, float* w) {
+  if (!h) return MK_ERR_BAD_ARG;
+  if (h->last_batch < 1) return MK_ERR_NOT_SCHEDULED;
+  const mk_config& c = h->cfg;
+  const int B = h->last_batch, K = c.top_k, Bm = c.max_batch;
+  std::vector<int32_t> ti((size_t)c.n_layers * Bm * K);
+  std::vector<float> tw((size_t)c.n_layers * Bm * K);
+  if (cudaMemcpy(ti.data(), h->base.ridx, ti.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(tw.data(), h->base.rw, tw.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  for (int l = 0; l < c.n_layers; l++)
+    for (int b = 0; b < B; b++)
+      for (int j = 0; j < K; j++) {
+        const size_t src = ((size_t)l * Bm + b) * K + j, dst = ((size_t)l * B + b) * K + j;
+        if (idx) idx[dst] = ti[src];
+        if (w) w[dst] = tw[src];
+      }
+  return MK_OK;
+}
+
+int mk_read_scratch(mk_handle* h, int which, int layer, void* dst, size_t bytes, size_t* size_out) {
+  if (!h) return MK_ERR_BAD_ARG;
+  const mk_config& c = h->cfg;
+  const Params& p = h->base;
+  const int B = h->last_batch > 0 ? h->last_batch : 1, Bm = c.max_batch, L = c.n_layers;
+  const int H = c.hidden, hq = c.n_q_heads, d = c.head_dim, hkv = c.n_kv_heads;
+  const int maxl = (which == MK_SCRATCH_H || which == MK_SCRATCH_X) ? L : L - 1;
+  if (layer < 0 || layer > maxl) return MK_ERR_BAD_ARG;
+  // (base pointer of the layer, bytes per sequence row, rows, row stride in bytes)
+  const uint8_t* base = nullptr;
+  size_t row = 0, rows = (size_t)B, stride = 0;
+  switch (which) {
+    case MK_SCRATCH_H: row = (size_t)H * 4; stride = row; base = (const uint8_t*)(p.h + (size_t)layer * Bm * H); break;
+    case MK_SCRATCH_X: row = (size_t)H * 2; stride = row; base = (const uint8_t*)(p.x + (size_t)layer * Bm * H); break;
+    case MK_SCRATCH_Q: row = (size_t)hq * d * 2; stride = row; base = (const uint8_t*)(p.q + (size_t)layer * Bm * hq * d); break;
+    case MK_SCRATCH_ATTN: row = (size_t)hq * d * 2; stride = row; base = (const uint8_t*)(p.attn_out + (size_t)layer * Bm * hq * d); break;
+    case MK_SCRATCH_ROUTER: row = (size_t)c.n_experts * 4; stride = row; base = (const uint8_t*)(p.rlog + (size_t)layer * Bm * c.n_experts); break;
+    case MK_SCRATCH_OPROJ: {
+      const size_t full = (size_t)hkv * B * H * 4;
+      if (size_out) *size_out = full;
+      std::vector<uint8_t> tmp(full);
+      for (int g = 0; g < hkv; g++)
+        if (cudaMemcpy(tmp.data() + (size_t)g * B * H * 4, p.oproj + ((size_t)layer * hkv + g) * Bm * H,
+                       (size_t)B * H * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+          return MK_ERR_CUDA;
+      if (dst) memcpy(dst, tmp.data(), std::min(bytes, full));
+      return MK_OK;
+    }
+    case MK_SCRATCH_MOE: row = (size_t)c.top_k * H * 4; stride = row; base = (const uint8_t*)(p.ybuf + (size_t)layer * Bm * c.top_k * H); break;
+    default: return MK_ERR_BAD_ARG;
+  }
+  const size_t full = row * rows;
+  if (size_out) *size_out = full;
+  if (dst && cudaMemcpy(dst, base, std::min(bytes, full), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  (void)stride;
+  return MK_OK;
+}
+
+int mk_debug_bump_wait(mk_handle* h, int layer, int delta) {
+  if (!h || layer < 0 || layer > h->cfg.n_layers) return MK_ERR_BAD_ARG;
+  cudaDeviceSynchronize();
+  h->bump_layer = delta ? layer : -1;
+  h->bump = delta;
+  free_plans(h);
+  return MK_OK;
+}
+
+size_t mk_device_bytes(const mk_handle* h) { return h ? h->dev_bytes : 0; }
+int mk_num_sms(const mk_handle* h) { return h ? h->n_sm : 0; }
+size_t mk_step_upload_bytes(const mk_handle* h, int batch) {
+  if (!h) return 0;
+  return step_upload_bytes(h->cfg, batch, h->scheduled ? h->n_items : 0);
+}
+
+}  // extern "C"

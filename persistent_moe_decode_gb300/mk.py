@@ -1,0 +1,285 @@
+"""Python binding of the C ABI in include/mk.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of the decode step: the step runs in the CUDA kernels of libmk.so.
+The library is loaded on first use; if it has not been built the binding
+raises (there is no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import numpy as np
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmk.so")
+_lock = threading.Lock()
+_lib = None
+
+MK_OK = 0
+MK_ERR_BAD_CONFIG = -1
+MK_ERR_OOM = -2
+MK_ERR_BAD_PAGE = -3
+MK_ERR_BATCH_TOO_LARGE = -4
+MK_ERR_NOT_SCHEDULED = -5
+MK_ERR_TIMEOUT = -6
+MK_ERR_CUDA = -7
+MK_ERR_BAD_ARG = -8
+MK_ERR_DEVICE = -9
+
+MK_WAVES_DEFAULT, MK_WAVES_ATTN_FIRST, MK_WAVES_INTERLEAVED = 0, 1, 2
+(MK_SCRATCH_H, MK_SCRATCH_X, MK_SCRATCH_Q, MK_SCRATCH_ATTN, MK_SCRATCH_ROUTER,
+ MK_SCRATCH_OPROJ, MK_SCRATCH_MOE) = range(7)
+
+# every symbol include/mk.h declares
+EXPORTS = ("mk_create", "mk_schedule_step", "mk_decode_step", "mk_step_status", "mk_get_routing",
+           "mk_read_scratch", "mk_plan", "mk_debug_bump_wait", "mk_device_bytes", "mk_num_sms",
+           "mk_step_upload_bytes", "mk_destroy", "mk_strerror", "mk_abi_version")
+
+
+class mk_config(C.Structure):
+    _fields_ = [("n_layers", C.c_int), ("hidden", C.c_int), ("n_q_heads", C.c_int),
+                ("n_kv_heads", C.c_int), ("head_dim", C.c_int), ("n_experts", C.c_int),
+                ("top_k", C.c_int), ("moe_inter", C.c_int), ("vocab", C.c_int),
+                ("page_size", C.c_int), ("rope_theta", C.c_double), ("rms_eps", C.c_float),
+                ("max_batch", C.c_int), ("max_pages_per_seq", C.c_int), ("num_kv_pages", C.c_int),
+                ("max_attn_items", C.c_int), ("wave_order", C.c_int), ("n_attn_claimers", C.c_int),
+                ("n_moe_claimers", C.c_int), ("kv_split_tokens", C.c_int), ("sm_cap", C.c_int),
+                ("timeout_ms", C.c_int)]
+
+
+_VPP = C.POINTER(C.c_void_p)
+
+
+class mk_weights(C.Structure):
+    _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p), ("final_norm", C.c_void_p),
+                ("attn_norm", _VPP), ("w_qkv", _VPP), ("w_o", _VPP), ("w_router", _VPP),
+                ("w_gate", _VPP), ("w_up", _VPP), ("w_down", _VPP), ("k_pool", _VPP),
+                ("v_pool", _VPP)]
+
+
+class mk_error(C.Structure):
+    _fields_ = [("code", C.c_int), ("sm", C.c_int), ("task", C.c_int), ("op", C.c_int),
+                ("barrier", C.c_int), ("value", C.c_uint), ("target", C.c_uint)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class MkError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {mk_strerror(code)} ({code})")
+        self.code = code
+
+
+def lib():
+    """Load libmk.so; raise if it is missing (no CPU fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(f"{_LIB_PATH} is not built: run `python -m "
+                                   "persistent_moe_decode_gb300.build` (needs nvcc)")
+            L = C.CDLL(_LIB_PATH)
+            vp, i32 = C.c_void_p, C.c_int
+            L.mk_create.argtypes = [C.POINTER(mk_config), C.POINTER(mk_weights), C.POINTER(vp)]
+            L.mk_schedule_step.argtypes = [vp, i32, vp, vp, vp, vp, vp]
+            L.mk_decode_step.argtypes = [vp, vp, vp]
+            L.mk_step_status.argtypes = [vp, C.POINTER(mk_error)]
+            L.mk_get_routing.argtypes = [vp, vp, vp]
+            L.mk_read_scratch.argtypes = [vp, i32, i32, vp, C.c_size_t, C.POINTER(C.c_size_t)]
+            L.mk_plan.argtypes = [C.POINTER(mk_config), i32, i32, vp, vp, C.POINTER(i32),
+                                  C.POINTER(i32)]
+            L.mk_debug_bump_wait.argtypes = [vp, i32, i32]
+            L.mk_device_bytes.argtypes = [vp]
+            L.mk_device_bytes.restype = C.c_size_t
+            L.mk_num_sms.argtypes = [vp]
+            L.mk_step_upload_bytes.argtypes = [vp, i32]
+            L.mk_step_upload_bytes.restype = C.c_size_t
+            L.mk_destroy.argtypes = [vp]
+            L.mk_destroy.restype = None
+            L.mk_strerror.argtypes = [i32]
+            L.mk_strerror.restype = C.c_char_p
+            _lib = L
+    return _lib
+
+
+def _check(rc: int, where: str) -> int:
+    if rc != MK_OK:
+        raise MkError(rc, where)
+    return rc
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        return None
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+# ------------------------------------------------------------- entry points
+
+def mk_strerror(code: int) -> str:
+    return lib().mk_strerror(int(code)).decode()
+
+
+def mk_abi_version() -> int:
+    return int(lib().mk_abi_version())
+
+
+def mk_create(cfg: mk_config, weights: mk_weights):
+    h = C.c_void_p()
+    _check(lib().mk_create(C.byref(cfg), C.byref(weights), C.byref(h)), "mk_create")
+    return h
+
+
+def mk_schedule_step(h, batch: int, seq_ids, tokens, page_tables, seq_lens, stream=None) -> int:
+    tok, pt, sl = _i32(tokens), _i32(page_tables), _i32(seq_lens)
+    sid = _i32(seq_ids) if seq_ids is not None else None
+    return _check(lib().mk_schedule_step(h, int(batch), _ptr(sid) if sid is not None else None,
+                                         _ptr(tok), _ptr(pt), _ptr(sl), _stream_ptr(stream)),
+                  "mk_schedule_step")
+
+
+def mk_decode_step(h, logits_ptr: int, stream=None) -> int:
+    return _check(lib().mk_decode_step(h, C.c_void_p(int(logits_ptr)), _stream_ptr(stream)),
+                  "mk_decode_step")
+
+
+def mk_step_status(h):
+    e = mk_error()
+    rc = lib().mk_step_status(h, C.byref(e))
+    return rc, e
+
+
+def mk_get_routing(h, n_layers: int, batch: int, top_k: int):
+    idx = np.empty((n_layers, batch, top_k), dtype=np.int32)
+    w = np.empty((n_layers, batch, top_k), dtype=np.float32)
+    _check(lib().mk_get_routing(h, _ptr(idx), _ptr(w)), "mk_get_routing")
+    return idx, w
+
+
+def mk_read_scratch(h, which: int, layer: int) -> bytes:
+    size = C.c_size_t(0)
+    _check(lib().mk_read_scratch(h, int(which), int(layer), None, 0, C.byref(size)), "mk_read_scratch")
+    buf = (C.c_uint8 * size.value)()
+    _check(lib().mk_read_scratch(h, int(which), int(layer), C.cast(buf, C.c_void_p), size.value, None),
+           "mk_read_scratch")
+    return bytes(buf)
+
+
+def mk_plan(cfg: mk_config, n_sm: int, batch: int):
+    n_tasks, n_bars = C.c_int(0), C.c_int(0)
+    _check(lib().mk_plan(C.byref(cfg), int(n_sm), int(batch), None, None, C.byref(n_tasks),
+                         C.byref(n_bars)), "mk_plan")
+    tasks = np.empty((n_tasks.value, 32), dtype=np.int32)
+    off = np.empty(n_sm + 1, dtype=np.int32)
+    _check(lib().mk_plan(C.byref(cfg), int(n_sm), int(batch), _ptr(tasks), _ptr(off), None, None),
+           "mk_plan")
+    return tasks, off, n_bars.value
+
+
+def mk_debug_bump_wait(h, layer: int, delta: int) -> int:
+    return _check(lib().mk_debug_bump_wait(h, int(layer), int(delta)), "mk_debug_bump_wait")
+
+
+def mk_device_bytes(h) -> int:
+    return int(lib().mk_device_bytes(h))
+
+
+def mk_num_sms(h) -> int:
+    return int(lib().mk_num_sms(h))
+
+
+def mk_step_upload_bytes(h, batch: int) -> int:
+    return int(lib().mk_step_upload_bytes(h, int(batch)))
+
+
+def mk_destroy(h) -> None:
+    if h:
+        lib().mk_destroy(h)
+
+
+# ---------------------------------------------------------- convenience
+
+def make_config(dims, max_batch: int, max_pages_per_seq: int, num_kv_pages: int, **kw) -> mk_config:
+    """mk_config from a ModelDims plus capacity / schedule fields."""
+    c = mk_config(n_layers=dims.n_layers, hidden=dims.hidden, n_q_heads=dims.n_q_heads,
+                  n_kv_heads=dims.n_kv_heads, head_dim=dims.head_dim, n_experts=dims.n_experts,
+                  top_k=dims.top_k, moe_inter=dims.moe_inter, vocab=dims.vocab,
+                  page_size=dims.page_size, rope_theta=float(dims.rope_theta),
+                  rms_eps=float(dims.rms_eps), max_batch=int(max_batch),
+                  max_pages_per_seq=int(max_pages_per_seq), num_kv_pages=int(num_kv_pages))
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+class Decoder:
+    """Owns one mk handle over caller-owned device tensors (weights, KV pools).
+
+    ``model`` has the stacked BF16 device tensors of ``synth.SynthModel``;
+    ``k_pool`` / ``v_pool`` are [L, pages, hkv, P, d] BF16 device tensors.
+    The tensors are kept referenced for the lifetime of the decoder.
+    """
+
+    def __init__(self, model, k_pool, v_pool, max_batch: int, max_pages_per_seq: int, **cfg_kw):
+        self.dims = model.dims
+        self.model, self.k_pool, self.v_pool = model, k_pool, v_pool
+        L = self.dims.n_layers
+        self.cfg = make_config(self.dims, max_batch, max_pages_per_seq, k_pool.shape[1], **cfg_kw)
+        self._keep = []
+
+        def arr(t):
+            a = (C.c_void_p * L)(*[t[l].data_ptr() for l in range(L)])
+            self._keep.append(a)
+            return C.cast(a, _VPP)
+
+        self.weights = mk_weights(embed=model.embed.data_ptr(), lm_head=model.lm_head.data_ptr(),
+                                  final_norm=model.final_norm.data_ptr(),
+                                  attn_norm=arr(model.attn_norm), w_qkv=arr(model.w_qkv),
+                                  w_o=arr(model.w_o), w_router=arr(model.w_router),
+                                  w_gate=arr(model.w_gate), w_up=arr(model.w_up),
+                                  w_down=arr(model.w_down), k_pool=arr(k_pool), v_pool=arr(v_pool))
+        self.h = mk_create(self.cfg, self.weights)
+        self.batch = 0
+
+    def schedule(self, tokens, page_tables, seq_lens, seq_ids=None, stream=None):
+        self.batch = len(tokens)
+        pt = _i32(page_tables)
+        if pt.shape[1] != self.cfg.max_pages_per_seq:
+            full = np.full((pt.shape[0], self.cfg.max_pages_per_seq), -1, dtype=np.int32)
+            full[:, :pt.shape[1]] = pt
+            pt = full
+        return mk_schedule_step(self.h, self.batch, seq_ids, tokens, pt, seq_lens, stream)
+
+    def decode(self, logits, stream=None):
+        return mk_decode_step(self.h, logits.data_ptr(), stream)
+
+    def status(self):
+        return mk_step_status(self.h)
+
+    def routing(self):
+        return mk_get_routing(self.h, self.dims.n_layers, self.batch, self.dims.top_k)
+
+    def scratch(self, which: int, layer: int) -> bytes:
+        return mk_read_scratch(self.h, which, layer)
+
+    def close(self):
+        if self.h:
+            mk_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

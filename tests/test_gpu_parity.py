@@ -1,0 +1,203 @@
+"""Parity of the CUDA decode step with the CPU oracle, through the C ABI.
+
+Both sides get the same seeded weights, KV pools, page tables and tokens.  The
+trajectory is teacher-forced by the GPU: each step both consume the GPU's
+greedy token; each keeps its own KV cache.  Acceptance per step: logits
+max-abs <= 2e-2 and relative L2 <= 1e-2; the expert set of every (layer,
+token) equal to the oracle's wherever the oracle's k-th / (k+1)-th router-logit
+gap exceeds 1e-3; greedy argmax equal on >= 99% of steps.  The oracle runs in
+its BF16-storage mode (x, q, attention output and expert hidden rounded to
+BF16 where the kernel stores them).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from persistent_moe_decode_gb300 import mk
+from persistent_moe_decode_gb300.configs import WORKLOADS
+from tests._util import dims_dict, host_pool, host_weights
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, REL_L2, GAP = 2e-2, 1e-2, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from persistent_moe_decode_gb300 import build
+    build.build()
+    oracle.build()
+
+
+class Pair:
+    """GPU runner + oracle over the same inputs."""
+
+    def __init__(self, wl, **cfg_kw):
+        from persistent_moe_decode_gb300.runner import StepRunner
+        self.wl = wl
+        self.run = StepRunner(wl, device="cuda", **cfg_kw)
+        self.orc = oracle.Oracle(dims_dict(wl.dims), host_weights(self.run.model),
+                                 host_pool(self.run.k_pool), host_pool(self.run.v_pool))
+
+    def step(self, trace=False):
+        b = self.run.batch
+        b.prepare_step()
+        tokens, lens, pt = b.tokens.copy(), b.seq_lens.copy(), b.page_tables.copy()
+        self.run.step()
+        torch.cuda.synchronize()
+        self.run.check_status()
+        gpu = self.run.logits.double().cpu().numpy()
+        out = self.orc.decode_step(tokens, lens, pt, flags=oracle.ALL_BF16, trace=trace)
+        ref, tr = (out if trace else (out, None))
+        return gpu, ref, tr
+
+    def advance(self, tokens):
+        ch = self.run.advance(tokens)
+        if ch is not None:        # mirror the refilled pages into the oracle's pools
+            slot, pages = ch
+            idx = torch.as_tensor(pages, dtype=torch.long, device=self.run.k_pool.device)
+            self.orc.k_pool[:, pages] = host_pool(self.run.k_pool[:, idx])
+            self.orc.v_pool[:, pages] = host_pool(self.run.v_pool[:, idx])
+
+    def close(self):
+        self.run.close()
+
+
+def check_logits(gpu, ref, where=""):
+    err = np.abs(gpu - ref).max()
+    rel = np.linalg.norm(gpu - ref) / np.linalg.norm(ref)
+    assert np.all(np.isfinite(gpu)), f"{where}: non-finite logits"
+    assert err <= MAX_ABS and rel <= REL_L2, f"{where}: max-abs {err:.3e} rel-L2 {rel:.3e}"
+    return err, rel
+
+
+def check_routing(pair, tr):
+    idx, _ = pair.run.dec.routing()
+    ok = tr["gap"] > GAP
+    for l in range(idx.shape[0]):
+        for b in range(idx.shape[1]):
+            if ok[l, b]:
+                assert set(idx[l, b]) == set(tr["idx"][l, b]), (l, b, idx[l, b], tr["idx"][l, b])
+    return int((~ok).sum())
+
+
+def run_trajectory(pair, steps, trace_every=1):
+    agree, exempt = 0, 0
+    for s in range(steps):
+        gpu, ref, tr = pair.step(trace=(s % trace_every == 0))
+        check_logits(gpu, ref, f"step {s}")
+        if tr is not None:
+            exempt += check_routing(pair, tr)
+        g_tok, r_tok = gpu.argmax(1), ref.argmax(1)
+        agree += int((g_tok == r_tok).all())
+        pair.advance(g_tok.astype(np.int32))
+    assert agree >= 0.99 * steps or steps - agree <= 0, f"argmax agreed on {agree}/{steps} steps"
+    return exempt
+
+
+def test_tiny_intermediates_match_layer_by_layer():
+    pair = Pair(WORKLOADS["tiny"])
+    try:
+        gpu, ref, tr = pair.step(trace=True)
+        d = pair.wl.dims
+        B = pair.wl.batch
+        dec = pair.run.dec
+        for l in range(d.n_layers + 1):
+            h = np.frombuffer(dec.scratch(mk.MK_SCRATCH_H, l), dtype=np.float32).reshape(B, d.hidden)
+            np.testing.assert_allclose(h, tr["h_in"][l], atol=2e-3, rtol=1e-2, err_msg=f"h layer {l}")
+        for l in range(d.n_layers):
+            x = np.frombuffer(dec.scratch(mk.MK_SCRATCH_X, l), dtype=np.uint16).reshape(B, d.hidden)
+            np.testing.assert_allclose(oracle.bf16_to_f64(x), tr["x"][l], atol=2e-2, rtol=1e-2,
+                                       err_msg=f"x layer {l}")
+            q = np.frombuffer(dec.scratch(mk.MK_SCRATCH_Q, l), dtype=np.uint16).reshape(B, -1)
+            np.testing.assert_allclose(oracle.bf16_to_f64(q), tr["q"][l], atol=2e-2, rtol=1e-2,
+                                       err_msg=f"q layer {l}")
+            r = np.frombuffer(dec.scratch(mk.MK_SCRATCH_ROUTER, l), dtype=np.float32).reshape(B, -1)
+            np.testing.assert_allclose(r, tr["router"][l], atol=1e-3, rtol=1e-3,
+                                       err_msg=f"router layer {l}")
+            a = np.frombuffer(dec.scratch(mk.MK_SCRATCH_ATTN, l), dtype=np.uint16).reshape(B, -1)
+            np.testing.assert_allclose(oracle.bf16_to_f64(a), tr["attn"][l], atol=2e-2, rtol=2e-2,
+                                       err_msg=f"attn layer {l}")
+            o = np.frombuffer(dec.scratch(mk.MK_SCRATCH_OPROJ, l), dtype=np.float32)
+            o = o.reshape(d.n_kv_heads, B, d.hidden).sum(0)
+            np.testing.assert_allclose(o, tr["attn_proj"][l], atol=2e-3, rtol=1e-2,
+                                       err_msg=f"oproj layer {l}")
+            y = np.frombuffer(dec.scratch(mk.MK_SCRATCH_MOE, l), dtype=np.float32)
+            y = y.reshape(B, d.top_k, d.hidden).sum(1)
+            np.testing.assert_allclose(y, tr["moe"][l], atol=2e-3, rtol=1e-2,
+                                       err_msg=f"moe layer {l}")
+        check_logits(gpu, ref)
+        check_routing(pair, tr)
+        # the new K/V landed in the pool at the token's slot, as the oracle wrote it
+        P = d.page_size
+        pos = int(pair.run.batch.seq_lens[0])
+        pg = int(pair.run.batch.page_tables[0, pos // P])
+        kp = host_pool(pair.run.k_pool[:, pg])
+        np.testing.assert_allclose(oracle.bf16_to_f64(kp[:, :, pos % P]),
+                                   oracle.bf16_to_f64(pair.orc.k_pool[:, pg, :, pos % P]), atol=3e-2)
+    finally:
+        pair.close()
+
+
+def test_tiny_trajectory():
+    pair = Pair(WORKLOADS["tiny"])
+    try:
+        run_trajectory(pair, WORKLOADS["tiny"].steps)
+    finally:
+        pair.close()
+
+
+@pytest.mark.parametrize("order", [mk.MK_WAVES_DEFAULT, mk.MK_WAVES_ATTN_FIRST, mk.MK_WAVES_INTERLEAVED])
+@pytest.mark.parametrize("sm_cap", [0, 1, 7])
+def test_tiny_schedules_give_identical_logits(order, sm_cap):
+    """Any wave order and any SM count produce bit-identical output (all sums have a fixed order)."""
+    wl = WORKLOADS["tiny"]
+    from persistent_moe_decode_gb300.runner import StepRunner
+    ref_run = StepRunner(wl, device="cuda")
+    ref_run.step()
+    torch.cuda.synchronize()
+    ref_run.check_status()
+    ref = ref_run.logits.clone()
+    ref_run.close()
+    run = StepRunner(wl, device="cuda", wave_order=order, sm_cap=sm_cap, n_attn_claimers=3,
+                     n_moe_claimers=5)
+    run.step()
+    torch.cuda.synchronize()
+    run.check_status()
+    assert torch.equal(run.logits, ref)
+    run.close()
+
+
+def test_mid_trajectory_and_split_kv():
+    wl = WORKLOADS["mid_8k"].with_(steps=4)
+    pair = Pair(wl)
+    try:
+        run_trajectory(pair, wl.steps)
+    finally:
+        pair.close()
+
+
+def test_device_timeout_is_reported_and_recoverable():
+    """A wait target that nothing can reach runs out (short limit) and reports
+    MK_ERR_TIMEOUT; the context stays usable and the next step is correct."""
+    from persistent_moe_decode_gb300.runner import StepRunner
+    wl = WORKLOADS["tiny"]
+    run = StepRunner(wl, device="cuda", timeout_ms=200)
+    try:
+        mk.mk_debug_bump_wait(run.dec.h, 1, 1000)
+        run.step()
+        torch.cuda.synchronize()
+        rc, err = run.dec.status()
+        assert rc == mk.MK_ERR_TIMEOUT, (rc, err.as_dict())
+        mk.mk_debug_bump_wait(run.dec.h, 1, 0)
+        run.step()
+        torch.cuda.synchronize()
+        run.check_status()
+        assert torch.isfinite(run.logits).all()
+    finally:
+        run.close()
