@@ -81,7 +81,7 @@ def lib():
             L.orc_paged_attention.argtypes = [C.POINTER(_Dims), vp, vp, vp, i32, i32, vp, vp]
             L.orc_paged_attention.restype = i32
             L.orc_route.argtypes = [i32, i32, vp, vp, vp, vp]
-            L.orc_moe.argtypes = [C.POINTER(_Dims), C.POINTER(_Model), i32, vp, vp, vp,
+            L.orc_moe.argtypes = [C.POINTER(_Dims), C.POINTER(_Model), i32, vp, i32, vp, vp,
                                   C.c_uint, vp]
             L.orc_decode_step.argtypes = [C.POINTER(_Dims), C.POINTER(_Model), i32, vp, vp, vp,
                                           i32, C.c_uint, vp, C.POINTER(_Trace)]
@@ -236,9 +236,11 @@ class Oracle:
         x = _f64(x)
         idx = np.ascontiguousarray(idx, dtype=np.int32)
         w = _f64(w)
+        assert idx.shape == w.shape and idx.ndim == 1
+        assert np.all((idx >= 0) & (idx < self.dims["n_experts"]))
         out = np.empty(self.dims["hidden"], dtype=np.float64)
-        lib().orc_moe(C.byref(self._dm), C.byref(self._m), int(layer), _p(x), _p(idx), _p(w),
-                      int(flags), _p(out))
+        lib().orc_moe(C.byref(self._dm), C.byref(self._m), int(layer), _p(x), int(idx.size), _p(idx),
+                      _p(w), int(flags), _p(out))
         return out
 
     def decode_step(self, tokens, seq_lens, page_tables, flags: int = 0, trace: bool = False):

@@ -190,14 +190,14 @@ void orc_route(int n_experts, int top_k, const double* logits, int32_t* idx, dou
 /* ----------------------------------------------------------------- MoE
  * §Tasks, MOE_UPGATE_ACT / MOE_DOWN / MOE_COMBINE: for each kept expert e,
  * a = SiLU(W_g^e x) * (W_u^e x), y = W_d^e a; out = sum_j w_j y_j. */
-void orc_moe(const orc_dims* dm, const orc_model* m, int layer, const double* x,
+void orc_moe(const orc_dims* dm, const orc_model* m, int layer, const double* x, int n_sel,
              const int32_t* idx, const double* w, unsigned flags, double* out) {
   const int H = dm->hidden, I = dm->moe_inter;
   double* g = (double*)malloc(sizeof(double) * (size_t)I);
   double* u = (double*)malloc(sizeof(double) * (size_t)I);
   double* y = (double*)malloc(sizeof(double) * (size_t)H);
   for (int i = 0; i < H; i++) out[i] = 0.0;
-  for (int j = 0; j < dm->top_k; j++) {
+  for (int j = 0; j < n_sel; j++) {
     int e = idx[j];
     const uint16_t* wg = m->w_gate[layer] + (size_t)e * I * H;
     const uint16_t* wu = m->w_up[layer] + (size_t)e * I * H;
@@ -296,7 +296,7 @@ static int layer_body(const orc_dims* dm, const orc_model* m, int l, int B,
     double gap;
     orc_route(E, K, rl + (size_t)b * E, idx + (size_t)b * K, wt + (size_t)b * K, &gap);
     if (tr && tr->gap) tr->gap[(size_t)l * B + b] = gap;
-    orc_moe(dm, m, l, x + (size_t)b * H, idx + (size_t)b * K, wt + (size_t)b * K, flags,
+    orc_moe(dm, m, l, x + (size_t)b * H, K, idx + (size_t)b * K, wt + (size_t)b * K, flags,
             mo + (size_t)b * H);
   }
   if (tr && tr->router) memcpy(tr->router + (size_t)l * B * E, rl, sizeof(double) * (size_t)B * E);

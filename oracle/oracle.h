@@ -87,7 +87,7 @@ int orc_paged_attention(const orc_dims* dm, const uint16_t* k_pool, const uint16
                         const double* q, double* out);
 void orc_route(int n_experts, int top_k, const double* logits, int32_t* idx, double* w,
                double* gap);
-void orc_moe(const orc_dims* dm, const orc_model* m, int layer, const double* x,
+void orc_moe(const orc_dims* dm, const orc_model* m, int layer, const double* x, int n_sel,
              const int32_t* idx, const double* w, unsigned flags, double* out);
 
 /* ---- one decode step for a batch ----
