@@ -88,6 +88,7 @@ typedef struct {
   int kv_split_tokens;    /* split-KV chunk (multiple of 64); 0 = per step       */
   int sm_cap;             /* use at most this many SMs; 0 = all                  */
   int timeout_ms;         /* device spin limit per wait; 0 = 2000                */
+  int trace_records;      /* per-SM task timeline records kept; 0 = tracing off  */
 } mk_config;
 
 /*
@@ -180,13 +181,14 @@ int mk_get_routing(mk_handle* h, int32_t* idx, float* w);
  * (X and H take L for the final norm).  Copies min(bytes, size) bytes to the
  * HOST buffer dst and returns the full size in *size_out (may be NULL). */
 enum mk_scratch {
-  MK_SCRATCH_H = 0,       /* fp32 [batch][H]  residual entering the layer     */
-  MK_SCRATCH_X = 1,       /* bf16 [batch][H]  normalised layer input          */
-  MK_SCRATCH_Q = 2,       /* bf16 [batch][hq][d]  query after RoPE            */
-  MK_SCRATCH_ATTN = 3,    /* bf16 [batch][hq*d]   attention output            */
-  MK_SCRATCH_ROUTER = 4,  /* fp32 [batch][E]  router logits                   */
-  MK_SCRATCH_OPROJ = 5,   /* fp32 [hkv][batch][H]  O-proj split-K partials    */
-  MK_SCRATCH_MOE = 6      /* fp32 [batch][top_k][H] weighted expert outputs   */
+  MK_SCRATCH_H = 0,       /* fp32 [batch][H]  residual entering the layer         */
+  MK_SCRATCH_X = 1,       /* fp32 [batch][H]  normalised layer input              */
+  MK_SCRATCH_Q = 2,       /* fp32 [batch][hq][d]  query after RoPE                */
+  MK_SCRATCH_ATTN = 3,    /* fp32 [batch][hq*d]   attention output                */
+  MK_SCRATCH_ROUTER = 4,  /* fp32 [batch][E]  router logits                       */
+  MK_SCRATCH_OPROJ = 5,   /* fp32 [parts][batch][H]  O-proj output: 1 part for
+                             batch <= 8, hkv split-K parts (to be summed) above  */
+  MK_SCRATCH_MOE = 6      /* fp32 [batch][top_k][H] weighted expert outputs       */
 };
 int mk_read_scratch(mk_handle* h, int which, int layer, void* dst, size_t bytes,
                     size_t* size_out);
@@ -203,6 +205,19 @@ int mk_plan(const mk_config* cfg, int n_sm, int batch, int32_t* tasks, int32_t* 
  * can never complete and runs out after config.timeout_ms (the kernel then
  * stops every block and reports MK_ERR_TIMEOUT).  delta = 0 restores it. */
 int mk_debug_bump_wait(mk_handle* h, int layer, int delta);
+
+/* Task timeline of the last completed step (config.trace_records > 0):
+ * HOST buffer of int32 [n_sm][trace_records][16] records
+ *   {op, layer, tile or queue item, t_start_lo, t_start_hi, ready_ns, end_ns, sm,
+ *    first_stage_ns, stages_done_ns, reduced_ns, 0, 0, 0, 0, 0}
+ * where t_start is the %globaltimer value (ns) when the block took the task,
+ * ready_ns the offset at which its inputs were ready, end_ns the offset at
+ * which it signalled completion and the next three the offsets at which its
+ * first stage arrived, its last stage was consumed and its partial sums were
+ * reduced (equal to the start where a task has no such phase); unused records
+ * have op = -1.  Copies min(bytes, size) bytes; *size_out (may be NULL) gets
+ * the full size. */
+int mk_read_trace(mk_handle* h, void* dst, size_t bytes, size_t* size_out);
 
 /* Library-owned device bytes (counters, scratch, queues, task lists). */
 size_t mk_device_bytes(const mk_handle* h);

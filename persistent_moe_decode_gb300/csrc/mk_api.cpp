@@ -4,7 +4,7 @@
 // Mini Code", §The serving engine around the kernel: the page tables and
 // per-sequence state are snapshot into device memory (update_kv_page_tables),
 // the counters are zeroed (clear_scratch_and_barriers), the split-KV schedule
-// follows the longest live context (select_schedule(max_live_context)) and the
+// follows the live contexts (select_schedule(max_live_context)) and the
 // persistent kernel is launched (launch_megakernel).
 #include <cuda_runtime.h>
 #include <math.h>
@@ -58,6 +58,7 @@ struct mk_handle {
   int32_t* d_pt = nullptr;
   float* d_rope = nullptr;
   int32_t* d_items = nullptr;
+  int32_t* d_meta = nullptr;
   size_t step_bytes_cap = 0;
   Staging stage[2];
   int stage_idx = 0;
@@ -69,6 +70,8 @@ struct mk_handle {
   int last_batch = 0;
   uint32_t* d_bars = nullptr;   // err words live at the start
   size_t bar_words = 0;
+  int32_t* d_trace = nullptr;
+  size_t trace_words = 0;
 };
 
 namespace {
@@ -137,7 +140,7 @@ int ensure_plan(mk_handle* h, int batch, DevPlan** out) {
 
 size_t step_upload_bytes(const mk_config& c, int batch, int n_items) {
   return (size_t)batch * 4 * 2 + (size_t)batch * c.max_pages_per_seq * 4 +
-         (size_t)batch * (c.head_dim / 2) * 2 * 4 + (size_t)n_items * 8 * 4;
+         (size_t)batch * (c.head_dim / 2) * 2 * 4 + (size_t)n_items * 8 * 4 + (size_t)batch * 2 * 4;
 }
 
 }  // namespace
@@ -245,7 +248,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
 
   const size_t Ls = (size_t)L, Bs = (size_t)Bm;
   p.max_up = std::min(E, Bm * K) * (I / kRowsUp);
-  p.max_down = std::min(E, Bm * K) * (H / kRowsDown);
+  p.max_down = std::min(E, Bm * K) * (H / std::min(kRowsDownN, kRowsDownW));
   p.max_attn_items = c.max_attn_items;
   TRY(dalloc(h, &p.h, (Ls + 1) * Bs * H));
   TRY(dalloc(h, &p.x, (Ls + 1) * Bs * H));
@@ -261,8 +264,8 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
   TRY(dalloc(h, &p.upq, Ls * p.max_up));
   TRY(dalloc(h, &p.downq, Ls * p.max_down));
   TRY(dalloc(h, &p.qmeta, Ls * 4));
-  TRY(dalloc(h, &p.attn_part, (size_t)c.max_attn_items * grp * d));
-  TRY(dalloc(h, &p.attn_ml, (size_t)c.max_attn_items * grp * 2));
+  TRY(dalloc(h, &p.attn_part, (size_t)c.max_attn_items * hkv * grp * d));
+  TRY(dalloc(h, &p.attn_ml, (size_t)c.max_attn_items * hkv * grp * 2));
   TRY(dalloc(h, &p.attn_out, Ls * Bs * hq * d));
   TRY(dalloc(h, &p.oproj, Ls * hkv * Bs * H));
   TRY(dalloc(h, &p.abuf, Ls * Bs * K * I));
@@ -276,6 +279,13 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
   TRY(dalloc(h, &h->d_pt, Bs * c.max_pages_per_seq));
   TRY(dalloc(h, &h->d_rope, Bs * (d / 2) * 2));
   TRY(dalloc(h, &h->d_items, (size_t)c.max_attn_items * 8));
+  TRY(dalloc(h, &h->d_meta, Bs * 2));
+  if (c.trace_records > 0) {
+    h->trace_words = (size_t)h->n_sm * c.trace_records * kTraceWords;
+    TRY(dalloc(h, &h->d_trace, h->trace_words));
+    p.trace = h->d_trace;
+    p.trace_cap = c.trace_records;
+  }
   if (cudaMemset(h->d_bars, 0, h->bar_words * 4) != cudaSuccess) { mk_destroy(h); return MK_ERR_CUDA; }
   h->step_bytes_cap = step_upload_bytes(c, Bm, c.max_attn_items);
   for (auto& s : h->stage) {
@@ -295,9 +305,8 @@ int mk_schedule_step(mk_handle* h, int batch, const int32_t* seq_ids, const int3
   h->scheduled = false;
   if (batch < 1 || batch > c.max_batch) return MK_ERR_BATCH_TOO_LARGE;
   if (!tokens || !page_tables || !seq_lens) return MK_ERR_BAD_ARG;
-  const int P = c.page_size, MP = c.max_pages_per_seq, hkv = c.n_kv_heads, d = c.head_dim;
+  const int P = c.page_size, MP = c.max_pages_per_seq, d = c.head_dim;
   long long total_keys = 0;
-  int max_ctx = 0;
   for (int b = 0; b < batch; b++) {
     if (tokens[b] < 0 || tokens[b] >= c.vocab) return MK_ERR_BAD_ARG;
     if (seq_lens[b] < 0) return MK_ERR_BAD_ARG;
@@ -308,23 +317,22 @@ int mk_schedule_step(mk_handle* h, int batch, const int32_t* seq_ids, const int3
       if (pg < 0 || pg >= c.num_kv_pages) return MK_ERR_BAD_PAGE;
     }
     total_keys += seq_lens[b] + 1;
-    max_ctx = std::max(max_ctx, seq_lens[b] + 1);
   }
-  // select_schedule: split-KV chunk from the live contexts, about two items per SM
+  // select_schedule: split-KV chunk from the live contexts, about one item
+  // (all KV heads of one key range) per SM
   int S = c.kv_split_tokens;
   if (S <= 0) {
-    long long want = (total_keys * hkv + 2LL * h->n_sm - 1) / (2LL * h->n_sm);
+    long long want = (total_keys + h->n_sm - 1) / h->n_sm;
     want = (want + 63) / 64 * 64;
-    S = (int)std::max<long long>(256, std::min<long long>(want, 1 << 22));
+    S = (int)std::max<long long>(64, std::min<long long>(want, 1 << 22));
   }
   auto count_items = [&](int s) {
     long long n = 0;
-    for (int b = 0; b < batch; b++) n += (long long)hkv * ((seq_lens[b] + 1 + s - 1) / s);
+    for (int b = 0; b < batch; b++) n += (seq_lens[b] + 1 + s - 1) / s;
     return n;
   };
   while (count_items(S) > c.max_attn_items) S *= 2;
   const int n_items = (int)count_items(S);
-  (void)max_ctx;
 
   DevPlan* plan = nullptr;
   int rc = ensure_plan(h, batch, &plan);
@@ -342,6 +350,7 @@ int mk_schedule_step(mk_handle* h, int batch, const int32_t* seq_ids, const int3
   int32_t* s_pos = (int32_t*)cur; cur += (size_t)batch * 4;
   int32_t* s_pt = (int32_t*)cur; cur += (size_t)batch * MP * 4;
   float* s_rope = (float*)cur; cur += (size_t)batch * (d / 2) * 2 * 4;
+  int32_t* s_meta = (int32_t*)cur; cur += (size_t)batch * 2 * 4;
   int32_t* s_items = (int32_t*)cur;
   memcpy(s_tok, tokens, (size_t)batch * 4);
   memcpy(s_pos, seq_lens, (size_t)batch * 4);
@@ -358,14 +367,14 @@ int mk_schedule_step(mk_handle* h, int batch, const int32_t* seq_ids, const int3
   for (int b = 0; b < batch; b++) {
     const int keys = seq_lens[b] + 1;
     const int ns = (keys + S - 1) / S;
-    for (int g = 0; g < hkv; g++) {
-      const int base = k;
-      for (int s = 0; s < ns; s++, k++) {
-        int32_t* it = s_items + (size_t)k * 8;
-        it[AI_B] = b; it[AI_G] = g; it[AI_S] = s; it[AI_NSPLIT] = ns;
-        it[AI_T0] = s * S; it[AI_T1] = std::min(keys, (s + 1) * S);
-        it[AI_BASE] = base; it[AI_POS] = seq_lens[b];
-      }
+    s_meta[b * 2 + 0] = k;
+    s_meta[b * 2 + 1] = ns;
+    const int base = k;
+    for (int s = 0; s < ns; s++, k++) {
+      int32_t* it = s_items + (size_t)k * 8;
+      it[AI_B] = b; it[AI_S] = s; it[AI_NSPLIT] = ns;
+      it[AI_T0] = s * S; it[AI_T1] = std::min(keys, (s + 1) * S);
+      it[AI_BASE] = base; it[AI_POS] = seq_lens[b]; it[7] = 0;
     }
   }
   cudaStream_t sm = (cudaStream_t)stream;
@@ -373,6 +382,7 @@ int mk_schedule_step(mk_handle* h, int batch, const int32_t* seq_ids, const int3
             cudaMemcpyAsync(h->d_pos, s_pos, (size_t)batch * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
             cudaMemcpyAsync(h->d_pt, s_pt, (size_t)batch * MP * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
             cudaMemcpyAsync(h->d_rope, s_rope, (size_t)batch * (d / 2) * 2 * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
+            cudaMemcpyAsync(h->d_meta, s_meta, (size_t)batch * 2 * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
             cudaMemcpyAsync(h->d_items, s_items, (size_t)n_items * 8 * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
             cudaEventRecord(st.done, sm) == cudaSuccess;
   if (!ok) return MK_ERR_CUDA;
@@ -392,9 +402,13 @@ int mk_decode_step(mk_handle* h, float* logits, void* stream) {
   if (rc) return rc;
   cudaStream_t sm = (cudaStream_t)stream;
   if (cudaMemsetAsync(h->d_bars, 0, h->bar_words * 4, sm) != cudaSuccess) return MK_ERR_CUDA;
+  if (h->d_trace && cudaMemsetAsync(h->d_trace, 0xff, h->trace_words * 4, sm) != cudaSuccess)
+    return MK_ERR_CUDA;
   Params p = h->base;
   p.B = h->batch;
+  p.wide = wide_path(h->batch) ? 1 : 0;
   p.n_attn_items = h->n_items;
+  p.attn_meta = h->d_meta;
   p.tokens = h->d_tokens;
   p.pos = h->d_pos;
   p.page_tables = h->d_pt;
@@ -463,36 +477,46 @@ int mk_read_scratch(mk_handle* h, int which, int layer, void* dst, size_t bytes,
   const int H = c.hidden, hq = c.n_q_heads, d = c.head_dim, hkv = c.n_kv_heads;
   const int maxl = (which == MK_SCRATCH_H || which == MK_SCRATCH_X) ? L : L - 1;
   if (layer < 0 || layer > maxl) return MK_ERR_BAD_ARG;
-  // (base pointer of the layer, bytes per sequence row, rows, row stride in bytes)
   const uint8_t* base = nullptr;
-  size_t row = 0, rows = (size_t)B, stride = 0;
+  size_t row = 0;
   switch (which) {
-    case MK_SCRATCH_H: row = (size_t)H * 4; stride = row; base = (const uint8_t*)(p.h + (size_t)layer * Bm * H); break;
-    case MK_SCRATCH_X: row = (size_t)H * 2; stride = row; base = (const uint8_t*)(p.x + (size_t)layer * Bm * H); break;
-    case MK_SCRATCH_Q: row = (size_t)hq * d * 2; stride = row; base = (const uint8_t*)(p.q + (size_t)layer * Bm * hq * d); break;
-    case MK_SCRATCH_ATTN: row = (size_t)hq * d * 2; stride = row; base = (const uint8_t*)(p.attn_out + (size_t)layer * Bm * hq * d); break;
-    case MK_SCRATCH_ROUTER: row = (size_t)c.n_experts * 4; stride = row; base = (const uint8_t*)(p.rlog + (size_t)layer * Bm * c.n_experts); break;
+    case MK_SCRATCH_H: row = (size_t)H * 4; base = (const uint8_t*)(p.h + (size_t)layer * Bm * H); break;
+    case MK_SCRATCH_X: row = (size_t)H * 4; base = (const uint8_t*)(p.x + (size_t)layer * Bm * H); break;
+    case MK_SCRATCH_Q: row = (size_t)hq * d * 4; base = (const uint8_t*)(p.q + (size_t)layer * Bm * hq * d); break;
+    case MK_SCRATCH_ATTN: row = (size_t)hq * d * 4; base = (const uint8_t*)(p.attn_out + (size_t)layer * Bm * hq * d); break;
+    case MK_SCRATCH_ROUTER: row = (size_t)c.n_experts * 4; base = (const uint8_t*)(p.rlog + (size_t)layer * Bm * c.n_experts); break;
     case MK_SCRATCH_OPROJ: {
-      const size_t full = (size_t)hkv * B * H * 4;
+      const int parts = wide_path(B) ? hkv : 1;
+      const size_t full = (size_t)parts * B * H * 4;
       if (size_out) *size_out = full;
       std::vector<uint8_t> tmp(full);
-      for (int g = 0; g < hkv; g++)
+      for (int g = 0; g < parts; g++)
         if (cudaMemcpy(tmp.data() + (size_t)g * B * H * 4, p.oproj + ((size_t)layer * hkv + g) * Bm * H,
                        (size_t)B * H * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
           return MK_ERR_CUDA;
       if (dst) memcpy(dst, tmp.data(), std::min(bytes, full));
       return MK_OK;
     }
-    case MK_SCRATCH_MOE: row = (size_t)c.top_k * H * 4; stride = row; base = (const uint8_t*)(p.ybuf + (size_t)layer * Bm * c.top_k * H); break;
+    case MK_SCRATCH_MOE: row = (size_t)c.top_k * H * 4; base = (const uint8_t*)(p.ybuf + (size_t)layer * Bm * c.top_k * H); break;
     default: return MK_ERR_BAD_ARG;
   }
-  const size_t full = row * rows;
+  const size_t full = row * (size_t)B;
   if (size_out) *size_out = full;
   if (dst && cudaMemcpy(dst, base, std::min(bytes, full), cudaMemcpyDeviceToHost) != cudaSuccess) {
     cudaGetLastError();
     return MK_ERR_CUDA;
   }
-  (void)stride;
+  return MK_OK;
+}
+
+int mk_read_trace(mk_handle* h, void* dst, size_t bytes, size_t* size_out) {
+  if (!h) return MK_ERR_BAD_ARG;
+  const size_t full = h->trace_words * 4;
+  if (size_out) *size_out = full;
+  if (dst && full && cudaMemcpy(dst, h->d_trace, std::min(bytes, full), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
   return MK_OK;
 }
 

@@ -10,6 +10,12 @@
 #pragma once
 #include <stdint.h>
 
+#ifdef __CUDACC__
+#define MK_HD __host__ __device__
+#else
+#define MK_HD
+#endif
+
 namespace mk {
 
 constexpr int kDescWords = 32;
@@ -19,11 +25,12 @@ enum Op : int32_t {
   OP_NORM = 1,       // fused residual add + RMSNorm of one layer (or the final norm)
   OP_QKV = 2,        // QKV GEMV tile with RoPE in the epilogue, appends K/V
   OP_ROUTER = 3,     // router GEMV tile; the last tile runs top-k + route setup
-  OP_ATTN = 4,       // claimer on the split-KV attention queue (+ combine)
+  OP_ATTN = 4,       // claimer on the split-KV attention queue
   OP_MOE_UP = 5,     // claimer on the expert gate/up queue (SiLU * up epilogue)
   OP_MOE_DOWN = 6,   // claimer on the expert down queue (routing weight epilogue)
-  OP_OPROJ = 7,      // O-proj tile of one KV-head group (split-K = hkv)
-  OP_LMHEAD = 8      // LM-head GEMV tile
+  OP_OPROJ = 7,      // O-proj tile (full contraction, or one KV-head group on the wide path)
+  OP_LMHEAD = 8,     // LM-head GEMV tile
+  OP_COMBINE = 9     // merge the split-KV partials of one (sequence, KV head)
 };
 
 // descriptor words (host-built, read by the producer warp)
@@ -33,26 +40,41 @@ enum : int {
   F_W1 = 5, F_T1 = 6,
   F_SIG = 7, F_INC = 8,    // counter signalled on completion, increment (-1: none)
   F_PW = 9, F_PT = 10,     // producer-side wait before loading (MoE claimers: routing)
-  F_SEQ = 11               // position in the flattened step order (error reports)
+  F_SEQ = 11,              // position in the flattened step order (error reports)
+  F_ARG = 12               // op-specific argument (ATTN_COMBINE: tasks per KV group)
 };
 
-// tile geometry (rows of output per tile; every tile is at most two 16-row groups)
-constexpr int kRowsQKV = 32;    // 16 rows + their RoPE partners d/2 further
+// Tile geometry.  Two GEMV paths share the task structure:
+//  narrow (batch <= 8): CUDA-core FMA on whole contiguous weight rows, one bulk
+//    copy of up to 32 KB per stage;
+//  wide (batch 9..16): warp-level tensor-core MMA on 16-row stages padded for
+//    conflict-free fragment loads.
+constexpr int kRowsQKVHalf = 16;  // a QKV tile: 16 rows + their RoPE partners d/2 further
 constexpr int kRowsRouter = 16;
-constexpr int kRowsOProj = 32;
-constexpr int kRowsUp = 16;     // 16 gate rows + the same 16 up rows
-constexpr int kRowsDown = 32;
-constexpr int kRowsLM = 32;
+constexpr int kRowsUp = 16;       // 16 gate rows + the same 16 up rows
+constexpr int kRowsDownN = 64, kRowsDownW = 32;
+constexpr int kRowsLMN = 64, kRowsLMW = 32;
+constexpr int kRowsOProj = 32;    // narrow: full contraction; wide: one KV group's columns
+constexpr int kNarrowMaxBatch = 8;
 
 // persistent block shape: 8 consumer warps + 1 producer warp
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 5;              // weight / KV stage ring depth
-constexpr int kStageRows = 16;
-constexpr int kStageKcMax = 1024;       // columns per stage row
+constexpr int kStages = 6;              // weight / KV stage ring depth
+constexpr int kStageData = 32768;       // narrow stages: up to 32 KB of whole rows
+constexpr int kStageRows = 16;          // wide stages: 16 rows x up to 1024 columns, padded
+constexpr int kStageKcMax = 1024;
 constexpr int kStageBytes = kStageRows * (kStageKcMax * 2 + 64);   // 33,792
 constexpr int kTaskSlots = 8;           // resolved-task ring depth
 constexpr int kMaxBatch = 16;
+constexpr int kTraceWords = 16;         // words per timeline record
+
+// rows of a [rows][K] BF16 matrix that one narrow stage carries
+MK_HD inline int narrow_rows_per_stage(int K) {
+  int r = 1;
+  while (r * 2 * 2 * K <= kStageData && r < 128) r *= 2;
+  return r;
+}
 
 // Counter block of one layer.  Index = layer * per_layer + offset.
 struct BarLayout {
@@ -61,11 +83,11 @@ struct BarLayout {
   int qkv;        // + g: QKV tiles of KV group g done          (target (grp + 2) * d / 32)
   int route;      // routing + queues written                   (target 1)
   int up;         // + e: gate/up tiles of expert e done        (target I / kRowsUp)
-  int attn;       // + g: attention of group g combined         (target B)
-  int o;          // O-proj tiles done                          (target hkv * H / kRowsOProj)
-  int moe;        // down tiles done, weighted by token count   (target B * k * H / kRowsDown)
+  int items;      // + b: split-KV items of sequence b done     (target: its split count)
+  int attn;       // combines done                              (target B * hkv * tasks per group)
+  int o;          // O-proj tiles done                          (target: O-proj tile count)
+  int moe;        // down tiles done, weighted by token count   (target B * k * H / rows)
   int tk_router;  // ticket: last router tile runs top-k
-  int tk_attn;    // + b * hkv + g: ticket of the split-KV combine
   int claim;      // + q: claim counters of the three queues
 };
 
@@ -76,11 +98,11 @@ inline BarLayout bar_layout(int hkv, int n_experts, int max_batch) {
   b.qkv = o; o += hkv;
   b.route = o; o += 1;
   b.up = o; o += n_experts;
-  b.attn = o; o += hkv;
+  b.items = o; o += max_batch;
+  b.attn = o; o += 1;
   b.o = o; o += 1;
   b.moe = o; o += 1;
   b.tk_router = o; o += 1;
-  b.tk_attn = o; o += max_batch * hkv;
   b.claim = o; o += 3;
   b.per_layer = (o + 31) & ~31;
   return b;
@@ -93,9 +115,8 @@ enum : int { E_CODE = 0, E_SM = 1, E_TASK = 2, E_OP = 3, E_BAR = 4, E_VAL = 5, E
 enum : uint32_t { DEV_TIMEOUT = 1, DEV_BAD_PAGE = 2, DEV_BAD_ITEM = 3, DEV_BAD_OP = 4,
                   DEV_SMEM_TIMEOUT = 5 };
 
-// attention queue item: 8 int32 words
-enum : int { AI_B = 0, AI_G = 1, AI_S = 2, AI_NSPLIT = 3, AI_T0 = 4, AI_T1 = 5, AI_BASE = 6,
-             AI_POS = 7 };
+// attention queue item: 8 int32 words (one sequence, all KV heads, keys [t0, t1))
+enum : int { AI_B = 0, AI_S = 1, AI_NSPLIT = 2, AI_T0 = 3, AI_T1 = 4, AI_BASE = 5, AI_POS = 6 };
 
 struct Params {
   // model
@@ -117,12 +138,14 @@ struct Params {
   uint16_t* const* v_pool;
   // this step
   int B;
+  int wide;                    // 1: tensor-core GEMV path (batch > 8)
   int n_attn_items;
   const int32_t* tokens;       // [B]
   const int32_t* pos;          // [B] position of the new token (= cached length)
   const int32_t* page_tables;  // [B][max_pages]
   const float* rope;           // [B][d/2][2] cos, sin
   const int32_t* attn_items;   // [n_attn_items][8]
+  const int32_t* attn_meta;    // [B][2]: first item of the sequence, its split count
   float* logits;               // [B][V] caller buffer
   // task lists
   const int32_t* tasks;        // [n][32]
@@ -133,11 +156,13 @@ struct Params {
   BarLayout bl;
   uint32_t* err;
   unsigned long long timeout_ns;
-  // scratch (per-layer strides use Bmax)
-  float* h;          // [L+1][Bmax][H]
-  uint16_t* x;       // [L+1][Bmax][H]
-  uint16_t* q;       // [L][Bmax][hq d]
-  uint16_t* knew;    // [L][Bmax][hkv d]
+  int32_t* trace;      // [n_sm][trace_cap][kTraceWords] task timeline (nullptr: off)
+  int trace_cap;
+  // scratch (per-layer strides use Bmax); activations are fp32
+  float* h;          // [L+1][Bmax][H]  residual entering the layer
+  float* x;          // [L+1][Bmax][H]  normalised layer input
+  float* q;          // [L][Bmax][hq d] query after RoPE
+  uint16_t* knew;    // [L][Bmax][hkv d] new key after RoPE (BF16, as cached)
   uint16_t* vnew;    // [L][Bmax][hkv d]
   float* rlog;       // [L][Bmax][E]
   int32_t* ridx;     // [L][Bmax][k]
@@ -149,13 +174,13 @@ struct Params {
   int32_t* downq;    // [L][max_down]
   int32_t* qmeta;    // [L][4]        n_up, n_down, n_active
   int max_up, max_down;
-  float* attn_part;  // [max_attn_items][grp][d]   unnormalised split outputs
-  float* attn_ml;    // [max_attn_items][grp][2]   (max, sum) in the log2 domain
+  float* attn_part;  // [max_attn_items][hkv][grp][d] unnormalised split outputs
+  float* attn_ml;    // [max_attn_items][hkv][grp][2] (max, sum) in the log2 domain
   int max_attn_items;
-  uint16_t* attn_out;  // [L][Bmax][hq d]
-  float* oproj;        // [L][hkv][Bmax][H]
-  uint16_t* abuf;      // [L][Bmax * k][I]
-  float* ybuf;         // [L][Bmax][k][H]
+  float* attn_out;   // [L][Bmax][hq d]
+  float* oproj;      // [L][hkv][Bmax][H] (narrow path: slot 0 holds the full product)
+  float* abuf;       // [L][Bmax * k][I]
+  float* ybuf;       // [L][Bmax][k][H]
 };
 
 }  // namespace mk

@@ -14,27 +14,38 @@
 
 namespace mk {
 
+// contraction lengths of the wide (tensor-core) GEMV path
 static bool supported_k(int k) {
   return k == 128 || k == 256 || k == 512 || k == 768 || k == 1024 || k == 2048;
 }
+
+// contraction lengths of the narrow (CUDA-core, whole-row) GEMV path
+static bool narrow_k(int k) { return k == 128 || (k % 256 == 0 && k <= 4096); }
 
 int validate_config(const mk_config& c) {
   if (c.n_layers < 1 || c.hidden < 32 || c.n_q_heads < 1 || c.n_kv_heads < 1) return MK_ERR_BAD_CONFIG;
   if (c.n_q_heads % c.n_kv_heads) return MK_ERR_BAD_CONFIG;
   const int grp = c.n_q_heads / c.n_kv_heads;
-  if (grp > 8) return MK_ERR_BAD_CONFIG;
+  if (grp > 8 || kConsumerWarps % c.n_kv_heads) return MK_ERR_BAD_CONFIG;
   if (c.head_dim != 64 && c.head_dim != 128) return MK_ERR_BAD_CONFIG;
+  // both GEMV paths must be able to run every matrix of the model
   if (!supported_k(c.hidden) || !supported_k(c.moe_inter) || !supported_k(grp * c.head_dim))
     return MK_ERR_BAD_CONFIG;
-  if (c.hidden % kRowsOProj || c.hidden % kRowsDown || c.moe_inter % kRowsUp) return MK_ERR_BAD_CONFIG;
+  if (!narrow_k(c.hidden) || !narrow_k(c.moe_inter) || !narrow_k(c.n_q_heads * c.head_dim))
+    return MK_ERR_BAD_CONFIG;
+  if (c.hidden % kRowsOProj || c.hidden % kRowsDownN || c.hidden % kRowsDownW ||
+      c.moe_inter % kRowsUp)
+    return MK_ERR_BAD_CONFIG;
   if (c.n_experts < 1 || c.n_experts > 256 || c.top_k < 1 || c.top_k > 8 || c.top_k > c.n_experts)
     return MK_ERR_BAD_CONFIG;
   if (c.vocab < 1 || c.page_size != 16) return MK_ERR_BAD_CONFIG;
+  // one 16-token page of every KV head (K or V) must fit half a stage
+  if (c.n_kv_heads * c.page_size * c.head_dim * 2 > kStageData / 2) return MK_ERR_BAD_CONFIG;
   if (c.max_batch < 1 || c.max_batch > kMaxBatch) return MK_ERR_BAD_CONFIG;
   if (c.max_pages_per_seq < 1 || c.num_kv_pages < 1) return MK_ERR_BAD_CONFIG;
   if (!(c.rope_theta > 0.0) || !(c.rms_eps >= 0.f)) return MK_ERR_BAD_CONFIG;
   if (c.max_attn_items < 0 || c.n_attn_claimers < 0 || c.n_moe_claimers < 0 || c.sm_cap < 0 ||
-      c.timeout_ms < 0)
+      c.timeout_ms < 0 || c.trace_records < 0)
     return MK_ERR_BAD_CONFIG;
   if (c.kv_split_tokens < 0 || c.kv_split_tokens % 64) return MK_ERR_BAD_CONFIG;
   if (c.wave_order < MK_WAVES_DEFAULT || c.wave_order > MK_WAVES_INTERLEAVED) return MK_ERR_BAD_CONFIG;
@@ -56,7 +67,7 @@ Desc blank(int op, int layer, int tile) {
   return d;
 }
 
-enum Wave { W_NORM, W_QKV, W_ROUTER, W_ATTN, W_UP, W_DOWN, W_OPROJ };
+enum Wave { W_NORM, W_QKV, W_ROUTER, W_ATTN, W_COMBINE, W_UP, W_DOWN, W_OPROJ };
 
 }  // namespace
 
@@ -64,28 +75,30 @@ int build_plan(const mk_config& c, int n_sm, int batch, Plan* out, int bump_laye
   if (validate_config(c) != MK_OK || n_sm < 1 || batch < 1 || batch > c.max_batch)
     return MK_ERR_BAD_CONFIG;
   const BarLayout bl = bar_layout(c.n_kv_heads, c.n_experts, c.max_batch);
-  const int L = c.n_layers, H = c.hidden, d = c.head_dim, hkv = c.n_kv_heads;
-  const int grp = c.n_q_heads / hkv;
+  const int L = c.n_layers, d = c.head_dim, hkv = c.n_kv_heads;
   auto bar = [&](int layer, int off) { return layer * bl.per_layer + off; };
   const int n_attn_c = c.n_attn_claimers > 0 ? c.n_attn_claimers : n_sm;
   const int n_moe_c = c.n_moe_claimers > 0 ? c.n_moe_claimers : n_sm;
+  const int cpg = combine_split(c, batch);
 
   std::vector<Desc> flat;
+  auto norm_task = [&](int l) {
+    Desc t = blank(OP_NORM, l, 0);
+    if (l > 0) {
+      t[F_W0] = bar(l - 1, bl.o);
+      t[F_T0] = oproj_tiles(c, batch) + (l == bump_layer ? bump : 0);
+      t[F_W1] = bar(l - 1, bl.moe);
+      t[F_T1] = moe_target(c, batch);
+    }
+    t[F_SIG] = bar(l, bl.x);
+    t[F_INC] = 1;
+    flat.push_back(t);
+  };
   auto wave = [&](Wave w, int l) {
     switch (w) {
-      case W_NORM: {
-        Desc t = blank(OP_NORM, l, 0);
-        if (l > 0) {
-          t[F_W0] = bar(l - 1, bl.o);
-          t[F_T0] = oproj_tiles(c) + (l == bump_layer ? bump : 0);
-          t[F_W1] = bar(l - 1, bl.moe);
-          t[F_T1] = moe_target(c, batch);
-        }
-        t[F_SIG] = bar(l, bl.x);
-        t[F_INC] = 1;
-        flat.push_back(t);
+      case W_NORM:
+        norm_task(l);
         break;
-      }
       case W_QKV: {
         const int tph = d / 32, heads = c.n_q_heads + 2 * hkv;
         for (int i = 0; i < heads * tph; i++) {
@@ -109,6 +122,21 @@ int build_plan(const mk_config& c, int n_sm, int batch, Plan* out, int bump_laye
       case W_ATTN:
         for (int i = 0; i < n_attn_c; i++) flat.push_back(blank(OP_ATTN, l, i));
         break;
+      case W_COMBINE:
+        // ATTN_COMBINE tasks per (sequence, KV head); the wait target is the
+        // sequence's split count of the step, read by the kernel
+        for (int b = 0; b < batch; b++)
+          for (int g = 0; g < hkv; g++)
+            for (int cc = 0; cc < cpg; cc++) {
+              Desc t = blank(OP_COMBINE, l, (b * hkv + g) * cpg + cc);
+              t[F_W0] = bar(l, bl.items + b);
+              t[F_T0] = -1;
+              t[F_SIG] = bar(l, bl.attn);
+              t[F_INC] = 1;
+              t[F_ARG] = cpg;
+              flat.push_back(t);
+            }
+        break;
       case W_UP:
       case W_DOWN:
         for (int i = 0; i < n_moe_c; i++) {
@@ -119,38 +147,30 @@ int build_plan(const mk_config& c, int n_sm, int batch, Plan* out, int bump_laye
         }
         break;
       case W_OPROJ: {
-        const int per = H / kRowsOProj;
-        for (int g = 0; g < hkv; g++)
-          for (int r = 0; r < per; r++) {
-            Desc t = blank(OP_OPROJ, l, g * per + r);
-            t[F_W0] = bar(l, bl.attn + g);
-            t[F_T0] = batch;
-            t[F_SIG] = bar(l, bl.o);
-            t[F_INC] = 1;
-            flat.push_back(t);
-          }
+        const int n = oproj_tiles(c, batch);
+        for (int i = 0; i < n; i++) {
+          Desc t = blank(OP_OPROJ, l, i);
+          t[F_W0] = bar(l, bl.attn);
+          t[F_T0] = batch * hkv * cpg;
+          t[F_SIG] = bar(l, bl.o);
+          t[F_INC] = 1;
+          flat.push_back(t);
+        }
         break;
       }
     }
   };
 
-  static const Wave orders[3][7] = {
-      {W_NORM, W_QKV, W_ROUTER, W_ATTN, W_UP, W_DOWN, W_OPROJ},
-      {W_NORM, W_QKV, W_ROUTER, W_ATTN, W_OPROJ, W_UP, W_DOWN},
-      {W_NORM, W_QKV, W_ROUTER, W_UP, W_ATTN, W_DOWN, W_OPROJ}};
+  static const Wave orders[3][8] = {
+      {W_NORM, W_QKV, W_ROUTER, W_ATTN, W_COMBINE, W_UP, W_DOWN, W_OPROJ},
+      {W_NORM, W_QKV, W_ROUTER, W_ATTN, W_COMBINE, W_OPROJ, W_UP, W_DOWN},
+      {W_NORM, W_QKV, W_ROUTER, W_UP, W_ATTN, W_DOWN, W_COMBINE, W_OPROJ}};
   for (int l = 0; l < L; l++)
     for (Wave w : orders[c.wave_order]) wave(w, l);
   // final norm and LM head
+  norm_task(L);
   {
-    Desc t = blank(OP_NORM, L, 0);
-    t[F_W0] = bar(L - 1, bl.o);
-    t[F_T0] = oproj_tiles(c) + (L == bump_layer ? bump : 0);
-    t[F_W1] = bar(L - 1, bl.moe);
-    t[F_T1] = moe_target(c, batch);
-    t[F_SIG] = bar(L, bl.x);
-    t[F_INC] = 1;
-    flat.push_back(t);
-    const int n = (c.vocab + kRowsLM - 1) / kRowsLM;
+    const int n = (c.vocab + rows_lm(batch) - 1) / rows_lm(batch);
     for (int i = 0; i < n; i++) {
       Desc u = blank(OP_LMHEAD, L, i);
       u[F_W0] = bar(L, bl.x);
@@ -158,7 +178,6 @@ int build_plan(const mk_config& c, int n_sm, int batch, Plan* out, int bump_laye
       flat.push_back(u);
     }
   }
-  (void)grp;
 
   // deal round-robin
   std::vector<std::vector<int>> per_sm(n_sm);

@@ -25,12 +25,21 @@ int build_plan(const mk_config& c, int n_sm, int batch, Plan* out, int bump_laye
                int bump = 0);
 
 // counter targets shared by the scheduler and the kernel's own bookkeeping
-inline int qkv_tiles_per_group(const mk_config& c) {
-  return (c.n_q_heads / c.n_kv_heads + 2) * (c.head_dim / 32);
+inline bool wide_path(int batch) { return batch > kNarrowMaxBatch; }
+inline int oproj_tiles(const mk_config& c, int batch) {
+  return (wide_path(batch) ? c.n_kv_heads : 1) * c.hidden / kRowsOProj;
 }
-inline int oproj_tiles(const mk_config& c) { return c.n_kv_heads * c.hidden / kRowsOProj; }
+inline int rows_down(int batch) { return wide_path(batch) ? kRowsDownW : kRowsDownN; }
+inline int rows_lm(int batch) { return wide_path(batch) ? kRowsLMW : kRowsLMN; }
+// ATTN_COMBINE tasks per (sequence, KV group): 2 query heads each at batch <= 2,
+// up to 4 above
+inline int combine_split(const mk_config& c, int batch) {
+  const int grp = c.n_q_heads / c.n_kv_heads;
+  const int hp = batch <= 2 ? (grp < 2 ? grp : 2) : (grp < 4 ? grp : 4);
+  return grp / hp;
+}
 inline int moe_target(const mk_config& c, int batch) {
-  return batch * c.top_k * (c.hidden / kRowsDown);
+  return batch * c.top_k * (c.hidden / rows_down(batch));
 }
 
 }  // namespace mk

@@ -35,7 +35,7 @@ MK_WAVES_DEFAULT, MK_WAVES_ATTN_FIRST, MK_WAVES_INTERLEAVED = 0, 1, 2
 # every symbol include/mk.h declares
 EXPORTS = ("mk_create", "mk_schedule_step", "mk_decode_step", "mk_step_status", "mk_get_routing",
            "mk_read_scratch", "mk_plan", "mk_debug_bump_wait", "mk_device_bytes", "mk_num_sms",
-           "mk_step_upload_bytes", "mk_destroy", "mk_strerror", "mk_abi_version")
+           "mk_step_upload_bytes", "mk_destroy", "mk_strerror", "mk_abi_version", "mk_read_trace")
 
 
 class mk_config(C.Structure):
@@ -46,7 +46,7 @@ class mk_config(C.Structure):
                 ("max_batch", C.c_int), ("max_pages_per_seq", C.c_int), ("num_kv_pages", C.c_int),
                 ("max_attn_items", C.c_int), ("wave_order", C.c_int), ("n_attn_claimers", C.c_int),
                 ("n_moe_claimers", C.c_int), ("kv_split_tokens", C.c_int), ("sm_cap", C.c_int),
-                ("timeout_ms", C.c_int)]
+                ("timeout_ms", C.c_int), ("trace_records", C.c_int)]
 
 
 _VPP = C.POINTER(C.c_void_p)
@@ -92,6 +92,7 @@ def lib():
             L.mk_plan.argtypes = [C.POINTER(mk_config), i32, i32, vp, vp, C.POINTER(i32),
                                   C.POINTER(i32)]
             L.mk_debug_bump_wait.argtypes = [vp, i32, i32]
+            L.mk_read_trace.argtypes = [vp, vp, C.c_size_t, C.POINTER(C.c_size_t)]
             L.mk_device_bytes.argtypes = [vp]
             L.mk_device_bytes.restype = C.c_size_t
             L.mk_num_sms.argtypes = [vp]
@@ -187,6 +188,14 @@ def mk_plan(cfg: mk_config, n_sm: int, batch: int):
     return tasks, off, n_bars.value
 
 
+def mk_read_trace(h) -> np.ndarray:
+    size = C.c_size_t(0)
+    _check(lib().mk_read_trace(h, None, 0, C.byref(size)), "mk_read_trace")
+    out = np.empty(size.value // 4, dtype=np.int32)
+    _check(lib().mk_read_trace(h, _ptr(out), size.value, None), "mk_read_trace")
+    return out.reshape(-1, 16)
+
+
 def mk_debug_bump_wait(h, layer: int, delta: int) -> int:
     return _check(lib().mk_debug_bump_wait(h, int(layer), int(delta)), "mk_debug_bump_wait")
 
@@ -269,6 +278,9 @@ class Decoder:
 
     def routing(self):
         return mk_get_routing(self.h, self.dims.n_layers, self.batch, self.dims.top_k)
+
+    def trace(self) -> np.ndarray:
+        return mk_read_trace(self.h)
 
     def scratch(self, which: int, layer: int) -> bytes:
         return mk_read_scratch(self.h, which, layer)

@@ -5,9 +5,13 @@ trajectory is teacher-forced by the GPU: each step both consume the GPU's
 greedy token; each keeps its own KV cache.  Acceptance per step: logits
 max-abs <= 2e-2 and relative L2 <= 1e-2; the expert set of every (layer,
 token) equal to the oracle's wherever the oracle's k-th / (k+1)-th router-logit
-gap exceeds 1e-3; greedy argmax equal on >= 99% of steps.  The oracle runs in
-its BF16-storage mode (x, q, attention output and expert hidden rounded to
-BF16 where the kernel stores them).
+gap exceeds 1e-3; greedy argmax equal on >= 99% of steps.
+
+For batch <= 8 the kernel keeps every activation in fp32 (only the appended
+K/V are BF16, as the cache is) and is compared with the oracle's plain fp64
+definition.  For batch 9..16 its tensor-core GEMVs round the activations they
+consume to BF16; the oracle then rounds at the same points (x, attention
+output, expert hidden).
 """
 from __future__ import annotations
 
@@ -23,6 +27,10 @@ from tests._util import dims_dict, host_pool, host_weights
 pytestmark = pytest.mark.gpu
 
 MAX_ABS, REL_L2, GAP = 2e-2, 1e-2, 1e-3
+
+
+def oracle_flags(batch: int) -> int:
+    return 0 if batch <= 8 else (oracle.BF16_X | oracle.BF16_ATTN | oracle.BF16_A)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -52,7 +60,7 @@ class Pair:
         torch.cuda.synchronize()
         self.run.check_status()
         gpu = self.run.logits.double().cpu().numpy()
-        out = self.orc.decode_step(tokens, lens, pt, flags=oracle.ALL_BF16, trace=trace)
+        out = self.orc.decode_step(tokens, lens, pt, flags=oracle_flags(self.wl.batch), trace=trace)
         ref, tr = (out if trace else (out, None))
         return gpu, ref, tr
 
@@ -109,27 +117,25 @@ def test_tiny_intermediates_match_layer_by_layer():
         dec = pair.run.dec
         for l in range(d.n_layers + 1):
             h = np.frombuffer(dec.scratch(mk.MK_SCRATCH_H, l), dtype=np.float32).reshape(B, d.hidden)
-            np.testing.assert_allclose(h, tr["h_in"][l], atol=2e-3, rtol=1e-2, err_msg=f"h layer {l}")
+            np.testing.assert_allclose(h, tr["h_in"][l], atol=1e-4, rtol=1e-3, err_msg=f"h layer {l}")
         for l in range(d.n_layers):
-            x = np.frombuffer(dec.scratch(mk.MK_SCRATCH_X, l), dtype=np.uint16).reshape(B, d.hidden)
-            np.testing.assert_allclose(oracle.bf16_to_f64(x), tr["x"][l], atol=2e-2, rtol=1e-2,
-                                       err_msg=f"x layer {l}")
-            q = np.frombuffer(dec.scratch(mk.MK_SCRATCH_Q, l), dtype=np.uint16).reshape(B, -1)
-            np.testing.assert_allclose(oracle.bf16_to_f64(q), tr["q"][l], atol=2e-2, rtol=1e-2,
-                                       err_msg=f"q layer {l}")
+            x = np.frombuffer(dec.scratch(mk.MK_SCRATCH_X, l), dtype=np.float32).reshape(B, d.hidden)
+            np.testing.assert_allclose(x, tr["x"][l], atol=1e-4, rtol=1e-4, err_msg=f"x layer {l}")
+            q = np.frombuffer(dec.scratch(mk.MK_SCRATCH_Q, l), dtype=np.float32).reshape(B, -1)
+            np.testing.assert_allclose(q, tr["q"][l], atol=1e-4, rtol=1e-4, err_msg=f"q layer {l}")
             r = np.frombuffer(dec.scratch(mk.MK_SCRATCH_ROUTER, l), dtype=np.float32).reshape(B, -1)
-            np.testing.assert_allclose(r, tr["router"][l], atol=1e-3, rtol=1e-3,
+            np.testing.assert_allclose(r, tr["router"][l], atol=1e-4, rtol=1e-4,
                                        err_msg=f"router layer {l}")
-            a = np.frombuffer(dec.scratch(mk.MK_SCRATCH_ATTN, l), dtype=np.uint16).reshape(B, -1)
-            np.testing.assert_allclose(oracle.bf16_to_f64(a), tr["attn"][l], atol=2e-2, rtol=2e-2,
+            a = np.frombuffer(dec.scratch(mk.MK_SCRATCH_ATTN, l), dtype=np.float32).reshape(B, -1)
+            np.testing.assert_allclose(a, tr["attn"][l], atol=1e-4, rtol=1e-3,
                                        err_msg=f"attn layer {l}")
             o = np.frombuffer(dec.scratch(mk.MK_SCRATCH_OPROJ, l), dtype=np.float32)
-            o = o.reshape(d.n_kv_heads, B, d.hidden).sum(0)
-            np.testing.assert_allclose(o, tr["attn_proj"][l], atol=2e-3, rtol=1e-2,
+            o = o.reshape(-1, B, d.hidden).sum(0)
+            np.testing.assert_allclose(o, tr["attn_proj"][l], atol=1e-4, rtol=1e-3,
                                        err_msg=f"oproj layer {l}")
             y = np.frombuffer(dec.scratch(mk.MK_SCRATCH_MOE, l), dtype=np.float32)
             y = y.reshape(B, d.top_k, d.hidden).sum(1)
-            np.testing.assert_allclose(y, tr["moe"][l], atol=2e-3, rtol=1e-2,
+            np.testing.assert_allclose(y, tr["moe"][l], atol=1e-4, rtol=1e-3,
                                        err_msg=f"moe layer {l}")
         check_logits(gpu, ref)
         check_routing(pair, tr)
@@ -155,22 +161,35 @@ def test_tiny_trajectory():
 @pytest.mark.parametrize("order", [mk.MK_WAVES_DEFAULT, mk.MK_WAVES_ATTN_FIRST, mk.MK_WAVES_INTERLEAVED])
 @pytest.mark.parametrize("sm_cap", [0, 1, 7])
 def test_tiny_schedules_give_identical_logits(order, sm_cap):
-    """Any wave order and any SM count produce bit-identical output (all sums have a fixed order)."""
+    """Any wave order, SM count and claimer count gives bit-identical output
+    for a fixed split-KV chunk: every sum has a fixed order whatever SM
+    computes it."""
     wl = WORKLOADS["tiny"]
     from persistent_moe_decode_gb300.runner import StepRunner
-    ref_run = StepRunner(wl, device="cuda")
+    ref_run = StepRunner(wl, device="cuda", kv_split_tokens=64)
     ref_run.step()
     torch.cuda.synchronize()
     ref_run.check_status()
     ref = ref_run.logits.clone()
     ref_run.close()
     run = StepRunner(wl, device="cuda", wave_order=order, sm_cap=sm_cap, n_attn_claimers=3,
-                     n_moe_claimers=5)
+                     n_moe_claimers=5, kv_split_tokens=64)
     run.step()
     torch.cuda.synchronize()
     run.check_status()
     assert torch.equal(run.logits, ref)
     run.close()
+
+
+def test_tiny_forced_split_kv_matches_oracle():
+    """64-token splits: the step's 65 keys make two items and a real combine."""
+    pair = Pair(WORKLOADS["tiny"], kv_split_tokens=64)
+    try:
+        gpu, ref, tr = pair.step(trace=True)
+        check_logits(gpu, ref)
+        check_routing(pair, tr)
+    finally:
+        pair.close()
 
 
 def test_mid_trajectory_and_split_kv():
