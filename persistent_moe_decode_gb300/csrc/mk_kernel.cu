@@ -69,8 +69,8 @@ struct __align__(128) Smem {
   uint32_t cstage[kConsumerWarps];          // per consumer warp: stages consumed
   uint32_t cphase[kConsumerWarps];          // per consumer warp: barrier phases passed
   unsigned long long t_ready;               // timeline: when the task's inputs were ready
-  int32_t seen_bar;                         // last counter this block saw reach...
-  uint32_t seen_val;                        // ...this value (waits at or below it are free)
+  int32_t seen_bar[kConsumerWarps];         // per consumer warp: last counter waited on...
+  int32_t seen_tgt[kConsumerWarps];         // ...and the target it reached (lower ones are free)
   unsigned long long t_mark[4];             // timeline: in-task phases (first stage, stages
                                             // done, reduce / merge done, epilogue done)
   volatile int32_t abort_flag;
@@ -565,21 +565,21 @@ struct Cons {
   }
 
   // cross-SM wait (thread 0 spins, the other consumers wait at the barrier).
-  // A counter this block has already seen at or above the target needs no
-  // new wait: the cache is written before a barrier and read after one, so
-  // every warp takes the same branch.
+  // Counters only grow, so a wait on the counter and target this block last
+  // passed (or a lower target) needs no new wait.  Every warp keeps its own
+  // copy of that (counter, target) pair, written only by itself after the
+  // barrier: the copies agree because every warp makes the same sequence of
+  // calls, and no warp can observe another's update half-way.
   __device__ __forceinline__ bool wait_counter(int bar, int target) {
     if (bar < 0) return true;
-    if (bar == S.seen_bar && (uint32_t)target <= S.seen_val) return true;
-    if (tid == 0) {
-      if (!spin_counter(p, bar, (uint32_t)target, t[R_TASK], t[R_OP])) {
-        S.abort_flag = 1;
-      } else {
-        S.seen_bar = bar;
-        S.seen_val = ld_relaxed_u32(p.bars + bar);
-      }
-    }
+    if (bar == S.seen_bar[warp] && target <= S.seen_tgt[warp]) return true;
+    if (tid == 0 && !spin_counter(p, bar, (uint32_t)target, t[R_TASK], t[R_OP])) S.abort_flag = 1;
     const bool ok = csync();
+    if (ok && lane == 0) {
+      S.seen_bar[warp] = bar;
+      S.seen_tgt[warp] = target;
+    }
+    __syncwarp();
     if (tid == 0) S.t_ready = gtime_ns();
     return ok;
   }
@@ -1626,8 +1626,10 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
     }
     mbar_init(&S.cbar, kConsumerWarps);
     for (int w = 0; w < kConsumerWarps; w++) S.cstage[w] = S.cphase[w] = 0;
-    S.seen_bar = -1;
-    S.seen_val = 0;
+    for (int w = 0; w < kConsumerWarps; w++) {
+      S.seen_bar[w] = -1;
+      S.seen_tgt[w] = 0;
+    }
     S.abort_flag = 0;
     mbar_fence_init();
   }
