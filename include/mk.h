@@ -219,6 +219,31 @@ int mk_debug_bump_wait(mk_handle* h, int layer, int delta);
  * the full size. */
 int mk_read_trace(mk_handle* h, void* dst, size_t bytes, size_t* size_out);
 
+/* Words of the fixed device-resident counter block used by
+ * mk_decode_step_static (256 KB per device). */
+#define MK_STATIC_COUNTER_WORDS 65536
+
+/* mk_decode_step with the step's counters, queue claim heads and error words
+ * in a fixed device array of MK_STATIC_COUNTER_WORDS words instead of the
+ * handle's own; the pages describe no such variant (their host loop clears
+ * and reuses one scratch area per engine).  The call allocates nothing: the
+ * schedule for the batch is the one mk_schedule_step built, and the words the
+ * step uses are cleared to zero on `stream` before the launch.  After the
+ * kernel, the error words are copied on `stream` into the handle's own error
+ * block, so mk_step_status reports this step as usual.  Same results as
+ * mk_decode_step for the same scheduled batch.
+ * Errors: MK_ERR_BAD_CONFIG if the handle needs more counter words than the
+ * array holds (32 + (n_layers + 1) * a per-layer block of at most 320 words),
+ * MK_ERR_NOT_SCHEDULED, MK_ERR_BAD_ARG (NULL logits, or the current device is
+ * not the handle's), MK_ERR_CUDA.
+ * One array serves every handle on a device: two calls of this function whose
+ * executions overlap (other streams, other handles, other threads) share the
+ * counters and corrupt each other's step; serialise them.  mk_decode_step
+ * does not touch the array.  The first call on a device looks up the array's
+ * address and sets the kernel's shared-memory limit; make that first call
+ * outside any stream capture. */
+int mk_decode_step_static(mk_handle* h, float* logits, void* stream);
+
 /* Library-owned device bytes (counters, scratch, queues, task lists). */
 size_t mk_device_bytes(const mk_handle* h);
 /* SMs the persistent grid uses. */

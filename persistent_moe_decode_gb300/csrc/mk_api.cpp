@@ -23,6 +23,7 @@
 namespace mk {
 cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream);
 size_t step_smem_bytes();
+int static_counters(int device, uint32_t** out);
 }  // namespace mk
 
 using namespace mk;
@@ -421,6 +422,49 @@ int mk_decode_step(mk_handle* h, float* logits, void* stream) {
     cudaGetLastError();
     return MK_ERR_CUDA;
   }
+  h->last_batch = h->batch;
+  return MK_OK;
+}
+
+int mk_decode_step_static(mk_handle* h, float* logits, void* stream) {
+  if (!h || !logits) return MK_ERR_BAD_ARG;
+  if (h->bar_words > (size_t)MK_STATIC_COUNTER_WORDS) return MK_ERR_BAD_CONFIG;
+  if (!h->scheduled) return MK_ERR_NOT_SCHEDULED;
+  auto it = h->plans.find(h->batch);
+  if (it == h->plans.end()) return MK_ERR_NOT_SCHEDULED;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) {
+    cudaGetLastError();
+    return MK_ERR_BAD_ARG;
+  }
+  uint32_t* ctr = nullptr;
+  int rc = static_counters(dev, &ctr);
+  if (rc) return rc;
+  cudaStream_t sm = (cudaStream_t)stream;
+  if (cudaMemsetAsync(ctr, 0, h->bar_words * 4, sm) != cudaSuccess) return MK_ERR_CUDA;
+  if (h->d_trace && cudaMemsetAsync(h->d_trace, 0xff, h->trace_words * 4, sm) != cudaSuccess)
+    return MK_ERR_CUDA;
+  Params p = h->base;
+  p.err = ctr;
+  p.bars = ctr + kErrWords;
+  p.B = h->batch;
+  p.wide = wide_path(h->batch) ? 1 : 0;
+  p.n_attn_items = h->n_items;
+  p.attn_meta = h->d_meta;
+  p.tokens = h->d_tokens;
+  p.pos = h->d_pos;
+  p.page_tables = h->d_pt;
+  p.rope = h->d_rope;
+  p.attn_items = h->d_items;
+  p.logits = logits;
+  p.tasks = it->second.tasks;
+  p.task_off = it->second.off;
+  if (launch_step(p, h->n_sm, sm) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  if (cudaMemcpyAsync(h->d_bars, ctr, kErrWords * 4, cudaMemcpyDeviceToDevice, sm) != cudaSuccess)
+    return MK_ERR_CUDA;
   h->last_batch = h->batch;
   return MK_OK;
 }

@@ -35,7 +35,8 @@ MK_WAVES_DEFAULT, MK_WAVES_ATTN_FIRST, MK_WAVES_INTERLEAVED = 0, 1, 2
 # every symbol include/mk.h declares
 EXPORTS = ("mk_create", "mk_schedule_step", "mk_decode_step", "mk_step_status", "mk_get_routing",
            "mk_read_scratch", "mk_plan", "mk_debug_bump_wait", "mk_device_bytes", "mk_num_sms",
-           "mk_step_upload_bytes", "mk_destroy", "mk_strerror", "mk_abi_version", "mk_read_trace")
+           "mk_step_upload_bytes", "mk_destroy", "mk_strerror", "mk_abi_version", "mk_read_trace",
+           "mk_decode_step_static")
 
 
 class mk_config(C.Structure):
@@ -86,6 +87,7 @@ def lib():
             L.mk_create.argtypes = [C.POINTER(mk_config), C.POINTER(mk_weights), C.POINTER(vp)]
             L.mk_schedule_step.argtypes = [vp, i32, vp, vp, vp, vp, vp]
             L.mk_decode_step.argtypes = [vp, vp, vp]
+            L.mk_decode_step_static.argtypes = [vp, vp, vp]
             L.mk_step_status.argtypes = [vp, C.POINTER(mk_error)]
             L.mk_get_routing.argtypes = [vp, vp, vp]
             L.mk_read_scratch.argtypes = [vp, i32, i32, vp, C.c_size_t, C.POINTER(C.c_size_t)]
@@ -155,6 +157,11 @@ def mk_decode_step(h, logits_ptr: int, stream=None) -> int:
                   "mk_decode_step")
 
 
+def mk_decode_step_static(h, logits_ptr: int, stream=None) -> int:
+    return _check(lib().mk_decode_step_static(h, C.c_void_p(int(logits_ptr)), _stream_ptr(stream)),
+                  "mk_decode_step_static")
+
+
 def mk_step_status(h):
     e = mk_error()
     rc = lib().mk_step_status(h, C.byref(e))
@@ -190,9 +197,11 @@ def mk_plan(cfg: mk_config, n_sm: int, batch: int):
 
 def mk_read_trace(h) -> np.ndarray:
     size = C.c_size_t(0)
-    _check(lib().mk_read_trace(h, None, 0, C.byref(size)), "mk_read_trace")
+    _check(lib().mk_read_trace(h, None, 0, C.byref(size)), "mk_read_trace",
+           "mk_decode_step_static")
     out = np.empty(size.value // 4, dtype=np.int32)
-    _check(lib().mk_read_trace(h, _ptr(out), size.value, None), "mk_read_trace")
+    _check(lib().mk_read_trace(h, _ptr(out), size.value, None), "mk_read_trace",
+           "mk_decode_step_static")
     return out.reshape(-1, 16)
 
 
@@ -272,6 +281,9 @@ class Decoder:
 
     def decode(self, logits, stream=None):
         return mk_decode_step(self.h, logits.data_ptr(), stream)
+
+    def decode_static(self, logits, stream=None):
+        return mk_decode_step_static(self.h, logits.data_ptr(), stream)
 
     def status(self):
         return mk_step_status(self.h)
