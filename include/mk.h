@@ -183,12 +183,11 @@ int mk_get_routing(mk_handle* h, int32_t* idx, float* w);
 enum mk_scratch {
   MK_SCRATCH_H = 0,       /* fp32 [batch][H]  residual entering the layer         */
   MK_SCRATCH_X = 1,       /* fp32 [batch][H]  normalised layer input              */
-  MK_SCRATCH_Q = 2,       /* fp32 [batch][hq][d]  query after RoPE                */
+  MK_SCRATCH_QKV = 2,     /* fp32 [batch][(hq + 2 hkv) d]  q, k, v before RoPE    */
   MK_SCRATCH_ATTN = 3,    /* fp32 [batch][hq*d]   attention output                */
   MK_SCRATCH_ROUTER = 4,  /* fp32 [batch][E]  router logits                       */
-  MK_SCRATCH_OPROJ = 5,   /* fp32 [parts][batch][H]  O-proj output: 1 part for
-                             batch <= 8, hkv split-K parts (to be summed) above  */
-  MK_SCRATCH_MOE = 6      /* fp32 [batch][top_k][H] weighted expert outputs       */
+  MK_SCRATCH_OPROJ = 5,   /* fp32 [batch][H]  O-proj output                       */
+  MK_SCRATCH_MOE = 6      /* fp32 [batch][H]  weighted sum of the routed experts  */
 };
 int mk_read_scratch(mk_handle* h, int which, int layer, void* dst, size_t bytes,
                     size_t* size_out);
@@ -233,7 +232,7 @@ int mk_read_trace(mk_handle* h, void* dst, size_t bytes, size_t* size_out);
  * block, so mk_step_status reports this step as usual.  Same results as
  * mk_decode_step for the same scheduled batch.
  * Errors: MK_ERR_BAD_CONFIG if the handle needs more counter words than the
- * array holds (32 + (n_layers + 1) * a per-layer block of at most 320 words),
+ * array holds (32 + n_layers * a per-layer block of 32 words),
  * MK_ERR_NOT_SCHEDULED, MK_ERR_BAD_ARG (NULL logits, or the current device is
  * not the handle's), MK_ERR_CUDA.
  * One array serves every handle on a device: two calls of this function whose

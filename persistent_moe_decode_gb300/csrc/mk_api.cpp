@@ -23,6 +23,7 @@
 namespace mk {
 cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream);
 size_t step_smem_bytes();
+int step_kernel_regs();
 int static_counters(int device, uint32_t** out);
 }  // namespace mk
 
@@ -59,6 +60,7 @@ struct mk_handle {
   int32_t* d_pt = nullptr;
   float* d_rope = nullptr;
   int32_t* d_items = nullptr;
+  int32_t* d_smoff = nullptr;
   int32_t* d_meta = nullptr;
   size_t step_bytes_cap = 0;
   Staging stage[2];
@@ -68,6 +70,7 @@ struct mk_handle {
   int batch = 0;
   int n_items = 0;
   int split = 0;
+  std::vector<int32_t> items, smoff, meta;
   int last_batch = 0;
   uint32_t* d_bars = nullptr;   // err words live at the start
   size_t bar_words = 0;
@@ -139,9 +142,10 @@ int ensure_plan(mk_handle* h, int batch, DevPlan** out) {
   return MK_OK;
 }
 
-size_t step_upload_bytes(const mk_config& c, int batch, int n_items) {
+size_t step_upload_bytes(const mk_config& c, int n_sm, int batch, int n_items) {
   return (size_t)batch * 4 * 2 + (size_t)batch * c.max_pages_per_seq * 4 +
-         (size_t)batch * (c.head_dim / 2) * 2 * 4 + (size_t)n_items * 8 * 4 + (size_t)batch * 2 * 4;
+         (size_t)batch * (c.head_dim / 2) * 2 * 4 + (size_t)n_items * 8 * 4 + (size_t)batch * 2 * 4 +
+         (size_t)(n_sm + 1) * 4;
 }
 
 }  // namespace
@@ -216,6 +220,9 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
   int coop = 0;
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device);
   if (!coop || prop.sharedMemPerBlockOptin < step_smem_bytes()) { delete h; return MK_ERR_CUDA; }
+  // the kernel's warpgroups re-split the block's registers; the split adds up
+  // only for the launch allocation it was designed for
+  if (step_kernel_regs() != kLaunchRegs) { delete h; return MK_ERR_CUDA; }
   h->n_sm = prop.multiProcessorCount;
   if (c.sm_cap > 0) h->n_sm = std::min(h->n_sm, c.sm_cap);
 
@@ -227,13 +234,14 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
   p.L = L; p.H = H; p.hq = hq; p.hkv = hkv; p.d = d; p.E = E; p.topk = K; p.I = I;
   p.V = c.vocab; p.P = c.page_size; p.grp = grp; p.qkv_rows = (hq + 2 * hkv) * d;
   p.max_pages = c.max_pages_per_seq; p.num_pages = c.num_kv_pages; p.Bmax = Bm;
+  p.n_sm = h->n_sm;
   p.rms_eps = c.rms_eps;
   p.attn_scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
   p.embed = (const uint16_t*)w->embed;
   p.lm_head = (const uint16_t*)w->lm_head;
   p.final_norm = (const uint16_t*)w->final_norm;
   p.timeout_ns = (unsigned long long)c.timeout_ms * 1000000ull;
-  p.bl = bar_layout(hkv, E, Bm);
+  p.bl = bar_layout(Bm);
   p.bar_per_layer = p.bl.per_layer;
 
 #define TRY(x) do { int _r = (x); if (_r) { mk_destroy(h); return _r; } } while (0)
@@ -247,31 +255,24 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
   TRY(upload_ptrs(h, (const void* const*)w->k_pool, L, (const void* const**)&p.k_pool));
   TRY(upload_ptrs(h, (const void* const*)w->v_pool, L, (const void* const**)&p.v_pool));
 
-  const size_t Ls = (size_t)L, Bs = (size_t)Bm;
-  p.max_up = std::min(E, Bm * K) * (I / kRowsUp);
-  p.max_down = std::min(E, Bm * K) * (H / std::min(kRowsDownN, kRowsDownW));
+  const size_t Ls = (size_t)L, Bs = (size_t)Bm, Ns = (size_t)h->n_sm;
   p.max_attn_items = c.max_attn_items;
-  TRY(dalloc(h, &p.h, (Ls + 1) * Bs * H));
-  TRY(dalloc(h, &p.x, (Ls + 1) * Bs * H));
-  TRY(dalloc(h, &p.q, Ls * Bs * hq * d));
-  TRY(dalloc(h, &p.knew, Ls * Bs * hkv * d));
-  TRY(dalloc(h, &p.vnew, Ls * Bs * hkv * d));
+  TRY(dalloc(h, &p.hloc, Ns * Bs * H));
+  TRY(dalloc(h, &p.xloc, Ns * Bs * H));
+  TRY(dalloc(h, &p.hdbg, (Ls + 1) * Bs * H));
+  TRY(dalloc(h, &p.xdbg, (Ls + 1) * Bs * H));
+  TRY(dalloc(h, &p.qkv, Ls * Bs * p.qkv_rows));
   TRY(dalloc(h, &p.rlog, Ls * Bs * E));
   TRY(dalloc(h, &p.ridx, Ls * Bs * K));
   TRY(dalloc(h, &p.rw, Ls * Bs * K));
-  TRY(dalloc(h, &p.ecnt, Ls * E));
-  TRY(dalloc(h, &p.eoff, Ls * (E + 1)));
-  TRY(dalloc(h, &p.elist, Ls * Bs * K));
-  TRY(dalloc(h, &p.upq, Ls * p.max_up));
-  TRY(dalloc(h, &p.downq, Ls * p.max_down));
-  TRY(dalloc(h, &p.qmeta, Ls * 4));
   TRY(dalloc(h, &p.attn_part, (size_t)c.max_attn_items * hkv * grp * d));
   TRY(dalloc(h, &p.attn_ml, (size_t)c.max_attn_items * hkv * grp * 2));
   TRY(dalloc(h, &p.attn_out, Ls * Bs * hq * d));
-  TRY(dalloc(h, &p.oproj, Ls * hkv * Bs * H));
   TRY(dalloc(h, &p.abuf, Ls * Bs * K * I));
-  TRY(dalloc(h, &p.ybuf, Ls * Bs * K * H));
-  h->bar_words = kErrWords + (size_t)(L + 1) * p.bl.per_layer;
+  TRY(dalloc(h, &p.oproj, Ls * Bs * H));
+  TRY(dalloc(h, &p.moe, Ls * Bs * H));
+  TRY(dalloc(h, &p.delta, Ls * Bs * H));
+  h->bar_words = kErrWords + (size_t)L * p.bl.per_layer;
   TRY(dalloc(h, &h->d_bars, h->bar_words));
   p.err = h->d_bars;
   p.bars = h->d_bars + kErrWords;
@@ -280,6 +281,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
   TRY(dalloc(h, &h->d_pt, Bs * c.max_pages_per_seq));
   TRY(dalloc(h, &h->d_rope, Bs * (d / 2) * 2));
   TRY(dalloc(h, &h->d_items, (size_t)c.max_attn_items * 8));
+  TRY(dalloc(h, &h->d_smoff, Ns + 1));
   TRY(dalloc(h, &h->d_meta, Bs * 2));
   if (c.trace_records > 0) {
     h->trace_words = (size_t)h->n_sm * c.trace_records * kTraceWords;
@@ -288,7 +290,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
     p.trace_cap = c.trace_records;
   }
   if (cudaMemset(h->d_bars, 0, h->bar_words * 4) != cudaSuccess) { mk_destroy(h); return MK_ERR_CUDA; }
-  h->step_bytes_cap = step_upload_bytes(c, Bm, c.max_attn_items);
+  h->step_bytes_cap = step_upload_bytes(c, h->n_sm, Bm, c.max_attn_items);
   for (auto& s : h->stage) {
     if (cudaMallocHost(&s.host, h->step_bytes_cap) != cudaSuccess) { cudaGetLastError(); mk_destroy(h); return MK_ERR_OOM; }
     if (cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming) != cudaSuccess) { mk_destroy(h); return MK_ERR_CUDA; }
@@ -319,21 +321,10 @@ int mk_schedule_step(mk_handle* h, int batch, const int32_t* seq_ids, const int3
     }
     total_keys += seq_lens[b] + 1;
   }
-  // select_schedule: split-KV chunk from the live contexts, about one item
-  // (all KV heads of one key range) per SM
-  int S = c.kv_split_tokens;
-  if (S <= 0) {
-    long long want = (total_keys + h->n_sm - 1) / h->n_sm;
-    want = (want + 63) / 64 * 64;
-    S = (int)std::max<long long>(64, std::min<long long>(want, 1 << 22));
-  }
-  auto count_items = [&](int s) {
-    long long n = 0;
-    for (int b = 0; b < batch; b++) n += (seq_lens[b] + 1 + s - 1) / s;
-    return n;
-  };
-  while (count_items(S) > c.max_attn_items) S *= 2;
-  const int n_items = (int)count_items(S);
+  // select_schedule: the live contexts' pages cut into one run per SM
+  const int S = split_kv(c, h->n_sm, batch, seq_lens, &h->items, &h->smoff, &h->meta);
+  if (S < 0) return MK_ERR_BAD_CONFIG;
+  const int n_items = (int)(h->items.size() / 8);
 
   DevPlan* plan = nullptr;
   int rc = ensure_plan(h, batch, &plan);
@@ -352,6 +343,7 @@ int mk_schedule_step(mk_handle* h, int batch, const int32_t* seq_ids, const int3
   int32_t* s_pt = (int32_t*)cur; cur += (size_t)batch * MP * 4;
   float* s_rope = (float*)cur; cur += (size_t)batch * (d / 2) * 2 * 4;
   int32_t* s_meta = (int32_t*)cur; cur += (size_t)batch * 2 * 4;
+  int32_t* s_smoff = (int32_t*)cur; cur += (size_t)(h->n_sm + 1) * 4;
   int32_t* s_items = (int32_t*)cur;
   memcpy(s_tok, tokens, (size_t)batch * 4);
   memcpy(s_pos, seq_lens, (size_t)batch * 4);
@@ -364,26 +356,16 @@ int mk_schedule_step(mk_handle* h, int batch, const int32_t* seq_ids, const int3
       s_rope[((size_t)b * (d / 2) + i) * 2 + 1] = (float)sin(ang);
     }
   }
-  int k = 0;
-  for (int b = 0; b < batch; b++) {
-    const int keys = seq_lens[b] + 1;
-    const int ns = (keys + S - 1) / S;
-    s_meta[b * 2 + 0] = k;
-    s_meta[b * 2 + 1] = ns;
-    const int base = k;
-    for (int s = 0; s < ns; s++, k++) {
-      int32_t* it = s_items + (size_t)k * 8;
-      it[AI_B] = b; it[AI_S] = s; it[AI_NSPLIT] = ns;
-      it[AI_T0] = s * S; it[AI_T1] = std::min(keys, (s + 1) * S);
-      it[AI_BASE] = base; it[AI_POS] = seq_lens[b]; it[7] = 0;
-    }
-  }
+  memcpy(s_meta, h->meta.data(), (size_t)batch * 2 * 4);
+  memcpy(s_smoff, h->smoff.data(), (size_t)(h->n_sm + 1) * 4);
+  memcpy(s_items, h->items.data(), (size_t)n_items * 8 * 4);
   cudaStream_t sm = (cudaStream_t)stream;
   bool ok = cudaMemcpyAsync(h->d_tokens, s_tok, (size_t)batch * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
             cudaMemcpyAsync(h->d_pos, s_pos, (size_t)batch * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
             cudaMemcpyAsync(h->d_pt, s_pt, (size_t)batch * MP * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
             cudaMemcpyAsync(h->d_rope, s_rope, (size_t)batch * (d / 2) * 2 * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
             cudaMemcpyAsync(h->d_meta, s_meta, (size_t)batch * 2 * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
+            cudaMemcpyAsync(h->d_smoff, s_smoff, (size_t)(h->n_sm + 1) * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
             cudaMemcpyAsync(h->d_items, s_items, (size_t)n_items * 8 * 4, cudaMemcpyHostToDevice, sm) == cudaSuccess &&
             cudaEventRecord(st.done, sm) == cudaSuccess;
   if (!ok) return MK_ERR_CUDA;
@@ -395,6 +377,32 @@ int mk_schedule_step(mk_handle* h, int batch, const int32_t* seq_ids, const int3
   return MK_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// kernel parameters of the scheduled step
+Params step_params(const mk_handle* h, const DevPlan& plan, float* logits) {
+  Params p = h->base;
+  p.B = h->batch;
+  p.n_attn_items = h->n_items;
+  p.attn_meta = h->d_meta;
+  p.attn_sm_off = h->d_smoff;
+  p.tokens = h->d_tokens;
+  p.pos = h->d_pos;
+  p.page_tables = h->d_pt;
+  p.rope = h->d_rope;
+  p.attn_items = h->d_items;
+  p.logits = logits;
+  p.tasks = plan.tasks;
+  p.task_off = plan.off;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
 int mk_decode_step(mk_handle* h, float* logits, void* stream) {
   if (!h || !logits) return MK_ERR_BAD_ARG;
   if (!h->scheduled) return MK_ERR_NOT_SCHEDULED;
@@ -405,19 +413,7 @@ int mk_decode_step(mk_handle* h, float* logits, void* stream) {
   if (cudaMemsetAsync(h->d_bars, 0, h->bar_words * 4, sm) != cudaSuccess) return MK_ERR_CUDA;
   if (h->d_trace && cudaMemsetAsync(h->d_trace, 0xff, h->trace_words * 4, sm) != cudaSuccess)
     return MK_ERR_CUDA;
-  Params p = h->base;
-  p.B = h->batch;
-  p.wide = wide_path(h->batch) ? 1 : 0;
-  p.n_attn_items = h->n_items;
-  p.attn_meta = h->d_meta;
-  p.tokens = h->d_tokens;
-  p.pos = h->d_pos;
-  p.page_tables = h->d_pt;
-  p.rope = h->d_rope;
-  p.attn_items = h->d_items;
-  p.logits = logits;
-  p.tasks = plan->tasks;
-  p.task_off = plan->off;
+  const Params p = step_params(h, *plan, logits);
   if (launch_step(p, h->n_sm, sm) != cudaSuccess) {
     cudaGetLastError();
     return MK_ERR_CUDA;
@@ -444,21 +440,9 @@ int mk_decode_step_static(mk_handle* h, float* logits, void* stream) {
   if (cudaMemsetAsync(ctr, 0, h->bar_words * 4, sm) != cudaSuccess) return MK_ERR_CUDA;
   if (h->d_trace && cudaMemsetAsync(h->d_trace, 0xff, h->trace_words * 4, sm) != cudaSuccess)
     return MK_ERR_CUDA;
-  Params p = h->base;
+  Params p = step_params(h, it->second, logits);
   p.err = ctr;
   p.bars = ctr + kErrWords;
-  p.B = h->batch;
-  p.wide = wide_path(h->batch) ? 1 : 0;
-  p.n_attn_items = h->n_items;
-  p.attn_meta = h->d_meta;
-  p.tokens = h->d_tokens;
-  p.pos = h->d_pos;
-  p.page_tables = h->d_pt;
-  p.rope = h->d_rope;
-  p.attn_items = h->d_items;
-  p.logits = logits;
-  p.tasks = it->second.tasks;
-  p.task_off = it->second.off;
   if (launch_step(p, h->n_sm, sm) != cudaSuccess) {
     cudaGetLastError();
     return MK_ERR_CUDA;
@@ -518,33 +502,22 @@ int mk_read_scratch(mk_handle* h, int which, int layer, void* dst, size_t bytes,
   const mk_config& c = h->cfg;
   const Params& p = h->base;
   const int B = h->last_batch > 0 ? h->last_batch : 1, Bm = c.max_batch, L = c.n_layers;
-  const int H = c.hidden, hq = c.n_q_heads, d = c.head_dim, hkv = c.n_kv_heads;
+  const int H = c.hidden;
   const int maxl = (which == MK_SCRATCH_H || which == MK_SCRATCH_X) ? L : L - 1;
   if (layer < 0 || layer > maxl) return MK_ERR_BAD_ARG;
-  const uint8_t* base = nullptr;
-  size_t row = 0;
+  const float* base = nullptr;
+  size_t row = 0;   // floats per sequence
   switch (which) {
-    case MK_SCRATCH_H: row = (size_t)H * 4; base = (const uint8_t*)(p.h + (size_t)layer * Bm * H); break;
-    case MK_SCRATCH_X: row = (size_t)H * 4; base = (const uint8_t*)(p.x + (size_t)layer * Bm * H); break;
-    case MK_SCRATCH_Q: row = (size_t)hq * d * 4; base = (const uint8_t*)(p.q + (size_t)layer * Bm * hq * d); break;
-    case MK_SCRATCH_ATTN: row = (size_t)hq * d * 4; base = (const uint8_t*)(p.attn_out + (size_t)layer * Bm * hq * d); break;
-    case MK_SCRATCH_ROUTER: row = (size_t)c.n_experts * 4; base = (const uint8_t*)(p.rlog + (size_t)layer * Bm * c.n_experts); break;
-    case MK_SCRATCH_OPROJ: {
-      const int parts = wide_path(B) ? hkv : 1;
-      const size_t full = (size_t)parts * B * H * 4;
-      if (size_out) *size_out = full;
-      std::vector<uint8_t> tmp(full);
-      for (int g = 0; g < parts; g++)
-        if (cudaMemcpy(tmp.data() + (size_t)g * B * H * 4, p.oproj + ((size_t)layer * hkv + g) * Bm * H,
-                       (size_t)B * H * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
-          return MK_ERR_CUDA;
-      if (dst) memcpy(dst, tmp.data(), std::min(bytes, full));
-      return MK_OK;
-    }
-    case MK_SCRATCH_MOE: row = (size_t)c.top_k * H * 4; base = (const uint8_t*)(p.ybuf + (size_t)layer * Bm * c.top_k * H); break;
+    case MK_SCRATCH_H: row = H; base = p.hdbg + (size_t)layer * Bm * H; break;
+    case MK_SCRATCH_X: row = H; base = p.xdbg + (size_t)layer * Bm * H; break;
+    case MK_SCRATCH_QKV: row = p.qkv_rows; base = p.qkv + (size_t)layer * Bm * p.qkv_rows; break;
+    case MK_SCRATCH_ATTN: row = (size_t)p.hq * p.d; base = p.attn_out + (size_t)layer * Bm * row; break;
+    case MK_SCRATCH_ROUTER: row = c.n_experts; base = p.rlog + (size_t)layer * Bm * row; break;
+    case MK_SCRATCH_OPROJ: row = H; base = p.oproj + (size_t)layer * Bm * H; break;
+    case MK_SCRATCH_MOE: row = H; base = p.moe + (size_t)layer * Bm * H; break;
     default: return MK_ERR_BAD_ARG;
   }
-  const size_t full = row * (size_t)B;
+  const size_t full = row * 4 * (size_t)B;
   if (size_out) *size_out = full;
   if (dst && cudaMemcpy(dst, base, std::min(bytes, full), cudaMemcpyDeviceToHost) != cudaSuccess) {
     cudaGetLastError();
@@ -577,7 +550,7 @@ size_t mk_device_bytes(const mk_handle* h) { return h ? h->dev_bytes : 0; }
 int mk_num_sms(const mk_handle* h) { return h ? h->n_sm : 0; }
 size_t mk_step_upload_bytes(const mk_handle* h, int batch) {
   if (!h) return 0;
-  return step_upload_bytes(h->cfg, batch, h->scheduled ? h->n_items : 0);
+  return step_upload_bytes(h->cfg, h->n_sm, batch, h->scheduled ? h->n_items : 0);
 }
 
 }  // extern "C"

@@ -1,12 +1,15 @@
 // Host task scheduler: builds the per-SM task lists of one decode step.
 //
 // "Inside the megakernel serving engine for North Mini Code", §The task
-// scheduler: the host builds named waves for each layer, chooses an order,
-// flattens them into one task list and deals task k to SM k mod nSM
-// (round-robin).  Any order without a circular wait is correct; the default
-// puts the router and route setup ahead of attention.  Attention and expert
-// tiles are not listed one by one: a fixed number of claimer tasks per wave
-// drain shared queues whose length is known only during the step.
+// scheduler: the host builds named waves for each layer, chooses an order and
+// gives each SM its list.  Here every wave is cut into one equal share per SM
+// (rows of a weight matrix, query heads to merge, hidden rows to produce), so
+// an SM's list holds one task per wave and layer; the shares whose size
+// depends on routing (the experts' rows) are fixed as "slice s of n" and
+// resolved on the device once the routing is known.  Any order of the waves
+// in which ROUTE precedes UP and ATTN precedes COMBINE precedes OUT has no
+// circular wait (every wait points at an earlier wave of the same layer, or
+// at the previous layer).
 #include "mk_sched.h"
 
 #include <algorithm>
@@ -14,40 +17,34 @@
 
 namespace mk {
 
-// contraction lengths of the wide (tensor-core) GEMV path
-static bool supported_k(int k) {
-  return k == 128 || k == 256 || k == 512 || k == 768 || k == 1024 || k == 2048;
-}
-
-// contraction lengths of the narrow (CUDA-core, whole-row) GEMV path
-static bool narrow_k(int k) { return k == 128 || (k % 256 == 0 && k <= 4096); }
+// contraction lengths the GEMV supports: whole 256-column segments, or one
+// partial segment of a multiple of 8 columns
+static bool gemv_k(int k) { return (k >= 8 && k < 256 && k % 8 == 0) || (k % 256 == 0 && k <= 8192); }
 
 int validate_config(const mk_config& c) {
-  if (c.n_layers < 1 || c.hidden < 32 || c.n_q_heads < 1 || c.n_kv_heads < 1) return MK_ERR_BAD_CONFIG;
+  if (c.n_layers < 1 || c.hidden < 8 || c.n_q_heads < 1 || c.n_kv_heads < 1) return MK_ERR_BAD_CONFIG;
   if (c.n_q_heads % c.n_kv_heads) return MK_ERR_BAD_CONFIG;
   const int grp = c.n_q_heads / c.n_kv_heads;
   if (grp > 8 || kConsumerWarps % c.n_kv_heads) return MK_ERR_BAD_CONFIG;
   if (c.head_dim != 64 && c.head_dim != 128) return MK_ERR_BAD_CONFIG;
-  // both GEMV paths must be able to run every matrix of the model
-  if (!supported_k(c.hidden) || !supported_k(c.moe_inter) || !supported_k(grp * c.head_dim))
+  if (!gemv_k(c.hidden) || !gemv_k(c.moe_inter) || !gemv_k(c.n_q_heads * c.head_dim))
     return MK_ERR_BAD_CONFIG;
-  if (!narrow_k(c.hidden) || !narrow_k(c.moe_inter) || !narrow_k(c.n_q_heads * c.head_dim))
-    return MK_ERR_BAD_CONFIG;
-  if (c.hidden % kRowsOProj || c.hidden % kRowsDownN || c.hidden % kRowsDownW ||
-      c.moe_inter % kRowsUp)
-    return MK_ERR_BAD_CONFIG;
+  // the attention keeps every query head's BF16 high and low halves in the
+  // 16 KB reduction buffer
+  if (c.n_q_heads * c.head_dim > 4096) return MK_ERR_BAD_CONFIG;
   if (c.n_experts < 1 || c.n_experts > 256 || c.top_k < 1 || c.top_k > 8 || c.top_k > c.n_experts)
     return MK_ERR_BAD_CONFIG;
   if (c.vocab < 1 || c.page_size != 16) return MK_ERR_BAD_CONFIG;
   // one 16-token page of every KV head (K or V) must fit half a stage
-  if (c.n_kv_heads * c.page_size * c.head_dim * 2 > kStageData / 2) return MK_ERR_BAD_CONFIG;
-  if (c.max_batch < 1 || c.max_batch > kMaxBatch) return MK_ERR_BAD_CONFIG;
+  if (c.n_kv_heads * c.page_size * c.head_dim * 2 > kStageBytes / 2) return MK_ERR_BAD_CONFIG;
+  if (c.max_batch < 1 || c.max_batch > kMaxBatch || c.max_batch * c.top_k > kMaxActive)
+    return MK_ERR_BAD_CONFIG;
   if (c.max_pages_per_seq < 1 || c.num_kv_pages < 1) return MK_ERR_BAD_CONFIG;
   if (!(c.rope_theta > 0.0) || !(c.rms_eps >= 0.f)) return MK_ERR_BAD_CONFIG;
   if (c.max_attn_items < 0 || c.n_attn_claimers < 0 || c.n_moe_claimers < 0 || c.sm_cap < 0 ||
       c.timeout_ms < 0 || c.trace_records < 0)
     return MK_ERR_BAD_CONFIG;
-  if (c.kv_split_tokens < 0 || c.kv_split_tokens % 64) return MK_ERR_BAD_CONFIG;
+  if (c.kv_split_tokens < 0 || c.kv_split_tokens % 16) return MK_ERR_BAD_CONFIG;
   if (c.wave_order < MK_WAVES_DEFAULT || c.wave_order > MK_WAVES_INTERLEAVED) return MK_ERR_BAD_CONFIG;
   return MK_OK;
 }
@@ -56,145 +53,137 @@ namespace {
 
 using Desc = std::array<int32_t, kDescWords>;
 
-Desc blank(int op, int layer, int tile) {
+Desc task(int op, int layer, int a0, int a1) {
   Desc d;
   d.fill(0);
   d[F_OP] = op;
   d[F_LAYER] = layer;
-  d[F_TILE] = tile;
-  d[F_W0] = d[F_W1] = d[F_SIG] = d[F_PW] = -1;
-  d[F_T0] = d[F_T1] = d[F_INC] = d[F_PT] = 0;
+  d[F_A0] = a0;
+  d[F_A1] = a1;
   return d;
 }
-
-enum Wave { W_NORM, W_QKV, W_ROUTER, W_ATTN, W_COMBINE, W_UP, W_DOWN, W_OPROJ };
 
 }  // namespace
 
 int build_plan(const mk_config& c, int n_sm, int batch, Plan* out, int bump_layer, int bump) {
   if (validate_config(c) != MK_OK || n_sm < 1 || batch < 1 || batch > c.max_batch)
     return MK_ERR_BAD_CONFIG;
-  const BarLayout bl = bar_layout(c.n_kv_heads, c.n_experts, c.max_batch);
-  const int L = c.n_layers, d = c.head_dim, hkv = c.n_kv_heads;
-  auto bar = [&](int layer, int off) { return layer * bl.per_layer + off; };
-  const int n_attn_c = c.n_attn_claimers > 0 ? c.n_attn_claimers : n_sm;
-  const int n_moe_c = c.n_moe_claimers > 0 ? c.n_moe_claimers : n_sm;
-  const int cpg = combine_split(c, batch);
+  const BarLayout bl = bar_layout(c.max_batch);
+  const int L = c.n_layers;
+  const long long rows1 = c.n_experts + (long long)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  const long long units = (long long)batch * c.n_q_heads;
+  const int nmoe = moe_sms(c, n_sm);
 
-  std::vector<Desc> flat;
-  auto norm_task = [&](int l) {
-    Desc t = blank(OP_NORM, l, 0);
-    if (l > 0) {
-      t[F_W0] = bar(l - 1, bl.o);
-      t[F_T0] = oproj_tiles(c, batch) + (l == bump_layer ? bump : 0);
-      t[F_W1] = bar(l - 1, bl.moe);
-      t[F_T1] = moe_target(c, batch);
-    }
-    t[F_SIG] = bar(l, bl.x);
-    t[F_INC] = 1;
-    flat.push_back(t);
-  };
-  auto wave = [&](Wave w, int l) {
-    switch (w) {
-      case W_NORM:
-        norm_task(l);
-        break;
-      case W_QKV: {
-        const int tph = d / 32, heads = c.n_q_heads + 2 * hkv;
-        for (int i = 0; i < heads * tph; i++) {
-          Desc t = blank(OP_QKV, l, i);
-          t[F_W0] = bar(l, bl.x);
-          t[F_T0] = 1;
-          flat.push_back(t);     // the signalled counter depends on the head: set by the kernel
-        }
-        break;
-      }
-      case W_ROUTER: {
-        const int n = (c.n_experts + kRowsRouter - 1) / kRowsRouter;
-        for (int i = 0; i < n; i++) {
-          Desc t = blank(OP_ROUTER, l, i);
-          t[F_W0] = bar(l, bl.x);
-          t[F_T0] = 1;
-          flat.push_back(t);
-        }
-        break;
-      }
-      case W_ATTN:
-        for (int i = 0; i < n_attn_c; i++) flat.push_back(blank(OP_ATTN, l, i));
-        break;
-      case W_COMBINE:
-        // ATTN_COMBINE tasks per (sequence, KV head); the wait target is the
-        // sequence's split count of the step, read by the kernel
-        for (int b = 0; b < batch; b++)
-          for (int g = 0; g < hkv; g++)
-            for (int cc = 0; cc < cpg; cc++) {
-              Desc t = blank(OP_COMBINE, l, (b * hkv + g) * cpg + cc);
-              t[F_W0] = bar(l, bl.items + b);
-              t[F_T0] = -1;
-              t[F_SIG] = bar(l, bl.attn);
-              t[F_INC] = 1;
-              t[F_ARG] = cpg;
-              flat.push_back(t);
-            }
-        break;
-      case W_UP:
-      case W_DOWN:
-        for (int i = 0; i < n_moe_c; i++) {
-          Desc t = blank(w == W_UP ? OP_MOE_UP : OP_MOE_DOWN, l, i);
-          t[F_PW] = bar(l, bl.route);
-          t[F_PT] = 1;
-          flat.push_back(t);
-        }
-        break;
-      case W_OPROJ: {
-        const int n = oproj_tiles(c, batch);
-        for (int i = 0; i < n; i++) {
-          Desc t = blank(OP_OPROJ, l, i);
-          t[F_W0] = bar(l, bl.attn);
-          t[F_T0] = batch * hkv * cpg;
-          t[F_SIG] = bar(l, bl.o);
-          t[F_INC] = 1;
-          flat.push_back(t);
-        }
-        break;
-      }
-    }
-  };
+  static const int orders[3][6] = {
+      {OP_P1, OP_ROUTE, OP_ATTN, OP_UP, OP_COMBINE, OP_OUT},
+      {OP_P1, OP_ROUTE, OP_ATTN, OP_COMBINE, OP_UP, OP_OUT},
+      {OP_P1, OP_ROUTE, OP_UP, OP_ATTN, OP_COMBINE, OP_OUT}};
 
-  static const Wave orders[3][8] = {
-      {W_NORM, W_QKV, W_ROUTER, W_ATTN, W_COMBINE, W_UP, W_DOWN, W_OPROJ},
-      {W_NORM, W_QKV, W_ROUTER, W_ATTN, W_COMBINE, W_OPROJ, W_UP, W_DOWN},
-      {W_NORM, W_QKV, W_ROUTER, W_UP, W_ATTN, W_DOWN, W_COMBINE, W_OPROJ}};
-  for (int l = 0; l < L; l++)
-    for (Wave w : orders[c.wave_order]) wave(w, l);
-  // final norm and LM head
-  norm_task(L);
-  {
-    const int n = (c.vocab + rows_lm(batch) - 1) / rows_lm(batch);
-    for (int i = 0; i < n; i++) {
-      Desc u = blank(OP_LMHEAD, L, i);
-      u[F_W0] = bar(L, bl.x);
-      u[F_T0] = 1;
-      flat.push_back(u);
-    }
-  }
-
-  // deal round-robin
-  std::vector<std::vector<int>> per_sm(n_sm);
-  for (size_t k = 0; k < flat.size(); k++) {
-    flat[k][F_SEQ] = (int32_t)k;
-    per_sm[k % n_sm].push_back((int)k);
-  }
   out->tasks.clear();
-  out->tasks.reserve(flat.size() * kDescWords);
   out->off.assign(n_sm + 1, 0);
   for (int s = 0; s < n_sm; s++) {
     out->off[s] = (int32_t)(out->tasks.size() / kDescWords);
-    for (int k : per_sm[s]) out->tasks.insert(out->tasks.end(), flat[k].begin(), flat[k].end());
+    std::vector<Desc> list;
+    for (int l = 0; l < L; l++) {
+      for (int op : orders[c.wave_order]) {
+        int lo = 0, hi = 0;
+        switch (op) {
+          case OP_P1: share(rows1, n_sm, s, &lo, &hi); break;
+          case OP_COMBINE: share(units, n_sm, s, &lo, &hi); break;
+          case OP_OUT: share(c.hidden, n_sm, s, &lo, &hi); break;
+          case OP_UP:
+            lo = s < nmoe ? s : -1;
+            hi = nmoe;
+            break;
+          default: break;
+        }
+        Desc t = task(op, l, lo, hi);
+        if (op == OP_P1 && l == bump_layer) t[F_BUMP] = bump;
+        list.push_back(t);
+      }
+    }
+    {
+      int lo, hi;
+      share(c.vocab, n_sm, s, &lo, &hi);
+      Desc t = task(OP_FINAL, L, lo, hi);
+      if (L == bump_layer) t[F_BUMP] = bump;
+      list.push_back(t);
+    }
+    for (size_t k = 0; k < list.size(); k++) {
+      list[k][F_SEQ] = (int32_t)k;
+      out->tasks.insert(out->tasks.end(), list[k].begin(), list[k].end());
+    }
   }
   out->off[n_sm] = (int32_t)(out->tasks.size() / kDescWords);
-  out->n_bars = (L + 1) * bl.per_layer;
+  out->n_bars = L * bl.per_layer;
   return MK_OK;
+}
+
+int split_kv(const mk_config& c, int n_sm, int batch, const int32_t* seq_lens,
+             std::vector<int32_t>* items, std::vector<int32_t>* sm_off, std::vector<int32_t>* meta) {
+  const int P = c.page_size;
+  const int na = attn_sms(c, n_sm);
+  items->clear();
+  sm_off->assign(n_sm + 1, 0);
+  meta->assign((size_t)batch * 2, 0);
+  auto add = [&](int b, int t0, int t1) {
+    const int32_t it[8] = {b, 0, 0, t0, t1, 0, seq_lens[b], 0};
+    items->insert(items->end(), it, it + 8);
+  };
+  int split = c.kv_split_tokens;
+  if (split > 0) {
+    // fixed split size: items in sequence order, dealt out in contiguous runs
+    long long n_items = 0;
+    for (;;) {
+      n_items = 0;
+      for (int b = 0; b < batch; b++) n_items += (seq_lens[b] + 1 + split - 1) / split;
+      if (n_items <= c.max_attn_items || split >= (1 << 24)) break;
+      split *= 2;
+    }
+    if (n_items > c.max_attn_items) return -1;
+    for (int b = 0; b < batch; b++) {
+      const int keys = seq_lens[b] + 1;
+      for (int t0 = 0; t0 < keys; t0 += split) add(b, t0, std::min(keys, t0 + split));
+    }
+    for (int s = 0; s <= n_sm; s++)
+      (*sm_off)[s] = (int32_t)(s >= na ? n_items : n_items * s / na);
+  } else {
+    // balanced: the concatenated pages of all sequences cut into na equal runs
+    std::vector<long long> first(batch + 1, 0);
+    for (int b = 0; b < batch; b++) first[b + 1] = first[b] + (seq_lens[b] + 1 + P - 1) / P;
+    const long long T = first[batch];
+    int b = 0;
+    for (int s = 0; s < n_sm; s++) {
+      (*sm_off)[s] = (int32_t)(items->size() / 8);
+      if (s >= na) continue;
+      const long long g0 = T * s / na, g1 = T * (s + 1) / na;
+      while (b < batch && first[b + 1] <= g0) b++;
+      for (int bb = b; bb < batch && first[bb] < g1; bb++) {
+        const long long p0 = std::max(g0, first[bb]) - first[bb];
+        const long long p1 = std::min(g1, first[bb + 1]) - first[bb];
+        if (p1 <= p0) continue;
+        const int keys = seq_lens[bb] + 1;
+        add(bb, (int)(p0 * P), (int)std::min<long long>(keys, p1 * P));
+      }
+    }
+    (*sm_off)[n_sm] = (int32_t)(items->size() / 8);
+    if ((long long)(items->size() / 8) > c.max_attn_items) return -1;
+    split = 0;
+  }
+  // split index, count and first item of every sequence (items of a sequence are contiguous)
+  const int n = (int)(items->size() / 8);
+  for (int k = 0; k < n; k++) {
+    int32_t* it = items->data() + (size_t)k * 8;
+    const int b = it[AI_B];
+    if ((*meta)[b * 2 + 1] == 0) (*meta)[b * 2 + 0] = k;
+    it[AI_S] = (*meta)[b * 2 + 1]++;
+  }
+  for (int k = 0; k < n; k++) {
+    int32_t* it = items->data() + (size_t)k * 8;
+    it[AI_NSPLIT] = (*meta)[it[AI_B] * 2 + 1];
+    it[AI_BASE] = (*meta)[it[AI_B] * 2 + 0];
+  }
+  return split;
 }
 
 }  // namespace mk

@@ -29,7 +29,7 @@ MK_ERR_BAD_ARG = -8
 MK_ERR_DEVICE = -9
 
 MK_WAVES_DEFAULT, MK_WAVES_ATTN_FIRST, MK_WAVES_INTERLEAVED = 0, 1, 2
-(MK_SCRATCH_H, MK_SCRATCH_X, MK_SCRATCH_Q, MK_SCRATCH_ATTN, MK_SCRATCH_ROUTER,
+(MK_SCRATCH_H, MK_SCRATCH_X, MK_SCRATCH_QKV, MK_SCRATCH_ATTN, MK_SCRATCH_ROUTER,
  MK_SCRATCH_OPROJ, MK_SCRATCH_MOE) = range(7)
 
 # every symbol include/mk.h declares
@@ -197,11 +197,9 @@ def mk_plan(cfg: mk_config, n_sm: int, batch: int):
 
 def mk_read_trace(h) -> np.ndarray:
     size = C.c_size_t(0)
-    _check(lib().mk_read_trace(h, None, 0, C.byref(size)), "mk_read_trace",
-           "mk_decode_step_static")
+    _check(lib().mk_read_trace(h, None, 0, C.byref(size)), "mk_read_trace")
     out = np.empty(size.value // 4, dtype=np.int32)
-    _check(lib().mk_read_trace(h, _ptr(out), size.value, None), "mk_read_trace",
-           "mk_decode_step_static")
+    _check(lib().mk_read_trace(h, _ptr(out), size.value, None), "mk_read_trace")
     return out.reshape(-1, 16)
 
 

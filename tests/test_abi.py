@@ -56,7 +56,8 @@ def test_struct_layout_matches_header(lib):
 def test_create_rejects_bad_configs_before_touching_the_device(lib):
     w = mk.mk_weights()
     for bad in (dict(head_dim=96), dict(n_q_heads=5), dict(max_batch=17), dict(page_size=8),
-                dict(n_experts=300), dict(kv_split_tokens=100), dict(hidden=1536)):
+                dict(n_experts=300), dict(kv_split_tokens=100), dict(hidden=1000),
+                dict(n_q_heads=64, n_kv_heads=8, head_dim=128)):
         cfg = mk.make_config(TINY, 1, 8, 16)
         for k, v in bad.items():
             setattr(cfg, k, v)

@@ -65,7 +65,7 @@ def test_static_counter_step_rejects_handles_beyond_the_array():
     one = dataclasses.replace(TINY, n_layers=1)
     model = make_model(one, 7, torch.device("cuda"))
     kp, vp = make_kv_pools(one, 8, 1.0, 7, torch.device("cuda"))
-    L = 1100   # 32 + 1101 * 64 words > 65536
+    L = 2100   # 32 + 2100 * 32 words > 65536
     cfg = mk.make_config(dataclasses.replace(TINY, n_layers=L), 16, 4, 8)
     keep = []
 
