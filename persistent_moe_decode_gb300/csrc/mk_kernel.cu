@@ -96,10 +96,14 @@ static_assert(sizeof(Smem) <= 232448, "shared memory of one block exceeds the sm
 // resolved task words (written by the producer into the task ring)
 enum : int {
   R_OP = 0, R_LAYER, R_TASK, R_KIND, R_FLAGS, R_ROW0, R_NROWS, R_K, R_NT, R_NBLK, R_A, R_E,
-  R_REL0, R_ITEM, R_B, R_TT0, R_TT1, R_POS, R_NST, R_U0, R_U1, R_BUMP
+  R_REL0, R_ITEM, R_B, R_TT0, R_TT1, R_POS, R_NST, R_U0, R_U1, R_BUMP, R_ROW1, R_NROWS1, R_NGRP
 };
-// GEMV chunk kinds
-enum : int { K_ROUTER = 0, K_QKV = 1, K_UP = 2, K_OPROJ = 3, K_DOWN = 4, K_LM = 5 };
+// GEMV chunk kinds; K_P1 (router rows, then QKV rows) and K_DOWNALL (every
+// routed expert's down rows of one hidden-row range) are the one-token forms
+enum : int { K_ROUTER = 0, K_QKV = 1, K_UP = 2, K_OPROJ = 3, K_DOWN = 4, K_LM = 5, K_P1 = 6,
+             K_DOWNALL = 7 };
+// rows of one single-token GEMV chunk (one result per row in a 2048-float buffer)
+constexpr int kRowChunk = kPartFloats;
 // chunk flags: first chunk of its task (P1 / FINAL run the norm first), last
 // chunk of its task (signals completion), last block of an OUT row chunk
 enum : int { FL_FIRST = 1, FL_LAST = 2, FL_CLAST = 4 };
@@ -109,7 +113,7 @@ __device__ __forceinline__ bool stopped(const Params& p) {
   return *(volatile uint32_t*)&p.err[E_CODE] != 0;
 }
 
-__device__ void report(const Params& p, uint32_t code, int task, int op, int bar, uint32_t val,
+__device__ __noinline__ void report(const Params& p, uint32_t code, int task, int op, int bar, uint32_t val,
                        uint32_t tgt) {
   if (atomicCAS(&p.err[E_CODE], 0u, code) == 0u) {
     p.err[E_SM] = blockIdx.x;
@@ -124,12 +128,13 @@ __device__ void report(const Params& p, uint32_t code, int task, int op, int bar
 
 // Bounded wait on a shared-memory mbarrier phase, called by a whole warp.  All
 // lanes poll; lane 0 alone decides to give up (stop word or time limit) and the
-// decision is broadcast, so the warp leaves together.  false = give up.
-__device__ bool wait_phase(const Params& p, uint64_t* bar, uint32_t parity, int task, int op,
-                           unsigned mult = 1) {
-  bool done = mbar_try_wait(bar, parity);
-  if (__all_sync(0xffffffffu, done)) return true;
+// decision is broadcast, so the warp leaves together.  false = give up.  The
+// polling loop is out of line: the fast path (phase already complete) is the
+// common case, and one shared copy of the loop keeps the kernel's code small.
+__device__ __forceinline__ bool wait_phase_slow(const Params& p, uint64_t* bar, uint32_t parity, int task,
+                                             int op, unsigned mult) {
   const unsigned long long t0 = gtime_ns();
+  bool done = false;
   for (uint32_t it = 1;; ++it) {
     done = done || mbar_try_wait(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
@@ -148,8 +153,14 @@ __device__ bool wait_phase(const Params& p, uint64_t* bar, uint32_t parity, int 
   }
 }
 
+__device__ __forceinline__ bool wait_phase(const Params& p, uint64_t* bar, uint32_t parity, int task,
+                                           int op, unsigned mult = 1) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  return wait_phase_slow(p, bar, parity, task, op, mult);
+}
+
 // bounded spin on a global counter (Listing 2's wait, with a time limit)
-__device__ bool spin_counter(const Params& p, int bar, uint32_t target, int task, int op) {
+__device__ __forceinline__ bool spin_counter(const Params& p, int bar, uint32_t target, int task, int op) {
   const uint32_t* c = p.bars + bar;
   uint32_t v = ld_acquire_u32(c);
   if (v >= target) return true;
@@ -202,7 +213,7 @@ struct Prod {
   __device__ __forceinline__ Prod(const Params& pp, Smem& ss) : p(pp), S(ss), lane(threadIdx.x & 31) {}
 
   // reserve the next task slot, zero it and write the header; nullptr on give-up
-  __device__ __forceinline__ int32_t* begin() {
+  __device__ __noinline__ int32_t* begin() {
     const uint32_t slot = task_seq % kTaskSlots;
     if (!wait_phase(p, &S.tempty[slot], ((task_seq / kTaskSlots) & 1u) ^ 1u, ti, op)) return nullptr;
     int32_t* w = S.task[slot];
@@ -223,14 +234,14 @@ struct Prod {
     task_seq++;
   }
 
-  __device__ __forceinline__ bool acquire_stage(uint32_t& slot) {
+  __device__ __noinline__ bool acquire_stage(uint32_t& slot) {
     slot = stage_seq % kStages;
     return wait_phase(p, &S.empty[slot], ((stage_seq / kStages) & 1u) ^ 1u, ti, op);
   }
 
   // rows [row0, row0 + nrows) of a row-major [*, K] matrix, whole rows, one
   // bulk copy per stage
-  __device__ __forceinline__ bool stream_rows(const uint16_t* w, int row0, int nrows, int K) {
+  __device__ __noinline__ bool stream_rows(const uint16_t* w, int row0, int nrows, int K) {
     const int rps = rows_per_stage(K);
     for (int done = 0; done < nrows; done += rps) {
       const int rows = min(rps, nrows - done);
@@ -248,7 +259,7 @@ struct Prod {
   }
 
   // pages [pg0, pg0 + npages) of sequence b, all KV heads: K pages then V pages
-  __device__ __forceinline__ bool stream_attn(int b, int pg0, int npages) {
+  __device__ __noinline__ bool stream_attn(int b, int pg0, int npages) {
     const int pb = attn_page_bytes(p);
     const int pps = attn_pps(p);
     const uint16_t* kp = p.k_pool[l];
@@ -279,7 +290,7 @@ struct Prod {
   }
 
   // one GEMV chunk of nblk blocks x nrows rows: publish, then stream each block
-  __device__ __forceinline__ bool chunk(int kind, int flags, int row0, int nrows, int nblk, int K, int nt,
+  __device__ __noinline__ bool chunk(int kind, int flags, int row0, int nrows, int nblk, int K, int nt,
                                         int a, int e, int rel0, const uint16_t* w0, const uint16_t* w1) {
     int32_t* w = begin();
     if (!w) return false;
@@ -302,7 +313,7 @@ struct Prod {
   }
 
   // rows [lo, hi) of w in chunks of cr; `first` / `last` mark the task's ends
-  __device__ __forceinline__ bool rows_task(int kind, const uint16_t* w, int lo, int hi, int cr, int K,
+  __device__ __noinline__ bool rows_task(int kind, const uint16_t* w, int lo, int hi, int cr, int K,
                                             int nt, bool first, bool last) {
     for (int c0 = lo; c0 < hi; c0 += cr) {
       const int flags = (first && c0 == lo ? FL_FIRST : 0) | (last && c0 + cr >= hi ? FL_LAST : 0);
@@ -312,15 +323,50 @@ struct Prod {
   }
 
   // the routing of layer l is in shared memory (written by this block's consumers)
-  __device__ __forceinline__ bool wait_route() {
+  __device__ __noinline__ bool wait_route() {
     if ((int)route_seen > l) return true;
     if (!wait_phase(p, &S.route_bar, (uint32_t)l & 1u, ti, op, 2)) return false;
     route_seen = l + 1;
     return true;
   }
 
-  __device__ __forceinline__ bool do_p1_final(int a0, int a1) {
+  // one-token P1 / FINAL: chunks of up to kRowChunk rows; a P1 chunk holds its
+  // router rows and its QKV rows as two groups
+  __device__ __noinline__ bool do_p1_final_1(int a0, int a1) {
+    const int H = p.H;
+    if (a1 <= a0) return chunk(op == OP_P1 ? K_P1 : K_LM, FL_FIRST | FL_LAST, 0, 0, 1, H, 1, 0, 0, 0, nullptr, nullptr);
+    for (int c0 = a0; c0 < a1; c0 += kRowChunk) {
+      const int c1 = min(a1, c0 + kRowChunk);
+      const int flags = (c0 == a0 ? FL_FIRST : 0) | (c1 == a1 ? FL_LAST : 0);
+      if (op == OP_FINAL) {
+        if (!chunk(K_LM, flags, c0, c1 - c0, 1, H, 1, 0, 0, 0, p.lm_head, nullptr)) return false;
+        continue;
+      }
+      const int r0 = min(c0, p.E), r1 = min(c1, p.E);
+      const int q0 = max(c0, p.E) - p.E, q1 = max(c1, p.E) - p.E;
+      int32_t* w = begin();
+      if (!w) return false;
+      if (lane == 0) {
+        w[R_KIND] = K_P1;
+        w[R_FLAGS] = flags;
+        w[R_ROW0] = r0;
+        w[R_NROWS] = r1 - r0;
+        w[R_ROW1] = q0;
+        w[R_NROWS1] = q1 - q0;
+        w[R_NGRP] = 2;
+        w[R_K] = H;
+        w[R_NT] = 1;
+      }
+      commit();
+      if (r1 > r0 && !stream_rows(p.w_router[l], r0, r1 - r0, H)) return false;
+      if (q1 > q0 && !stream_rows(p.w_qkv[l], q0, q1 - q0, H)) return false;
+    }
+    return true;
+  }
+
+  __device__ __noinline__ bool do_p1_final(int a0, int a1) {
     const int H = p.H, B = p.B;
+    if (B == 1) return do_p1_final_1(a0, a1);
     const int cr = gemv_chunk_rows(H, B);
     if (op == OP_FINAL) {
       if (a1 <= a0) return chunk(K_LM, FL_FIRST | FL_LAST, 0, 0, 1, H, B, 0, 0, 0, nullptr, nullptr);
@@ -335,7 +381,7 @@ struct Prod {
     return true;
   }
 
-  __device__ __forceinline__ bool do_attn() {
+  __device__ __noinline__ bool do_attn() {
     const int pps = attn_pps(p);
     const int sm = blockIdx.x;
     const int i0 = p.attn_sm_off[sm], i1 = p.attn_sm_off[sm + 1];
@@ -362,7 +408,7 @@ struct Prod {
     return true;
   }
 
-  __device__ __forceinline__ bool do_up(int a0, int a1) {
+  __device__ __noinline__ bool do_up(int a0, int a1) {
     const int H = p.H;
     if (!wait_route()) return false;
     const int n_act = S.rt.n_act;
@@ -372,7 +418,7 @@ struct Prod {
     int n_chunks = 0;
     for (int a = p0 / p.I; a < n_act && a * p.I < p1; a++) {
       const int i0 = max(p0 - a * p.I, 0), i1 = min(p1 - a * p.I, p.I);
-      const int cp = max(1, gemv_chunk_rows(H, S.rt.off[a + 1] - S.rt.off[a]) / 2);
+      const int cp = p.B == 1 ? kRowChunk / 2 : max(1, gemv_chunk_rows(H, S.rt.off[a + 1] - S.rt.off[a]) / 2);
       n_chunks += (i1 - i0 + cp - 1) / cp;
     }
     if (n_chunks == 0) return chunk(K_UP, FL_LAST, 0, 0, 2, H, 0, 0, 0, 0, nullptr, nullptr);
@@ -380,7 +426,7 @@ struct Prod {
       const int i0 = max(p0 - a * p.I, 0), i1 = min(p1 - a * p.I, p.I);
       const int e = S.rt.act[a];
       const int cnt = S.rt.off[a + 1] - S.rt.off[a];
-      const int cp = max(1, gemv_chunk_rows(H, cnt) / 2);
+      const int cp = p.B == 1 ? kRowChunk / 2 : max(1, gemv_chunk_rows(H, cnt) / 2);
       const size_t eo = (size_t)e * p.I * H;
       for (int c0 = i0; c0 < i1; c0 += cp) {
         n_chunks--;
@@ -392,13 +438,13 @@ struct Prod {
     return true;
   }
 
-  __device__ __forceinline__ bool do_out(int a0, int a1) {
+  __device__ __noinline__ bool do_out(int a0, int a1) {
     const int H = p.H, B = p.B;
     if (!wait_route()) return false;
     const int n_act = S.rt.n_act;
     const int KO = p.hq * p.d;
     if (a1 <= a0) return chunk(K_OPROJ, FL_LAST, 0, 0, 1, KO, B, 0, 0, 0, nullptr, nullptr);
-    const int co = gemv_chunk_rows(KO, B);
+    const int co = B == 1 ? kRowChunk : gemv_chunk_rows(KO, B);
     for (int h0 = a0; h0 < a1; h0 += kOutRows) {
       const int h1 = min(a1, h0 + kOutRows);
       const int fin = FL_CLAST | (h1 == a1 ? FL_LAST : 0);
@@ -407,6 +453,25 @@ struct Prod {
         if (!chunk(K_OPROJ, (n_act == 0 && c0 + co >= h1) ? fin : 0, c0, min(co, h1 - c0), 1, KO, B, 0, 0,
                    c0 - h0, p.w_o[l], nullptr))
           return false;
+      if (B == 1 && n_act > 0) {
+        // one token: every routed expert's down rows of [h0, h1) in one chunk,
+        // one group per expert
+        int32_t* w = begin();
+        if (!w) return false;
+        if (lane == 0) {
+          w[R_KIND] = K_DOWNALL;
+          w[R_FLAGS] = fin;
+          w[R_ROW0] = h0;
+          w[R_NROWS] = h1 - h0;
+          w[R_NGRP] = n_act;
+          w[R_K] = p.I;
+          w[R_NT] = 1;
+        }
+        commit();
+        for (int a = 0; a < n_act; a++)
+          if (!stream_rows(p.w_down[l] + (size_t)S.rt.act[a] * H * p.I, h0, h1 - h0, p.I)) return false;
+        continue;
+      }
       // every routed expert's down rows
       for (int a = 0; a < n_act; a++) {
         const int e = S.rt.act[a];
@@ -771,6 +836,146 @@ struct Cons {
     return true;
   }
 
+  // ------------------------------------------------ one-token GEMV chunk
+  // Row r of the chunk (rows numbered across its groups) belongs to warp
+  // r % 8, which computes the whole row: lane l multiplies the 8-column
+  // chunks l, l + 32, ... (consecutive 16-byte shared-memory reads across the
+  // warp) against x in registers, then one warp reduction gives res[r].  No
+  // cross-warp partial sums.  A down chunk (one group per routed expert)
+  // loads the next expert's activations while it works on the current one.
+  __device__ __forceinline__ int row_groups() const {
+    const int kind = t[R_KIND];
+    return (kind == K_P1 || kind == K_UP) ? 2 : kind == K_DOWNALL ? t[R_NGRP] : 1;
+  }
+  __device__ __forceinline__ int group_rows(int g) const {
+    return (t[R_KIND] == K_P1 && g == 1) ? t[R_NROWS1] : t[R_NROWS];
+  }
+  __device__ __forceinline__ const float* row_x(int g) const {
+    const size_t Bm = (size_t)p.Bmax;
+    switch (t[R_KIND]) {
+      case K_OPROJ: return p.attn_out + (size_t)t[R_LAYER] * Bm * p.hq * p.d;
+      case K_DOWNALL: return p.abuf + ((size_t)t[R_LAYER] * Bm * p.topk + S.rt.off[g]) * p.I;
+      default: return p.xloc + (size_t)blockIdx.x * Bm * p.H;
+    }
+  }
+  template <int NCK>
+  __device__ __forceinline__ void row_load_x(float (&x)[NCK][8], const float* src, int K) const {
+#pragma unroll
+    for (int c = 0; c < NCK; c++) {
+      const int col = (lane + 32 * c) * 8;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+      if (col < K) {
+        a = __ldcg((const float4*)(src + col));
+        b = __ldcg((const float4*)(src + col + 4));
+      }
+      x[c][0] = a.x; x[c][1] = a.y; x[c][2] = a.z; x[c][3] = a.w;
+      x[c][4] = b.x; x[c][5] = b.y; x[c][6] = b.z; x[c][7] = b.w;
+    }
+  }
+  template <int NCK>
+  __device__ __forceinline__ bool gemv_row(float* res) {
+    const int K = t[R_K];
+    const bool per_group_x = t[R_KIND] == K_DOWNALL;
+    const int ngrp = row_groups();
+    const int rps = rows_per_stage(K);
+    constexpr int NXB = NCK <= 4 ? NCK : 1;       // prefetch buffer (short rows only)
+    float xa[NCK][8], xb[NXB][8];
+    row_load_x<NCK>(xa, row_x(0), K);
+    if (NCK <= 4 && per_group_x && ngrp > 1) row_load_x<NXB>(xb, row_x(1), K);
+    int rbase = 0;
+    for (int g = 0; g < ngrp; g++) {
+      const int nr = group_rows(g);
+      for (int done = 0; done < nr; done += rps) {
+        const int rows = min(rps, nr - done);
+        uint32_t slot;
+        if (!stage_full(slot)) return false;
+        if (tid == 0 && rbase + done == 0) S.t_mark[0] = gtime_ns();
+        const uint8_t* base = S.stage[slot];
+        for (int rr = (warp - (rbase + done) % 8 + 8) % 8; rr < rows; rr += 8) {
+          const uint8_t* wrow = base + (size_t)rr * K * 2;
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+          for (int c = 0; c < NCK; c++) {
+            if ((lane + 32 * c) * 8 < K) {
+              const uint4 w = lds128(wrow + (lane + 32 * c) * 16);
+              a0 = fmaf(bf16lo(w.x), xa[c][0], a0);
+              a1 = fmaf(bf16hi(w.x), xa[c][1], a1);
+              a0 = fmaf(bf16lo(w.y), xa[c][2], a0);
+              a1 = fmaf(bf16hi(w.y), xa[c][3], a1);
+              a0 = fmaf(bf16lo(w.z), xa[c][4], a0);
+              a1 = fmaf(bf16hi(w.z), xa[c][5], a1);
+              a0 = fmaf(bf16lo(w.w), xa[c][6], a0);
+              a1 = fmaf(bf16hi(w.w), xa[c][7], a1);
+            }
+          }
+          float v = a0 + a1;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) res[rbase + done + rr] = v;
+        }
+        stage_release(slot);
+      }
+      rbase += nr;
+      if (per_group_x && g + 1 < ngrp) {
+        if (NCK <= 4) {
+#pragma unroll
+          for (int c = 0; c < NXB; c++)
+#pragma unroll
+            for (int j = 0; j < 8; j++) xa[c][j] = xb[c][j];
+          if (g + 2 < ngrp) row_load_x<NXB>(xb, row_x(g + 2), K);
+        } else {
+          row_load_x<NCK>(xa, row_x(g + 1), K);
+        }
+      }
+    }
+    if (tid == 0) S.t_mark[1] = gtime_ns();
+    return true;
+  }
+
+  // epilogue of a one-token chunk (after the barrier); token 0 throughout
+  __device__ __forceinline__ void epilogue_row(const float* res) {
+    const int l = t[R_LAYER], kind = t[R_KIND];
+    const int nr = t[R_NROWS], row0 = t[R_ROW0];
+    const size_t Bm = (size_t)p.Bmax;
+    switch (kind) {
+      case K_P1: {
+        const int nq = t[R_NROWS1], q0 = t[R_ROW1];
+        for (int i = tid; i < nr + nq; i += 256) {
+          if (i < nr) __stcg(p.rlog + (size_t)l * Bm * p.E + row0 + i, res[i]);
+          else __stcg(p.qkv + (size_t)l * Bm * p.qkv_rows + q0 + i - nr, res[i]);
+        }
+        break;
+      }
+      case K_UP: {
+        const int slot = S.rt.off[t[R_A]];
+        for (int i = tid; i < nr; i += 256)
+          __stcg(p.abuf + ((size_t)l * Bm * p.topk + slot) * p.I + row0 + i, silu_mul(res[i], res[nr + i]));
+        break;
+      }
+      case K_OPROJ:
+        for (int i = tid; i < nr; i += 256) {
+          S.acc_o[t[R_REL0] + i][0] = res[i];
+          S.acc_m[t[R_REL0] + i][0] = 0.f;
+        }
+        break;
+      case K_DOWNALL: {
+        const int na = t[R_NGRP];
+        for (int i = tid; i < nr; i += 256) {
+          float m = 0.f;
+          for (int a = 0; a < na; a++) {
+            const int j = S.rt.ent[S.rt.off[a]] % p.topk;
+            m += S.rt.w[0][j] * res[a * nr + i];
+          }
+          S.acc_m[i][0] += m;
+        }
+        break;
+      }
+      default:   // K_LM
+        for (int i = tid; i < nr; i += 256) p.logits[row0 + i] = res[i];
+        break;
+    }
+  }
+
   // fixed-order sum over the contraction segments of element (row, n)
   __device__ __forceinline__ float seg_sum(const float* part, int row, int n, int nseg, int nt) const {
     float s = 0.f;
@@ -850,56 +1055,51 @@ struct Cons {
         v[i] = e < E ? __ldcg(rl + e) : -INFINITY;
       }
       uint32_t taken = 0;
-      float vals[8];
-      int idxs[8];
+#pragma unroll 1
+      for (int j = 0; j < K; j++) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
 #pragma unroll
-      for (int j = 0; j < 8; j++) {
-        vals[j] = 0.f;
-        idxs[j] = 0;
-        if (j < K) {
-          float bv = -INFINITY;
-          int bi = 0x7fffffff;
-#pragma unroll
-          for (int i = 0; i < 8; i++) {
-            const int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-              bv = v[i];
-              bi = e;
-            }
+        for (int i = 0; i < 8; i++) {
+          const int e = lane + 32 * i;
+          if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+            bv = v[i];
+            bi = e;
           }
+        }
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-              bv = ov;
-              bi = oi;
-            }
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (ov > bv || (ov == bv && oi < bi)) {
+            bv = ov;
+            bi = oi;
           }
-          if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-          vals[j] = bv;
-          idxs[j] = bi;
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == 0) {
+          rt.idx[n][j] = bi;
+          rt.w[n][j] = bv;     // the logit; replaced by the weight below
         }
       }
+      __syncwarp();
       if (lane == 0) {
+        const float top = rt.w[n][0];
         float den = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; j++)
-          if (j < K) den += expf(vals[j] - vals[0]);
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-          if (j < K) {
-            const float w = expf(vals[j] - vals[0]) / den;
-            rt.idx[n][j] = idxs[j];
-            rt.w[n][j] = w;
-            if (blockIdx.x == 0) {
-              p.ridx[((size_t)l * Bm + n) * K + j] = idxs[j];
-              p.rw[((size_t)l * Bm + n) * K + j] = w;
-            }
+#pragma unroll 1
+        for (int j = 0; j < K; j++) den += expf(rt.w[n][j] - top);
+#pragma unroll 1
+        for (int j = 0; j < K; j++) {
+          const float w = expf(rt.w[n][j] - top) / den;
+          rt.w[n][j] = w;
+          if (blockIdx.x == 0) {
+            p.ridx[((size_t)l * Bm + n) * K + j] = rt.idx[n][j];
+            p.rw[((size_t)l * Bm + n) * K + j] = w;
           }
         }
       }
     }
+    if (tid == 0) S.t_mark[0] = gtime_ns();
     if (!csync()) return false;
     for (int e = tid; e < E; e += 256) {
       int c = 0;
@@ -908,6 +1108,7 @@ struct Cons {
       rt.ecount[e] = c;
     }
     if (!csync()) return false;
+    if (tid == 0) S.t_mark[1] = gtime_ns();
     if (warp == 0) {
       // warp-wide exclusive scans over E <= 256 experts, 8 per lane
       int cnt[8], act[8], sc = 0, sa = 0;
@@ -945,6 +1146,7 @@ struct Cons {
       }
     }
     if (!csync()) return false;
+    if (tid == 0) S.t_mark[2] = gtime_ns();
     for (int e = tid; e < E; e += 256) {
       const int a = rt.eslot[e];
       if (a < 0) continue;
@@ -1291,6 +1493,50 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
   return ok;
 }
 
+// one-token chunk: one copy of the wrapper (norm, waits, epilogue,
+// completion) around the GEMV shape for the row length
+__device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* t) {
+  Cons c(p, S, t);
+  const int op = t[R_OP], kind = t[R_KIND], flags = t[R_FLAGS], l = t[R_LAYER];
+  bool ok = true;
+  if ((op == OP_P1 || op == OP_FINAL) && (flags & FL_FIRST)) ok = c.norm(l, op == OP_FINAL);
+  int rows = t[R_NROWS];
+  if (kind == K_P1) rows += t[R_NROWS1];
+  const bool run = rows > 0;
+  if (ok && run && kind == K_OPROJ) ok = c.wait_counter(bar_index(p, l, p.bl.comb), p.n_sm);
+  if (ok && run && kind == K_DOWNALL) ok = c.wait_counter(bar_index(p, l, p.bl.up), p.n_sm);
+  float* res = S.red + (S.cchunk[c.warp] & 1u) * kPartFloats;
+  if (ok && run) {
+    const int K = t[R_K];
+    ok = K <= 256 ? c.gemv_row<1>(res) : K <= 768 ? c.gemv_row<3>(res)
+       : K <= 2048 ? c.gemv_row<8>(res) : c.gemv_row<16>(res);
+    ok = ok && c.csync();
+  }
+  if (ok && run) {
+    c.epilogue_row(res);
+    if (c.tid == 0) S.t_mark[2] = gtime_ns();
+    if (c.lane == 0) S.cchunk[c.warp]++;
+  }
+  if (ok && (flags & FL_CLAST)) {
+    ok = c.csync();
+    if (ok) {
+      const int a0 = p.tasks[(size_t)t[R_TASK] * kDescWords + F_A0];
+      const int a1 = p.tasks[(size_t)t[R_TASK] * kDescWords + F_A1];
+      const int h0 = a0 + ((t[R_ROW0] - a0) / kOutRows) * kOutRows;
+      c.out_write(h0, min(kOutRows, a1 - h0));
+    }
+  }
+  if (ok && (flags & FL_LAST)) {
+    int bar = -1;
+    if (op == OP_P1) bar = p.bl.p1;
+    else if (op == OP_UP) bar = p.bl.up;
+    else if (op == OP_OUT) bar = p.bl.out;
+    ok = bar >= 0 ? c.signal(bar_index(p, l, bar), 1) : c.csync();
+  }
+  c.save();
+  return ok;
+}
+
 __device__ __forceinline__ bool op_route(const Params& p, Smem& S, const int32_t* t) {
   Cons c(p, S, t);
   const bool ok = c.route();
@@ -1326,7 +1572,10 @@ __device__ __forceinline__ bool op_combine(const Params& p, Smem& S, const int32
   return ok;
 }
 
-// consumer main loop: take the next resolved task, run it, record its timeline
+// consumer main loop: take the next resolved task, run it, record its timeline.
+// ONE: the batch has one token (one-token GEMV paths only; a separate kernel
+// instance keeps each instance's union of inlined paths within registers).
+template <bool ONE>
 __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
   const int tid = threadIdx.x, lane = tid & 31;
   uint32_t task_seq = 0;
@@ -1351,9 +1600,14 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
       case OP_OUT:
       case OP_FINAL: {
         const int nt = t[R_NT];
-        // one token, or up to eight per pass (two GEMV shapes keep the
-        // inlined union of paths within the register budget)
-        ok = nt <= 1 ? op_chunk<1>(p, S, t) : op_chunk<8>(p, S, t);
+        // one token: whole rows per warp, by the row's length; more tokens:
+        // up to eight per pass
+        if constexpr (ONE) {
+          ok = op_row(p, S, t);
+        } else {
+          ok = op_chunk<8>(p, S, t);
+        }
+        (void)nt;
         break;
       }
       case OP_ROUTE: ok = op_route(p, S, t); break;
@@ -1387,6 +1641,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
   }
 }
 
+template <bool ONE>
 __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_constant__ Params p) {
   static_assert(kThreads == 384 && kLaunchRegs == 168, "register split assumes 384 threads x 168");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1422,18 +1677,20 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs) : "memory");
-    consumer_loop(p, S);
+    consumer_loop<ONE>(p, S);
   }
 }
 
-// registers per thread the kernel was built with (the split above needs kLaunchRegs)
+// registers per thread both kernel instances were built with (the split
+// above needs kLaunchRegs); -1 if they differ or cannot be read
 int step_kernel_regs() {
-  cudaFuncAttributes a;
-  if (cudaFuncGetAttributes(&a, mk_step_kernel) != cudaSuccess) {
+  cudaFuncAttributes a, b;
+  if (cudaFuncGetAttributes(&a, mk_step_kernel<true>) != cudaSuccess ||
+      cudaFuncGetAttributes(&b, mk_step_kernel<false>) != cudaSuccess) {
     cudaGetLastError();
     return -1;
   }
-  return a.numRegs;
+  return a.numRegs == b.numRegs ? a.numRegs : -1;
 }
 
 size_t step_smem_bytes() { return sizeof(Smem); }
@@ -1441,8 +1698,11 @@ size_t step_smem_bytes() { return sizeof(Smem); }
 cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(mk_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(mk_step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)sizeof(Smem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mk_step_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sizeof(Smem));
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -1456,7 +1716,8 @@ cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mk_step_kernel, p);
+  return p.B == 1 ? cudaLaunchKernelEx(&cfg, mk_step_kernel<true>, p)
+                  : cudaLaunchKernelEx(&cfg, mk_step_kernel<false>, p);
 }
 
 }  // namespace mk

@@ -17,9 +17,10 @@
 
 namespace mk {
 
-// contraction lengths the GEMV supports: whole 256-column segments, or one
+// contraction lengths the GEMV supports: whole 256-column segments (at most
+// 16, the one-token path holds a lane's share of a row in registers), or one
 // partial segment of a multiple of 8 columns
-static bool gemv_k(int k) { return (k >= 8 && k < 256 && k % 8 == 0) || (k % 256 == 0 && k <= 8192); }
+static bool gemv_k(int k) { return (k >= 8 && k < 256 && k % 8 == 0) || (k % 256 == 0 && k <= 4096); }
 
 int validate_config(const mk_config& c) {
   if (c.n_layers < 1 || c.hidden < 8 || c.n_q_heads < 1 || c.n_kv_heads < 1) return MK_ERR_BAD_CONFIG;
