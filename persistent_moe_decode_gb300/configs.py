@@ -100,6 +100,14 @@ WORKLOADS = {
                         ragged=(1024, 32768), churn=True, join_context=1024),
     # same model, batch 1 at 256K cached tokens, 32 steps
     "a3b_256k": Workload("a3b_256k", A3B, batch=1, context=262144, steps=32),
+    # small multi-sequence cases for the parity tests: ragged contexts with
+    # churn, one token pass (5 sequences) and two passes (12, 16 sequences)
+    "tiny_b5": Workload("tiny_b5", TINY, batch=5, context=0, steps=6, ragged=(10, 300),
+                        churn=True, join_context=40),
+    "tiny_b12": Workload("tiny_b12", TINY, batch=12, context=0, steps=6, ragged=(1, 200),
+                         churn=True, join_context=17),
+    "mid_b16": Workload("mid_b16", MID, batch=16, context=0, steps=3, ragged=(64, 2048),
+                        churn=True, join_context=100),
 }
 
 

@@ -211,6 +211,38 @@ def test_mid_trajectory_and_split_kv():
         pair.close()
 
 
+@pytest.mark.parametrize("name", ["tiny_b5", "tiny_b12", "mid_b16"])
+def test_multi_sequence_trajectory_with_churn(name):
+    """Several ragged sequences per step (one and two GEMV token passes), one
+    sequence retiring and a new one joining every step."""
+    wl = WORKLOADS[name]
+    pair = Pair(wl)
+    try:
+        run_trajectory(pair, wl.steps)
+    finally:
+        pair.close()
+
+
+def test_tiny_b12_intermediates():
+    pair = Pair(WORKLOADS["tiny_b12"])
+    try:
+        gpu, ref, tr = pair.step(trace=True)
+        d = pair.wl.dims
+        B = pair.wl.batch
+        dec = pair.run.dec
+        for l in range(d.n_layers):
+            x = np.frombuffer(dec.scratch(mk.MK_SCRATCH_X, l), dtype=np.float32).reshape(B, d.hidden)
+            np.testing.assert_allclose(x, tr["x"][l], atol=1e-4, rtol=1e-4, err_msg=f"x layer {l}")
+            a = np.frombuffer(dec.scratch(mk.MK_SCRATCH_ATTN, l), dtype=np.float32).reshape(B, -1)
+            np.testing.assert_allclose(a, tr["attn"][l], atol=1e-4, rtol=1e-3, err_msg=f"attn layer {l}")
+            y = np.frombuffer(dec.scratch(mk.MK_SCRATCH_MOE, l), dtype=np.float32).reshape(B, d.hidden)
+            np.testing.assert_allclose(y, tr["moe"][l], atol=1e-4, rtol=1e-3, err_msg=f"moe layer {l}")
+        check_logits(gpu, ref)
+        check_routing(pair, tr)
+    finally:
+        pair.close()
+
+
 def test_device_timeout_is_reported_and_recoverable():
     """A wait target that nothing can reach runs out (short limit) and reports
     MK_ERR_TIMEOUT; the context stays usable and the next step is correct."""
