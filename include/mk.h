@@ -54,12 +54,15 @@ enum mk_status {
   MK_ERR_DEVICE = -9           /* the kernel reported an inconsistent task/queue  */
 };
 
-/* Wave orders of the host scheduler (§The task scheduler, the static part:
- * named waves per layer, one chosen order, task k dealt to SM k mod nSM). */
+/* Wave orders of the host scheduler when every SM runs every phase (§The
+ * task scheduler, the static part: named waves per layer, one chosen order).
+ * Each SM's list holds, per layer, one share of every wave:
+ *   P1 (norm + router / QKV rows), ROUTE (top-k), ATTN (split-KV items),
+ *   UP (expert gate/up rows), COMBINE (split merges), OUT (O-proj + down rows). */
 enum mk_wave_order {
-  MK_WAVES_DEFAULT = 0,    /* qkv, router(+top-k, route setup), attention, MoE up, MoE down, O-proj, norm */
-  MK_WAVES_ATTN_FIRST = 1, /* qkv, router, attention, O-proj, MoE up, MoE down, norm */
-  MK_WAVES_INTERLEAVED = 2 /* qkv, router, MoE up, attention, MoE down, O-proj, norm */
+  MK_WAVES_DEFAULT = 0,    /* P1, ROUTE, ATTN, UP, COMBINE, OUT  */
+  MK_WAVES_ATTN_FIRST = 1, /* P1, ROUTE, ATTN, COMBINE, UP, OUT  */
+  MK_WAVES_INTERLEAVED = 2 /* P1, ROUTE, UP, ATTN, COMBINE, OUT  */
 };
 
 typedef struct {
@@ -83,8 +86,13 @@ typedef struct {
   int max_attn_items;     /* split-KV items per layer; 0 = 8192                  */
   /* schedule */
   int wave_order;         /* enum mk_wave_order                                  */
-  int n_attn_claimers;    /* ATTN claimer tasks per layer; 0 = one per SM        */
-  int n_moe_claimers;     /* claimers per MoE drain wave; 0 = one per SM         */
+  int n_attn_claimers;    /* SMs that run the attention branch (split-KV items,
+                             combines); the others run the routed experts.
+                             0 = chosen per step from the KV bytes against the
+                             experts' bytes; >= the SM count = every SM runs
+                             every phase in wave_order                         */
+  int n_moe_claimers;     /* with every SM running every phase: SMs that take
+                             expert slices; 0 = all                             */
   int kv_split_tokens;    /* split-KV chunk (multiple of 64); 0 = per step       */
   int sm_cap;             /* use at most this many SMs; 0 = all                  */
   int timeout_ms;         /* device spin limit per wait; 0 = 2000                */

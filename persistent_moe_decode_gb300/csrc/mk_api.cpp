@@ -35,7 +35,11 @@ struct DevPlan {
   int32_t* tasks = nullptr;
   int32_t* off = nullptr;
   size_t n_tasks = 0;
+  int n_comb_sms = 0, n_up_sms = 0;
 };
+
+// plans are cached per (batch, attention SMs)
+inline int plan_key(int batch, int n_attn) { return batch * 4096 + n_attn; }
 
 struct Staging {
   uint8_t* host = nullptr;   // pinned
@@ -70,6 +74,7 @@ struct mk_handle {
   int batch = 0;
   int n_items = 0;
   int split = 0;
+  int n_attn = 0;
   std::vector<int32_t> items, smoff, meta;
   int last_batch = 0;
   uint32_t* d_bars = nullptr;   // err words live at the start
@@ -118,14 +123,16 @@ void free_plans(mk_handle* h) {
   h->plans.clear();
 }
 
-int ensure_plan(mk_handle* h, int batch, DevPlan** out) {
-  auto it = h->plans.find(batch);
+int ensure_plan(mk_handle* h, int batch, int n_attn, DevPlan** out) {
+  auto it = h->plans.find(plan_key(batch, n_attn));
   if (it == h->plans.end()) {
     Plan plan;
-    int rc = build_plan(h->cfg, h->n_sm, batch, &plan, h->bump_layer, h->bump);
+    int rc = build_plan(h->cfg, h->n_sm, batch, n_attn, &plan, h->bump_layer, h->bump);
     if (rc) return rc;
     DevPlan dp;
     dp.n_tasks = plan.tasks.size() / kDescWords;
+    dp.n_comb_sms = plan.n_comb_sms;
+    dp.n_up_sms = plan.n_up_sms;
     if (cudaMalloc(&dp.tasks, std::max<size_t>(plan.tasks.size() * 4, 16)) != cudaSuccess ||
         cudaMalloc(&dp.off, plan.off.size() * 4) != cudaSuccess) {
       cudaGetLastError();
@@ -136,7 +143,7 @@ int ensure_plan(mk_handle* h, int batch, DevPlan** out) {
             cudaSuccess ||
         cudaMemcpy(dp.off, plan.off.data(), plan.off.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
       return MK_ERR_CUDA;
-    it = h->plans.emplace(batch, dp).first;
+    it = h->plans.emplace(plan_key(batch, n_attn), dp).first;
   }
   *out = &it->second;
   return MK_OK;
@@ -174,7 +181,8 @@ int mk_plan(const mk_config* cfg, int n_sm, int batch, int32_t* tasks, int32_t* 
             int* n_tasks_out, int* n_barriers_out) {
   if (!cfg) return MK_ERR_BAD_ARG;
   Plan plan;
-  int rc = build_plan(*cfg, n_sm, batch, &plan);
+  const int n_attn = cfg->n_attn_claimers > 0 && cfg->n_attn_claimers < n_sm ? cfg->n_attn_claimers : n_sm;
+  int rc = build_plan(*cfg, n_sm, batch, n_attn, &plan);
   if (rc) return rc;
   if (n_tasks_out) *n_tasks_out = (int)(plan.tasks.size() / kDescWords);
   if (n_barriers_out) *n_barriers_out = plan.n_bars;
@@ -322,12 +330,13 @@ int mk_schedule_step(mk_handle* h, int batch, const int32_t* seq_ids, const int3
     total_keys += seq_lens[b] + 1;
   }
   // select_schedule: the live contexts' pages cut into one run per SM
-  const int S = split_kv(c, h->n_sm, batch, seq_lens, &h->items, &h->smoff, &h->meta);
+  const int na = attention_sms(c, h->n_sm, batch, seq_lens);
+  const int S = split_kv(c, h->n_sm, na, batch, seq_lens, &h->items, &h->smoff, &h->meta);
   if (S < 0) return MK_ERR_BAD_CONFIG;
   const int n_items = (int)(h->items.size() / 8);
 
   DevPlan* plan = nullptr;
-  int rc = ensure_plan(h, batch, &plan);
+  int rc = ensure_plan(h, batch, na, &plan);
   if (rc) return rc;
 
   // stage the step state in pinned memory, then one upload per array
@@ -374,6 +383,7 @@ int mk_schedule_step(mk_handle* h, int batch, const int32_t* seq_ids, const int3
   h->batch = batch;
   h->n_items = n_items;
   h->split = S;
+  h->n_attn = na;
   return MK_OK;
 }
 
@@ -396,6 +406,8 @@ Params step_params(const mk_handle* h, const DevPlan& plan, float* logits) {
   p.logits = logits;
   p.tasks = plan.tasks;
   p.task_off = plan.off;
+  p.n_comb_sms = plan.n_comb_sms;
+  p.n_up_sms = plan.n_up_sms;
   return p;
 }
 
@@ -407,7 +419,7 @@ int mk_decode_step(mk_handle* h, float* logits, void* stream) {
   if (!h || !logits) return MK_ERR_BAD_ARG;
   if (!h->scheduled) return MK_ERR_NOT_SCHEDULED;
   DevPlan* plan = nullptr;
-  int rc = ensure_plan(h, h->batch, &plan);
+  int rc = ensure_plan(h, h->batch, h->n_attn, &plan);
   if (rc) return rc;
   cudaStream_t sm = (cudaStream_t)stream;
   if (cudaMemsetAsync(h->d_bars, 0, h->bar_words * 4, sm) != cudaSuccess) return MK_ERR_CUDA;
@@ -426,7 +438,7 @@ int mk_decode_step_static(mk_handle* h, float* logits, void* stream) {
   if (!h || !logits) return MK_ERR_BAD_ARG;
   if (h->bar_words > (size_t)MK_STATIC_COUNTER_WORDS) return MK_ERR_BAD_CONFIG;
   if (!h->scheduled) return MK_ERR_NOT_SCHEDULED;
-  auto it = h->plans.find(h->batch);
+  auto it = h->plans.find(plan_key(h->batch, h->n_attn));
   if (it == h->plans.end()) return MK_ERR_NOT_SCHEDULED;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) {

@@ -64,6 +64,8 @@ struct RouteTab {
 
 struct __align__(128) Smem {
   uint8_t stage[kStages][kStageBytes];
+  float xs[kXsFloats];                      // one token: the GEMV's activations (x of the
+                                            // layer, the attention output, the experts' hidden)
   float red[2 * kPartFloats];               // GEMV partial sums (two buffers) / attention
                                             // query fragments and merge / combine sums
   float acc_o[kOutRows][kMaxBatch];         // OUT chunk: O-proj rows
@@ -658,25 +660,48 @@ struct Cons {
     float* hl = p.hloc + (size_t)blockIdx.x * Bm * H;
     float* xl = p.xloc + (size_t)blockIdx.x * Bm * H;
     const bool keep = blockIdx.x == 0;
+    const uint16_t* gain = final_norm ? p.final_norm : p.attn_norm[l];
+    constexpr int NI = 4;                       // H <= 4096: at most 4 float4 per thread
     for (int n = 0; n < B; n++) {
-      float ssl = 0.f;
-      for (int i4 = tid; i4 < H4; i4 += 256) {
-        float4 h;
-        if (l == 0) {
-          const uint2 e = *(const uint2*)(p.embed + (size_t)p.tokens[n] * H + i4 * 4);
-          h = make_float4(bf16lo(e.x), bf16hi(e.x), bf16lo(e.y), bf16hi(e.y));
-        } else {
-          const float4 a = __ldcg((const float4*)(hl + n * H) + i4);
-          const float4 d = __ldcg((const float4*)(p.delta + ((size_t)(l - 1) * Bm + n) * H) + i4);
-          h = make_float4(a.x + d.x, a.y + d.y, a.z + d.z, a.w + d.w);
+      // every load of this token first, then the arithmetic and the stores
+      float4 h[NI];
+#pragma unroll
+      for (int k = 0; k < NI; k++) {
+        const int i4 = tid + 256 * k;
+        h[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i4 < H4) {
+          if (l == 0) {
+            const uint2 e = *(const uint2*)(p.embed + (size_t)p.tokens[n] * H + i4 * 4);
+            h[k] = make_float4(bf16lo(e.x), bf16hi(e.x), bf16lo(e.y), bf16hi(e.y));
+          } else {
+            const float4 a = __ldcg((const float4*)(hl + n * H) + i4);
+            const float4 d = __ldcg((const float4*)(p.delta + ((size_t)(l - 1) * Bm + n) * H) + i4);
+            h[k] = make_float4(a.x + d.x, a.y + d.y, a.z + d.z, a.w + d.w);
+          }
         }
-        if (!final_norm) __stcg((float4*)(hl + n * H) + i4, h);
-        if (keep) __stcg((float4*)(p.hdbg + ((size_t)l * Bm + n) * H) + i4, h);
-        ssl += h.x * h.x + h.y * h.y + h.z * h.z + h.w * h.w;
+      }
+      float ssl = 0.f;
+#pragma unroll
+      for (int k = 0; k < NI; k++) {
+        const int i4 = tid + 256 * k;
+        if (i4 < H4) {
+          if (!final_norm) __stcg((float4*)(hl + n * H) + i4, h[k]);
+          if (keep) __stcg((float4*)(p.hdbg + ((size_t)l * Bm + n) * H) + i4, h[k]);
+          ssl += h[k].x * h[k].x + h[k].y * h[k].y + h[k].z * h[k].z + h[k].w * h[k].w;
+        }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ssl += __shfl_xor_sync(0xffffffffu, ssl, o);
       if (lane == 0) S.nred[warp][n] = ssl;
+      if (B == 1) {
+        // one token: keep h for the second pass in shared memory (the staging
+        // buffer is free at the start of a layer)
+#pragma unroll
+        for (int k = 0; k < NI; k++) {
+          const int i4 = tid + 256 * k;
+          if (i4 < H4) *(float4*)&S.xs[i4 * 4] = h[k];
+        }
+      }
     }
     if (!csync()) return false;
     if (tid < B) {
@@ -685,13 +710,14 @@ struct Cons {
       S.rinv[tid] = 1.0f / sqrtf(sum / (float)H + p.rms_eps);
     }
     if (!csync()) return false;
-    const uint16_t* gain = final_norm ? p.final_norm : p.attn_norm[l];
     for (int i4 = tid; i4 < H4; i4 += 256) {
       const uint2 gv = *(const uint2*)(gain + i4 * 4);
       const float g0 = bf16lo(gv.x), g1 = bf16hi(gv.x), g2 = bf16lo(gv.y), g3 = bf16hi(gv.y);
       for (int n = 0; n < B; n++) {
         float4 h;
-        if (final_norm) {
+        if (B == 1) {
+          h = *(const float4*)&S.xs[i4 * 4];
+        } else if (final_norm) {
           const float4 a = __ldcg((const float4*)(hl + n * H) + i4);
           const float4 d = __ldcg((const float4*)(p.delta + ((size_t)(l - 1) * Bm + n) * H) + i4);
           h = make_float4(a.x + d.x, a.y + d.y, a.z + d.z, a.w + d.w);
@@ -700,8 +726,40 @@ struct Cons {
         }
         const float r = S.rinv[n];
         const float4 x = make_float4(h.x * r * g0, h.y * r * g1, h.z * r * g2, h.w * r * g3);
+        if (B == 1) *(float4*)&S.xs[i4 * 4] = x;
         __stcg((float4*)(xl + n * H) + i4, x);
         if (keep) __stcg((float4*)(p.xdbg + ((size_t)l * Bm + n) * H) + i4, x);
+      }
+    }
+    return csync();
+  }
+
+  // one token: stage this chunk's activations in shared memory (the O-proj's
+  // attention output, or the hidden vector of every routed expert), one
+  // coalesced global read per block instead of one per warp
+  __device__ __forceinline__ bool stage_x() {
+    const int l = t[R_LAYER], kind = t[R_KIND];
+    const size_t Bm = (size_t)p.Bmax;
+    if (kind == K_OPROJ) {
+      const int n4 = p.hq * p.d / 4;
+      const float4* src = (const float4*)(p.attn_out + (size_t)l * Bm * p.hq * p.d);
+      float4 v[4];
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const int i = tid + 256 * k;
+        v[k] = i < n4 ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const int i = tid + 256 * k;
+        if (i < n4) *(float4*)&S.xs[i * 4] = v[k];
+      }
+    } else {   // K_DOWNALL: expert a's hidden at xs[a * I]
+      const int na = t[R_NGRP], I4 = p.I / 4;
+      const float* base = p.abuf + (size_t)l * Bm * p.topk * p.I;
+      for (int i = tid; i < na * I4; i += 256) {
+        const int a = i / I4, k = i % I4;
+        *(float4*)&S.xs[a * p.I + k * 4] = __ldcg((const float4*)(base + (size_t)S.rt.off[a] * p.I) + k);
       }
     }
     return csync();
@@ -850,13 +908,9 @@ struct Cons {
   __device__ __forceinline__ int group_rows(int g) const {
     return (t[R_KIND] == K_P1 && g == 1) ? t[R_NROWS1] : t[R_NROWS];
   }
+  // the chunk's activations of group g, in shared memory
   __device__ __forceinline__ const float* row_x(int g) const {
-    const size_t Bm = (size_t)p.Bmax;
-    switch (t[R_KIND]) {
-      case K_OPROJ: return p.attn_out + (size_t)t[R_LAYER] * Bm * p.hq * p.d;
-      case K_DOWNALL: return p.abuf + ((size_t)t[R_LAYER] * Bm * p.topk + S.rt.off[g]) * p.I;
-      default: return p.xloc + (size_t)blockIdx.x * Bm * p.H;
-    }
+    return t[R_KIND] == K_DOWNALL ? S.xs + g * p.I : S.xs;
   }
   template <int NCK>
   __device__ __forceinline__ void row_load_x(float (&x)[NCK][8], const float* src, int K) const {
@@ -865,8 +919,8 @@ struct Cons {
       const int col = (lane + 32 * c) * 8;
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
       if (col < K) {
-        a = __ldcg((const float4*)(src + col));
-        b = __ldcg((const float4*)(src + col + 4));
+        a = *(const float4*)(src + col);
+        b = *(const float4*)(src + col + 4);
       }
       x[c][0] = a.x; x[c][1] = a.y; x[c][2] = a.z; x[c][3] = a.w;
       x[c][4] = b.x; x[c][5] = b.y; x[c][6] = b.z; x[c][7] = b.w;
@@ -1187,20 +1241,39 @@ struct Cons {
     uint8_t* qlo = qhi + hq * D * 2;
     const float* qraw = p.qkv + ((size_t)l * Bm + b) * p.qkv_rows;
     const float* rope = p.rope + (size_t)b * (D / 2) * 2;
-    for (int i = tid; i < hq * (D / 2); i += 256) {
-      const int h = i / (D / 2), k = i % (D / 2);
-      const float x1 = __ldcg(qraw + h * D + k), x2 = __ldcg(qraw + h * D + k + D / 2);
-      const float c = rope[k * 2], s = rope[k * 2 + 1];
-      const float y1 = x1 * c - x2 * s, y2 = x2 * c + x1 * s;
-      const uint16_t h1 = f2bf(y1), h2 = f2bf(y2);
-      const uint16_t l1 = f2bf(y1 - bf16f(h1)), l2 = f2bf(y2 - bf16f(h2));
-      const int k2 = k + D / 2;
-      const int o1 = h * D * 2 + (((k >> 3) ^ (h & 7)) << 4) + (k & 7) * 2;
-      const int o2 = h * D * 2 + (((k2 >> 3) ^ (h & 7)) << 4) + (k2 & 7) * 2;
-      *(uint16_t*)(qhi + o1) = h1;
-      *(uint16_t*)(qhi + o2) = h2;
-      *(uint16_t*)(qlo + o1) = l1;
-      *(uint16_t*)(qlo + o2) = l2;
+    {
+      // hq * D / 2 <= 2048 rotation pairs: at most 8 per thread, all loads first
+      constexpr int NQ = 8;
+      float x1[NQ], x2[NQ], cs[NQ], sn[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; q++) {
+        const int i = tid + 256 * q;
+        x1[q] = x2[q] = cs[q] = sn[q] = 0.f;
+        if (i < hq * (D / 2)) {
+          const int h = i / (D / 2), k = i % (D / 2);
+          x1[q] = __ldcg(qraw + h * D + k);
+          x2[q] = __ldcg(qraw + h * D + k + D / 2);
+          cs[q] = rope[k * 2];
+          sn[q] = rope[k * 2 + 1];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < NQ; q++) {
+        const int i = tid + 256 * q;
+        if (i < hq * (D / 2)) {
+          const int h = i / (D / 2), k = i % (D / 2);
+          const float y1 = x1[q] * cs[q] - x2[q] * sn[q], y2 = x2[q] * cs[q] + x1[q] * sn[q];
+          const uint16_t h1 = f2bf(y1), h2 = f2bf(y2);
+          const uint16_t l1 = f2bf(y1 - bf16f(h1)), l2 = f2bf(y2 - bf16f(h2));
+          const int k2 = k + D / 2;
+          const int o1 = h * D * 2 + (((k >> 3) ^ (h & 7)) << 4) + (k & 7) * 2;
+          const int o2 = h * D * 2 + (((k2 >> 3) ^ (h & 7)) << 4) + (k2 & 7) * 2;
+          *(uint16_t*)(qhi + o1) = h1;
+          *(uint16_t*)(qhi + o2) = h2;
+          *(uint16_t*)(qlo + o1) = l1;
+          *(uint16_t*)(qlo + o2) = l2;
+        }
+      }
     }
     if (!csync()) return false;
 
@@ -1260,24 +1333,30 @@ struct Cons {
           }
           __syncwarp();
         }
-        // scores: 16 tokens x 8 heads, q = high + low halves
+        // scores: 16 tokens x 8 heads, q = high + low halves; four independent
+        // accumulators keep the tensor-core chain short
         float s[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ch++) {
-          const uint8_t* a = kp + gl * D * 2 + ch * 64 + cq * 16;
-          const uint4 lo = lds128(a);
-          const uint4 hi = lds128(a + 8 * D * 2);
-          uint4 qh = make_uint4(0, 0, 0, 0), ql = qh;
-          if (qon) {
-            const int c = ch * 4 + cq;
-            const int off = qh_row * D * 2 + ((c ^ (qh_row & 7)) << 4);
-            qh = lds128(qhi + off);
-            ql = lds128(qlo + off);
+          for (int ch = 0; ch < D / 32; ch++) {
+            const uint8_t* a = kp + gl * D * 2 + ch * 64 + cq * 16;
+            const uint4 lo = lds128(a);
+            const uint4 hi = lds128(a + 8 * D * 2);
+            uint4 qh = make_uint4(0, 0, 0, 0), ql = qh;
+            if (qon) {
+              const int c = ch * 4 + cq;
+              const int off = qh_row * D * 2 + ((c ^ (qh_row & 7)) << 4);
+              qh = lds128(qhi + off);
+              ql = lds128(qlo + off);
+            }
+            mma_bf16(s, lo.x, hi.x, lo.y, hi.y, qh.x, qh.y);
+            mma_bf16(s1, lo.z, hi.z, lo.w, hi.w, qh.z, qh.w);
+            mma_bf16(s2, lo.x, hi.x, lo.y, hi.y, ql.x, ql.y);
+            mma_bf16(s3, lo.z, hi.z, lo.w, hi.w, ql.z, ql.w);
           }
-          mma_bf16(s, lo.x, hi.x, lo.y, hi.y, qh.x, qh.y);
-          mma_bf16(s, lo.z, hi.z, lo.w, hi.w, qh.z, qh.w);
-          mma_bf16(s, lo.x, hi.x, lo.y, hi.y, ql.x, ql.y);
-          mma_bf16(s, lo.z, hi.z, lo.w, hi.w, ql.z, ql.w);
+#pragma unroll
+          for (int j = 0; j < 4; j++) s[j] = (s[j] + s1[j]) + (s2[j] + s3[j]);
         }
         const int lo_t = max(tt0 - tk0, 0), hi_t = min(tt1 - tk0, P);   // valid rows [lo_t, hi_t)
         const bool v0 = gl >= lo_t && gl < hi_t, v1 = gl + 8 >= lo_t && gl + 8 < hi_t;
@@ -1463,8 +1542,8 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
   bool ok = true;
   if ((op == OP_P1 || op == OP_FINAL) && (flags & FL_FIRST)) ok = c.norm(l, op == OP_FINAL);
   const bool run = t[R_NROWS] > 0 && t[R_NT] > 0;
-  if (ok && run && kind == K_OPROJ) ok = c.wait_counter(bar_index(p, l, p.bl.comb), p.n_sm);
-  if (ok && run && kind == K_DOWN) ok = c.wait_counter(bar_index(p, l, p.bl.up), p.n_sm);
+  if (ok && run && kind == K_OPROJ) ok = c.wait_counter(bar_index(p, l, p.bl.comb), p.n_comb_sms);
+  if (ok && run && kind == K_DOWN) ok = c.wait_counter(bar_index(p, l, p.bl.up), p.n_up_sms);
   float* part = S.red + (S.cchunk[c.warp] & 1u) * kPartFloats;
   if (ok && run) ok = c.gemv<NB>(part) && c.csync();
   if (ok && run) {
@@ -1503,8 +1582,8 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
   int rows = t[R_NROWS];
   if (kind == K_P1) rows += t[R_NROWS1];
   const bool run = rows > 0;
-  if (ok && run && kind == K_OPROJ) ok = c.wait_counter(bar_index(p, l, p.bl.comb), p.n_sm);
-  if (ok && run && kind == K_DOWNALL) ok = c.wait_counter(bar_index(p, l, p.bl.up), p.n_sm);
+  if (ok && run && kind == K_OPROJ) ok = c.wait_counter(bar_index(p, l, p.bl.comb), p.n_comb_sms) && c.stage_x();
+  if (ok && run && kind == K_DOWNALL) ok = c.wait_counter(bar_index(p, l, p.bl.up), p.n_up_sms) && c.stage_x();
   float* res = S.red + (S.cchunk[c.warp] & 1u) * kPartFloats;
   if (ok && run) {
     const int K = t[R_K];

@@ -64,7 +64,8 @@ constexpr int kProducerRegs = 72;
 constexpr int kConsumerRegs = 216;
 static_assert(128 * kProducerRegs + 256 * kConsumerRegs == kThreads * kLaunchRegs,
               "register split must add up to the launch allocation");
-constexpr int kStages = 6;              // weight / KV stage ring depth
+constexpr int kStages = 5;              // weight / KV stage ring depth
+constexpr int kXsFloats = 8192;         // one-token activations staged in shared memory
 constexpr int kStageBytes = 32768;      // one stage: whole weight rows or one KV page group
 constexpr int kTaskSlots = 8;           // resolved-task ring depth
 constexpr int kMaxBatch = 16;
@@ -123,6 +124,7 @@ struct Params {
   // model
   int L, H, hq, hkv, d, E, topk, I, V, P, grp, qkv_rows;
   int max_pages, num_pages, Bmax, n_sm;
+  int n_comb_sms, n_up_sms;    // SMs that signal the COMBINE / UP counters of a layer
   float rms_eps, attn_scale_log2;
   // caller weights (device pointers; per-layer arrays are device arrays of L pointers)
   const uint16_t* embed;

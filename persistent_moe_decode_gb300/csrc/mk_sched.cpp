@@ -2,9 +2,10 @@
 //
 // "Inside the megakernel serving engine for North Mini Code", §The task
 // scheduler: the host builds named waves for each layer, chooses an order and
-// gives each SM its list.  Here every wave is cut into one equal share per SM
-// (rows of a weight matrix, query heads to merge, hidden rows to produce), so
-// an SM's list holds one task per wave and layer; the shares whose size
+// gives each SM its list.  Here every wave is cut into equal shares (rows of
+// a weight matrix, query heads to merge, hidden rows to produce) over the SMs
+// that run it: all of them, or the SMs of one branch of the parallel layer.
+// An SM's list holds one task per wave and layer; the shares whose size
 // depends on routing (the experts' rows) are fixed as "slice s of n" and
 // resolved on the device once the routing is known.  Any order of the waves
 // in which ROUTE precedes UP and ATTN precedes COMBINE precedes OUT has no
@@ -33,6 +34,8 @@ int validate_config(const mk_config& c) {
   // the attention keeps every query head's BF16 high and low halves in the
   // 16 KB reduction buffer
   if (c.n_q_heads * c.head_dim > 4096) return MK_ERR_BAD_CONFIG;
+  // one token: the hidden vectors of all routed experts are staged together
+  if (c.top_k * c.moe_inter > kXsFloats) return MK_ERR_BAD_CONFIG;
   if (c.n_experts < 1 || c.n_experts > 256 || c.top_k < 1 || c.top_k > 8 || c.top_k > c.n_experts)
     return MK_ERR_BAD_CONFIG;
   if (c.vocab < 1 || c.page_size != 16) return MK_ERR_BAD_CONFIG;
@@ -66,36 +69,68 @@ Desc task(int op, int layer, int a0, int a1) {
 
 }  // namespace
 
-int build_plan(const mk_config& c, int n_sm, int batch, Plan* out, int bump_layer, int bump) {
-  if (validate_config(c) != MK_OK || n_sm < 1 || batch < 1 || batch > c.max_batch)
+int attention_sms(const mk_config& c, int n_sm, int batch, const int32_t* seq_lens) {
+  if (n_sm < 2) return n_sm;
+  if (c.n_attn_claimers > 0) return c.n_attn_claimers < n_sm ? c.n_attn_claimers : n_sm;
+  double kv = 0.0;
+  for (int b = 0; b < batch; b++) kv += (double)(seq_lens[b] + 1);
+  kv *= 2.0 * c.n_kv_heads * c.head_dim * 2.0;
+  const double experts = (double)std::min(c.n_experts, batch * c.top_k);
+  const double up = experts * 2.0 * c.moe_inter * c.hidden * 2.0;
+  int na = (int)(n_sm * kv / (kv + up) + 0.5);
+  return std::max(1, std::min(n_sm - 1, na));
+}
+
+int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, int bump_layer, int bump) {
+  if (validate_config(c) != MK_OK || n_sm < 1 || batch < 1 || batch > c.max_batch || n_attn < 1 ||
+      n_attn > n_sm)
     return MK_ERR_BAD_CONFIG;
   const BarLayout bl = bar_layout(c.max_batch);
   const int L = c.n_layers;
   const long long rows1 = c.n_experts + (long long)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
   const long long units = (long long)batch * c.n_q_heads;
-  const int nmoe = moe_sms(c, n_sm);
+  const bool roles = n_attn < n_sm;
+  const int nmoe = roles ? n_sm - n_attn : moe_sms(c, n_sm);
+  const int ncomb = roles ? n_attn : n_sm;
 
   static const int orders[3][6] = {
       {OP_P1, OP_ROUTE, OP_ATTN, OP_UP, OP_COMBINE, OP_OUT},
       {OP_P1, OP_ROUTE, OP_ATTN, OP_COMBINE, OP_UP, OP_OUT},
       {OP_P1, OP_ROUTE, OP_UP, OP_ATTN, OP_COMBINE, OP_OUT}};
+  static const int attn_role[5] = {OP_P1, OP_ATTN, OP_COMBINE, OP_ROUTE, OP_OUT};
+  static const int moe_role[4] = {OP_P1, OP_ROUTE, OP_UP, OP_OUT};
 
   out->tasks.clear();
   out->off.assign(n_sm + 1, 0);
   for (int s = 0; s < n_sm; s++) {
     out->off[s] = (int32_t)(out->tasks.size() / kDescWords);
+    const int* ops;
+    int nops;
+    if (!roles) {
+      ops = orders[c.wave_order];
+      nops = 6;
+    } else if (s < n_attn) {
+      ops = attn_role;
+      nops = 5;
+    } else {
+      ops = moe_role;
+      nops = 4;
+    }
     std::vector<Desc> list;
     for (int l = 0; l < L; l++) {
-      for (int op : orders[c.wave_order]) {
+      for (int k = 0; k < nops; k++) {
+        const int op = ops[k];
         int lo = 0, hi = 0;
         switch (op) {
           case OP_P1: share(rows1, n_sm, s, &lo, &hi); break;
-          case OP_COMBINE: share(units, n_sm, s, &lo, &hi); break;
+          case OP_COMBINE: share(units, ncomb, s, &lo, &hi); break;
           case OP_OUT: share(c.hidden, n_sm, s, &lo, &hi); break;
-          case OP_UP:
-            lo = s < nmoe ? s : -1;
+          case OP_UP: {
+            const int slice = roles ? s - n_attn : s;
+            lo = slice < nmoe ? slice : -1;
             hi = nmoe;
             break;
+          }
           default: break;
         }
         Desc t = task(op, l, lo, hi);
@@ -117,13 +152,15 @@ int build_plan(const mk_config& c, int n_sm, int batch, Plan* out, int bump_laye
   }
   out->off[n_sm] = (int32_t)(out->tasks.size() / kDescWords);
   out->n_bars = L * bl.per_layer;
+  out->n_comb_sms = ncomb;
+  out->n_up_sms = roles ? nmoe : n_sm;
   return MK_OK;
 }
 
-int split_kv(const mk_config& c, int n_sm, int batch, const int32_t* seq_lens,
+int split_kv(const mk_config& c, int n_sm, int n_attn, int batch, const int32_t* seq_lens,
              std::vector<int32_t>* items, std::vector<int32_t>* sm_off, std::vector<int32_t>* meta) {
   const int P = c.page_size;
-  const int na = attn_sms(c, n_sm);
+  const int na = n_attn;
   items->clear();
   sm_off->assign(n_sm + 1, 0);
   meta->assign((size_t)batch * 2, 0);

@@ -168,11 +168,20 @@ def test_tiny_trajectory():
         pair.close()
 
 
-@pytest.mark.parametrize("order", [mk.MK_WAVES_DEFAULT, mk.MK_WAVES_ATTN_FIRST, mk.MK_WAVES_INTERLEAVED])
-@pytest.mark.parametrize("sm_cap", [0, 1, 7])
-def test_tiny_schedules_give_identical_logits(order, sm_cap):
-    """Any wave order, SM count and claimer count gives bit-identical output
-    for a fixed split-KV chunk: every sum has a fixed order whatever SM
+SCHEDULES = (
+    # every SM runs every phase, in each wave order, on all / one / seven SMs
+    [dict(n_attn_claimers=10000, wave_order=o, sm_cap=c, n_moe_claimers=5)
+     for o in (mk.MK_WAVES_DEFAULT, mk.MK_WAVES_ATTN_FIRST, mk.MK_WAVES_INTERLEAVED)
+     for c in (0, 1, 7)]
+    # SM roles: one or three attention SMs, the rest on the experts
+    + [dict(n_attn_claimers=a, sm_cap=c) for a in (1, 3) for c in (0, 7)]
+)
+
+
+@pytest.mark.parametrize("kw", SCHEDULES, ids=lambda kw: "-".join(f"{k}{v}" for k, v in kw.items()))
+def test_tiny_schedules_give_identical_logits(kw):
+    """Any wave order, SM count, role split and slice count gives bit-identical
+    output for a fixed split-KV chunk: every sum has a fixed order whatever SM
     computes it."""
     wl = WORKLOADS["tiny"]
     from persistent_moe_decode_gb300.runner import StepRunner
@@ -182,8 +191,7 @@ def test_tiny_schedules_give_identical_logits(order, sm_cap):
     ref_run.check_status()
     ref = ref_run.logits.clone()
     ref_run.close()
-    run = StepRunner(wl, device="cuda", wave_order=order, sm_cap=sm_cap, n_attn_claimers=3,
-                     n_moe_claimers=5, kv_split_tokens=64)
+    run = StepRunner(wl, device="cuda", kv_split_tokens=64, **kw)
     run.step()
     torch.cuda.synchronize()
     run.check_status()
