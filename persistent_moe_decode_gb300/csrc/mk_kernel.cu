@@ -653,7 +653,82 @@ struct Cons {
   // h_l = h_{l-1} + delta_{l-1} (the embedding row at l = 0), this SM's own
   // copy; x_l = h_l / sqrt(mean(h_l^2) + eps) * gain.  Thread t owns columns
   // 4 t + 1024 i.  SM 0 also keeps every layer's h and x for inspection.
+  // one token: every load (own residual copy, the previous layer's update,
+  // the gain) issued together, each thread sums the eight warp partials
+  // itself (same order in every thread), x goes to the staging buffer
+  __device__ __forceinline__ bool norm1(int l, bool final_norm) {
+    const int H = p.H, H4 = H / 4;
+    const size_t Bm = (size_t)p.Bmax;
+    float* hl = p.hloc + (size_t)blockIdx.x * Bm * H;
+    float* xl = p.xloc + (size_t)blockIdx.x * Bm * H;
+    const uint16_t* gain = final_norm ? p.final_norm : p.attn_norm[l];
+    constexpr int NI = 4;                       // H <= 4096: at most 4 float4 per thread
+    float4 h[NI];
+    uint2 g[NI];
+#pragma unroll
+    for (int k = 0; k < NI; k++) {              // loads that do not wait for the previous layer
+      const int i4 = tid + 256 * k;
+      h[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      g[k] = make_uint2(0, 0);
+      if (i4 < H4) {
+        g[k] = *(const uint2*)(gain + i4 * 4);
+        if (l == 0) {
+          const uint2 e = *(const uint2*)(p.embed + (size_t)p.tokens[0] * H + i4 * 4);
+          h[k] = make_float4(bf16lo(e.x), bf16hi(e.x), bf16lo(e.y), bf16hi(e.y));
+        } else {
+          h[k] = __ldcg((const float4*)hl + i4);
+        }
+      }
+    }
+    if (l > 0) {
+      if (!wait_counter(bar_index(p, l - 1, p.bl.out), p.n_sm + t[R_BUMP])) return false;
+      const float4* dl = (const float4*)(p.delta + (size_t)(l - 1) * Bm * H);
+      float4 d[NI];
+#pragma unroll
+      for (int k = 0; k < NI; k++) {
+        const int i4 = tid + 256 * k;
+        d[k] = i4 < H4 ? __ldcg(dl + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < NI; k++) {
+        h[k].x += d[k].x; h[k].y += d[k].y; h[k].z += d[k].z; h[k].w += d[k].w;
+      }
+    }
+    const bool keep = blockIdx.x == 0;
+    float ssl = 0.f;
+#pragma unroll
+    for (int k = 0; k < NI; k++) {
+      const int i4 = tid + 256 * k;
+      if (i4 < H4) {
+        if (!final_norm) __stcg((float4*)hl + i4, h[k]);
+        if (keep) __stcg((float4*)(p.hdbg + (size_t)l * Bm * H) + i4, h[k]);
+        ssl += h[k].x * h[k].x + h[k].y * h[k].y + h[k].z * h[k].z + h[k].w * h[k].w;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ssl += __shfl_xor_sync(0xffffffffu, ssl, o);
+    if (lane == 0) S.nred[warp][0] = ssl;
+    if (!csync()) return false;
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; w++) sum += S.nred[w][0];
+    const float r = 1.0f / sqrtf(sum / (float)H + p.rms_eps);
+#pragma unroll
+    for (int k = 0; k < NI; k++) {
+      const int i4 = tid + 256 * k;
+      if (i4 < H4) {
+        const float4 x = make_float4(h[k].x * r * bf16lo(g[k].x), h[k].y * r * bf16hi(g[k].x),
+                                     h[k].z * r * bf16lo(g[k].y), h[k].w * r * bf16hi(g[k].y));
+        *(float4*)&S.xs[i4 * 4] = x;
+        __stcg((float4*)xl + i4, x);
+        if (keep) __stcg((float4*)(p.xdbg + (size_t)l * Bm * H) + i4, x);
+      }
+    }
+    return csync();
+  }
+
   __device__ __forceinline__ bool norm(int l, bool final_norm) {
+    if (p.B == 1) return norm1(l, final_norm);
     const int H = p.H, B = p.B, H4 = H / 4;
     const size_t Bm = (size_t)p.Bmax;
     if (l > 0 && !wait_counter(bar_index(p, l - 1, p.bl.out), p.n_sm + t[R_BUMP])) return false;
@@ -1216,16 +1291,23 @@ struct Cons {
 
   // -------------------------------------------------------- attention
   // One split-KV item: sequence b, keys [tt0, tt1), every KV head.  The NWG =
-  // 8 / hkv warps of KV group g = w % hkv all score every page of the item
-  // (QK^T is cheap) and each accumulates its own 1 / NWG of the head dims in
-  // PV, so no warp merges with another.  The query (RoPE applied here) sits in
-  // shared memory as BF16 high + low halves, 16-byte chunks swizzled by row so
-  // that the fragment loads are conflict-free.  DPL = head dims per lane.
-  template <int D, int DPL>
+  // 8 / hkv warps of KV group g = w % hkv all score every page of the item and
+  // each accumulates its own DW = d / NWG head dims (NT = DW / 8 tiles of 8).
+  // Both products run on the tensor cores (m16n8k16, BF16 in, fp32 out) with
+  // the group's query heads as the 16-row A operand (8 used):
+  //   S[head][token] = Q K^T  with Q, K fragments read as 16-byte chunks (the
+  //   same permutation of the contraction index on both operands),
+  //   O[head][dim] += P V     where the score accumulators already have the A
+  //   fragment layout of P, and V comes from ldmatrix.trans.
+  // The fp32 query and probabilities are split into BF16 high + low halves
+  // (two products each), so the contraction keeps about 16 bits of their
+  // mantissa.  Online softmax per head in fp32 (log2 domain) with a per-lane
+  // rescale.  The query (RoPE applied here) is staged in shared memory once
+  // per item, 16-byte chunks swizzled by row.
+  template <int D, int NT>
   __device__ __forceinline__ bool attn() {
     const int hkv = p.hkv, grp = p.grp, P = p.P, hq = p.hq;
     const int NWG = kConsumerWarps / hkv;
-    const int DW = D / NWG;                // head dims of this warp
     const int g = warp % hkv, jw = warp / hkv;
     const int l = t[R_LAYER], b = t[R_B];
     const int tt0 = t[R_TT0], tt1 = t[R_TT1], pos = t[R_POS];
@@ -1233,6 +1315,7 @@ struct Cons {
     const int hb = P * D * 2;             // bytes of one head's 16-token page
     const int pb = hkv * hb;              // bytes of one page, all heads
     const int pps = attn_pps(p);
+    (void)NWG;
     if (!wait_counter(bar_index(p, l, p.bl.p1), p.n_sm)) return false;
 
     // query with RoPE -> BF16 hi / lo planes: [head][D] in 16-byte chunks, chunk c
@@ -1277,17 +1360,27 @@ struct Cons {
     }
     if (!csync()) return false;
 
-    const int qh_row = g * grp + gl;      // this lane's query head (MMA column gl)
+    // this lane's query head (A row gl) as fragments for the whole item
     const bool qon = gl < grp;
-    const int d0 = jw * DW + lane * DPL;  // first head dim of this lane in PV
-    const bool don = lane * DPL < DW;
+    const int qrow = g * grp + gl;
+    uint4 qh[D / 32], ql[D / 32];
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ch++) {
+      qh[ch] = make_uint4(0, 0, 0, 0);
+      ql[ch] = qh[ch];
+      if (qon) {
+        const int c = ch * 4 + cq;
+        const int off = qrow * D * 2 + ((c ^ (qrow & 7)) << 4);
+        qh[ch] = lds128(qhi + off);
+        ql[ch] = lds128(qlo + off);
+      }
+    }
 
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    float o[8][DPL];
+    const int d0 = jw * (NT * 8);         // first head dim of this warp
+    float m_run = -INFINITY, l_run = 0.f;
+    float o[NT][4];
 #pragma unroll
-    for (int h = 0; h < 8; h++)
-#pragma unroll
-      for (int j = 0; j < DPL; j++) o[h][j] = 0.f;
+    for (int j = 0; j < NT; j++) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
     const int pg0 = tt0 / P;
     const int npages = (tt1 + P - 1) / P - pg0;
@@ -1333,89 +1426,75 @@ struct Cons {
           }
           __syncwarp();
         }
-        // scores: 16 tokens x 8 heads, q = high + low halves; four independent
-        // accumulators keep the tensor-core chain short
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        // S = Q K^T: tile 0 = tokens 0..7 (K rows gl), tile 1 = tokens 8..15
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
         {
-          float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
+          float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int ch = 0; ch < D / 32; ch++) {
             const uint8_t* a = kp + gl * D * 2 + ch * 64 + cq * 16;
-            const uint4 lo = lds128(a);
-            const uint4 hi = lds128(a + 8 * D * 2);
-            uint4 qh = make_uint4(0, 0, 0, 0), ql = qh;
-            if (qon) {
-              const int c = ch * 4 + cq;
-              const int off = qh_row * D * 2 + ((c ^ (qh_row & 7)) << 4);
-              qh = lds128(qhi + off);
-              ql = lds128(qlo + off);
-            }
-            mma_bf16(s, lo.x, hi.x, lo.y, hi.y, qh.x, qh.y);
-            mma_bf16(s1, lo.z, hi.z, lo.w, hi.w, qh.z, qh.w);
-            mma_bf16(s2, lo.x, hi.x, lo.y, hi.y, ql.x, ql.y);
-            mma_bf16(s3, lo.z, hi.z, lo.w, hi.w, ql.z, ql.w);
+            const uint4 k0 = lds128(a);
+            const uint4 k1 = lds128(a + 8 * D * 2);
+            mma_bf16(s0, qh[ch].x, 0u, qh[ch].y, 0u, k0.x, k0.y);
+            mma_bf16(s0, qh[ch].z, 0u, qh[ch].w, 0u, k0.z, k0.w);
+            mma_bf16(s1, qh[ch].x, 0u, qh[ch].y, 0u, k1.x, k1.y);
+            mma_bf16(s1, qh[ch].z, 0u, qh[ch].w, 0u, k1.z, k1.w);
+            mma_bf16(t0, ql[ch].x, 0u, ql[ch].y, 0u, k0.x, k0.y);
+            mma_bf16(t0, ql[ch].z, 0u, ql[ch].w, 0u, k0.z, k0.w);
+            mma_bf16(t1, ql[ch].x, 0u, ql[ch].y, 0u, k1.x, k1.y);
+            mma_bf16(t1, ql[ch].z, 0u, ql[ch].w, 0u, k1.z, k1.w);
           }
-#pragma unroll
-          for (int j = 0; j < 4; j++) s[j] = (s[j] + s1[j]) + (s2[j] + s3[j]);
+          s0[0] += t0[0]; s0[1] += t0[1];
+          s1[0] += t1[0]; s1[1] += t1[1];
         }
+        // this lane: head gl, tokens 2cq, 2cq + 1 (tile 0) and 8 + 2cq, 9 + 2cq (tile 1)
         const int lo_t = max(tt0 - tk0, 0), hi_t = min(tt1 - tk0, P);   // valid rows [lo_t, hi_t)
-        const bool v0 = gl >= lo_t && gl < hi_t, v1 = gl + 8 >= lo_t && gl + 8 < hi_t;
-        s[0] = v0 ? s[0] * sc : -INFINITY;
-        s[1] = v0 ? s[1] * sc : -INFINITY;
-        s[2] = v1 ? s[2] * sc : -INFINITY;
-        s[3] = v1 ? s[3] * sc : -INFINITY;
+        float sv[4];
 #pragma unroll
-        for (int hh = 0; hh < 2; hh++) {
-          float mx = fmaxf(s[hh], s[2 + hh]);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mn = fmaxf(m_run[hh], mx);
-          const float al = (mn == -INFINITY) ? 1.f : exp2f(m_run[hh] - mn);
-          const float p0 = (mn == -INFINITY) ? 0.f : exp2f(s[hh] - mn);
-          const float p1 = (mn == -INFINITY) ? 0.f : exp2f(s[2 + hh] - mn);
-          float sm = p0 + p1;
-          sm += __shfl_xor_sync(0xffffffffu, sm, 4);
-          sm += __shfl_xor_sync(0xffffffffu, sm, 8);
-          sm += __shfl_xor_sync(0xffffffffu, sm, 16);
-          l_run[hh] = l_run[hh] * al + sm;
-          m_run[hh] = mn;
-          if (gl == 0) S.alpha[warp][2 * cq + hh] = al;
-          S.pbuf[warp][gl][2 * cq + hh] = p0;
-          S.pbuf[warp][gl + 8][2 * cq + hh] = p1;
+        for (int k = 0; k < 4; k++) {
+          const int tok = (k >> 1) * 8 + 2 * cq + (k & 1);
+          const float v = (k < 2 ? s0[k & 1] : s1[k & 1]) * sc;
+          sv[k] = (tok >= lo_t && tok < hi_t) ? v : -INFINITY;
         }
-        __syncwarp();
-        if (don) {
-          const float4 a0 = *(const float4*)&S.alpha[warp][0];
-          const float4 a1 = *(const float4*)&S.alpha[warp][4];
-          const float al[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m_run, mx);
+        const float al = (mn == -INFINITY) ? 1.f : exp2f(m_run - mn);
+        float pv[4];
 #pragma unroll
-          for (int h = 0; h < 8; h++)
+        for (int k = 0; k < 4; k++) pv[k] = (mn == -INFINITY) ? 0.f : exp2f(sv[k] - mn);
+        float sm = (pv[0] + pv[1]) + (pv[2] + pv[3]);
+        sm += __shfl_xor_sync(0xffffffffu, sm, 1);
+        sm += __shfl_xor_sync(0xffffffffu, sm, 2);
+        l_run = l_run * al + sm;
+        m_run = mn;
+        // P as the A operand (rows gl: tokens 2cq.. of tile 0 and 8 + 2cq.. of tile 1)
+        uint32_t ph0, ph1, pl0, pl1;
+        {
+          const uint16_t h0 = f2bf(pv[0]), h1 = f2bf(pv[1]), h2 = f2bf(pv[2]), h3 = f2bf(pv[3]);
+          ph0 = (uint32_t)h0 | ((uint32_t)h1 << 16);
+          ph1 = (uint32_t)h2 | ((uint32_t)h3 << 16);
+          pl0 = (uint32_t)f2bf(pv[0] - bf16f(h0)) | ((uint32_t)f2bf(pv[1] - bf16f(h1)) << 16);
+          pl1 = (uint32_t)f2bf(pv[2] - bf16f(h2)) | ((uint32_t)f2bf(pv[3] - bf16f(h3)) << 16);
+        }
+        // O += P V over this warp's dims, two 8-dim tiles per ldmatrix
+        const uint8_t* vrow = vp + (size_t)((lane >> 3) & 1) * 8 * D * 2 + (lane & 7) * D * 2 +
+                              (size_t)(d0 + (lane >> 4) * 8) * 2;
 #pragma unroll
-            for (int j = 0; j < DPL; j++) o[h][j] *= al[h];
-          const uint8_t* vrow = vp + d0 * 2;
-          for (int tk = lo_t; tk < hi_t; tk++) {
-            const float4 p0 = *(const float4*)&S.pbuf[warp][tk][0];
-            const float4 p1 = *(const float4*)&S.pbuf[warp][tk][4];
-            const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-            float vv[DPL];
-            if (DPL == 4) {
-              const uint2 u = *(const uint2*)(vrow + tk * D * 2);
-              vv[0] = bf16lo(u.x);
-              vv[1 % DPL] = bf16hi(u.x);
-              vv[2 % DPL] = bf16lo(u.y);
-              vv[3 % DPL] = bf16hi(u.y);
-            } else if (DPL == 2) {
-              const uint32_t u = *(const uint32_t*)(vrow + tk * D * 2);
-              vv[0] = bf16lo(u);
-              vv[1 % DPL] = bf16hi(u);
-            } else {
-              vv[0] = bf16f(*(const uint16_t*)(vrow + tk * D * 2));
-            }
+        for (int j = 0; j < NT; j++) {
+          o[j][0] *= al;
+          o[j][1] *= al;
+        }
 #pragma unroll
-            for (int h = 0; h < 8; h++)
-#pragma unroll
-              for (int j = 0; j < DPL; j++) o[h][j] = fmaf(pv[h], vv[j], o[h][j]);
+        for (int j = 0; j < NT; j += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_trans(b0, b1, b2, b3, vrow + j * 16);
+          mma_bf16(o[j], ph0, 0u, ph1, 0u, b0, b1);
+          mma_bf16(o[j], pl0, 0u, pl1, 0u, b0, b1);
+          if (j + 1 < NT) {
+            mma_bf16(o[j + 1], ph0, 0u, ph1, 0u, b2, b3);
+            mma_bf16(o[j + 1], pl0, 0u, pl1, 0u, b2, b3);
           }
         }
         if (has_new) fence_proxy_async_smem();
@@ -1425,27 +1504,16 @@ struct Cons {
     }
 
     if (tid == 0) S.t_mark[1] = gtime_ns();
-    // this warp's partials: heads of group g, its head dims; (max, sum) by warp jw = 0
+    // this warp's partials: head gl of group g, dims d0 + 8j + 2cq, +1; (max, sum) by warp jw = 0
     const int item = t[R_ITEM];
-    const size_t it0 = ((size_t)item * hkv + g) * grp;
-    if (don) {
+    if (qon) {
+      const size_t it = ((size_t)item * hkv + g) * grp + gl;
+      float* dst = p.attn_part + it * D + d0 + 2 * cq;
 #pragma unroll
-      for (int h = 0; h < 8; h++) {
-        if (h < grp) {
-          float* dst = p.attn_part + (it0 + h) * D + d0;
-#pragma unroll
-          for (int j = 0; j < DPL; j++) __stcg(dst + j, o[h][j]);
-        }
-      }
-    }
-    if (jw == 0 && gl == 0) {
-#pragma unroll
-      for (int hh = 0; hh < 2; hh++) {
-        const int h = 2 * cq + hh;
-        if (h < grp) {
-          __stcg(p.attn_ml + (it0 + h) * 2 + 0, m_run[hh]);
-          __stcg(p.attn_ml + (it0 + h) * 2 + 1, l_run[hh]);
-        }
+      for (int j = 0; j < NT; j++) __stcg((float2*)(dst + j * 8), make_float2(o[j][0], o[j][1]));
+      if (jw == 0 && cq == 0) {
+        __stcg(p.attn_ml + it * 2 + 0, m_run);
+        __stcg(p.attn_ml + it * 2 + 1, l_run);
       }
     }
     if (tid == 0) S.t_mark[2] = gtime_ns();
@@ -1623,24 +1691,25 @@ __device__ __forceinline__ bool op_route(const Params& p, Smem& S, const int32_t
   return ok;
 }
 
-template <int D, int DPL>
+template <int D, int NT>
 __device__ __forceinline__ bool op_attn(const Params& p, Smem& S, const int32_t* t) {
   Cons c(p, S, t);
-  const bool ok = c.attn<D, DPL>();
+  const bool ok = c.attn<D, NT>();
   c.save();
   return ok;
 }
 
-// head dims per lane when the group's 8 / hkv warps split the head dims
+// head-dim tiles of 8 per warp when the group's 8 / hkv warps split the head dims
 __device__ __forceinline__ bool op_attn_any(const Params& p, Smem& S, const int32_t* t) {
-  const int dw = p.d / (kConsumerWarps / p.hkv);
+  const int nt = p.d / (kConsumerWarps / p.hkv) / 8;
   if (p.d == 128) {
-    if (dw >= 128) return op_attn<128, 4>(p, S, t);
-    if (dw >= 64) return op_attn<128, 2>(p, S, t);
-    return op_attn<128, 1>(p, S, t);
+    if (nt >= 8) return op_attn<128, 8>(p, S, t);
+    if (nt >= 4) return op_attn<128, 4>(p, S, t);
+    return op_attn<128, 2>(p, S, t);
   }
-  if (dw >= 64) return op_attn<64, 2>(p, S, t);
-  return op_attn<64, 1>(p, S, t);
+  if (nt >= 8) return op_attn<64, 8>(p, S, t);
+  if (nt >= 4) return op_attn<64, 4>(p, S, t);
+  return op_attn<64, 2>(p, S, t);
 }
 
 template <int D>

@@ -92,6 +92,15 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
   return v;
 }
 
+// four 8x8 BF16 tiles from shared memory, transposed (B fragments of a
+// row-major [k][n] matrix); lanes 8i..8i+7 give the row addresses of tile i
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                              const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+
 // D += A * B, m16n8k16, A row-major BF16, B column-major BF16, fp32 accumulate
 __device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {

@@ -29,6 +29,10 @@ int validate_config(const mk_config& c) {
   const int grp = c.n_q_heads / c.n_kv_heads;
   if (grp > 8 || kConsumerWarps % c.n_kv_heads) return MK_ERR_BAD_CONFIG;
   if (c.head_dim != 64 && c.head_dim != 128) return MK_ERR_BAD_CONFIG;
+  // the warps of a KV group split the head dims: 16 to 64 dims per warp
+  // (pairs of 8-dim MMA tiles; more would not fit the registers)
+  const int dims_per_warp = c.head_dim / (kConsumerWarps / c.n_kv_heads);
+  if (dims_per_warp < 16 || dims_per_warp > 64) return MK_ERR_BAD_CONFIG;
   if (!gemv_k(c.hidden) || !gemv_k(c.moe_inter) || !gemv_k(c.n_q_heads * c.head_dim))
     return MK_ERR_BAD_CONFIG;
   // the attention keeps every query head's BF16 high and low halves in the
@@ -97,7 +101,9 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
       {OP_P1, OP_ROUTE, OP_ATTN, OP_UP, OP_COMBINE, OP_OUT},
       {OP_P1, OP_ROUTE, OP_ATTN, OP_COMBINE, OP_UP, OP_OUT},
       {OP_P1, OP_ROUTE, OP_UP, OP_ATTN, OP_COMBINE, OP_OUT}};
-  static const int attn_role[5] = {OP_P1, OP_ATTN, OP_COMBINE, OP_ROUTE, OP_OUT};
+  // attention SMs route between their items and the combine: the routing
+  // only needs P1 (long done) and fills the wait for the other items
+  static const int attn_role[5] = {OP_P1, OP_ATTN, OP_ROUTE, OP_COMBINE, OP_OUT};
   static const int moe_role[4] = {OP_P1, OP_ROUTE, OP_UP, OP_OUT};
 
   out->tasks.clear();

@@ -23,7 +23,7 @@ int validate_config(const mk_config& c);
 // Per-SM task lists of one step for `batch` sequences: for every layer one
 // task of each phase per SM, then the FINAL task.  With n_attn < n_sm the SMs
 // take roles: SMs [0, n_attn) run the attention branch of the parallel layer
-// (P1, ATTN, COMBINE, ROUTE, OUT), the others the expert branch (P1, ROUTE,
+// (P1, ATTN, ROUTE, COMBINE, OUT), the others the expert branch (P1, ROUTE,
 // UP, OUT), so the two branches run side by side; with n_attn == n_sm every
 // SM runs every phase in the configured wave order.  `bump_layer` / `bump`
 // make the P1 task of that layer wait for a counter value that is never
