@@ -58,11 +58,12 @@ enum mk_status {
  * task scheduler, the static part: named waves per layer, one chosen order).
  * Each SM's list holds, per layer, one share of every wave:
  *   P1 (norm + router / QKV rows), ROUTE (top-k), ATTN (split-KV items),
- *   UP (expert gate/up rows), COMBINE (split merges), OUT (O-proj + down rows). */
+ *   UP (expert gate/up rows), COMBINE (split merges), DOWN (expert down rows),
+ *   OUT (O-proj rows). */
 enum mk_wave_order {
-  MK_WAVES_DEFAULT = 0,    /* P1, ROUTE, ATTN, UP, COMBINE, OUT  */
-  MK_WAVES_ATTN_FIRST = 1, /* P1, ROUTE, ATTN, COMBINE, UP, OUT  */
-  MK_WAVES_INTERLEAVED = 2 /* P1, ROUTE, UP, ATTN, COMBINE, OUT  */
+  MK_WAVES_DEFAULT = 0,    /* P1, ROUTE, ATTN, UP, COMBINE, DOWN, OUT  */
+  MK_WAVES_ATTN_FIRST = 1, /* P1, ROUTE, ATTN, COMBINE, UP, DOWN, OUT  */
+  MK_WAVES_INTERLEAVED = 2 /* P1, ROUTE, UP, ATTN, DOWN, COMBINE, OUT  */
 };
 
 typedef struct {
@@ -87,7 +88,9 @@ typedef struct {
   /* schedule */
   int wave_order;         /* enum mk_wave_order                                  */
   int n_attn_claimers;    /* SMs that run the attention branch (split-KV items,
-                             combines); the others run the routed experts.
+                             combines); the others run the routed experts
+                             (routing, gate/up, down); every SM takes O-proj
+                             rows.
                              0 = chosen per step from the KV bytes against the
                              experts' bytes; >= the SM count = every SM runs
                              every phase in wave_order                         */

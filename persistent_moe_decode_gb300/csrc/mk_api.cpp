@@ -35,7 +35,7 @@ struct DevPlan {
   int32_t* tasks = nullptr;
   int32_t* off = nullptr;
   size_t n_tasks = 0;
-  int n_comb_sms = 0, n_up_sms = 0;
+  int n_comb_sms = 0, n_up_sms = 0, n_down_sms = 0, n_rtr_sms = 0;
 };
 
 // plans are cached per (batch, attention SMs)
@@ -133,6 +133,8 @@ int ensure_plan(mk_handle* h, int batch, int n_attn, DevPlan** out) {
     dp.n_tasks = plan.tasks.size() / kDescWords;
     dp.n_comb_sms = plan.n_comb_sms;
     dp.n_up_sms = plan.n_up_sms;
+    dp.n_down_sms = plan.n_down_sms;
+    dp.n_rtr_sms = plan.n_rtr_sms;
     if (cudaMalloc(&dp.tasks, std::max<size_t>(plan.tasks.size() * 4, 16)) != cudaSuccess ||
         cudaMalloc(&dp.off, plan.off.size() * 4) != cudaSuccess) {
       cudaGetLastError();
@@ -279,7 +281,6 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
   TRY(dalloc(h, &p.abuf, Ls * Bs * K * I));
   TRY(dalloc(h, &p.oproj, Ls * Bs * H));
   TRY(dalloc(h, &p.moe, Ls * Bs * H));
-  TRY(dalloc(h, &p.delta, Ls * Bs * H));
   h->bar_words = kErrWords + (size_t)L * p.bl.per_layer;
   TRY(dalloc(h, &h->d_bars, h->bar_words));
   p.err = h->d_bars;
@@ -408,6 +409,8 @@ Params step_params(const mk_handle* h, const DevPlan& plan, float* logits) {
   p.task_off = plan.off;
   p.n_comb_sms = plan.n_comb_sms;
   p.n_up_sms = plan.n_up_sms;
+  p.n_down_sms = plan.n_down_sms;
+  p.n_rtr_sms = plan.n_rtr_sms;
   return p;
 }
 

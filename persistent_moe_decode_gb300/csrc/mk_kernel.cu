@@ -68,8 +68,7 @@ struct __align__(128) Smem {
                                             // layer, the attention output, the experts' hidden)
   float red[2 * kPartFloats];               // GEMV partial sums (two buffers) / attention
                                             // query fragments and merge / combine sums
-  float acc_o[kOutRows][kMaxBatch];         // OUT chunk: O-proj rows
-  float acc_m[kOutRows][kMaxBatch];         // OUT chunk: weighted expert outputs
+  float acc_m[kOutRows][kMaxBatch];         // DOWN row chunk (several tokens): weighted expert outputs
   float pbuf[kConsumerWarps][16][8];        // attention probabilities of one page per warp
   float alpha[kConsumerWarps][8];           // attention rescale per head per warp
   float wstat[kConsumerWarps][8][2];        // attention (max, sum) per warp per head
@@ -440,29 +439,36 @@ struct Prod {
     return true;
   }
 
+  // OUT: O-proj rows [a0, a1) (needs no routing)
   __device__ __noinline__ bool do_out(int a0, int a1) {
-    const int H = p.H, B = p.B;
-    if (!wait_route()) return false;
-    const int n_act = S.rt.n_act;
+    const int B = p.B;
     const int KO = p.hq * p.d;
     if (a1 <= a0) return chunk(K_OPROJ, FL_LAST, 0, 0, 1, KO, B, 0, 0, 0, nullptr, nullptr);
     const int co = B == 1 ? kRowChunk : gemv_chunk_rows(KO, B);
-    for (int h0 = a0; h0 < a1; h0 += kOutRows) {
-      const int h1 = min(a1, h0 + kOutRows);
-      const int fin = FL_CLAST | (h1 == a1 ? FL_LAST : 0);
-      // O-proj rows, in sub-chunks the partial buffer can hold
-      for (int c0 = h0; c0 < h1; c0 += co)
-        if (!chunk(K_OPROJ, (n_act == 0 && c0 + co >= h1) ? fin : 0, c0, min(co, h1 - c0), 1, KO, B, 0, 0,
-                   c0 - h0, p.w_o[l], nullptr))
-          return false;
-      if (B == 1 && n_act > 0) {
-        // one token: every routed expert's down rows of [h0, h1) in one chunk,
-        // one group per expert
+    for (int c0 = a0; c0 < a1; c0 += co)
+      if (!chunk(K_OPROJ, c0 + co >= a1 ? FL_LAST : 0, c0, min(co, a1 - c0), 1, KO, B, 0, 0, 0, p.w_o[l],
+                 nullptr))
+        return false;
+    return true;
+  }
+
+  // DOWN: hidden rows [a0, a1) of every routed expert's down projection
+  __device__ __noinline__ bool do_down(int a0, int a1) {
+    const int H = p.H, B = p.B;
+    if (!wait_route()) return false;
+    const int n_act = S.rt.n_act;
+    if (a1 <= a0 || n_act == 0) return chunk(K_DOWN, FL_LAST, 0, 0, 1, p.I, 0, 0, 0, 0, nullptr, nullptr);
+    if (B == 1) {
+      // one token: every routed expert's rows of [h0, h1) in one chunk, one
+      // group per expert (the result buffer holds n_act x rows)
+      const int cr = kRowChunk / n_act;
+      for (int h0 = a0; h0 < a1; h0 += cr) {
+        const int h1 = min(a1, h0 + cr);
         int32_t* w = begin();
         if (!w) return false;
         if (lane == 0) {
           w[R_KIND] = K_DOWNALL;
-          w[R_FLAGS] = fin;
+          w[R_FLAGS] = h1 == a1 ? FL_LAST : 0;
           w[R_ROW0] = h0;
           w[R_NROWS] = h1 - h0;
           w[R_NGRP] = n_act;
@@ -472,9 +478,14 @@ struct Prod {
         commit();
         for (int a = 0; a < n_act; a++)
           if (!stream_rows(p.w_down[l] + (size_t)S.rt.act[a] * H * p.I, h0, h1 - h0, p.I)) return false;
-        continue;
       }
-      // every routed expert's down rows
+      return true;
+    }
+    // several tokens: row chunks of kOutRows, each expert's rows accumulated
+    // in shared memory in expert order
+    for (int h0 = a0; h0 < a1; h0 += kOutRows) {
+      const int h1 = min(a1, h0 + kOutRows);
+      const int fin = FL_CLAST | (h1 == a1 ? FL_LAST : 0);
       for (int a = 0; a < n_act; a++) {
         const int e = S.rt.act[a];
         const int cnt = S.rt.off[a + 1] - S.rt.off[a];
@@ -518,6 +529,7 @@ struct Prod {
         case OP_ATTN: ok = do_attn(); break;
         case OP_UP: ok = do_up(a0, a1); break;
         case OP_OUT: ok = do_out(a0, a1); break;
+        case OP_DOWN: ok = do_down(a0, a1); break;
         default:
           if (lane == 0) report(p, DEV_BAD_OP, ti, op, -1, 0, 0);
           ok = false;
@@ -615,6 +627,28 @@ struct Cons {
     return true;
   }
 
+  // the task's last chunk is done: bump its phase counter (P1 shares that
+  // hold router rows also bump the router counter)
+  __device__ __forceinline__ bool complete() {
+    const int op = t[R_OP], l = t[R_LAYER];
+    int bar = -1;
+    if (op == OP_P1) bar = p.bl.p1;
+    else if (op == OP_UP) bar = p.bl.up;
+    else if (op == OP_OUT || op == OP_DOWN) bar = p.bl.out;
+    if (bar < 0) return csync();
+    if (!csync()) return false;
+    if (tid == 0) {
+      __threadfence();
+      if (op == OP_P1) {
+        const int a0 = p.tasks[(size_t)t[R_TASK] * kDescWords + F_A0];
+        const int a1 = p.tasks[(size_t)t[R_TASK] * kDescWords + F_A1];
+        if (a1 > a0 && a0 < p.E) atomicAdd(p.bars + bar_index(p, l, p.bl.rtr), 1u);
+      }
+      atomicAdd(p.bars + bar_index(p, l, bar), 1u);
+    }
+    return true;
+  }
+
   __device__ __forceinline__ bool stage_full(uint32_t& slot) {
     slot = stage_seq % kStages;
     const unsigned long long w0 = (tid == 0 && p.trace) ? gtime_ns() : 0ull;
@@ -649,10 +683,22 @@ struct Cons {
     }
   }
 
+  // OUT and DOWN tasks of a layer: the next layer's residual is complete
+  __device__ __forceinline__ int out_target() const { return p.n_sm + p.n_down_sms; }
+
+  // residual update of layer l, token n, float4 i4: O-proj + experts
+  __device__ __forceinline__ float4 delta4(int l, int n, int i4) const {
+    const size_t at = ((size_t)l * p.Bmax + n) * p.H;
+    const float4 o = __ldcg((const float4*)(p.oproj + at) + i4);
+    const float4 m = __ldcg((const float4*)(p.moe + at) + i4);
+    return make_float4(o.x + m.x, o.y + m.y, o.z + m.z, o.w + m.w);
+  }
+
   // ------------------------------------------------------------ RMSNorm
-  // h_l = h_{l-1} + delta_{l-1} (the embedding row at l = 0), this SM's own
-  // copy; x_l = h_l / sqrt(mean(h_l^2) + eps) * gain.  Thread t owns columns
-  // 4 t + 1024 i.  SM 0 also keeps every layer's h and x for inspection.
+  // h_l = h_{l-1} + (oproj_{l-1} + moe_{l-1}) (the embedding row at l = 0),
+  // this SM's own copy; x_l = h_l / sqrt(mean(h_l^2) + eps) * gain.  Thread t
+  // owns columns 4 t + 1024 i.  SM 0 also keeps every layer's h and x for
+  // inspection.
   // one token: every load (own residual copy, the previous layer's update,
   // the gain) issued together, each thread sums the eight warp partials
   // itself (same order in every thread), x goes to the staging buffer
@@ -681,17 +727,22 @@ struct Cons {
       }
     }
     if (l > 0) {
-      if (!wait_counter(bar_index(p, l - 1, p.bl.out), p.n_sm + t[R_BUMP])) return false;
-      const float4* dl = (const float4*)(p.delta + (size_t)(l - 1) * Bm * H);
-      float4 d[NI];
+      if (!wait_counter(bar_index(p, l - 1, p.bl.out), out_target() + t[R_BUMP])) return false;
+      const float4* ol = (const float4*)(p.oproj + (size_t)(l - 1) * Bm * H);
+      const float4* ml = (const float4*)(p.moe + (size_t)(l - 1) * Bm * H);
+      float4 o[NI], m[NI];
 #pragma unroll
       for (int k = 0; k < NI; k++) {
         const int i4 = tid + 256 * k;
-        d[k] = i4 < H4 ? __ldcg(dl + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        o[k] = i4 < H4 ? __ldcg(ol + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        m[k] = i4 < H4 ? __ldcg(ml + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int k = 0; k < NI; k++) {
-        h[k].x += d[k].x; h[k].y += d[k].y; h[k].z += d[k].z; h[k].w += d[k].w;
+        h[k].x += o[k].x + m[k].x;
+        h[k].y += o[k].y + m[k].y;
+        h[k].z += o[k].z + m[k].z;
+        h[k].w += o[k].w + m[k].w;
       }
     }
     const bool keep = blockIdx.x == 0;
@@ -731,7 +782,7 @@ struct Cons {
     if (p.B == 1) return norm1(l, final_norm);
     const int H = p.H, B = p.B, H4 = H / 4;
     const size_t Bm = (size_t)p.Bmax;
-    if (l > 0 && !wait_counter(bar_index(p, l - 1, p.bl.out), p.n_sm + t[R_BUMP])) return false;
+    if (l > 0 && !wait_counter(bar_index(p, l - 1, p.bl.out), out_target() + t[R_BUMP])) return false;
     float* hl = p.hloc + (size_t)blockIdx.x * Bm * H;
     float* xl = p.xloc + (size_t)blockIdx.x * Bm * H;
     const bool keep = blockIdx.x == 0;
@@ -750,7 +801,7 @@ struct Cons {
             h[k] = make_float4(bf16lo(e.x), bf16hi(e.x), bf16lo(e.y), bf16hi(e.y));
           } else {
             const float4 a = __ldcg((const float4*)(hl + n * H) + i4);
-            const float4 d = __ldcg((const float4*)(p.delta + ((size_t)(l - 1) * Bm + n) * H) + i4);
+            const float4 d = delta4(l - 1, n, i4);
             h[k] = make_float4(a.x + d.x, a.y + d.y, a.z + d.z, a.w + d.w);
           }
         }
@@ -794,7 +845,7 @@ struct Cons {
           h = *(const float4*)&S.xs[i4 * 4];
         } else if (final_norm) {
           const float4 a = __ldcg((const float4*)(hl + n * H) + i4);
-          const float4 d = __ldcg((const float4*)(p.delta + ((size_t)(l - 1) * Bm + n) * H) + i4);
+          const float4 d = delta4(l - 1, n, i4);
           h = make_float4(a.x + d.x, a.y + d.y, a.z + d.z, a.w + d.w);
         } else {
           h = __ldcg((const float4*)(hl + n * H) + i4);
@@ -1082,12 +1133,10 @@ struct Cons {
         break;
       }
       case K_OPROJ:
-        for (int i = tid; i < nr; i += 256) {
-          S.acc_o[t[R_REL0] + i][0] = res[i];
-          S.acc_m[t[R_REL0] + i][0] = 0.f;
-        }
+        for (int i = tid; i < nr; i += 256) __stcg(p.oproj + (size_t)l * Bm * p.H + row0 + i, res[i]);
         break;
       case K_DOWNALL: {
+        // the routed experts' rows weighted by the routing, in expert order
         const int na = t[R_NGRP];
         for (int i = tid; i < nr; i += 256) {
           float m = 0.f;
@@ -1095,7 +1144,7 @@ struct Cons {
             const int j = S.rt.ent[S.rt.off[a]] % p.topk;
             m += S.rt.w[0][j] * res[a * nr + i];
           }
-          S.acc_m[i][0] += m;
+          __stcg(p.moe + (size_t)l * Bm * p.H + row0 + i, m);
         }
         break;
       }
@@ -1138,8 +1187,7 @@ struct Cons {
           break;
         }
         case K_OPROJ:
-          S.acc_o[t[R_REL0] + r][n] = v;
-          S.acc_m[t[R_REL0] + r][n] = 0.f;
+          __stcg(p.oproj + ((size_t)l * Bm + n) * p.H + row0 + r, v);
           break;
         default: {   // K_DOWN: weighted by the token's routing weight
           const int ent = S.rt.ent[S.rt.off[t[R_A]] + n];
@@ -1151,17 +1199,15 @@ struct Cons {
     }
   }
 
-  // OUT row chunk done: residual update = O-proj + weighted experts, rows [h0, h0 + n)
-  __device__ __forceinline__ void out_write(int h0, int n) {
+  // DOWN row chunk done: the weighted experts' sum of rows [h0, h0 + n) of
+  // every token; the accumulators are cleared for the next row chunk
+  __device__ __forceinline__ void moe_write(int h0, int n) {
     const int l = t[R_LAYER];
     const size_t Bm = (size_t)p.Bmax;
     for (int i = tid; i < n * p.B; i += 256) {
       const int b = i / n, r = i % n;
-      const float o = S.acc_o[r][b], m = S.acc_m[r][b];
-      const size_t at = ((size_t)l * Bm + b) * p.H + h0 + r;
-      __stcg(p.oproj + at, o);
-      __stcg(p.moe + at, m);
-      __stcg(p.delta + at, o + m);
+      __stcg(p.moe + ((size_t)l * Bm + b) * p.H + h0 + r, S.acc_m[r][b]);
+      S.acc_m[r][b] = 0.f;
     }
   }
 
@@ -1173,7 +1219,7 @@ struct Cons {
     const int l = t[R_LAYER];
     const int E = p.E, K = p.topk, B = p.B;
     const size_t Bm = (size_t)p.Bmax;
-    if (!wait_counter(bar_index(p, l, p.bl.p1), p.n_sm)) return false;
+    if (!wait_counter(bar_index(p, l, p.bl.rtr), p.n_rtr_sms)) return false;
     RouteTab& rt = S.rt;
     for (int n = warp; n < B; n += kConsumerWarps) {
       float v[8];
@@ -1221,7 +1267,7 @@ struct Cons {
         for (int j = 0; j < K; j++) {
           const float w = expf(rt.w[n][j] - top) / den;
           rt.w[n][j] = w;
-          if (blockIdx.x == 0) {
+          if (blockIdx.x == p.n_sm - 1) {   // an SM of the expert branch
             p.ridx[((size_t)l * Bm + n) * K + j] = rt.idx[n][j];
             p.rw[((size_t)l * Bm + n) * K + j] = w;
           }
@@ -1620,22 +1666,16 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
     if (c.lane == 0) S.cchunk[c.warp]++;
   }
   if (ok && (flags & FL_CLAST)) {
-    // the last block of an OUT row chunk: write the residual update
+    // the last block of a DOWN row chunk: write the experts' sum
     ok = c.csync();
     if (ok) {
       const int a0 = p.tasks[(size_t)t[R_TASK] * kDescWords + F_A0];
       const int a1 = p.tasks[(size_t)t[R_TASK] * kDescWords + F_A1];
       const int h0 = a0 + ((t[R_ROW0] - a0) / kOutRows) * kOutRows;
-      c.out_write(h0, min(kOutRows, a1 - h0));
+      c.moe_write(h0, min(kOutRows, a1 - h0));
     }
   }
-  if (ok && (flags & FL_LAST)) {
-    int bar = -1;
-    if (op == OP_P1) bar = p.bl.p1;
-    else if (op == OP_UP) bar = p.bl.up;
-    else if (op == OP_OUT) bar = p.bl.out;
-    ok = bar >= 0 ? c.signal(bar_index(p, l, bar), 1) : c.csync();
-  }
+  if (ok && (flags & FL_LAST)) ok = c.complete();
   c.save();
   return ok;
 }
@@ -1664,22 +1704,7 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
     if (c.tid == 0) S.t_mark[2] = gtime_ns();
     if (c.lane == 0) S.cchunk[c.warp]++;
   }
-  if (ok && (flags & FL_CLAST)) {
-    ok = c.csync();
-    if (ok) {
-      const int a0 = p.tasks[(size_t)t[R_TASK] * kDescWords + F_A0];
-      const int a1 = p.tasks[(size_t)t[R_TASK] * kDescWords + F_A1];
-      const int h0 = a0 + ((t[R_ROW0] - a0) / kOutRows) * kOutRows;
-      c.out_write(h0, min(kOutRows, a1 - h0));
-    }
-  }
-  if (ok && (flags & FL_LAST)) {
-    int bar = -1;
-    if (op == OP_P1) bar = p.bl.p1;
-    else if (op == OP_UP) bar = p.bl.up;
-    else if (op == OP_OUT) bar = p.bl.out;
-    ok = bar >= 0 ? c.signal(bar_index(p, l, bar), 1) : c.csync();
-  }
+  if (ok && (flags & FL_LAST)) ok = c.complete();
   c.save();
   return ok;
 }
@@ -1745,6 +1770,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
     switch (op) {
       case OP_P1:
       case OP_UP:
+      case OP_DOWN:
       case OP_OUT:
       case OP_FINAL: {
         const int nt = t[R_NT];
@@ -1805,6 +1831,8 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
     }
     mbar_init(&S.cbar, kConsumerWarps);
     mbar_init(&S.route_bar, 1);
+    for (int r = 0; r < kOutRows; r++)
+      for (int b = 0; b < kMaxBatch; b++) S.acc_m[r][b] = 0.f;
     for (int w = 0; w < kConsumerWarps; w++) {
       S.cstage[w] = S.cphase[w] = S.cchunk[w] = 0;
       S.seen_bar[w] = -1;

@@ -15,9 +15,11 @@
 //   ATTN    its split-KV attention items (pages of one sequence, all KV heads)
 //   UP      its share of the routed experts' (gate, up) row pairs
 //   COMBINE its (sequence, query head) merges of the split-KV partials
-//   OUT     its hidden rows: O-proj plus every routed expert's down rows,
-//           summed into the residual update of the layer
-// and after the last layer FINAL: local final norm and its LM-head rows.
+//   DOWN    its hidden rows of every routed expert's down projection, weighted
+//           by the routing: the expert branch's share of the residual update
+//   OUT     its hidden rows of the O-proj: the attention branch's share
+// and after the last layer FINAL: local final norm and its LM-head rows.  The
+// next layer adds both shares to the residual.
 #pragma once
 #include <stdint.h>
 
@@ -39,15 +41,16 @@ enum Op : int32_t {
   OP_UP = 4,
   OP_COMBINE = 5,
   OP_OUT = 6,
-  OP_FINAL = 7
+  OP_FINAL = 7,
+  OP_DOWN = 8
 };
 
 // descriptor words (host-built, read by the producer warp)
 enum : int {
   F_OP = 0, F_LAYER = 1,
   F_A0 = 2, F_A1 = 3,      // op-specific range: P1 rows of [W_router; W_qkv], COMBINE
-                           // units, OUT hidden rows, FINAL vocabulary rows; UP: slice
-                           // index and slice count
+                           // units, OUT and DOWN hidden rows, FINAL vocabulary rows;
+                           // UP: slice index and slice count
   F_SEQ = 4,               // position in the SM's list (error reports)
   F_BUMP = 5               // P1 / FINAL: added to the wait target (testing aid)
 };
@@ -72,7 +75,7 @@ constexpr int kMaxBatch = 16;
 constexpr int kTraceWords = 16;         // words per timeline record
 constexpr int kPartFloats = 2048;       // one of the two GEMV partial-sum buffers
 constexpr int kTokPass = 8;             // tokens per GEMV pass (activations in registers)
-constexpr int kOutRows = 32;            // hidden rows per OUT chunk
+constexpr int kOutRows = 32;            // hidden rows per DOWN chunk (several tokens)
 constexpr int kMaxActive = 128;         // routed experts of one step (B * k <= 128)
 
 // whole rows of a [rows][K] BF16 matrix that one stage carries
@@ -95,9 +98,10 @@ MK_HD inline int gemv_chunk_rows(int K, int nt) {
 struct BarLayout {
   int per_layer;
   int p1;      // P1 tasks done                                   (target n_sm)
-  int up;      // UP tasks done                                   (target n_sm)
-  int comb;    // COMBINE tasks done                              (target n_sm)
-  int out;     // OUT tasks done                                  (target n_sm)
+  int up;      // UP tasks done                                   (target n_up_sms)
+  int comb;    // COMBINE tasks done                              (target n_comb_sms)
+  int out;     // OUT and DOWN tasks done                         (target n_sm + n_down_sms)
+  int rtr;     // P1 tasks holding router rows done               (target n_rtr_sms)
   int items;   // + b: split-KV items of sequence b done          (target: its split count)
 };
 
@@ -107,8 +111,9 @@ inline BarLayout bar_layout(int max_batch) {
   b.up = 1;
   b.comb = 2;
   b.out = 3;
-  b.items = 4;
-  b.per_layer = (4 + max_batch + 31) & ~31;
+  b.rtr = 4;
+  b.items = 5;
+  b.per_layer = (5 + max_batch + 31) & ~31;
   return b;
 }
 
@@ -125,6 +130,7 @@ struct Params {
   int L, H, hq, hkv, d, E, topk, I, V, P, grp, qkv_rows;
   int max_pages, num_pages, Bmax, n_sm;
   int n_comb_sms, n_up_sms;    // SMs that signal the COMBINE / UP counters of a layer
+  int n_down_sms, n_rtr_sms;   // SMs with a DOWN task / with router rows in their P1 share
   float rms_eps, attn_scale_log2;
   // caller weights (device pointers; per-layer arrays are device arrays of L pointers)
   const uint16_t* embed;
@@ -177,7 +183,6 @@ struct Params {
   float* abuf;       // [L][Bmax * k][I] expert hidden, by grouped slot
   float* oproj;      // [L][Bmax][H] O-proj output
   float* moe;        // [L][Bmax][H] weighted sum of the routed experts' outputs
-  float* delta;      // [L][Bmax][H] oproj + moe: the layer's residual update
 };
 
 }  // namespace mk

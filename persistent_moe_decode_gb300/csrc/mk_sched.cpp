@@ -8,9 +8,9 @@
 // An SM's list holds one task per wave and layer; the shares whose size
 // depends on routing (the experts' rows) are fixed as "slice s of n" and
 // resolved on the device once the routing is known.  Any order of the waves
-// in which ROUTE precedes UP and ATTN precedes COMBINE precedes OUT has no
-// circular wait (every wait points at an earlier wave of the same layer, or
-// at the previous layer).
+// in which ROUTE precedes UP precedes DOWN and ATTN precedes COMBINE precedes
+// OUT has no circular wait (every wait points at an earlier wave of the same
+// layer, or at the previous layer).
 #include "mk_sched.h"
 
 #include <algorithm>
@@ -80,8 +80,8 @@ int attention_sms(const mk_config& c, int n_sm, int batch, const int32_t* seq_le
   for (int b = 0; b < batch; b++) kv += (double)(seq_lens[b] + 1);
   kv *= 2.0 * c.n_kv_heads * c.head_dim * 2.0;
   const double experts = (double)std::min(c.n_experts, batch * c.top_k);
-  const double up = experts * 2.0 * c.moe_inter * c.hidden * 2.0;
-  int na = (int)(n_sm * kv / (kv + up) + 0.5);
+  const double moe = experts * 3.0 * c.moe_inter * c.hidden * 2.0;   // gate, up and down
+  int na = (int)(n_sm * kv / (kv + moe) + 0.5);
   return std::max(1, std::min(n_sm - 1, na));
 }
 
@@ -96,15 +96,16 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
   const bool roles = n_attn < n_sm;
   const int nmoe = roles ? n_sm - n_attn : moe_sms(c, n_sm);
   const int ncomb = roles ? n_attn : n_sm;
+  const int ndown = roles ? n_sm - n_attn : n_sm;
 
-  static const int orders[3][6] = {
-      {OP_P1, OP_ROUTE, OP_ATTN, OP_UP, OP_COMBINE, OP_OUT},
-      {OP_P1, OP_ROUTE, OP_ATTN, OP_COMBINE, OP_UP, OP_OUT},
-      {OP_P1, OP_ROUTE, OP_UP, OP_ATTN, OP_COMBINE, OP_OUT}};
-  // attention SMs route between their items and the combine: the routing
-  // only needs P1 (long done) and fills the wait for the other items
-  static const int attn_role[5] = {OP_P1, OP_ATTN, OP_ROUTE, OP_COMBINE, OP_OUT};
-  static const int moe_role[4] = {OP_P1, OP_ROUTE, OP_UP, OP_OUT};
+  static const int orders[3][7] = {
+      {OP_P1, OP_ROUTE, OP_ATTN, OP_UP, OP_COMBINE, OP_DOWN, OP_OUT},
+      {OP_P1, OP_ROUTE, OP_ATTN, OP_COMBINE, OP_UP, OP_DOWN, OP_OUT},
+      {OP_P1, OP_ROUTE, OP_UP, OP_ATTN, OP_DOWN, OP_COMBINE, OP_OUT}};
+  // the attention branch needs no routing; the expert branch's down rows
+  // only wait for its own UP wave, so they run while attention is under way
+  static const int attn_role[4] = {OP_P1, OP_ATTN, OP_COMBINE, OP_OUT};
+  static const int moe_role[5] = {OP_P1, OP_ROUTE, OP_UP, OP_DOWN, OP_OUT};
 
   out->tasks.clear();
   out->off.assign(n_sm + 1, 0);
@@ -114,13 +115,13 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
     int nops;
     if (!roles) {
       ops = orders[c.wave_order];
-      nops = 6;
+      nops = 7;
     } else if (s < n_attn) {
       ops = attn_role;
-      nops = 5;
+      nops = 4;
     } else {
       ops = moe_role;
-      nops = 4;
+      nops = 5;
     }
     std::vector<Desc> list;
     for (int l = 0; l < L; l++) {
@@ -131,6 +132,11 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
           case OP_P1: share(rows1, n_sm, s, &lo, &hi); break;
           case OP_COMBINE: share(units, ncomb, s, &lo, &hi); break;
           case OP_OUT: share(c.hidden, n_sm, s, &lo, &hi); break;
+          case OP_DOWN: {
+            const int slice = roles ? s - n_attn : s;
+            share(c.hidden, ndown, slice, &lo, &hi);
+            break;
+          }
           case OP_UP: {
             const int slice = roles ? s - n_attn : s;
             lo = slice < nmoe ? slice : -1;
@@ -160,6 +166,15 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
   out->n_bars = L * bl.per_layer;
   out->n_comb_sms = ncomb;
   out->n_up_sms = roles ? nmoe : n_sm;
+  out->n_down_sms = ndown;
+  // P1 shares that hold router rows [0, E): SMs 0 .. the one holding row E - 1
+  int nr = 0;
+  for (int s = 0; s < n_sm; s++) {
+    int lo, hi;
+    share(rows1, n_sm, s, &lo, &hi);
+    if (hi > lo && lo < c.n_experts) nr++;
+  }
+  out->n_rtr_sms = nr;
   return MK_OK;
 }
 

@@ -15,6 +15,8 @@ struct Plan {
   int n_bars = 0;               // counter words the step uses (layers 0..L-1)
   int n_comb_sms = 0;           // SMs with a COMBINE task per layer
   int n_up_sms = 0;             // SMs with an UP task per layer
+  int n_down_sms = 0;           // SMs with a DOWN task per layer
+  int n_rtr_sms = 0;            // SMs whose P1 share holds router rows
 };
 
 // Checks everything the kernel relies on; returns MK_OK or MK_ERR_BAD_CONFIG.
@@ -23,9 +25,10 @@ int validate_config(const mk_config& c);
 // Per-SM task lists of one step for `batch` sequences: for every layer one
 // task of each phase per SM, then the FINAL task.  With n_attn < n_sm the SMs
 // take roles: SMs [0, n_attn) run the attention branch of the parallel layer
-// (P1, ATTN, ROUTE, COMBINE, OUT), the others the expert branch (P1, ROUTE,
-// UP, OUT), so the two branches run side by side; with n_attn == n_sm every
-// SM runs every phase in the configured wave order.  `bump_layer` / `bump`
+// (P1, ATTN, COMBINE, OUT), the others the expert branch (P1, ROUTE, UP,
+// DOWN, OUT), so the two branches run side by side and only the O-proj (OUT,
+// on every SM) follows the attention; with n_attn == n_sm every SM runs every
+// phase in the configured wave order.  `bump_layer` / `bump`
 // make the P1 task of that layer wait for a counter value that is never
 // reached (testing aid for the timeout path).
 int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, int bump_layer = -1,
@@ -44,8 +47,8 @@ inline int moe_sms(const mk_config& c, int n_sm) {
 
 // Attention SMs of a step: config.n_attn_claimers if set, else a share of the
 // SMs proportional to the attention's KV bytes against the routed experts'
-// gate/up bytes of a layer (the two branches that run side by side).  n_sm
-// means no roles.
+// gate/up/down bytes of a layer (the two branches that run side by side).
+// n_sm means no roles.
 int attention_sms(const mk_config& c, int n_sm, int batch, const int32_t* seq_lens);
 
 // Split-KV items of one step: each sequence's keys cut into page ranges,
