@@ -6,6 +6,8 @@
 // the counters are zeroed (clear_scratch_and_barriers), the split-KV schedule
 // follows the live contexts (select_schedule(max_live_context)) and the
 // persistent kernel is launched (launch_megakernel).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -112,6 +114,56 @@ int upload_ptrs(mk_handle* h, const void* const* src, int L, const void* const**
   if (rc) return rc;
   if (cudaMemcpy(d, src, sizeof(void*) * L, cudaMemcpyHostToDevice) != cudaSuccess) return MK_ERR_CUDA;
   *dst = (const void* const*)d;
+  return MK_OK;
+}
+
+// cuTensorMapEncodeTiled from the driver (through the runtime's entry-point
+// lookup, so the library needs no link against libcuda)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// tensor maps of every layer's K and V pool: 2-D [pages * hkv * page_size][d]
+// BF16, boxes of 64 dims x (hkv * page_size) rows (one page of every KV head,
+// half or all of its dims), 128-byte swizzle
+int make_kv_maps(mk_handle* h, const mk_weights* w, const uint8_t** out) {
+  static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
+  const mk_config& c = h->cfg;
+  const int L = c.n_layers;
+  auto enc = tensor_map_encoder();
+  if (!enc) return MK_ERR_CUDA;
+  std::vector<CUtensorMap> maps((size_t)2 * L);
+  const cuuint64_t dims[2] = {(cuuint64_t)c.head_dim,
+                              (cuuint64_t)c.num_kv_pages * c.n_kv_heads * c.page_size};
+  const cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)(c.n_kv_heads * c.page_size)};
+  const cuuint32_t es[2] = {1, 1};
+  if (dims[1] >= (1ull << 32)) return MK_ERR_BAD_CONFIG;
+  for (int l = 0; l < L; l++)
+    for (int kv = 0; kv < 2; kv++) {
+      void* base = kv ? w->v_pool[l] : w->k_pool[l];
+      if (enc(&maps[(size_t)2 * l + kv], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MK_ERR_BAD_ARG;
+    }
+  uint8_t* d = nullptr;
+  int rc = dalloc(h, &d, maps.size() * sizeof(CUtensorMap));
+  if (rc) return rc;
+  if (cudaMemcpy(d, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess)
+    return MK_ERR_CUDA;
+  *out = d;
   return MK_OK;
 }
 
@@ -264,6 +316,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
   TRY(upload_ptrs(h, (const void* const*)w->w_down, L, (const void* const**)&p.w_down));
   TRY(upload_ptrs(h, (const void* const*)w->k_pool, L, (const void* const**)&p.k_pool));
   TRY(upload_ptrs(h, (const void* const*)w->v_pool, L, (const void* const**)&p.v_pool));
+  TRY(make_kv_maps(h, w, &p.kv_maps));
 
   const size_t Ls = (size_t)L, Bs = (size_t)Bm, Ns = (size_t)h->n_sm;
   p.max_attn_items = c.max_attn_items;

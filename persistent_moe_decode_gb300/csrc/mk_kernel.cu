@@ -69,9 +69,6 @@ struct __align__(128) Smem {
   float red[2 * kPartFloats];               // GEMV partial sums (two buffers) / attention
                                             // query fragments and merge / combine sums
   float acc_m[kOutRows][kMaxBatch];         // DOWN row chunk (several tokens): weighted expert outputs
-  float pbuf[kConsumerWarps][16][8];        // attention probabilities of one page per warp
-  float alpha[kConsumerWarps][8];           // attention rescale per head per warp
-  float wstat[kConsumerWarps][8][2];        // attention (max, sum) per warp per head
   float nred[kConsumerWarps][kMaxBatch];    // norm / combine reductions
   float rinv[kMaxBatch];
   RouteTab rt;
@@ -92,7 +89,10 @@ struct __align__(128) Smem {
   unsigned long long t_swait;               // timeline: time warp 0 waited for stages
   volatile int32_t abort_flag;
 };
-static_assert(sizeof(Smem) <= 232448, "shared memory of one block exceeds the sm_103a limit");
+// the dynamic shared memory is rounded up to a 1024-byte boundary (the
+// swizzled tensor copies of KV pages need it), hence the extra 1 KB
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory of one block exceeds the sm_103a limit");
 
 // resolved task words (written by the producer into the task ring)
 enum : int {
@@ -259,13 +259,15 @@ struct Prod {
     return true;
   }
 
-  // pages [pg0, pg0 + npages) of sequence b, all KV heads: K pages then V pages
+  // pages [pg0, pg0 + npages) of sequence b, all KV heads: K pages then V
+  // pages, each as d / 64 swizzled boxes of (hkv * P rows) x 128 bytes
   __device__ __noinline__ bool stream_attn(int b, int pg0, int npages) {
     const int pb = attn_page_bytes(p);
     const int pps = attn_pps(p);
-    const uint16_t* kp = p.k_pool[l];
-    const uint16_t* vp = p.v_pool[l];
-    const size_t page_elems = (size_t)p.hkv * p.P * p.d;
+    const int rows = p.hkv * p.P;
+    const int nbox = p.d / 64;
+    const uint8_t* km = p.kv_maps + (size_t)l * 2 * 128;
+    const uint8_t* vm = km + 128;
     for (int st = 0; st * pps < npages; st++) {
       const int n = min(pps, npages - st * pps);
       int pg = -1;
@@ -279,11 +281,11 @@ struct Prod {
       if (!acquire_stage(slot)) return false;
       if (lane == 0) mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(2 * n * pb));
       __syncwarp();
-      if (lane < n) {
-        bulk_g2s(&S.stage[slot][lane * pb], kp + (size_t)pg * page_elems, (uint32_t)pb, &S.full[slot]);
-      } else if (lane < 2 * n) {
-        bulk_g2s(&S.stage[slot][(pps + lane - n) * pb], vp + (size_t)pg * page_elems, (uint32_t)pb,
-                 &S.full[slot]);
+      if (lane < 2 * n) {
+        const bool is_k = lane < n;
+        uint8_t* dst = &S.stage[slot][(is_k ? lane : pps + lane - n) * pb];
+        for (int bx = 0; bx < nbox; bx++)
+          tma_load_2d(dst + bx * rows * 128, is_k ? km : vm, bx * 64, pg * rows, &S.full[slot]);
       }
       stage_seq++;
     }
@@ -1336,32 +1338,43 @@ struct Cons {
   }
 
   // -------------------------------------------------------- attention
-  // One split-KV item: sequence b, keys [tt0, tt1), every KV head.  The NWG =
-  // 8 / hkv warps of KV group g = w % hkv all score every page of the item and
-  // each accumulates its own DW = d / NWG head dims (NT = DW / 8 tiles of 8).
-  // Both products run on the tensor cores (m16n8k16, BF16 in, fp32 out) with
-  // the group's query heads as the 16-row A operand (8 used):
-  //   S[head][token] = Q K^T  with Q, K fragments read as 16-byte chunks (the
-  //   same permutation of the contraction index on both operands),
-  //   O[head][dim] += P V     where the score accumulators already have the A
-  //   fragment layout of P, and V comes from ldmatrix.trans.
+  // byte offset of 16-byte chunk c (dims 8c .. 8c + 7) of row r in a page
+  // image of `rows` rows stored as 128-byte swizzled boxes of 64 dims
+  __device__ __forceinline__ static int kv_off(int r, int c, int rows) {
+    return (c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+  }
+
+  // One split-KV item: sequence b, keys [tt0, tt1), every KV head.  Warp w
+  // serves KV group g = w % hkv and takes every NWG-th page of the item (NWG =
+  // 8 / hkv warps per group), keeping its own online-softmax state; the NWG
+  // states of a group are merged at the end.  Both products run on the tensor
+  // cores (m16n8k16, BF16 in, fp32 out) with the page's 16 tokens as the M
+  // side and the group's (up to 8) query heads as N, so no row is padding:
+  //   S^T[token][head] = K Q^T:  A = the K rows (ldmatrix), B = Q^T held in
+  //                              registers for the whole item;
+  //   O^T[dim][head] += V^T P^T: A = V^T (ldmatrix.trans of the V rows),
+  //                              B = P^T, the score accumulators converted to
+  //                              BF16 and transposed in registers (movmatrix).
   // The fp32 query and probabilities are split into BF16 high + low halves
-  // (two products each), so the contraction keeps about 16 bits of their
-  // mantissa.  Online softmax per head in fp32 (log2 domain) with a per-lane
-  // rescale.  The query (RoPE applied here) is staged in shared memory once
-  // per item, 16-byte chunks swizzled by row.
-  template <int D, int NT>
+  // (two products each), so the contractions keep about 16 bits of their
+  // mantissa.  Softmax per head in fp32 (log2 domain): the running maximum is
+  // shared by the lanes of a head, the running sum is kept per lane and added
+  // up at the end.  The query (RoPE applied here) is staged in shared memory
+  // once per item, 16-byte chunks swizzled by row.  The KV pages arrive as
+  // 128-byte swizzled boxes (kv_off): the eight rows an ldmatrix reads fall in
+  // distinct banks.
+  template <int D>
   __device__ __forceinline__ bool attn() {
+    constexpr int KS = D / 16;            // QK k-steps = PV m-tiles
     const int hkv = p.hkv, grp = p.grp, P = p.P, hq = p.hq;
     const int NWG = kConsumerWarps / hkv;
     const int g = warp % hkv, jw = warp / hkv;
     const int l = t[R_LAYER], b = t[R_B];
     const int tt0 = t[R_TT0], tt1 = t[R_TT1], pos = t[R_POS];
     const size_t Bm = (size_t)p.Bmax;
-    const int hb = P * D * 2;             // bytes of one head's 16-token page
-    const int pb = hkv * hb;              // bytes of one page, all heads
+    const int pb = hkv * P * D * 2;       // bytes of one page, all heads
+    const int rows = hkv * P;             // rows of a page image (head-major)
     const int pps = attn_pps(p);
-    (void)NWG;
     if (!wait_counter(bar_index(p, l, p.bl.p1), p.n_sm)) return false;
 
     // query with RoPE -> BF16 hi / lo planes: [head][D] in 16-byte chunks, chunk c
@@ -1406,27 +1419,33 @@ struct Cons {
     }
     if (!csync()) return false;
 
-    // this lane's query head (A row gl) as fragments for the whole item
-    const bool qon = gl < grp;
+    // B fragments of Q^T (k = dims, n = heads) for the whole item: lane (gl, cq)
+    // holds head gl of the group, dims 16 s + 2 cq, +1 and 16 s + 8 + 2 cq, +1
     const int qrow = g * grp + gl;
-    uint4 qh[D / 32], ql[D / 32];
+    const bool qon = gl < grp;
+    uint32_t qbh[KS][2], qbl[KS][2];
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ch++) {
-      qh[ch] = make_uint4(0, 0, 0, 0);
-      ql[ch] = qh[ch];
-      if (qon) {
-        const int c = ch * 4 + cq;
-        const int off = qrow * D * 2 + ((c ^ (qrow & 7)) << 4);
-        qh[ch] = lds128(qhi + off);
-        ql[ch] = lds128(qlo + off);
+    for (int s = 0; s < KS; s++)
+#pragma unroll
+      for (int hf = 0; hf < 2; hf++) {
+        const int off = qrow * D * 2 + (((2 * s + hf) ^ (qrow & 7)) << 4) + 4 * cq;
+        qbh[s][hf] = qon ? *(const uint32_t*)(qhi + off) : 0u;
+        qbl[s][hf] = qon ? *(const uint32_t*)(qlo + off) : 0u;
       }
-    }
 
-    const int d0 = jw * (NT * 8);         // first head dim of this warp
-    float m_run = -INFINITY, l_run = 0.f;
-    float o[NT][4];
+    // this lane's softmax state: heads 2 cq, 2 cq + 1
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    // O^T accumulators: tile t, dims 16 t + gl (c0: head 2cq, c1: 2cq + 1) and
+    // 16 t + 8 + gl (c2, c3)
+    float o[KS][4];
 #pragma unroll
-    for (int j = 0; j < NT; j++) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    for (int s = 0; s < KS; s++) o[s][0] = o[s][1] = o[s][2] = o[s][3] = 0.f;
+
+    // ldmatrix rows of this lane: K (A of S^T): tile i = lane / 8 holds tokens
+    // (i & 1) * 8 + 0..7, dims chunk 2 s + (i >> 1); V (A of O^T, transposed):
+    // tokens (i >> 1) * 8 + 0..7, dims chunk 2 t + (i & 1)
+    const int kr = g * P + ((lane >> 3) & 1) * 8 + (lane & 7), kc = lane >> 4;
+    const int vr = g * P + (lane >> 4) * 8 + (lane & 7), vc = (lane >> 3) & 1;
 
     const int pg0 = tt0 / P;
     const int npages = (tt1 + P - 1) / P - pg0;
@@ -1439,109 +1458,98 @@ struct Cons {
       for (int qi = 0; qi < pps; qi++) {
         const int page = st * pps + qi;
         if (page >= npages) break;
-        uint8_t* kp = S.stage[slot] + qi * pb + g * hb;
-        uint8_t* vp = S.stage[slot] + (pps + qi) * pb + g * hb;
+        if (page % NWG != jw) continue;
+        uint8_t* kp = S.stage[slot] + qi * pb;
+        uint8_t* vp = S.stage[slot] + (pps + qi) * pb;
         const int tk0 = (pg0 + page) * P;
         const bool has_new = pos >= tk0 && pos < tk0 + P;
         // the new token's K (RoPE applied here) and V come from this step's QKV
-        // output.  Every warp of the group patches the whole row into the staged
-        // page before reading it (the values are identical); the first one also
-        // writes them to the cache.
+        // output: patched into the staged page (group g's row) before it is
+        // read, and written to the cache
         if (has_new) {
           const int row = pos - tk0;
-          const float* kr = qraw + (size_t)(hq + g) * D;
-          const float* vr = qraw + (size_t)(hq + hkv + g) * D;
+          const float* krw = qraw + (size_t)(hq + g) * D;
+          const float* vrw = qraw + (size_t)(hq + hkv + g) * D;
           const int pg = p.page_tables[(size_t)b * p.max_pages + pos / P];
-          uint16_t* kc = p.k_pool[l] + (((size_t)pg * hkv + g) * P + row) * D;
-          uint16_t* vc = p.v_pool[l] + (((size_t)pg * hkv + g) * P + row) * D;
+          uint16_t* kcache = p.k_pool[l] + (((size_t)pg * hkv + g) * P + row) * D;
+          uint16_t* vcache = p.v_pool[l] + (((size_t)pg * hkv + g) * P + row) * D;
+          const int r = g * P + row;
           for (int k = lane; k < D / 2; k += 32) {
-            const float x1 = __ldcg(kr + k), x2 = __ldcg(kr + k + D / 2);
+            const float x1 = __ldcg(krw + k), x2 = __ldcg(krw + k + D / 2);
             const float c = rope[k * 2], s = rope[k * 2 + 1];
             const uint16_t k1 = f2bf(x1 * c - x2 * s), k2 = f2bf(x2 * c + x1 * s);
-            const uint16_t v1 = f2bf(__ldcg(vr + k)), v2 = f2bf(__ldcg(vr + k + D / 2));
-            ((uint16_t*)(kp + row * D * 2))[k] = k1;
-            ((uint16_t*)(kp + row * D * 2))[k + D / 2] = k2;
-            ((uint16_t*)(vp + row * D * 2))[k] = v1;
-            ((uint16_t*)(vp + row * D * 2))[k + D / 2] = v2;
-            if (jw == 0) {
-              kc[k] = k1;
-              kc[k + D / 2] = k2;
-              vc[k] = v1;
-              vc[k + D / 2] = v2;
-            }
+            const uint16_t v1 = f2bf(__ldcg(vrw + k)), v2 = f2bf(__ldcg(vrw + k + D / 2));
+            const int o1 = kv_off(r, k >> 3, rows) + (k & 7) * 2;
+            const int o2 = kv_off(r, (k + D / 2) >> 3, rows) + (k & 7) * 2;
+            *(uint16_t*)(kp + o1) = k1;
+            *(uint16_t*)(kp + o2) = k2;
+            *(uint16_t*)(vp + o1) = v1;
+            *(uint16_t*)(vp + o2) = v2;
+            kcache[k] = k1;
+            kcache[k + D / 2] = k2;
+            vcache[k] = v1;
+            vcache[k + D / 2] = v2;
           }
           __syncwarp();
         }
-        // S = Q K^T: tile 0 = tokens 0..7 (K rows gl), tile 1 = tokens 8..15
-        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-          float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T = K Q^T, four independent accumulators (k-step parity x hi / lo)
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        float ta[4] = {0.f, 0.f, 0.f, 0.f}, tb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int ch = 0; ch < D / 32; ch++) {
-            const uint8_t* a = kp + gl * D * 2 + ch * 64 + cq * 16;
-            const uint4 k0 = lds128(a);
-            const uint4 k1 = lds128(a + 8 * D * 2);
-            mma_bf16(s0, qh[ch].x, 0u, qh[ch].y, 0u, k0.x, k0.y);
-            mma_bf16(s0, qh[ch].z, 0u, qh[ch].w, 0u, k0.z, k0.w);
-            mma_bf16(s1, qh[ch].x, 0u, qh[ch].y, 0u, k1.x, k1.y);
-            mma_bf16(s1, qh[ch].z, 0u, qh[ch].w, 0u, k1.z, k1.w);
-            mma_bf16(t0, ql[ch].x, 0u, ql[ch].y, 0u, k0.x, k0.y);
-            mma_bf16(t0, ql[ch].z, 0u, ql[ch].w, 0u, k0.z, k0.w);
-            mma_bf16(t1, ql[ch].x, 0u, ql[ch].y, 0u, k1.x, k1.y);
-            mma_bf16(t1, ql[ch].z, 0u, ql[ch].w, 0u, k1.z, k1.w);
+        for (int s = 0; s < KS; s++) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(a0, a1, a2, a3, kp + kv_off(kr, 2 * s + kc, rows));
+          if (s & 1) {
+            mma_bf16(sb, a0, a1, a2, a3, qbh[s][0], qbh[s][1]);
+            mma_bf16(tb, a0, a1, a2, a3, qbl[s][0], qbl[s][1]);
+          } else {
+            mma_bf16(sa, a0, a1, a2, a3, qbh[s][0], qbh[s][1]);
+            mma_bf16(ta, a0, a1, a2, a3, qbl[s][0], qbl[s][1]);
           }
-          s0[0] += t0[0]; s0[1] += t0[1];
-          s1[0] += t1[0]; s1[1] += t1[1];
         }
-        // this lane: head gl, tokens 2cq, 2cq + 1 (tile 0) and 8 + 2cq, 9 + 2cq (tile 1)
+        // this lane: tokens gl (v0: head 2cq, v1: 2cq + 1) and gl + 8 (v2, v3)
         const int lo_t = max(tt0 - tk0, 0), hi_t = min(tt1 - tk0, P);   // valid rows [lo_t, hi_t)
-        float sv[4];
+        const bool ok0 = gl >= lo_t && gl < hi_t, ok1 = gl + 8 >= lo_t && gl + 8 < hi_t;
+        const float v0 = ok0 ? ((sa[0] + ta[0]) + (sb[0] + tb[0])) * sc : -INFINITY;
+        const float v1 = ok0 ? ((sa[1] + ta[1]) + (sb[1] + tb[1])) * sc : -INFINITY;
+        const float v2 = ok1 ? ((sa[2] + ta[2]) + (sb[2] + tb[2])) * sc : -INFINITY;
+        const float v3 = ok1 ? ((sa[3] + ta[3]) + (sb[3] + tb[3])) * sc : -INFINITY;
+        // per head maximum over the page's 16 tokens (the 8 lanes of equal cq)
+        float x0 = fmaxf(v0, v2), x1 = fmaxf(v1, v3);
 #pragma unroll
-        for (int k = 0; k < 4; k++) {
-          const int tok = (k >> 1) * 8 + 2 * cq + (k & 1);
-          const float v = (k < 2 ? s0[k & 1] : s1[k & 1]) * sc;
-          sv[k] = (tok >= lo_t && tok < hi_t) ? v : -INFINITY;
+        for (int sh = 4; sh < 32; sh <<= 1) {
+          x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, sh));
+          x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, sh));
         }
-        float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mn = fmaxf(m_run, mx);
-        const float al = (mn == -INFINITY) ? 1.f : exp2f(m_run - mn);
-        float pv[4];
+        const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+        const float al0 = (n0 == -INFINITY) ? 1.f : exp2f(m0 - n0);
+        const float al1 = (n1 == -INFINITY) ? 1.f : exp2f(m1 - n1);
+        const float p0 = (n0 == -INFINITY) ? 0.f : exp2f(v0 - n0);
+        const float p1 = (n1 == -INFINITY) ? 0.f : exp2f(v1 - n1);
+        const float p2 = (n0 == -INFINITY) ? 0.f : exp2f(v2 - n0);
+        const float p3 = (n1 == -INFINITY) ? 0.f : exp2f(v3 - n1);
+        l0 = l0 * al0 + (p0 + p2);
+        l1 = l1 * al1 + (p1 + p3);
+        m0 = n0;
+        m1 = n1;
+        // P^T as the B operand: each 8 x 8 block [token][head] of the score
+        // accumulators, transposed to [head][token]; high and low halves
+        const uint32_t h01 = pack_bf2(p0, p1), h23 = pack_bf2(p2, p3);
+        const uint32_t e01 = pack_bf2(p0 - bf16lo(h01), p1 - bf16hi(h01));
+        const uint32_t e23 = pack_bf2(p2 - bf16lo(h23), p3 - bf16hi(h23));
+        const uint32_t bh0 = movm_trans(h01), bh1 = movm_trans(h23);
+        const uint32_t bl0 = movm_trans(e01), bl1 = movm_trans(e23);
+        // O^T += V^T P^T
 #pragma unroll
-        for (int k = 0; k < 4; k++) pv[k] = (mn == -INFINITY) ? 0.f : exp2f(sv[k] - mn);
-        float sm = (pv[0] + pv[1]) + (pv[2] + pv[3]);
-        sm += __shfl_xor_sync(0xffffffffu, sm, 1);
-        sm += __shfl_xor_sync(0xffffffffu, sm, 2);
-        l_run = l_run * al + sm;
-        m_run = mn;
-        // P as the A operand (rows gl: tokens 2cq.. of tile 0 and 8 + 2cq.. of tile 1)
-        uint32_t ph0, ph1, pl0, pl1;
-        {
-          const uint16_t h0 = f2bf(pv[0]), h1 = f2bf(pv[1]), h2 = f2bf(pv[2]), h3 = f2bf(pv[3]);
-          ph0 = (uint32_t)h0 | ((uint32_t)h1 << 16);
-          ph1 = (uint32_t)h2 | ((uint32_t)h3 << 16);
-          pl0 = (uint32_t)f2bf(pv[0] - bf16f(h0)) | ((uint32_t)f2bf(pv[1] - bf16f(h1)) << 16);
-          pl1 = (uint32_t)f2bf(pv[2] - bf16f(h2)) | ((uint32_t)f2bf(pv[3] - bf16f(h3)) << 16);
-        }
-        // O += P V over this warp's dims, two 8-dim tiles per ldmatrix
-        const uint8_t* vrow = vp + (size_t)((lane >> 3) & 1) * 8 * D * 2 + (lane & 7) * D * 2 +
-                              (size_t)(d0 + (lane >> 4) * 8) * 2;
-#pragma unroll
-        for (int j = 0; j < NT; j++) {
-          o[j][0] *= al;
-          o[j][1] *= al;
-        }
-#pragma unroll
-        for (int j = 0; j < NT; j += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_trans(b0, b1, b2, b3, vrow + j * 16);
-          mma_bf16(o[j], ph0, 0u, ph1, 0u, b0, b1);
-          mma_bf16(o[j], pl0, 0u, pl1, 0u, b0, b1);
-          if (j + 1 < NT) {
-            mma_bf16(o[j + 1], ph0, 0u, ph1, 0u, b2, b3);
-            mma_bf16(o[j + 1], pl0, 0u, pl1, 0u, b2, b3);
-          }
+        for (int s = 0; s < KS; s++) {
+          o[s][0] *= al0;
+          o[s][1] *= al1;
+          o[s][2] *= al0;
+          o[s][3] *= al1;
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(a0, a1, a2, a3, vp + kv_off(vr, 2 * s + vc, rows));
+          mma_bf16(o[s], a0, a1, a2, a3, bh0, bh1);
+          mma_bf16(o[s], a0, a1, a2, a3, bl0, bl1);
         }
         if (has_new) fence_proxy_async_smem();
         __syncwarp();
@@ -1550,16 +1558,76 @@ struct Cons {
     }
 
     if (tid == 0) S.t_mark[1] = gtime_ns();
-    // this warp's partials: head gl of group g, dims d0 + 8j + 2cq, +1; (max, sum) by warp jw = 0
-    const int item = t[R_ITEM];
-    if (qon) {
-      const size_t it = ((size_t)item * hkv + g) * grp + gl;
-      float* dst = p.attn_part + it * D + d0 + 2 * cq;
+    // running sums: add up the lanes of each head
 #pragma unroll
-      for (int j = 0; j < NT; j++) __stcg((float2*)(dst + j * 8), make_float2(o[j][0], o[j][1]));
-      if (jw == 0 && cq == 0) {
-        __stcg(p.attn_ml + it * 2 + 0, m_run);
-        __stcg(p.attn_ml + it * 2 + 1, l_run);
+    for (int sh = 4; sh < 32; sh <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
+    }
+    // merge the NWG warps of each group: in round r the warps jw == r put
+    // (max, sum, O) in shared memory and the warps jw == 0 fold them in
+    // (the staged query is no longer needed: its fragments are in registers)
+    float* mo = S.red;   // [hkv][D][8]
+    if (!csync()) return false;
+    for (int r = 1; r < NWG; r++) {
+      if (jw == r) {
+#pragma unroll
+        for (int s = 0; s < KS; s++) {
+          float* row0 = mo + ((size_t)g * D + 16 * s + gl) * 8 + 2 * cq;
+          float* row1 = row0 + 8 * 8;
+          *(float2*)row0 = make_float2(o[s][0], o[s][1]);
+          *(float2*)row1 = make_float2(o[s][2], o[s][3]);
+        }
+        if (gl == 0) {
+          S.nred[warp][2 * cq] = m0;
+          S.nred[warp][2 * cq + 1] = m1;
+          S.nred[warp][8 + 2 * cq] = l0;
+          S.nred[warp][8 + 2 * cq + 1] = l1;
+        }
+      }
+      if (!csync()) return false;
+      if (jw == 0) {
+        const int src = r * hkv + g;
+        const float pm0 = S.nred[src][2 * cq], pm1 = S.nred[src][2 * cq + 1];
+        const float pl0 = S.nred[src][8 + 2 * cq], pl1 = S.nred[src][8 + 2 * cq + 1];
+        const float M0 = fmaxf(m0, pm0), M1 = fmaxf(m1, pm1);
+        const float a0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - M0), b0 = (pm0 == -INFINITY) ? 0.f : exp2f(pm0 - M0);
+        const float a1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - M1), b1 = (pm1 == -INFINITY) ? 0.f : exp2f(pm1 - M1);
+        l0 = l0 * a0 + pl0 * b0;
+        l1 = l1 * a1 + pl1 * b1;
+        m0 = M0;
+        m1 = M1;
+#pragma unroll
+        for (int s = 0; s < KS; s++) {
+          const float* row0 = mo + ((size_t)g * D + 16 * s + gl) * 8 + 2 * cq;
+          const float2 u = *(const float2*)row0, v = *(const float2*)(row0 + 8 * 8);
+          o[s][0] = o[s][0] * a0 + u.x * b0;
+          o[s][1] = o[s][1] * a1 + u.y * b1;
+          o[s][2] = o[s][2] * a0 + v.x * b0;
+          o[s][3] = o[s][3] * a1 + v.y * b1;
+        }
+      }
+      if (!csync()) return false;
+    }
+    // the group's partials: heads 2cq, 2cq + 1 (those below grp), dims 16 t + gl, + 8
+    const int item = t[R_ITEM];
+    if (jw == 0) {
+#pragma unroll
+      for (int e = 0; e < 2; e++) {
+        const int hh = 2 * cq + e;
+        if (hh < grp) {
+          const size_t it = ((size_t)item * hkv + g) * grp + hh;
+          float* dst = p.attn_part + it * D;
+#pragma unroll
+          for (int s = 0; s < KS; s++) {
+            __stcg(dst + 16 * s + gl, o[s][e]);
+            __stcg(dst + 16 * s + 8 + gl, o[s][2 + e]);
+          }
+          if (gl == 0) {
+            __stcg(p.attn_ml + it * 2 + 0, e ? m1 : m0);
+            __stcg(p.attn_ml + it * 2 + 1, e ? l1 : l0);
+          }
+        }
       }
     }
     if (tid == 0) S.t_mark[2] = gtime_ns();
@@ -1716,25 +1784,12 @@ __device__ __forceinline__ bool op_route(const Params& p, Smem& S, const int32_t
   return ok;
 }
 
-template <int D, int NT>
+template <int D>
 __device__ __forceinline__ bool op_attn(const Params& p, Smem& S, const int32_t* t) {
   Cons c(p, S, t);
-  const bool ok = c.attn<D, NT>();
+  const bool ok = c.attn<D>();
   c.save();
   return ok;
-}
-
-// head-dim tiles of 8 per warp when the group's 8 / hkv warps split the head dims
-__device__ __forceinline__ bool op_attn_any(const Params& p, Smem& S, const int32_t* t) {
-  const int nt = p.d / (kConsumerWarps / p.hkv) / 8;
-  if (p.d == 128) {
-    if (nt >= 8) return op_attn<128, 8>(p, S, t);
-    if (nt >= 4) return op_attn<128, 4>(p, S, t);
-    return op_attn<128, 2>(p, S, t);
-  }
-  if (nt >= 8) return op_attn<64, 8>(p, S, t);
-  if (nt >= 4) return op_attn<64, 4>(p, S, t);
-  return op_attn<64, 2>(p, S, t);
 }
 
 template <int D>
@@ -1785,7 +1840,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
         break;
       }
       case OP_ROUTE: ok = op_route(p, S, t); break;
-      case OP_ATTN: ok = op_attn_any(p, S, t); break;
+      case OP_ATTN: ok = (p.d == 128) ? op_attn<128>(p, S, t) : op_attn<64>(p, S, t); break;
       case OP_COMBINE: ok = (p.d == 128) ? op_combine<128>(p, S, t) : op_combine<64>(p, S, t); break;
       default: ok = false; break;
     }
@@ -1819,7 +1874,8 @@ template <bool ONE>
 __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_constant__ Params p) {
   static_assert(kThreads == 384 && kLaunchRegs == 168, "register split assumes 384 threads x 168");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  Smem& S = *reinterpret_cast<Smem*>(smem_raw + pad);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; s++) {
       mbar_init(&S.full[s], 1);
@@ -1869,23 +1925,23 @@ int step_kernel_regs() {
   return a.numRegs == b.numRegs ? a.numRegs : -1;
 }
 
-size_t step_smem_bytes() { return sizeof(Smem); }
+size_t step_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(mk_step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sizeof(Smem));
+                                         (int)kSmemBytes);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(mk_step_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)sizeof(Smem));
+                               (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_sm);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = sizeof(Smem);
+  cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;

@@ -145,6 +145,9 @@ struct Params {
   const uint16_t* const* w_down;
   uint16_t* const* k_pool;
   uint16_t* const* v_pool;
+  const uint8_t* kv_maps;      // [L][2] tensor maps (128 bytes each) of the K and V pools:
+                               // 2-D [rows = pages * hkv * page_size][d], boxes of
+                               // 64 dims x (hkv * page_size) rows, 128-byte swizzle
   // this step
   int B;
   int n_attn_items;

@@ -1,5 +1,5 @@
 // Thin inline-PTX helpers for the persistent decode kernel (sm_103a):
-// mbarriers, 1-D bulk async copies (TMA, global -> shared), acquire/release
+// mbarriers, 1-D bulk and 2-D tensor async copies (TMA, global -> shared), acquire/release
 // counter access, the warp-level BF16 tensor-core MMA and the global timer.
 #pragma once
 #include <stdint.h>
@@ -52,6 +52,22 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// 2-D tiled tensor copy global -> shared through a tensor map (a CUtensorMap
+// in global memory); x is the innermost coordinate.  The box lands in the
+// layout the map's swizzle mode gives.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// L2 prefetch of [src, src + bytes) (src and bytes multiples of 16)
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -99,6 +115,28 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t& r0, uint32_t& r1, uint32
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(smem_u32(p)));
+}
+
+// four 8x8 BF16 tiles from shared memory (A fragments of a row-major matrix);
+// lanes 8i..8i+7 give the row addresses of tile i
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+
+// transpose of an 8x8 BF16 matrix held as a warp fragment (lane 4r + c holds
+// row r, columns 2c and 2c + 1)
+__device__ __forceinline__ uint32_t movm_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// two fp32 -> packed BF16 pair (lo in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
 }
 
 // D += A * B, m16n8k16, A row-major BF16, B column-major BF16, fp32 accumulate

@@ -29,10 +29,6 @@ int validate_config(const mk_config& c) {
   const int grp = c.n_q_heads / c.n_kv_heads;
   if (grp > 8 || kConsumerWarps % c.n_kv_heads) return MK_ERR_BAD_CONFIG;
   if (c.head_dim != 64 && c.head_dim != 128) return MK_ERR_BAD_CONFIG;
-  // the warps of a KV group split the head dims: 16 to 64 dims per warp
-  // (pairs of 8-dim MMA tiles; more would not fit the registers)
-  const int dims_per_warp = c.head_dim / (kConsumerWarps / c.n_kv_heads);
-  if (dims_per_warp < 16 || dims_per_warp > 64) return MK_ERR_BAD_CONFIG;
   if (!gemv_k(c.hidden) || !gemv_k(c.moe_inter) || !gemv_k(c.n_q_heads * c.head_dim))
     return MK_ERR_BAD_CONFIG;
   // the attention keeps every query head's BF16 high and low halves in the
