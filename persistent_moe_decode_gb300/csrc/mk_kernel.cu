@@ -107,7 +107,7 @@ enum : int { K_ROUTER = 0, K_QKV = 1, K_UP = 2, K_OPROJ = 3, K_DOWN = 4, K_LM = 
 constexpr int kRowChunk = kPartFloats;
 // chunk flags: first chunk of its task (P1 / FINAL run the norm first), last
 // chunk of its task (signals completion), last block of an OUT row chunk
-enum : int { FL_FIRST = 1, FL_LAST = 2, FL_CLAST = 4 };
+enum : int { FL_FIRST = 1, FL_LAST = 2, FL_CLAST = 4, FL_RTR = 8 };   // FL_RTR: the P1 share holds router rows
 
 // ---------------------------------------------------------------- errors
 __device__ __forceinline__ bool stopped(const Params& p) {
@@ -317,9 +317,9 @@ struct Prod {
 
   // rows [lo, hi) of w in chunks of cr; `first` / `last` mark the task's ends
   __device__ __noinline__ bool rows_task(int kind, const uint16_t* w, int lo, int hi, int cr, int K,
-                                            int nt, bool first, bool last) {
+                                            int nt, bool first, bool last, int last_extra = 0) {
     for (int c0 = lo; c0 < hi; c0 += cr) {
-      const int flags = (first && c0 == lo ? FL_FIRST : 0) | (last && c0 + cr >= hi ? FL_LAST : 0);
+      const int flags = (first && c0 == lo ? FL_FIRST : 0) | (last && c0 + cr >= hi ? FL_LAST | last_extra : 0);
       if (!chunk(kind, flags, c0, min(cr, hi - c0), 1, K, nt, 0, 0, 0, w, nullptr)) return false;
     }
     return true;
@@ -340,7 +340,8 @@ struct Prod {
     if (a1 <= a0) return chunk(op == OP_P1 ? K_P1 : K_LM, FL_FIRST | FL_LAST, 0, 0, 1, H, 1, 0, 0, 0, nullptr, nullptr);
     for (int c0 = a0; c0 < a1; c0 += kRowChunk) {
       const int c1 = min(a1, c0 + kRowChunk);
-      const int flags = (c0 == a0 ? FL_FIRST : 0) | (c1 == a1 ? FL_LAST : 0);
+      const int flags = (c0 == a0 ? FL_FIRST : 0) | (c1 == a1 ? FL_LAST : 0) |
+                        (op == OP_P1 && c1 == a1 && a0 < p.E ? FL_RTR : 0);
       if (op == OP_FINAL) {
         if (!chunk(K_LM, flags, c0, c1 - c0, 1, H, 1, 0, 0, 0, p.lm_head, nullptr)) return false;
         continue;
@@ -379,8 +380,9 @@ struct Prod {
     const int r0 = min(a0, p.E), r1 = min(a1, p.E);
     const int q0 = max(a0, p.E) - p.E, q1 = max(a1, p.E) - p.E;
     if (r1 <= r0 && q1 <= q0) return chunk(K_ROUTER, FL_FIRST | FL_LAST, 0, 0, 1, H, B, 0, 0, 0, nullptr, nullptr);
-    if (r1 > r0 && !rows_task(K_ROUTER, p.w_router[l], r0, r1, cr, H, B, true, q1 <= q0)) return false;
-    if (q1 > q0 && !rows_task(K_QKV, p.w_qkv[l], q0, q1, cr, H, B, r1 <= r0, true)) return false;
+    const int rtr = r1 > r0 ? FL_RTR : 0;
+    if (r1 > r0 && !rows_task(K_ROUTER, p.w_router[l], r0, r1, cr, H, B, true, q1 <= q0, rtr)) return false;
+    if (q1 > q0 && !rows_task(K_QKV, p.w_qkv[l], q0, q1, cr, H, B, r1 <= r0, true, rtr)) return false;
     return true;
   }
 
@@ -622,10 +624,7 @@ struct Cons {
   // publish: every consumer's global stores are done; one thread releases the counter
   __device__ __forceinline__ bool signal(int bar, int inc) {
     if (!csync()) return false;
-    if (tid == 0) {
-      __threadfence();
-      atomicAdd(p.bars + bar, (uint32_t)inc);
-    }
+    if (tid == 0) red_release_add(p.bars + bar, (uint32_t)inc);
     return true;
   }
 
@@ -640,13 +639,10 @@ struct Cons {
     if (bar < 0) return csync();
     if (!csync()) return false;
     if (tid == 0) {
-      __threadfence();
-      if (op == OP_P1) {
-        const int a0 = p.tasks[(size_t)t[R_TASK] * kDescWords + F_A0];
-        const int a1 = p.tasks[(size_t)t[R_TASK] * kDescWords + F_A1];
-        if (a1 > a0 && a0 < p.E) atomicAdd(p.bars + bar_index(p, l, p.bl.rtr), 1u);
-      }
-      atomicAdd(p.bars + bar_index(p, l, bar), 1u);
+      // release: the block's stores (ordered before this thread by the
+      // barrier above) are visible before the counter moves
+      if (t[R_FLAGS] & FL_RTR) red_release_add(p.bars + bar_index(p, l, p.bl.rtr), 1u);
+      red_release_add(p.bars + bar_index(p, l, bar), 1u);
     }
     return true;
   }
@@ -1214,6 +1210,80 @@ struct Cons {
   }
 
   // ------------------------------------------------------------ routing
+  // one token: top-k, weights and the grouping in warp 0 alone.  Lane j < k
+  // keeps the j-th pick; its rank among the picks (ascending expert id) is its
+  // active slot, and with one token every active expert has one entry.
+  __device__ __forceinline__ bool route1(int l) {
+    const int E = p.E, K = p.topk;
+    RouteTab& rt = S.rt;
+    if (warp == 0) {
+      float v[8];
+      const float* rl = p.rlog + (size_t)l * p.Bmax * E;
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? __ldcg(rl + e) : -INFINITY;
+      }
+      uint32_t taken = 0;
+      float my_v = -INFINITY;
+      int my_e = 0x7fffffff;
+#pragma unroll 1
+      for (int j = 0; j < K; j++) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+          const int e = lane + 32 * i;
+          if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+            bv = v[i];
+            bi = e;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (ov > bv || (ov == bv && oi < bi)) {
+            bv = ov;
+            bi = oi;
+          }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+          my_v = bv;
+          my_e = bi;
+        }
+      }
+      // softmax over the picks (the top-k of the softmax = the top-k of the logits)
+      const float top = __shfl_sync(0xffffffffu, my_v, 0);
+      const float ex = lane < K ? expf(my_v - top) : 0.f;
+      float den = 0.f;
+      for (int j = 0; j < K; j++) den += __shfl_sync(0xffffffffu, ex, j);   // fixed order
+      const float w = ex / den;
+      int rank = 0;
+      for (int j = 0; j < K; j++) rank += __shfl_sync(0xffffffffu, my_e, j) < my_e;
+      if (lane < K) {
+        rt.idx[0][lane] = my_e;
+        rt.w[0][lane] = w;
+        rt.act[rank] = my_e;
+        rt.off[rank] = rank;
+        rt.ent[rank] = lane;
+        if (blockIdx.x == p.n_sm - 1) {   // an SM of the expert branch keeps the routing
+          p.ridx[(size_t)l * p.Bmax * K + lane] = my_e;
+          p.rw[(size_t)l * p.Bmax * K + lane] = w;
+        }
+      }
+      if (lane == 0) {
+        rt.n_act = K;
+        rt.off[K] = K;
+      }
+    }
+    if (tid == 0) S.t_mark[0] = gtime_ns();
+    if (!csync()) return false;
+    if (tid == 0) mbar_arrive(&S.route_bar);   // the producer may now resolve the experts
+    return true;
+  }
+
   // top-k per token (softmax order = logit order; ties to the lower index),
   // weights renormalised over the selected experts; then the per-expert
   // grouping: active experts ascending, tokens ascending within an expert.
@@ -1223,6 +1293,7 @@ struct Cons {
     const size_t Bm = (size_t)p.Bmax;
     if (!wait_counter(bar_index(p, l, p.bl.rtr), p.n_rtr_sms)) return false;
     RouteTab& rt = S.rt;
+    if (B == 1) return route1(l);
     for (int n = warp; n < B; n += kConsumerWarps) {
       float v[8];
       const float* rl = p.rlog + ((size_t)l * Bm + n) * E;
