@@ -167,6 +167,50 @@ int make_kv_maps(mk_handle* h, const mk_weights* w, const uint8_t** out) {
   return MK_OK;
 }
 
+// a 2-D tiled tensor map without swizzle: [outer][inner] elements of `esize`
+// bytes, boxes of box_in x box_out
+int make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
+                uint64_t outer, uint32_t box_in, uint32_t box_out) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return MK_ERR_CUDA;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * (uint64_t)esize};
+  const cuuint32_t box[2] = {box_in, box_out};
+  const cuuint32_t es[2] = {1, 1};
+  if (outer >= (1ull << 32)) return MK_ERR_BAD_CONFIG;
+  if (enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MK_ERR_BAD_ARG;
+  return MK_OK;
+}
+
+// one token: tensor maps of every layer's down projection, as column slices
+// of 8 n columns (n = 1..8) x 256 rows, and of the per-group partial buffer
+// (32 x 256 fp32)
+int make_moe_maps(mk_handle* h, const mk_weights* w, float* mpart, const uint8_t** wd, const uint8_t** mp) {
+  const mk_config& c = h->cfg;
+  const int L = c.n_layers;
+  std::vector<CUtensorMap> maps((size_t)L * 8 + 1);
+  for (int l = 0; l < L; l++)
+    for (int n = 1; n <= 8; n++) {
+      int rc = make_map_2d(&maps[(size_t)l * 8 + n - 1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w->w_down[l],
+                           (uint64_t)c.moe_inter, (uint64_t)c.n_experts * c.hidden, (uint32_t)(8 * n), 256);
+      if (rc) return rc;
+    }
+  int rc = make_map_2d(&maps[(size_t)L * 8], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, mpart, (uint64_t)c.hidden,
+                       (uint64_t)c.top_k * (c.moe_inter / 8), 32, 256);
+  if (rc) return rc;
+  uint8_t* d = nullptr;
+  rc = dalloc(h, &d, maps.size() * sizeof(CUtensorMap));
+  if (rc) return rc;
+  if (cudaMemcpy(d, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess)
+    return MK_ERR_CUDA;
+  *wd = d;
+  *mp = d + (size_t)L * 8 * sizeof(CUtensorMap);
+  return MK_OK;
+}
+
 void free_plans(mk_handle* h) {
   for (auto& kv : h->plans) {
     cudaFree(kv.second.tasks);
@@ -334,6 +378,8 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
   TRY(dalloc(h, &p.abuf, Ls * Bs * K * I));
   TRY(dalloc(h, &p.oproj, Ls * Bs * H));
   TRY(dalloc(h, &p.moe, Ls * Bs * H));
+  TRY(dalloc(h, &p.mpart, (size_t)K * (I / 8) * H));
+  TRY(make_moe_maps(h, w, p.mpart, &p.wd_maps, &p.mp_map));
   h->bar_words = kErrWords + (size_t)L * p.bl.per_layer;
   TRY(dalloc(h, &h->d_bars, h->bar_words));
   p.err = h->d_bars;

@@ -69,6 +69,7 @@ struct __align__(128) Smem {
   float red[2 * kPartFloats];               // GEMV partial sums (two buffers) / attention
                                             // query fragments and merge / combine sums
   float acc_m[kOutRows][kMaxBatch];         // DOWN row chunk (several tokens): weighted expert outputs
+  float actp[64];                           // one token: weighted hidden values of an UP piece
   float nred[kConsumerWarps][kMaxBatch];    // norm / combine reductions
   float rinv[kMaxBatch];
   RouteTab rt;
@@ -99,10 +100,11 @@ enum : int {
   R_OP = 0, R_LAYER, R_TASK, R_KIND, R_FLAGS, R_ROW0, R_NROWS, R_K, R_NT, R_NBLK, R_A, R_E,
   R_REL0, R_ITEM, R_B, R_TT0, R_TT1, R_POS, R_NST, R_U0, R_U1, R_BUMP, R_ROW1, R_NROWS1, R_NGRP
 };
-// GEMV chunk kinds; K_P1 (router rows, then QKV rows) and K_DOWNALL (every
-// routed expert's down rows of one hidden-row range) are the one-token forms
+// GEMV chunk kinds; K_P1 (router rows, then QKV rows) and K_MRED (the sum of
+// the experts' per-group partials of OUT's rows) are one-token forms, and a
+// one-token K_UP chunk also multiplies its columns of the down projection
 enum : int { K_ROUTER = 0, K_QKV = 1, K_UP = 2, K_OPROJ = 3, K_DOWN = 4, K_LM = 5, K_P1 = 6,
-             K_DOWNALL = 7 };
+             K_MRED = 7 };
 // rows of one single-token GEMV chunk (one result per row in a 2048-float buffer)
 constexpr int kRowChunk = kPartFloats;
 // chunk flags: first chunk of its task (P1 / FINAL run the norm first), last
@@ -210,8 +212,31 @@ struct Prod {
   bool ok = true;
   // header of the descriptor being resolved
   int op = 0, l = 0, ti = 0, bump = 0;
+  // weight pointers of layer ptr_layer (cur) and of the next layer (nxt), lane
+  // i holding matrix i (router, qkv, o, gate, up, down): the pointer tables
+  // are read a layer ahead, so no stream waits on one
+  const uint16_t* cur = nullptr;
+  const uint16_t* nxt = nullptr;
+  int ptr_layer = -1;
 
   __device__ __forceinline__ Prod(const Params& pp, Smem& ss) : p(pp), S(ss), lane(threadIdx.x & 31) {}
+
+  __device__ __forceinline__ const uint16_t* load_ptr(int layer) const {
+    if (layer >= p.L || lane >= 6) return nullptr;
+    const uint16_t* const* tab = lane == 0 ? p.w_router : lane == 1 ? p.w_qkv : lane == 2 ? p.w_o
+                                 : lane == 3 ? p.w_gate : lane == 4 ? p.w_up : p.w_down;
+    return tab[layer];
+  }
+  __device__ __forceinline__ void set_layer(int layer) {
+    if (layer == ptr_layer || layer >= p.L) return;
+    cur = (ptr_layer >= 0 && layer == ptr_layer + 1) ? nxt : load_ptr(layer);
+    nxt = load_ptr(layer + 1);
+    ptr_layer = layer;
+  }
+  // matrix i of the current layer
+  __device__ __forceinline__ const uint16_t* wptr(int i) const {
+    return (const uint16_t*)__shfl_sync(0xffffffffu, (unsigned long long)cur, i);
+  }
 
   // reserve the next task slot, zero it and write the header; nullptr on give-up
   __device__ __noinline__ int32_t* begin() {
@@ -260,34 +285,43 @@ struct Prod {
   }
 
   // pages [pg0, pg0 + npages) of sequence b, all KV heads: K pages then V
-  // pages, each as d / 64 swizzled boxes of (hkv * P rows) x 128 bytes
+  // pages, each as d / 64 swizzled boxes of (hkv * P rows) x 128 bytes.  The
+  // page ids are read 32 at a time (lane k holds page c0 + k), the next 32
+  // requested while the current ones stream, so no stage waits on a
+  // page-table read.
   __device__ __noinline__ bool stream_attn(int b, int pg0, int npages) {
     const int pb = attn_page_bytes(p);
-    const int pps = attn_pps(p);
+    const int pps = attn_pps(p);                 // a power of two <= 8: divides 32
     const int rows = p.hkv * p.P;
     const int nbox = p.d / 64;
     const uint8_t* km = p.kv_maps + (size_t)l * 2 * 128;
     const uint8_t* vm = km + 128;
-    for (int st = 0; st * pps < npages; st++) {
-      const int n = min(pps, npages - st * pps);
-      int pg = -1;
-      if (lane < 2 * n) pg = p.page_tables[(size_t)b * p.max_pages + pg0 + st * pps + (lane % n)];
-      const bool bad = (lane < 2 * n) && (pg < 0 || pg >= p.num_pages);
-      if (__any_sync(0xffffffffu, bad)) {
-        if (bad) report(p, DEV_BAD_PAGE, ti, OP_ATTN, -1, (uint32_t)pg, (uint32_t)p.num_pages);
-        return false;
+    const int32_t* ptab = p.page_tables + (size_t)b * p.max_pages + pg0;
+    int id_next = lane < npages ? ptab[lane] : 0;
+    for (int c0 = 0; c0 < npages; c0 += 32) {
+      const int id = id_next;
+      if (c0 + 32 + lane < npages) id_next = ptab[c0 + 32 + lane];
+      const int cn = min(32, npages - c0);
+      for (int q = 0; q < cn; q += pps) {
+        const int n = min(pps, cn - q);
+        const int pg = __shfl_sync(0xffffffffu, id, q + (lane % n));
+        const bool bad = (lane < 2 * n) && (pg < 0 || pg >= p.num_pages);
+        if (__any_sync(0xffffffffu, bad)) {
+          if (bad) report(p, DEV_BAD_PAGE, ti, OP_ATTN, -1, (uint32_t)pg, (uint32_t)p.num_pages);
+          return false;
+        }
+        uint32_t slot;
+        if (!acquire_stage(slot)) return false;
+        if (lane == 0) mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(2 * n * pb));
+        __syncwarp();
+        if (lane < 2 * n) {
+          const bool is_k = lane < n;
+          uint8_t* dst = &S.stage[slot][(is_k ? lane : pps + lane - n) * pb];
+          for (int bx = 0; bx < nbox; bx++)
+            tma_load_2d(dst + bx * rows * 128, is_k ? km : vm, bx * 64, pg * rows, &S.full[slot]);
+        }
+        stage_seq++;
       }
-      uint32_t slot;
-      if (!acquire_stage(slot)) return false;
-      if (lane == 0) mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(2 * n * pb));
-      __syncwarp();
-      if (lane < 2 * n) {
-        const bool is_k = lane < n;
-        uint8_t* dst = &S.stage[slot][(is_k ? lane : pps + lane - n) * pb];
-        for (int bx = 0; bx < nbox; bx++)
-          tma_load_2d(dst + bx * rows * 128, is_k ? km : vm, bx * 64, pg * rows, &S.full[slot]);
-      }
-      stage_seq++;
     }
     return true;
   }
@@ -362,8 +396,8 @@ struct Prod {
         w[R_NT] = 1;
       }
       commit();
-      if (r1 > r0 && !stream_rows(p.w_router[l], r0, r1 - r0, H)) return false;
-      if (q1 > q0 && !stream_rows(p.w_qkv[l], q0, q1 - q0, H)) return false;
+      if (r1 > r0 && !stream_rows(wptr(0), r0, r1 - r0, H)) return false;
+      if (q1 > q0 && !stream_rows(wptr(1), q0, q1 - q0, H)) return false;
     }
     return true;
   }
@@ -381,8 +415,8 @@ struct Prod {
     const int q0 = max(a0, p.E) - p.E, q1 = max(a1, p.E) - p.E;
     if (r1 <= r0 && q1 <= q0) return chunk(K_ROUTER, FL_FIRST | FL_LAST, 0, 0, 1, H, B, 0, 0, 0, nullptr, nullptr);
     const int rtr = r1 > r0 ? FL_RTR : 0;
-    if (r1 > r0 && !rows_task(K_ROUTER, p.w_router[l], r0, r1, cr, H, B, true, q1 <= q0, rtr)) return false;
-    if (q1 > q0 && !rows_task(K_QKV, p.w_qkv[l], q0, q1, cr, H, B, r1 <= r0, true, rtr)) return false;
+    if (r1 > r0 && !rows_task(K_ROUTER, wptr(0), r0, r1, cr, H, B, true, q1 <= q0, rtr)) return false;
+    if (q1 > q0 && !rows_task(K_QKV, wptr(1), q0, q1, cr, H, B, r1 <= r0, true, rtr)) return false;
     return true;
   }
 
@@ -413,9 +447,60 @@ struct Prod {
     return true;
   }
 
+  // one token: slice a0 of a1 over the routed experts' groups of 8
+  // intermediate columns.  Each piece (one expert, n <= 8 groups) streams its
+  // gate rows, its up rows and then its 8 n columns of the down projection,
+  // 256 rows per stage (one box of the n-group map: whole row pieces, so the
+  // copy engine moves 16 n bytes per row request).
+  __device__ __noinline__ bool do_up1(int a0, int a1) {
+    const int H = p.H, G = p.I / 8;
+    int g0 = 0, g1 = 0;
+    if (a0 >= 0) dshare(S.rt.n_act * G, a1, a0, g0, g1);
+    if (g1 <= g0) return chunk(K_UP, FL_LAST, 0, 0, 2, H, 0, 0, 0, 0, nullptr, nullptr);
+    const uint8_t* wdm = p.wd_maps + (size_t)l * 8 * 128;
+    for (int g = g0; g < g1;) {
+      const int a = g / G;
+      const int ge = min(min(g1, (a + 1) * G), g + 8);
+      const int e = S.rt.act[a];
+      const int i0 = (g - a * G) * 8, i1 = (ge - a * G) * 8;
+      const int ncb = ge - g;
+      int32_t* w = begin();
+      if (!w) return false;
+      if (lane == 0) {
+        w[R_KIND] = K_UP;
+        w[R_FLAGS] = (g == g0 ? FL_FIRST : 0) | (ge == g1 ? FL_LAST : 0);
+        w[R_ROW0] = i0;
+        w[R_NROWS] = i1 - i0;
+        w[R_NBLK] = 2;
+        w[R_K] = H;
+        w[R_NT] = 1;
+        w[R_A] = a;
+        w[R_E] = e;
+        w[R_REL0] = g;
+      }
+      commit();
+      const size_t eo = (size_t)e * p.I * H;
+      if (!stream_rows(wptr(3) + eo, i0, i1 - i0, H)) return false;
+      if (!stream_rows(wptr(4) + eo, i0, i1 - i0, H)) return false;
+      for (int r0 = 0; r0 < H; r0 += 256) {
+        uint32_t slot;
+        if (!acquire_stage(slot)) return false;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(ncb * 4096));
+          tma_load_2d(&S.stage[slot][0], wdm + (size_t)(ncb - 1) * 128, i0, e * H + r0, &S.full[slot]);
+        }
+        __syncwarp();
+        stage_seq++;
+      }
+      g = ge;
+    }
+    return true;
+  }
+
   __device__ __noinline__ bool do_up(int a0, int a1) {
     const int H = p.H;
     if (!wait_route()) return false;
+    if (p.B == 1) return do_up1(a0, a1);
     const int n_act = S.rt.n_act;
     int p0 = 0, p1 = 0;
     if (a0 >= 0) dshare(n_act * p.I, a1, a0, p0, p1);
@@ -436,21 +521,59 @@ struct Prod {
       for (int c0 = i0; c0 < i1; c0 += cp) {
         n_chunks--;
         if (!chunk(K_UP, n_chunks == 0 ? FL_LAST : 0, c0, min(cp, i1 - c0), 2, H, cnt, a, e, 0,
-                   p.w_gate[l] + eo, p.w_up[l] + eo))
+                   wptr(3) + eo, wptr(4) + eo))
           return false;
       }
     }
     return true;
   }
 
-  // OUT: O-proj rows [a0, a1) (needs no routing)
+  // OUT: O-proj rows [a0, a1) (needs no routing).  One token: then the
+  // experts' per-group partials of the same rows (K_MRED), streamed once every
+  // UP slice has written them: 256 groups x 32 rows per stage.
   __device__ __noinline__ bool do_out(int a0, int a1) {
     const int B = p.B;
     const int KO = p.hq * p.d;
+    if (B == 1) {
+      for (int c0 = a0; c0 < a1; c0 += kRowChunk)
+        if (!chunk(K_OPROJ, 0, c0, min(kRowChunk, a1 - c0), 1, KO, 1, 0, 0, 0, wptr(2), nullptr)) return false;
+      int32_t* w = begin();
+      if (!w) return false;
+      if (lane == 0) {
+        w[R_KIND] = K_MRED;
+        w[R_FLAGS] = FL_LAST;
+        w[R_ROW0] = a0;
+        w[R_NROWS] = max(a1 - a0, 0);
+        w[R_NT] = 1;
+      }
+      commit();
+      if (a1 <= a0) return true;
+      // the partials are written by other SMs (generic stores, released with
+      // the counter): acquire, then order the async-proxy reads after it
+      int good = 1;
+      if (lane == 0) {
+        good = spin_counter(p, bar_index(p, l, p.bl.up), (uint32_t)p.n_up_sms, ti, op);
+        if (good) fence_proxy_async_global();
+      }
+      if (!__shfl_sync(0xffffffffu, good, 0)) return false;
+      const int ng = p.topk * (p.I / 8);
+      for (int x0 = a0 & ~3; x0 < a1; x0 += 32)
+        for (int y0 = 0; y0 < ng; y0 += 256) {
+          uint32_t slot;
+          if (!acquire_stage(slot)) return false;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&S.full[slot], 32u * 256u * 4u);
+            tma_load_2d(&S.stage[slot][0], p.mp_map, x0, y0, &S.full[slot]);
+          }
+          __syncwarp();
+          stage_seq++;
+        }
+      return true;
+    }
     if (a1 <= a0) return chunk(K_OPROJ, FL_LAST, 0, 0, 1, KO, B, 0, 0, 0, nullptr, nullptr);
     const int co = B == 1 ? kRowChunk : gemv_chunk_rows(KO, B);
     for (int c0 = a0; c0 < a1; c0 += co)
-      if (!chunk(K_OPROJ, c0 + co >= a1 ? FL_LAST : 0, c0, min(co, a1 - c0), 1, KO, B, 0, 0, 0, p.w_o[l],
+      if (!chunk(K_OPROJ, c0 + co >= a1 ? FL_LAST : 0, c0, min(co, a1 - c0), 1, KO, B, 0, 0, 0, wptr(2),
                  nullptr))
         return false;
     return true;
@@ -462,29 +585,6 @@ struct Prod {
     if (!wait_route()) return false;
     const int n_act = S.rt.n_act;
     if (a1 <= a0 || n_act == 0) return chunk(K_DOWN, FL_LAST, 0, 0, 1, p.I, 0, 0, 0, 0, nullptr, nullptr);
-    if (B == 1) {
-      // one token: every routed expert's rows of [h0, h1) in one chunk, one
-      // group per expert (the result buffer holds n_act x rows)
-      const int cr = kRowChunk / n_act;
-      for (int h0 = a0; h0 < a1; h0 += cr) {
-        const int h1 = min(a1, h0 + cr);
-        int32_t* w = begin();
-        if (!w) return false;
-        if (lane == 0) {
-          w[R_KIND] = K_DOWNALL;
-          w[R_FLAGS] = h1 == a1 ? FL_LAST : 0;
-          w[R_ROW0] = h0;
-          w[R_NROWS] = h1 - h0;
-          w[R_NGRP] = n_act;
-          w[R_K] = p.I;
-          w[R_NT] = 1;
-        }
-        commit();
-        for (int a = 0; a < n_act; a++)
-          if (!stream_rows(p.w_down[l] + (size_t)S.rt.act[a] * H * p.I, h0, h1 - h0, p.I)) return false;
-      }
-      return true;
-    }
     // several tokens: row chunks of kOutRows, each expert's rows accumulated
     // in shared memory in expert order
     for (int h0 = a0; h0 < a1; h0 += kOutRows) {
@@ -494,7 +594,7 @@ struct Prod {
         const int e = S.rt.act[a];
         const int cnt = S.rt.off[a + 1] - S.rt.off[a];
         const int cd = gemv_chunk_rows(p.I, cnt);
-        const uint16_t* wd = p.w_down[l] + (size_t)e * H * p.I;
+        const uint16_t* wd = wptr(5) + (size_t)e * H * p.I;
         for (int c0 = h0; c0 < h1; c0 += cd)
           if (!chunk(K_DOWN, (a == n_act - 1 && c0 + cd >= h1) ? fin : 0, c0, min(cd, h1 - c0), 1, p.I, cnt,
                      a, e, c0 - h0, wd, nullptr))
@@ -514,6 +614,7 @@ struct Prod {
       const int a0 = __shfl_sync(0xffffffffu, word, F_A0);
       const int a1 = __shfl_sync(0xffffffffu, word, F_A1);
       bump = __shfl_sync(0xffffffffu, word, F_BUMP);
+      set_layer(l);
       switch (op) {
         case OP_P1:
         case OP_FINAL: ok = do_p1_final(a0, a1); break;
@@ -858,13 +959,12 @@ struct Cons {
     return csync();
   }
 
-  // one token: stage this chunk's activations in shared memory (the O-proj's
-  // attention output, or the hidden vector of every routed expert), one
-  // coalesced global read per block instead of one per warp
+  // one token: stage the O-proj's input (the attention output) in shared
+  // memory, one coalesced global read per block instead of one per warp
   __device__ __forceinline__ bool stage_x() {
-    const int l = t[R_LAYER], kind = t[R_KIND];
+    const int l = t[R_LAYER];
     const size_t Bm = (size_t)p.Bmax;
-    if (kind == K_OPROJ) {
+    {
       const int n4 = p.hq * p.d / 4;
       const float4* src = (const float4*)(p.attn_out + (size_t)l * Bm * p.hq * p.d);
       float4 v[4];
@@ -877,13 +977,6 @@ struct Cons {
       for (int k = 0; k < 4; k++) {
         const int i = tid + 256 * k;
         if (i < n4) *(float4*)&S.xs[i * 4] = v[k];
-      }
-    } else {   // K_DOWNALL: expert a's hidden at xs[a * I]
-      const int na = t[R_NGRP], I4 = p.I / 4;
-      const float* base = p.abuf + (size_t)l * Bm * p.topk * p.I;
-      for (int i = tid; i < na * I4; i += 256) {
-        const int a = i / I4, k = i % I4;
-        *(float4*)&S.xs[a * p.I + k * 4] = __ldcg((const float4*)(base + (size_t)S.rt.off[a] * p.I) + k);
       }
     }
     return csync();
@@ -1023,18 +1116,13 @@ struct Cons {
   // r % 8, which computes the whole row: lane l multiplies the 8-column
   // chunks l, l + 32, ... (consecutive 16-byte shared-memory reads across the
   // warp) against x in registers, then one warp reduction gives res[r].  No
-  // cross-warp partial sums.  A down chunk (one group per routed expert)
-  // loads the next expert's activations while it works on the current one.
+  // cross-warp partial sums.  The activations are in shared memory (xs).
   __device__ __forceinline__ int row_groups() const {
     const int kind = t[R_KIND];
-    return (kind == K_P1 || kind == K_UP) ? 2 : kind == K_DOWNALL ? t[R_NGRP] : 1;
+    return (kind == K_P1 || kind == K_UP) ? 2 : 1;
   }
   __device__ __forceinline__ int group_rows(int g) const {
     return (t[R_KIND] == K_P1 && g == 1) ? t[R_NROWS1] : t[R_NROWS];
-  }
-  // the chunk's activations of group g, in shared memory
-  __device__ __forceinline__ const float* row_x(int g) const {
-    return t[R_KIND] == K_DOWNALL ? S.xs + g * p.I : S.xs;
   }
   template <int NCK>
   __device__ __forceinline__ void row_load_x(float (&x)[NCK][8], const float* src, int K) const {
@@ -1053,13 +1141,10 @@ struct Cons {
   template <int NCK>
   __device__ __forceinline__ bool gemv_row(float* res) {
     const int K = t[R_K];
-    const bool per_group_x = t[R_KIND] == K_DOWNALL;
     const int ngrp = row_groups();
     const int rps = rows_per_stage(K);
-    constexpr int NXB = NCK <= 4 ? NCK : 1;       // prefetch buffer (short rows only)
-    float xa[NCK][8], xb[NXB][8];
-    row_load_x<NCK>(xa, row_x(0), K);
-    if (NCK <= 4 && per_group_x && ngrp > 1) row_load_x<NXB>(xb, row_x(1), K);
+    float xa[NCK][8];
+    row_load_x<NCK>(xa, S.xs, K);
     int rbase = 0;
     for (int g = 0; g < ngrp; g++) {
       const int nr = group_rows(g);
@@ -1094,17 +1179,6 @@ struct Cons {
         stage_release(slot);
       }
       rbase += nr;
-      if (per_group_x && g + 1 < ngrp) {
-        if (NCK <= 4) {
-#pragma unroll
-          for (int c = 0; c < NXB; c++)
-#pragma unroll
-            for (int j = 0; j < 8; j++) xa[c][j] = xb[c][j];
-          if (g + 2 < ngrp) row_load_x<NXB>(xb, row_x(g + 2), K);
-        } else {
-          row_load_x<NCK>(xa, row_x(g + 1), K);
-        }
-      }
     }
     if (tid == 0) S.t_mark[1] = gtime_ns();
     return true;
@@ -1125,31 +1199,98 @@ struct Cons {
         break;
       }
       case K_UP: {
+        // the hidden values of the piece; times the routing weight, they are
+        // the input of the piece's down-projection columns
         const int slot = S.rt.off[t[R_A]];
-        for (int i = tid; i < nr; i += 256)
-          __stcg(p.abuf + ((size_t)l * Bm * p.topk + slot) * p.I + row0 + i, silu_mul(res[i], res[nr + i]));
+        const float wa = S.rt.w[0][S.rt.ent[slot] % p.topk];
+        for (int i = tid; i < nr; i += 256) {
+          const float a = silu_mul(res[i], res[nr + i]);
+          __stcg(p.abuf + ((size_t)l * Bm * p.topk + slot) * p.I + row0 + i, a);
+          S.actp[i] = wa * a;
+        }
         break;
       }
       case K_OPROJ:
         for (int i = tid; i < nr; i += 256) __stcg(p.oproj + (size_t)l * Bm * p.H + row0 + i, res[i]);
         break;
-      case K_DOWNALL: {
-        // the routed experts' rows weighted by the routing, in expert order
-        const int na = t[R_NGRP];
-        for (int i = tid; i < nr; i += 256) {
-          float m = 0.f;
-          for (int a = 0; a < na; a++) {
-            const int j = S.rt.ent[S.rt.off[a]] % p.topk;
-            m += S.rt.w[0][j] * res[a * nr + i];
-          }
-          __stcg(p.moe + (size_t)l * Bm * p.H + row0 + i, m);
-        }
-        break;
-      }
       default:   // K_LM
         for (int i = tid; i < nr; i += 256) p.logits[row0 + i] = res[i];
         break;
     }
+  }
+
+  // one token, after the gate/up rows of an UP piece: its n = ncb groups of
+  // columns of the down projection, 256 hidden rows of 16 n bytes per stage.
+  // Thread t takes row r0 + t and writes one partial per group:
+  //   mpart[g][h] = sum_{c < 8} W_down[e][h][8 g' + c] * w_e * act[8 g' + c]
+  // Lane k starts at group (k % 8) >> (3 - tz(n)) (tz: trailing zero bits,
+  // at most 3), which puts the eight rows of a quarter-warp in distinct banks
+  // for every n.
+  __device__ __forceinline__ bool down_part() {
+    const int H = p.H, ncb = t[R_NROWS] / 8, g0 = t[R_REL0];
+    const int tz = min(__ffs(ncb) - 1, 3);
+    const int h0 = (lane & 7) >> (3 - tz);
+    for (int r0 = 0; r0 < H; r0 += 256) {
+      uint32_t slot;
+      if (!stage_full(slot)) return false;
+      const int row = r0 + tid;
+      if (row < H) {
+        const uint8_t* st = S.stage[slot] + tid * ncb * 16;
+        int j = h0 % ncb;
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+          if (c < ncb) {
+            const uint4 w = lds128(st + j * 16);
+            const float4 x0 = *(const float4*)&S.actp[8 * j];
+            const float4 x1 = *(const float4*)&S.actp[8 * j + 4];
+            float v = bf16lo(w.x) * x0.x;
+            v = fmaf(bf16hi(w.x), x0.y, v);
+            v = fmaf(bf16lo(w.y), x0.z, v);
+            v = fmaf(bf16hi(w.y), x0.w, v);
+            v = fmaf(bf16lo(w.z), x1.x, v);
+            v = fmaf(bf16hi(w.z), x1.y, v);
+            v = fmaf(bf16lo(w.w), x1.z, v);
+            v = fmaf(bf16hi(w.w), x1.w, v);
+            __stcg(p.mpart + (size_t)(g0 + j) * H + row, v);
+            j = j + 1 == ncb ? 0 : j + 1;
+          }
+        }
+      }
+      stage_release(slot);
+    }
+    return true;
+  }
+
+  // one token, OUT: rows [a0, a1) of the experts' share of the residual
+  // update = the sum of every group's partial, in group order.  The partials
+  // arrive as stages of 256 groups x 32 rows (from row a0 rounded down to a
+  // multiple of 4); warp w adds groups w, w + 8, ... and the warps' sums meet
+  // in shared memory in warp order.  red: 256 floats of scratch.
+  __device__ __forceinline__ bool moe_reduce(float* red) {
+    const int a0 = t[R_ROW0], a1 = a0 + t[R_NROWS], l = t[R_LAYER];
+    const int ng = p.topk * (p.I / 8);
+    for (int x0 = a0 & ~3; x0 < a1; x0 += 32) {
+      float s = 0.f;
+      for (int y0 = 0; y0 < ng; y0 += 256) {
+        uint32_t slot;
+        if (!stage_full(slot)) return false;
+        const float* st = (const float*)S.stage[slot];
+        const int n = min(256, ng - y0);
+        for (int g = warp; g < n; g += kConsumerWarps) s += st[g * 32 + lane];
+        stage_release(slot);
+      }
+      red[warp * 32 + lane] = s;
+      if (!csync()) return false;
+      if (tid < 32) {
+        const int h = x0 + tid;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; w++) v += red[w * 32 + tid];
+        if (h >= a0 && h < a1) __stcg(p.moe + (size_t)l * p.Bmax * p.H + h, v);
+      }
+      if (!csync()) return false;
+    }
+    return true;
   }
 
   // fixed-order sum over the contraction segments of element (row, n)
@@ -1829,20 +1970,25 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
   int rows = t[R_NROWS];
   if (kind == K_P1) rows += t[R_NROWS1];
   const bool run = rows > 0;
-  if (ok && run && kind == K_OPROJ) ok = c.wait_counter(bar_index(p, l, p.bl.comb), p.n_comb_sms) && c.stage_x();
-  if (ok && run && kind == K_DOWNALL) ok = c.wait_counter(bar_index(p, l, p.bl.up), p.n_up_sms) && c.stage_x();
   float* res = S.red + (S.cchunk[c.warp] & 1u) * kPartFloats;
-  if (ok && run) {
-    const int K = t[R_K];
-    ok = K <= 256 ? c.gemv_row<1>(res) : K <= 768 ? c.gemv_row<3>(res)
-       : K <= 2048 ? c.gemv_row<8>(res) : c.gemv_row<16>(res);
-    ok = ok && c.csync();
+  if (kind == K_MRED) {
+    if (ok && run) ok = c.moe_reduce(res);
+  } else {
+    if (ok && run && kind == K_OPROJ) ok = c.wait_counter(bar_index(p, l, p.bl.comb), p.n_comb_sms) && c.stage_x();
+    if (ok && run) {
+      const int K = t[R_K];
+      ok = K <= 256 ? c.gemv_row<1>(res) : K <= 768 ? c.gemv_row<3>(res)
+         : K <= 2048 ? c.gemv_row<8>(res) : c.gemv_row<16>(res);
+      ok = ok && c.csync();
+    }
+    if (ok && run) {
+      c.epilogue_row(res);
+      if (c.tid == 0) S.t_mark[2] = gtime_ns();
+    }
+    // an UP piece goes on with its columns of the down projection
+    if (ok && run && kind == K_UP) ok = c.csync() && c.down_part();
   }
-  if (ok && run) {
-    c.epilogue_row(res);
-    if (c.tid == 0) S.t_mark[2] = gtime_ns();
-    if (c.lane == 0) S.cchunk[c.warp]++;
-  }
+  if (ok && run && c.lane == 0) S.cchunk[c.warp]++;
   if (ok && (flags & FL_LAST)) ok = c.complete();
   c.save();
   return ok;

@@ -18,6 +18,10 @@
 //   DOWN    its hidden rows of every routed expert's down projection, weighted
 //           by the routing: the expert branch's share of the residual update
 //   OUT     its hidden rows of the O-proj: the attention branch's share
+// With one token there is no DOWN wave: each UP slice (whole groups of 8
+// intermediate columns) also multiplies its columns of the down projection,
+// giving one partial hidden vector per group, and OUT adds the groups'
+// partials of its rows in group order.
 // and after the last layer FINAL: local final norm and its LM-head rows.  The
 // next layer adds both shares to the residual.
 #pragma once
@@ -145,6 +149,9 @@ struct Params {
   const uint16_t* const* w_down;
   uint16_t* const* k_pool;
   uint16_t* const* v_pool;
+  const uint8_t* wd_maps;      // [L][8] tensor maps of w_down as 2-D [E * H rows][I], boxes
+                               // of 8 n columns x 256 rows, n = 1..8 (one token: column slices)
+  const uint8_t* mp_map;       // tensor map of mpart: 2-D [groups][H] fp32, boxes 32 x 256
   const uint8_t* kv_maps;      // [L][2] tensor maps (128 bytes each) of the K and V pools:
                                // 2-D [rows = pages * hkv * page_size][d], boxes of
                                // 64 dims x (hkv * page_size) rows, 128-byte swizzle
@@ -186,6 +193,8 @@ struct Params {
   float* abuf;       // [L][Bmax * k][I] expert hidden, by grouped slot
   float* oproj;      // [L][Bmax][H] O-proj output
   float* moe;        // [L][Bmax][H] weighted sum of the routed experts' outputs
+  float* mpart;      // one token: [k * I / 8][H] the down projection of each 8-column
+                     // group of the routed experts' hidden vectors, weighted
 };
 
 }  // namespace mk

@@ -63,9 +63,10 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, i
       : "memory");
 }
 
-// L2 prefetch of [src, src + bytes) (src and bytes multiples of 16)
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+// orders this thread's earlier (acquired) view of global memory before its
+// later async-proxy (bulk copy) reads
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
