@@ -453,9 +453,22 @@ struct Prod {
   // 256 rows per stage (one box of the n-group map: whole row pieces, so the
   // copy engine moves 16 n bytes per row request).
   __device__ __noinline__ bool do_up1(int a0, int a1) {
-    const int H = p.H, G = p.I / 8;
+    const int H = p.H, G = p.I / 8, n_act = S.rt.n_act;
     int g0 = 0, g1 = 0;
-    if (a0 >= 0) dshare(S.rt.n_act * G, a1, a0, g0, g1);
+    if (a0 >= 0) {
+      if (a1 >= n_act) {
+        // at least one slice per expert: expert a takes slices
+        // [a * a1 / n_act, (a + 1) * a1 / n_act), so no slice spans two experts
+        int a = 0;
+        while ((long long)(a + 1) * a1 / n_act <= a0) a++;
+        const int s0 = (int)((long long)a * a1 / n_act), s1 = (int)((long long)(a + 1) * a1 / n_act);
+        dshare(G, s1 - s0, a0 - s0, g0, g1);
+        g0 += a * G;
+        g1 += a * G;
+      } else {
+        dshare(n_act * G, a1, a0, g0, g1);
+      }
+    }
     if (g1 <= g0) return chunk(K_UP, FL_LAST, 0, 0, 2, H, 0, 0, 0, 0, nullptr, nullptr);
     const uint8_t* wdm = p.wd_maps + (size_t)l * 8 * 128;
     for (int g = g0; g < g1;) {
@@ -528,15 +541,26 @@ struct Prod {
     return true;
   }
 
-  // OUT: O-proj rows [a0, a1) (needs no routing).  One token: then the
-  // experts' per-group partials of the same rows (K_MRED), streamed once every
-  // UP slice has written them: 256 groups x 32 rows per stage.
+  // OUT: O-proj rows [a0, a1) (needs no routing)
   __device__ __noinline__ bool do_out(int a0, int a1) {
     const int B = p.B;
     const int KO = p.hq * p.d;
+    if (a1 <= a0) return chunk(K_OPROJ, FL_LAST, 0, 0, 1, KO, B, 0, 0, 0, nullptr, nullptr);
+    const int co = B == 1 ? kRowChunk : gemv_chunk_rows(KO, B);
+    for (int c0 = a0; c0 < a1; c0 += co)
+      if (!chunk(K_OPROJ, c0 + co >= a1 ? FL_LAST : 0, c0, min(co, a1 - c0), 1, KO, B, 0, 0, 0, wptr(2),
+                 nullptr))
+        return false;
+    return true;
+  }
+
+  // DOWN: hidden rows [a0, a1) of every routed expert's down projection.
+  // One token: the sum of the UP slices' per-group partials of those rows
+  // (K_MRED), streamed once every UP slice has written them: 256 groups x 32
+  // rows per stage.
+  __device__ __noinline__ bool do_down(int a0, int a1) {
+    const int H = p.H, B = p.B;
     if (B == 1) {
-      for (int c0 = a0; c0 < a1; c0 += kRowChunk)
-        if (!chunk(K_OPROJ, 0, c0, min(kRowChunk, a1 - c0), 1, KO, 1, 0, 0, 0, wptr(2), nullptr)) return false;
       int32_t* w = begin();
       if (!w) return false;
       if (lane == 0) {
@@ -570,18 +594,6 @@ struct Prod {
         }
       return true;
     }
-    if (a1 <= a0) return chunk(K_OPROJ, FL_LAST, 0, 0, 1, KO, B, 0, 0, 0, nullptr, nullptr);
-    const int co = B == 1 ? kRowChunk : gemv_chunk_rows(KO, B);
-    for (int c0 = a0; c0 < a1; c0 += co)
-      if (!chunk(K_OPROJ, c0 + co >= a1 ? FL_LAST : 0, c0, min(co, a1 - c0), 1, KO, B, 0, 0, 0, wptr(2),
-                 nullptr))
-        return false;
-    return true;
-  }
-
-  // DOWN: hidden rows [a0, a1) of every routed expert's down projection
-  __device__ __noinline__ bool do_down(int a0, int a1) {
-    const int H = p.H, B = p.B;
     if (!wait_route()) return false;
     const int n_act = S.rt.n_act;
     if (a1 <= a0 || n_act == 0) return chunk(K_DOWN, FL_LAST, 0, 0, 1, p.I, 0, 0, 0, 0, nullptr, nullptr);

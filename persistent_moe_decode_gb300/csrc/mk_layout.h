@@ -18,10 +18,10 @@
 //   DOWN    its hidden rows of every routed expert's down projection, weighted
 //           by the routing: the expert branch's share of the residual update
 //   OUT     its hidden rows of the O-proj: the attention branch's share
-// With one token there is no DOWN wave: each UP slice (whole groups of 8
-// intermediate columns) also multiplies its columns of the down projection,
-// giving one partial hidden vector per group, and OUT adds the groups'
-// partials of its rows in group order.
+// With one token each UP slice (whole groups of 8 intermediate columns) also
+// multiplies its columns of the down projection, giving one partial hidden
+// vector per group, and DOWN adds the groups' partials of its rows in group
+// order.
 // and after the last layer FINAL: local final norm and its LM-head rows.  The
 // next layer adds both shares to the residual.
 #pragma once

@@ -92,10 +92,9 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
   const bool roles = n_attn < n_sm;
   const int nmoe = roles ? n_sm - n_attn : moe_sms(c, n_sm);
   const int ncomb = roles ? n_attn : n_sm;
-  // one token: the UP slices also produce the down projection's per-group
-  // partials (no DOWN wave); OUT adds them up
-  const bool fused = batch == 1;
-  const int ndown = fused ? 0 : roles ? n_sm - n_attn : n_sm;
+  // (one token: the UP slices also produce the down projection's per-group
+  // partials and the DOWN wave adds them up, row by row)
+  const int ndown = roles ? n_sm - n_attn : n_sm;
 
   static const int orders[3][7] = {
       {OP_P1, OP_ROUTE, OP_ATTN, OP_UP, OP_COMBINE, OP_DOWN, OP_OUT},
@@ -126,7 +125,6 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
     for (int l = 0; l < L; l++) {
       for (int k = 0; k < nops; k++) {
         const int op = ops[k];
-        if (op == OP_DOWN && fused) continue;
         int lo = 0, hi = 0;
         switch (op) {
           case OP_P1: share(rows1, n_sm, s, &lo, &hi); break;

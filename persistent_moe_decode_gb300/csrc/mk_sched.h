@@ -28,8 +28,8 @@ int validate_config(const mk_config& c);
 // (P1, ATTN, COMBINE, OUT), the others the expert branch (P1, ROUTE, UP,
 // DOWN, OUT), so the two branches run side by side and only the O-proj (OUT,
 // on every SM) follows the attention; with n_attn == n_sm every SM runs every
-// phase in the configured wave order.  With one token there is no DOWN wave
-// (the UP slices produce the down projection's partials).  `bump_layer` / `bump`
+// phase in the configured wave order.  With one token the UP slices also
+// produce the down projection's per-group partials and DOWN sums them.  `bump_layer` / `bump`
 // make the P1 task of that layer wait for a counter value that is never
 // reached (testing aid for the timeout path).
 int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, int bump_layer = -1,
