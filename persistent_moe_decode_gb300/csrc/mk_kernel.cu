@@ -93,6 +93,7 @@ struct __align__(128) Smem {
 // the dynamic shared memory is rounded up to a 1024-byte boundary (the
 // swizzled tensor copies of KV pages need it), hence the extra 1 KB
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kOutRows * kMaxBatch >= 64 * kConsumerWarps, "split GEMV partials live in acc_m");
 static_assert(kSmemBytes <= 232448, "shared memory of one block exceeds the sm_103a limit");
 
 // resolved task words (written by the producer into the task ring)
@@ -197,6 +198,13 @@ __device__ __forceinline__ int attn_pps(const Params& p) {
 __device__ __forceinline__ void dshare(int total, int n, int s, int& lo, int& hi) {
   lo = (int)((long long)total * s / n);
   hi = (int)((long long)total * (s + 1) / n);
+}
+
+// one token: rows of a P1 / O-proj chunk.  With K = 2048 or 4096 the
+// consumers split the contraction over the warps and hold at most 64 rows'
+// partial sums, so every chunk (whatever the SM count) takes that path.
+__device__ __forceinline__ int split_rows(int K) {
+  return (K % 2048 == 0 && K <= 4096) ? 64 : kRowChunk;
 }
 
 // ===================================================================== producer
@@ -372,8 +380,9 @@ struct Prod {
   __device__ __noinline__ bool do_p1_final_1(int a0, int a1) {
     const int H = p.H;
     if (a1 <= a0) return chunk(op == OP_P1 ? K_P1 : K_LM, FL_FIRST | FL_LAST, 0, 0, 1, H, 1, 0, 0, 0, nullptr, nullptr);
-    for (int c0 = a0; c0 < a1; c0 += kRowChunk) {
-      const int c1 = min(a1, c0 + kRowChunk);
+    const int cr = op == OP_P1 ? split_rows(H) : kRowChunk;
+    for (int c0 = a0; c0 < a1; c0 += cr) {
+      const int c1 = min(a1, c0 + cr);
       const int flags = (c0 == a0 ? FL_FIRST : 0) | (c1 == a1 ? FL_LAST : 0) |
                         (op == OP_P1 && c1 == a1 && a0 < p.E ? FL_RTR : 0);
       if (op == OP_FINAL) {
@@ -546,7 +555,7 @@ struct Prod {
     const int B = p.B;
     const int KO = p.hq * p.d;
     if (a1 <= a0) return chunk(K_OPROJ, FL_LAST, 0, 0, 1, KO, B, 0, 0, 0, nullptr, nullptr);
-    const int co = B == 1 ? kRowChunk : gemv_chunk_rows(KO, B);
+    const int co = B == 1 ? split_rows(KO) : gemv_chunk_rows(KO, B);
     for (int c0 = a0; c0 < a1; c0 += co)
       if (!chunk(K_OPROJ, c0 + co >= a1 ? FL_LAST : 0, c0, min(co, a1 - c0), 1, KO, B, 0, 0, 0, wptr(2),
                  nullptr))
@@ -1155,6 +1164,10 @@ struct Cons {
     const int K = t[R_K];
     const int ngrp = row_groups();
     const int rps = rows_per_stage(K);
+    // K is below 256 (one partial chunk per lane) or a multiple of 256 (whole
+    // chunks): the chunk test is warp-uniform except in the first case
+    const int nch = K >= 256 ? K / 256 : 1;
+    const bool lane_on = K >= 256 || lane * 8 < K;
     float xa[NCK][8];
     row_load_x<NCK>(xa, S.xs, K);
     int rbase = 0;
@@ -1171,7 +1184,7 @@ struct Cons {
           float a0 = 0.f, a1 = 0.f;
 #pragma unroll
           for (int c = 0; c < NCK; c++) {
-            if ((lane + 32 * c) * 8 < K) {
+            if (c < nch && lane_on) {
               const uint4 w = lds128(wrow + (lane + 32 * c) * 16);
               a0 = fmaf(bf16lo(w.x), xa[c][0], a0);
               a1 = fmaf(bf16hi(w.x), xa[c][1], a1);
@@ -1193,6 +1206,105 @@ struct Cons {
       rbase += nr;
     }
     if (tid == 0) S.t_mark[1] = gtime_ns();
+    return true;
+  }
+
+  // one token, few rows per warp (P1 and O-proj chunks of at most 64 rows, K
+  // 2048 or 4096): the contraction is split over the warps instead of the
+  // rows.  Warp w takes columns [w K / 8, (w + 1) K / 8), lane l the 8-column
+  // chunks l, l + 32 of that range, so each warp holds only its eighth of x
+  // in registers.  A stage's RB = 8 / NC rows are reduced over the lanes
+  // together (transposed butterfly: 9 shuffles for 8 rows, 6 for 4); the
+  // eight warp sums of a row meet in shared memory (acc_m, [row][warp]) and
+  // are added in warp order after the barrier.
+  template <int NC>
+  __device__ __forceinline__ bool gemv_split(float* res) {
+    constexpr int RB = 8 / NC;                    // rows per stage (32 KB of 2 K-byte rows)
+    const int K = t[R_K];
+    const int ngrp = row_groups();
+    const int col0 = warp * (K / 8) + lane * 8;
+    float xa[NC][8];
+#pragma unroll
+    for (int c = 0; c < NC; c++) {
+      const float4 a = *(const float4*)(S.xs + col0 + 256 * c);
+      const float4 b = *(const float4*)(S.xs + col0 + 256 * c + 4);
+      xa[c][0] = a.x; xa[c][1] = a.y; xa[c][2] = a.z; xa[c][3] = a.w;
+      xa[c][4] = b.x; xa[c][5] = b.y; xa[c][6] = b.z; xa[c][7] = b.w;
+    }
+    float* part = &S.acc_m[0][0];
+    int rbase = 0;
+    for (int g = 0; g < ngrp; g++) {
+      const int nr = group_rows(g);
+      for (int done = 0; done < nr; done += RB) {
+        const int rows = min(RB, nr - done);
+        uint32_t slot;
+        if (!stage_full(slot)) return false;
+        if (tid == 0 && rbase + done == 0) S.t_mark[0] = gtime_ns();
+        const uint8_t* base = S.stage[slot] + col0 * 2;
+        float v[RB];
+#pragma unroll
+        for (int r = 0; r < RB; r++) {
+          float a0 = 0.f, a1 = 0.f;
+          if (r < rows) {
+            const uint8_t* wrow = base + (size_t)r * K * 2;
+#pragma unroll
+            for (int c = 0; c < NC; c++) {
+              const uint4 w = lds128(wrow + c * 512);
+              a0 = fmaf(bf16lo(w.x), xa[c][0], a0);
+              a1 = fmaf(bf16hi(w.x), xa[c][1], a1);
+              a0 = fmaf(bf16lo(w.y), xa[c][2], a0);
+              a1 = fmaf(bf16hi(w.y), xa[c][3], a1);
+              a0 = fmaf(bf16lo(w.z), xa[c][4], a0);
+              a1 = fmaf(bf16hi(w.z), xa[c][5], a1);
+              a0 = fmaf(bf16lo(w.w), xa[c][6], a0);
+              a1 = fmaf(bf16hi(w.w), xa[c][7], a1);
+            }
+          }
+          v[r] = a0 + a1;
+        }
+        stage_release(slot);
+        // transposed butterfly: each step halves the values a lane holds
+        float u[4];
+        if (RB == 8) {
+          const bool h = lane & 16;
+#pragma unroll
+          for (int j = 0; j < 4; j++) u[j] = (h ? v[j + 4] : v[j]) + __shfl_xor_sync(0xffffffffu, h ? v[j] : v[j + 4], 16);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; j++) u[j] = v[j % RB];
+        }
+        float w2[2];
+        {
+          const int o = RB == 8 ? 8 : 16;
+          const bool h = lane & o;
+#pragma unroll
+          for (int j = 0; j < 2; j++) w2[j] = (h ? u[j + 2] : u[j]) + __shfl_xor_sync(0xffffffffu, h ? u[j] : u[j + 2], o);
+        }
+        float q;
+        {
+          const int o = RB == 8 ? 4 : 8;
+          const bool h = lane & o;
+          q = (h ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, h ? w2[0] : w2[1], o);
+        }
+        // RB = 8: lane l now holds row (l >> 2) & 7 over lanes with equal l & 3;
+        // RB = 4: row (l >> 3) & 3 over lanes with equal l & 7
+        if (RB == 4) q += __shfl_xor_sync(0xffffffffu, q, 4);
+        q += __shfl_xor_sync(0xffffffffu, q, 2);
+        q += __shfl_xor_sync(0xffffffffu, q, 1);
+        const int row = RB == 8 ? (lane >> 2) & 7 : (lane >> 3) & 3;
+        if ((lane & (RB == 8 ? 3 : 7)) == 0 && row < rows)
+          part[(rbase + done + row) * kConsumerWarps + warp] = q;
+      }
+      rbase += nr;
+    }
+    if (tid == 0) S.t_mark[1] = gtime_ns();
+    if (!csync()) return false;
+    if (tid < rbase) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; w++) v += part[tid * kConsumerWarps + w];
+      res[tid] = v;
+    }
     return true;
   }
 
@@ -1989,8 +2101,10 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
     if (ok && run && kind == K_OPROJ) ok = c.wait_counter(bar_index(p, l, p.bl.comb), p.n_comb_sms) && c.stage_x();
     if (ok && run) {
       const int K = t[R_K];
-      ok = K <= 256 ? c.gemv_row<1>(res) : K <= 768 ? c.gemv_row<3>(res)
-         : K <= 2048 ? c.gemv_row<8>(res) : c.gemv_row<16>(res);
+      const bool split = (kind == K_P1 || kind == K_OPROJ) && rows <= 64 && split_rows(K) == 64;
+      if (split) ok = K == 2048 ? c.gemv_split<1>(res) : c.gemv_split<2>(res);
+      else ok = K <= 256 ? c.gemv_row<1>(res) : K <= 768 ? c.gemv_row<3>(res)
+              : K <= 2048 ? c.gemv_row<8>(res) : c.gemv_row<16>(res);
       ok = ok && c.csync();
     }
     if (ok && run) {
