@@ -247,7 +247,7 @@ struct Prod {
   }
 
   // reserve the next task slot, zero it and write the header; nullptr on give-up
-  __device__ __noinline__ int32_t* begin() {
+  __device__ __forceinline__ int32_t* begin() {
     const uint32_t slot = task_seq % kTaskSlots;
     if (!wait_phase(p, &S.tempty[slot], ((task_seq / kTaskSlots) & 1u) ^ 1u, ti, op)) return nullptr;
     int32_t* w = S.task[slot];
@@ -268,14 +268,14 @@ struct Prod {
     task_seq++;
   }
 
-  __device__ __noinline__ bool acquire_stage(uint32_t& slot) {
+  __device__ __forceinline__ bool acquire_stage(uint32_t& slot) {
     slot = stage_seq % kStages;
     return wait_phase(p, &S.empty[slot], ((stage_seq / kStages) & 1u) ^ 1u, ti, op);
   }
 
   // rows [row0, row0 + nrows) of a row-major [*, K] matrix, whole rows, one
   // bulk copy per stage
-  __device__ __noinline__ bool stream_rows(const uint16_t* w, int row0, int nrows, int K) {
+  __device__ __forceinline__ bool stream_rows(const uint16_t* w, int row0, int nrows, int K) {
     const int rps = rows_per_stage(K);
     for (int done = 0; done < nrows; done += rps) {
       const int rows = min(rps, nrows - done);
@@ -297,7 +297,7 @@ struct Prod {
   // page ids are read 32 at a time (lane k holds page c0 + k), the next 32
   // requested while the current ones stream, so no stage waits on a
   // page-table read.
-  __device__ __noinline__ bool stream_attn(int b, int pg0, int npages) {
+  __device__ __forceinline__ bool stream_attn(int b, int pg0, int npages) {
     const int pb = attn_page_bytes(p);
     const int pps = attn_pps(p);                 // a power of two <= 8: divides 32
     const int rows = p.hkv * p.P;
@@ -335,7 +335,7 @@ struct Prod {
   }
 
   // one GEMV chunk of nblk blocks x nrows rows: publish, then stream each block
-  __device__ __noinline__ bool chunk(int kind, int flags, int row0, int nrows, int nblk, int K, int nt,
+  __device__ __forceinline__ bool chunk(int kind, int flags, int row0, int nrows, int nblk, int K, int nt,
                                         int a, int e, int rel0, const uint16_t* w0, const uint16_t* w1) {
     int32_t* w = begin();
     if (!w) return false;
@@ -358,7 +358,7 @@ struct Prod {
   }
 
   // rows [lo, hi) of w in chunks of cr; `first` / `last` mark the task's ends
-  __device__ __noinline__ bool rows_task(int kind, const uint16_t* w, int lo, int hi, int cr, int K,
+  __device__ __forceinline__ bool rows_task(int kind, const uint16_t* w, int lo, int hi, int cr, int K,
                                             int nt, bool first, bool last, int last_extra = 0) {
     for (int c0 = lo; c0 < hi; c0 += cr) {
       const int flags = (first && c0 == lo ? FL_FIRST : 0) | (last && c0 + cr >= hi ? FL_LAST | last_extra : 0);
@@ -368,7 +368,7 @@ struct Prod {
   }
 
   // the routing of layer l is in shared memory (written by this block's consumers)
-  __device__ __noinline__ bool wait_route() {
+  __device__ __forceinline__ bool wait_route() {
     if ((int)route_seen > l) return true;
     if (!wait_phase(p, &S.route_bar, (uint32_t)l & 1u, ti, op, 2)) return false;
     route_seen = l + 1;
@@ -377,7 +377,7 @@ struct Prod {
 
   // one-token P1 / FINAL: chunks of up to kRowChunk rows; a P1 chunk holds its
   // router rows and its QKV rows as two groups
-  __device__ __noinline__ bool do_p1_final_1(int a0, int a1) {
+  __device__ __forceinline__ bool do_p1_final_1(int a0, int a1) {
     const int H = p.H;
     if (a1 <= a0) return chunk(op == OP_P1 ? K_P1 : K_LM, FL_FIRST | FL_LAST, 0, 0, 1, H, 1, 0, 0, 0, nullptr, nullptr);
     const int cr = op == OP_P1 ? split_rows(H) : kRowChunk;
@@ -411,7 +411,7 @@ struct Prod {
     return true;
   }
 
-  __device__ __noinline__ bool do_p1_final(int a0, int a1) {
+  __device__ __forceinline__ bool do_p1_final(int a0, int a1) {
     const int H = p.H, B = p.B;
     if (B == 1) return do_p1_final_1(a0, a1);
     const int cr = gemv_chunk_rows(H, B);
@@ -429,7 +429,7 @@ struct Prod {
     return true;
   }
 
-  __device__ __noinline__ bool do_attn() {
+  __device__ __forceinline__ bool do_attn() {
     const int pps = attn_pps(p);
     const int sm = blockIdx.x;
     const int i0 = p.attn_sm_off[sm], i1 = p.attn_sm_off[sm + 1];
@@ -461,7 +461,7 @@ struct Prod {
   // gate rows, its up rows and then its 8 n columns of the down projection,
   // 256 rows per stage (one box of the n-group map: whole row pieces, so the
   // copy engine moves 16 n bytes per row request).
-  __device__ __noinline__ bool do_up1(int a0, int a1) {
+  __device__ __forceinline__ bool do_up1(int a0, int a1) {
     const int H = p.H, G = p.I / 8, n_act = S.rt.n_act;
     int g0 = 0, g1 = 0;
     if (a0 >= 0) {
@@ -519,7 +519,7 @@ struct Prod {
     return true;
   }
 
-  __device__ __noinline__ bool do_up(int a0, int a1) {
+  __device__ __forceinline__ bool do_up(int a0, int a1) {
     const int H = p.H;
     if (!wait_route()) return false;
     if (p.B == 1) return do_up1(a0, a1);
@@ -551,7 +551,7 @@ struct Prod {
   }
 
   // OUT: O-proj rows [a0, a1) (needs no routing)
-  __device__ __noinline__ bool do_out(int a0, int a1) {
+  __device__ __forceinline__ bool do_out(int a0, int a1) {
     const int B = p.B;
     const int KO = p.hq * p.d;
     if (a1 <= a0) return chunk(K_OPROJ, FL_LAST, 0, 0, 1, KO, B, 0, 0, 0, nullptr, nullptr);
@@ -567,7 +567,7 @@ struct Prod {
   // One token: the sum of the UP slices' per-group partials of those rows
   // (K_MRED), streamed once every UP slice has written them: 256 groups x 32
   // rows per stage.
-  __device__ __noinline__ bool do_down(int a0, int a1) {
+  __device__ __forceinline__ bool do_down(int a0, int a1) {
     const int H = p.H, B = p.B;
     if (B == 1) {
       int32_t* w = begin();
@@ -1533,7 +1533,7 @@ struct Cons {
         rt.act[rank] = my_e;
         rt.off[rank] = rank;
         rt.ent[rank] = lane;
-        if (blockIdx.x == p.n_sm - 1) {   // an SM of the expert branch keeps the routing
+        if (blockIdx.x == 0) {   // block 0 is an expert-branch SM whenever the SMs take roles
           p.ridx[(size_t)l * p.Bmax * K + lane] = my_e;
           p.rw[(size_t)l * p.Bmax * K + lane] = w;
         }
@@ -1605,7 +1605,7 @@ struct Cons {
         for (int j = 0; j < K; j++) {
           const float w = expf(rt.w[n][j] - top) / den;
           rt.w[n][j] = w;
-          if (blockIdx.x == p.n_sm - 1) {   // an SM of the expert branch
+          if (blockIdx.x == 0) {   // block 0 routes in every schedule
             p.ridx[((size_t)l * Bm + n) * K + j] = rt.idx[n][j];
             p.rw[((size_t)l * Bm + n) * K + j] = w;
           }

@@ -114,7 +114,7 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
     if (!roles) {
       ops = orders[c.wave_order];
       nops = 7;
-    } else if (s < n_attn) {
+    } else if (is_attn_sm(s, n_sm, n_attn)) {
       ops = attn_role;
       nops = 4;
     } else {
@@ -128,15 +128,15 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
         int lo = 0, hi = 0;
         switch (op) {
           case OP_P1: share(rows1, n_sm, s, &lo, &hi); break;
-          case OP_COMBINE: share(units, ncomb, s, &lo, &hi); break;
+          case OP_COMBINE: share(units, ncomb, roles ? attn_before(s, n_sm, n_attn) : s, &lo, &hi); break;
           case OP_OUT: share(c.hidden, n_sm, s, &lo, &hi); break;
           case OP_DOWN: {
-            const int slice = roles ? s - n_attn : s;
+            const int slice = roles ? moe_rank(s, n_sm, n_attn) : s;
             share(c.hidden, ndown, slice, &lo, &hi);
             break;
           }
           case OP_UP: {
-            const int slice = roles ? s - n_attn : s;
+            const int slice = roles ? moe_rank(s, n_sm, n_attn) : s;
             lo = slice < nmoe ? slice : -1;
             hi = nmoe;
             break;
@@ -203,7 +203,7 @@ int split_kv(const mk_config& c, int n_sm, int n_attn, int batch, const int32_t*
       for (int t0 = 0; t0 < keys; t0 += split) add(b, t0, std::min(keys, t0 + split));
     }
     for (int s = 0; s <= n_sm; s++)
-      (*sm_off)[s] = (int32_t)(s >= na ? n_items : n_items * s / na);
+      (*sm_off)[s] = (int32_t)(n_items * attn_before(s, n_sm, na) / na);
   } else {
     // balanced: the concatenated pages of all sequences cut into na equal runs
     std::vector<long long> first(batch + 1, 0);
@@ -212,8 +212,9 @@ int split_kv(const mk_config& c, int n_sm, int n_attn, int batch, const int32_t*
     int b = 0;
     for (int s = 0; s < n_sm; s++) {
       (*sm_off)[s] = (int32_t)(items->size() / 8);
-      if (s >= na) continue;
-      const long long g0 = T * s / na, g1 = T * (s + 1) / na;
+      if (!is_attn_sm(s, n_sm, na)) continue;
+      const int r = attn_before(s, n_sm, na);
+      const long long g0 = T * r / na, g1 = T * (r + 1) / na;
       while (b < batch && first[b + 1] <= g0) b++;
       for (int bb = b; bb < batch && first[bb] < g1; bb++) {
         const long long p0 = std::max(g0, first[bb]) - first[bb];

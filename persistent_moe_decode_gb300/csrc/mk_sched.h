@@ -24,7 +24,7 @@ int validate_config(const mk_config& c);
 
 // Per-SM task lists of one step for `batch` sequences: for every layer one
 // task of each phase per SM, then the FINAL task.  With n_attn < n_sm the SMs
-// take roles: SMs [0, n_attn) run the attention branch of the parallel layer
+// take roles: n_attn SMs spread over the blocks run the attention branch of the parallel layer
 // (P1, ATTN, COMBINE, OUT), the others the expert branch (P1, ROUTE, UP,
 // DOWN, OUT), so the two branches run side by side and only the O-proj (OUT,
 // on every SM) follows the attention; with n_attn == n_sm every SM runs every
@@ -40,6 +40,17 @@ inline void share(long long total, int n, int s, int* lo, int* hi) {
   *lo = (int)(total * s / n);
   *hi = (int)(total * (s + 1) / n);
 }
+
+// SM roles: the na attention SMs of a role split are spread evenly over the
+// n_sm blocks (so the attention branch's KV streams do not crowd one part of
+// the chip).  SM s is an attention SM if the running count floor(s na / n_sm)
+// steps at s; attention SMs before s: floor(s na / n_sm).
+inline int attn_before(int s, int n_sm, int na) { return (int)((long long)s * na / n_sm); }
+inline bool is_attn_sm(int s, int n_sm, int na) {
+  return na >= n_sm || attn_before(s + 1, n_sm, na) > attn_before(s, n_sm, na);
+}
+// index among the expert-branch SMs (for an SM that is not an attention SM)
+inline int moe_rank(int s, int n_sm, int na) { return s - attn_before(s, n_sm, na); }
 
 // SMs that take UP slices when every SM runs every phase (0 in the config = all)
 inline int moe_sms(const mk_config& c, int n_sm) {
