@@ -110,7 +110,7 @@ enum : int { K_ROUTER = 0, K_QKV = 1, K_UP = 2, K_OPROJ = 3, K_DOWN = 4, K_LM = 
 constexpr int kRowChunk = kPartFloats;
 // chunk flags: first chunk of its task (P1 / FINAL run the norm first), last
 // chunk of its task (signals completion), last block of an OUT row chunk
-enum : int { FL_FIRST = 1, FL_LAST = 2, FL_CLAST = 4, FL_RTR = 8 };   // FL_RTR: the P1 share holds router rows
+enum : int { FL_FIRST = 1, FL_LAST = 2, FL_CLAST = 4, FL_RTR = 8 };   // FL_RTR: the chunk ends its router rows
 
 // ---------------------------------------------------------------- errors
 __device__ __forceinline__ bool stopped(const Params& p) {
@@ -205,6 +205,76 @@ __device__ __forceinline__ void dshare(int total, int n, int s, int& lo, int& hi
 // partial sums, so every chunk (whatever the SM count) takes that path.
 __device__ __forceinline__ int split_rows(int K) {
   return (K % 2048 == 0 && K <= 4096) ? 64 : kRowChunk;
+}
+
+// One token: top-k of the router logits of layer l, softmax weights over the
+// picks (the top-k of the softmax = the top-k of the logits; ties to the lower
+// expert id) and the grouping, by one warp.  Lane j < k keeps the j-th pick;
+// its rank among the picks (ascending expert id) is its active slot, and with
+// one token every active expert has one entry.  keep: also store the routing
+// in global memory (for inspection).
+__device__ __forceinline__ void route_one(const Params& p, RouteTab& rt, int l, int lane, bool keep) {
+  const int E = p.E, K = p.topk;
+  float v[8];
+  const float* rl = p.rlog + (size_t)l * p.Bmax * E;
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? __ldcg(rl + e) : -INFINITY;
+  }
+  uint32_t taken = 0;
+  float my_v = -INFINITY;
+  int my_e = 0x7fffffff;
+#pragma unroll 1
+  for (int j = 0; j < K; j++) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_v = bv;
+      my_e = bi;
+    }
+  }
+  const float top = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = lane < K ? expf(my_v - top) : 0.f;
+  float den = 0.f;
+  for (int j = 0; j < K; j++) den += __shfl_sync(0xffffffffu, ex, j);   // fixed order
+  const float w = ex / den;
+  int rank = 0;
+  for (int j = 0; j < K; j++) rank += __shfl_sync(0xffffffffu, my_e, j) < my_e;
+  if (lane < K) {
+    rt.idx[0][lane] = my_e;
+    rt.w[0][lane] = w;
+    rt.act[rank] = my_e;
+    rt.off[rank] = rank;
+    rt.ent[rank] = lane;
+    if (keep) {
+      p.ridx[(size_t)l * p.Bmax * K + lane] = my_e;
+      p.rw[(size_t)l * p.Bmax * K + lane] = w;
+    }
+  }
+  if (lane == 0) {
+    rt.n_act = K;
+    rt.off[K] = K;
+  }
+  __syncwarp();
 }
 
 // ===================================================================== producer
@@ -361,9 +431,44 @@ struct Prod {
   __device__ __forceinline__ bool rows_task(int kind, const uint16_t* w, int lo, int hi, int cr, int K,
                                             int nt, bool first, bool last, int last_extra = 0) {
     for (int c0 = lo; c0 < hi; c0 += cr) {
-      const int flags = (first && c0 == lo ? FL_FIRST : 0) | (last && c0 + cr >= hi ? FL_LAST | last_extra : 0);
+      const int flags = (first && c0 == lo ? FL_FIRST : 0) | (last && c0 + cr >= hi ? FL_LAST : 0) |
+                        (c0 + cr >= hi ? last_extra : 0);
       if (!chunk(kind, flags, c0, min(cr, hi - c0), 1, K, nt, 0, 0, 0, w, nullptr)) return false;
     }
+    return true;
+  }
+
+  // bounded spin of the whole warp on a global counter; every lane's load is
+  // an acquire, so each lane's later reads see what was released with it
+  __device__ __forceinline__ bool warp_spin(int bar, uint32_t target) {
+    const uint32_t* c = p.bars + bar;
+    const unsigned long long t0 = gtime_ns();
+    for (uint32_t it = 0;; ++it) {
+      const uint32_t v = ld_acquire_u32(c);
+      if (__all_sync(0xffffffffu, v >= target)) return true;
+      __nanosleep(32);
+      if ((it & 15u) == 15u) {
+        int give = 0;
+        if (lane == 0) {
+          if (stopped(p)) {
+            give = 1;
+          } else if (gtime_ns() - t0 > p.timeout_ns) {
+            report(p, DEV_TIMEOUT, ti, op, bar, v, target);
+            give = 1;
+          }
+        }
+        if (__shfl_sync(0xffffffffu, give, 0)) return false;
+      }
+    }
+  }
+
+  // one token: the producer routes layer l itself as soon as the router
+  // logits are complete, so the experts' weights stream while the consumers
+  // still work on P1
+  __device__ __forceinline__ bool route_here() {
+    if (!warp_spin(bar_index(p, l, p.bl.rtr), (uint32_t)p.n_rtr_sms)) return false;
+    route_one(p, S.rt, l, lane, blockIdx.x == 0);
+    route_seen = l + 1;
     return true;
   }
 
@@ -377,55 +482,73 @@ struct Prod {
 
   // one-token P1 / FINAL: chunks of up to kRowChunk rows; a P1 chunk holds its
   // router rows and its QKV rows as two groups
-  __device__ __forceinline__ bool do_p1_final_1(int a0, int a1) {
+  __device__ __forceinline__ bool do_p1_final_1(int a0, int a1, int b0, int b1) {
     const int H = p.H;
-    if (a1 <= a0) return chunk(op == OP_P1 ? K_P1 : K_LM, FL_FIRST | FL_LAST, 0, 0, 1, H, 1, 0, 0, 0, nullptr, nullptr);
-    const int cr = op == OP_P1 ? split_rows(H) : kRowChunk;
+    if (op == OP_FINAL) {
+      if (a1 <= a0) return chunk(K_LM, FL_FIRST | FL_LAST, 0, 0, 1, H, 1, 0, 0, 0, nullptr, nullptr);
+      for (int c0 = a0; c0 < a1; c0 += kRowChunk) {
+        const int c1 = min(a1, c0 + kRowChunk);
+        const int flags = (c0 == a0 ? FL_FIRST : 0) | (c1 == a1 ? FL_LAST : 0);
+        if (!chunk(K_LM, flags, c0, c1 - c0, 1, H, 1, 0, 0, 0, p.lm_head, nullptr)) return false;
+      }
+      return true;
+    }
+    // P1: the router rows [a0, a1) first, in a chunk of their own that
+    // releases the router counter, then the W_qkv rows [b0, b1)
+    if (a1 <= a0 && b1 <= b0) return chunk(K_P1, FL_FIRST | FL_LAST, 0, 0, 1, H, 1, 0, 0, 0, nullptr, nullptr);
+    const int cr = split_rows(H);
+    bool first = true;
     for (int c0 = a0; c0 < a1; c0 += cr) {
       const int c1 = min(a1, c0 + cr);
-      const int flags = (c0 == a0 ? FL_FIRST : 0) | (c1 == a1 ? FL_LAST : 0) |
-                        (op == OP_P1 && c1 == a1 && a0 < p.E ? FL_RTR : 0);
-      if (op == OP_FINAL) {
-        if (!chunk(K_LM, flags, c0, c1 - c0, 1, H, 1, 0, 0, 0, p.lm_head, nullptr)) return false;
-        continue;
-      }
-      const int r0 = min(c0, p.E), r1 = min(c1, p.E);
-      const int q0 = max(c0, p.E) - p.E, q1 = max(c1, p.E) - p.E;
-      int32_t* w = begin();
-      if (!w) return false;
-      if (lane == 0) {
-        w[R_KIND] = K_P1;
-        w[R_FLAGS] = flags;
-        w[R_ROW0] = r0;
-        w[R_NROWS] = r1 - r0;
-        w[R_ROW1] = q0;
-        w[R_NROWS1] = q1 - q0;
-        w[R_NGRP] = 2;
-        w[R_K] = H;
-        w[R_NT] = 1;
-      }
-      commit();
-      if (r1 > r0 && !stream_rows(wptr(0), r0, r1 - r0, H)) return false;
-      if (q1 > q0 && !stream_rows(wptr(1), q0, q1 - q0, H)) return false;
+      const int flags = (first ? FL_FIRST : 0) | (c1 == a1 ? FL_RTR : 0) | (c1 == a1 && b1 <= b0 ? FL_LAST : 0);
+      if (!p1_chunk(flags, c0, c1 - c0, 0, 0)) return false;
+      first = false;
+    }
+    for (int c0 = b0; c0 < b1; c0 += cr) {
+      const int c1 = min(b1, c0 + cr);
+      const int flags = (first ? FL_FIRST : 0) | (c1 == b1 ? FL_LAST : 0);
+      if (!p1_chunk(flags, 0, 0, c0, c1 - c0)) return false;
+      first = false;
     }
     return true;
   }
 
-  __device__ __forceinline__ bool do_p1_final(int a0, int a1) {
+  // one-token P1 chunk: router rows [r0, r0 + nr), then W_qkv rows [q0, q0 + nq)
+  __device__ __forceinline__ bool p1_chunk(int flags, int r0, int nr, int q0, int nq) {
+    const int H = p.H;
+    int32_t* w = begin();
+    if (!w) return false;
+    if (lane == 0) {
+      w[R_KIND] = K_P1;
+      w[R_FLAGS] = flags;
+      w[R_ROW0] = r0;
+      w[R_NROWS] = nr;
+      w[R_ROW1] = q0;
+      w[R_NROWS1] = nq;
+      w[R_NGRP] = 2;
+      w[R_K] = H;
+      w[R_NT] = 1;
+    }
+    commit();
+    if (nr > 0 && !stream_rows(wptr(0), r0, nr, H)) return false;
+    if (nq > 0 && !stream_rows(wptr(1), q0, nq, H)) return false;
+    return true;
+  }
+
+  __device__ __forceinline__ bool do_p1_final(int a0, int a1, int b0, int b1) {
     const int H = p.H, B = p.B;
-    if (B == 1) return do_p1_final_1(a0, a1);
+    if (B == 1) return do_p1_final_1(a0, a1, b0, b1);
     const int cr = gemv_chunk_rows(H, B);
     if (op == OP_FINAL) {
       if (a1 <= a0) return chunk(K_LM, FL_FIRST | FL_LAST, 0, 0, 1, H, B, 0, 0, 0, nullptr, nullptr);
       return rows_task(K_LM, p.lm_head, a0, a1, cr, H, B, true, true);
     }
-    // P1: rows [a0, a1) of [W_router; W_qkv]
-    const int r0 = min(a0, p.E), r1 = min(a1, p.E);
-    const int q0 = max(a0, p.E) - p.E, q1 = max(a1, p.E) - p.E;
+    // P1: router rows [a0, a1) (the last of their chunks releases the router
+    // counter), then W_qkv rows [b0, b1)
+    const int r0 = a0, r1 = a1, q0 = b0, q1 = b1;
     if (r1 <= r0 && q1 <= q0) return chunk(K_ROUTER, FL_FIRST | FL_LAST, 0, 0, 1, H, B, 0, 0, 0, nullptr, nullptr);
-    const int rtr = r1 > r0 ? FL_RTR : 0;
-    if (r1 > r0 && !rows_task(K_ROUTER, wptr(0), r0, r1, cr, H, B, true, q1 <= q0, rtr)) return false;
-    if (q1 > q0 && !rows_task(K_QKV, wptr(1), q0, q1, cr, H, B, r1 <= r0, true, rtr)) return false;
+    if (r1 > r0 && !rows_task(K_ROUTER, wptr(0), r0, r1, cr, H, B, true, q1 <= q0, FL_RTR)) return false;
+    if (q1 > q0 && !rows_task(K_QKV, wptr(1), q0, q1, cr, H, B, r1 <= r0, true)) return false;
     return true;
   }
 
@@ -638,9 +761,18 @@ struct Prod {
       set_layer(l);
       switch (op) {
         case OP_P1:
-        case OP_FINAL: ok = do_p1_final(a0, a1); break;
+        case OP_FINAL: {
+          const int b0 = __shfl_sync(0xffffffffu, word, F_B0);
+          const int b1 = __shfl_sync(0xffffffffu, word, F_B1);
+          ok = do_p1_final(a0, a1, b0, b1);
+          break;
+        }
         case OP_ROUTE:
         case OP_COMBINE: {
+          if (op == OP_ROUTE && p.B == 1 && !route_here()) {
+            ok = false;
+            break;
+          }
           int32_t* w = begin();
           ok = w != nullptr;
           if (ok) {
@@ -750,8 +882,7 @@ struct Cons {
     return true;
   }
 
-  // the task's last chunk is done: bump its phase counter (P1 shares that
-  // hold router rows also bump the router counter)
+  // the task's last chunk is done: bump its phase counter
   __device__ __forceinline__ bool complete() {
     const int op = t[R_OP], l = t[R_LAYER];
     int bar = -1;
@@ -763,7 +894,6 @@ struct Cons {
     if (tid == 0) {
       // release: the block's stores (ordered before this thread by the
       // barrier above) are visible before the counter moves
-      if (t[R_FLAGS] & FL_RTR) red_release_add(p.bars + bar_index(p, l, p.bl.rtr), 1u);
       red_release_add(p.bars + bar_index(p, l, bar), 1u);
     }
     return true;
@@ -1475,90 +1605,15 @@ struct Cons {
   }
 
   // ------------------------------------------------------------ routing
-  // one token: top-k, weights and the grouping in warp 0 alone.  Lane j < k
-  // keeps the j-th pick; its rank among the picks (ascending expert id) is its
-  // active slot, and with one token every active expert has one entry.
-  __device__ __forceinline__ bool route1(int l) {
-    const int E = p.E, K = p.topk;
-    RouteTab& rt = S.rt;
-    if (warp == 0) {
-      float v[8];
-      const float* rl = p.rlog + (size_t)l * p.Bmax * E;
-#pragma unroll
-      for (int i = 0; i < 8; i++) {
-        const int e = lane + 32 * i;
-        v[i] = e < E ? __ldcg(rl + e) : -INFINITY;
-      }
-      uint32_t taken = 0;
-      float my_v = -INFINITY;
-      int my_e = 0x7fffffff;
-#pragma unroll 1
-      for (int j = 0; j < K; j++) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-          const int e = lane + 32 * i;
-          if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-            bv = v[i];
-            bi = e;
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (ov > bv || (ov == bv && oi < bi)) {
-            bv = ov;
-            bi = oi;
-          }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == j) {
-          my_v = bv;
-          my_e = bi;
-        }
-      }
-      // softmax over the picks (the top-k of the softmax = the top-k of the logits)
-      const float top = __shfl_sync(0xffffffffu, my_v, 0);
-      const float ex = lane < K ? expf(my_v - top) : 0.f;
-      float den = 0.f;
-      for (int j = 0; j < K; j++) den += __shfl_sync(0xffffffffu, ex, j);   // fixed order
-      const float w = ex / den;
-      int rank = 0;
-      for (int j = 0; j < K; j++) rank += __shfl_sync(0xffffffffu, my_e, j) < my_e;
-      if (lane < K) {
-        rt.idx[0][lane] = my_e;
-        rt.w[0][lane] = w;
-        rt.act[rank] = my_e;
-        rt.off[rank] = rank;
-        rt.ent[rank] = lane;
-        if (blockIdx.x == 0) {   // block 0 is an expert-branch SM whenever the SMs take roles
-          p.ridx[(size_t)l * p.Bmax * K + lane] = my_e;
-          p.rw[(size_t)l * p.Bmax * K + lane] = w;
-        }
-      }
-      if (lane == 0) {
-        rt.n_act = K;
-        rt.off[K] = K;
-      }
-    }
-    if (tid == 0) S.t_mark[0] = gtime_ns();
-    if (!csync()) return false;
-    if (tid == 0) mbar_arrive(&S.route_bar);   // the producer may now resolve the experts
-    return true;
-  }
-
-  // top-k per token (softmax order = logit order; ties to the lower index),
-  // weights renormalised over the selected experts; then the per-expert
-  // grouping: active experts ascending, tokens ascending within an expert.
   __device__ __forceinline__ bool route() {
     const int l = t[R_LAYER];
     const int E = p.E, K = p.topk, B = p.B;
     const size_t Bm = (size_t)p.Bmax;
+    // one token: the producer warp has routed (the routing is in shared
+    // memory before this task was handed over)
+    if (B == 1) return true;
     if (!wait_counter(bar_index(p, l, p.bl.rtr), p.n_rtr_sms)) return false;
     RouteTab& rt = S.rt;
-    if (B == 1) return route1(l);
     for (int n = warp; n < B; n += kConsumerWarps) {
       float v[8];
       const float* rl = p.rlog + ((size_t)l * Bm + n) * E;
@@ -2079,6 +2134,8 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
       c.moe_write(h0, min(kOutRows, a1 - h0));
     }
   }
+  // the router rows are done: release the routing wait early
+  if (ok && (flags & FL_RTR)) ok = c.signal(bar_index(p, l, p.bl.rtr), 1);
   if (ok && (flags & FL_LAST)) ok = c.complete();
   c.save();
   return ok;
@@ -2115,6 +2172,8 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
     if (ok && run && kind == K_UP) ok = c.csync() && c.down_part();
   }
   if (ok && run && c.lane == 0) S.cchunk[c.warp]++;
+  // the router rows are done: release the routing wait early
+  if (ok && (flags & FL_RTR)) ok = c.signal(bar_index(p, l, p.bl.rtr), 1);
   if (ok && (flags & FL_LAST)) ok = c.complete();
   c.save();
   return ok;

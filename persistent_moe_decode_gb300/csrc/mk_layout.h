@@ -52,11 +52,12 @@ enum Op : int32_t {
 // descriptor words (host-built, read by the producer warp)
 enum : int {
   F_OP = 0, F_LAYER = 1,
-  F_A0 = 2, F_A1 = 3,      // op-specific range: P1 rows of [W_router; W_qkv], COMBINE
+  F_A0 = 2, F_A1 = 3,      // op-specific range: P1 rows of W_router, COMBINE
                            // units, OUT and DOWN hidden rows, FINAL vocabulary rows;
                            // UP: slice index and slice count
   F_SEQ = 4,               // position in the SM's list (error reports)
-  F_BUMP = 5               // P1 / FINAL: added to the wait target (testing aid)
+  F_BUMP = 5,              // P1 / FINAL: added to the wait target (testing aid)
+  F_B0 = 6, F_B1 = 7       // P1: rows of W_qkv (F_A0 / F_A1: rows of W_router)
 };
 
 // persistent block shape: two consumer warpgroups (8 warps) + one producer

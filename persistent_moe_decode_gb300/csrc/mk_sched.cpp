@@ -87,7 +87,7 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
     return MK_ERR_BAD_CONFIG;
   const BarLayout bl = bar_layout(c.max_batch);
   const int L = c.n_layers;
-  const long long rows1 = c.n_experts + (long long)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  const long long qrows = (long long)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
   const long long units = (long long)batch * c.n_q_heads;
   const bool roles = n_attn < n_sm;
   const int nmoe = roles ? n_sm - n_attn : moe_sms(c, n_sm);
@@ -104,6 +104,38 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
   // only wait for its own UP wave, so they run while attention is under way
   static const int attn_role[4] = {OP_P1, OP_ATTN, OP_COMBINE, OP_OUT};
   static const int moe_role[5] = {OP_P1, OP_ROUTE, OP_UP, OP_DOWN, OP_OUT};
+
+  // P1 rows.  The router rows go, 8 rows (one stage) per SM or more if there
+  // are few of them, to the first expert-branch SMs (all SMs when there are
+  // no roles); they run first and
+  // release the router counter on their own, so the routing can start soon
+  // after the norm; they take no W_qkv rows.  The W_qkv rows are split over
+  // the other SMs in proportion to their even share of all P1 rows.
+  const long long total1 = c.n_experts + qrows;
+  std::vector<int> r_lo(n_sm, 0), r_hi(n_sm, 0), q_lo(n_sm, 0), q_hi(n_sm, 0);
+  {
+    const int cand = roles ? n_sm - n_attn : n_sm;               // >= 1
+    const int per = std::max(8, (c.n_experts + cand - 1) / cand);
+    int next = 0;
+    for (int s = 0; s < n_sm && next < c.n_experts; s++) {
+      if (roles && is_attn_sm(s, n_sm, n_attn)) continue;
+      r_lo[s] = next;
+      r_hi[s] = std::min(c.n_experts, next + per);
+      next = r_hi[s];
+    }
+    std::vector<long long> wq(n_sm + 1, 0);
+    for (int pass = 0; pass < 2 && wq[n_sm] == 0; pass++)
+      for (int s = 0; s < n_sm; s++) {
+        int lo, hi;
+        share(total1, n_sm, s, &lo, &hi);
+        // router SMs take no W_qkv rows, unless every SM holds router rows
+        wq[s + 1] = wq[s] + ((pass == 0 && r_hi[s] > r_lo[s]) ? 0 : (hi - lo));
+      }
+    for (int s = 0; s < n_sm; s++) {
+      q_lo[s] = wq[n_sm] > 0 ? (int)(qrows * wq[s] / wq[n_sm]) : 0;
+      q_hi[s] = wq[n_sm] > 0 ? (int)(qrows * wq[s + 1] / wq[n_sm]) : 0;
+    }
+  }
 
   out->tasks.clear();
   out->off.assign(n_sm + 1, 0);
@@ -127,7 +159,7 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
         const int op = ops[k];
         int lo = 0, hi = 0;
         switch (op) {
-          case OP_P1: share(rows1, n_sm, s, &lo, &hi); break;
+          case OP_P1: lo = r_lo[s]; hi = r_hi[s]; break;   // router rows; W_qkv rows below
           case OP_COMBINE: share(units, ncomb, roles ? attn_before(s, n_sm, n_attn) : s, &lo, &hi); break;
           case OP_OUT: share(c.hidden, n_sm, s, &lo, &hi); break;
           case OP_DOWN: {
@@ -144,7 +176,11 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
           default: break;
         }
         Desc t = task(op, l, lo, hi);
-        if (op == OP_P1 && l == bump_layer) t[F_BUMP] = bump;
+        if (op == OP_P1) {
+          t[F_B0] = q_lo[s];
+          t[F_B1] = q_hi[s];
+          if (l == bump_layer) t[F_BUMP] = bump;
+        }
         list.push_back(t);
       }
     }
@@ -165,13 +201,10 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
   out->n_comb_sms = ncomb;
   out->n_up_sms = roles ? nmoe : n_sm;
   out->n_down_sms = ndown;
-  // P1 shares that hold router rows [0, E): SMs 0 .. the one holding row E - 1
+  // P1 shares that hold router rows (each such SM signals the router counter
+  // as soon as its router rows are done)
   int nr = 0;
-  for (int s = 0; s < n_sm; s++) {
-    int lo, hi;
-    share(rows1, n_sm, s, &lo, &hi);
-    if (hi > lo && lo < c.n_experts) nr++;
-  }
+  for (int s = 0; s < n_sm; s++) nr += r_hi[s] > r_lo[s];
   out->n_rtr_sms = nr;
   return MK_OK;
 }
