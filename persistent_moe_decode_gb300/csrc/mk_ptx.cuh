@@ -29,12 +29,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* b, uint32_t byte
                : "memory");
 }
 
-// true once the phase with the given parity has completed
+// true once the phase with the given parity has completed.  A non-blocking
+// test: the callers poll it in their own bounded loops (a suspending try_wait
+// measured slower here, its waiters resume later than the phase completes)
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 2000;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_u32(b)), "r"(parity)
