@@ -24,6 +24,7 @@
 
 namespace mk {
 cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream);
+cudaError_t relayout_down(const uint16_t* src, uint16_t* dst, int E, int H, int I);
 size_t step_smem_bytes();
 int step_kernel_regs();
 int static_counters(int device, uint32_t** out);
@@ -185,29 +186,34 @@ int make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* b
   return MK_OK;
 }
 
-// one token: tensor maps of every layer's down projection, as column slices
-// of 8 n columns (n = 1..8) x 256 rows, and of the per-group partial buffer
-// (32 x 256 fp32)
-int make_moe_maps(mk_handle* h, const mk_weights* w, float* mpart, const uint8_t** wd, const uint8_t** mp) {
+// one token: the tensor map of the per-group partial buffer (32 x 256 fp32)
+int make_moe_map(mk_handle* h, float* mpart, const uint8_t** mp) {
   const mk_config& c = h->cfg;
-  const int L = c.n_layers;
-  std::vector<CUtensorMap> maps((size_t)L * 8 + 1);
-  for (int l = 0; l < L; l++)
-    for (int n = 1; n <= 8; n++) {
-      int rc = make_map_2d(&maps[(size_t)l * 8 + n - 1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w->w_down[l],
-                           (uint64_t)c.moe_inter, (uint64_t)c.n_experts * c.hidden, (uint32_t)(8 * n), 256);
-      if (rc) return rc;
-    }
-  int rc = make_map_2d(&maps[(size_t)L * 8], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, mpart, (uint64_t)c.hidden,
+  CUtensorMap map;
+  int rc = make_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, mpart, (uint64_t)c.hidden,
                        (uint64_t)c.top_k * (c.moe_inter / 8), 32, 256);
   if (rc) return rc;
   uint8_t* d = nullptr;
-  rc = dalloc(h, &d, maps.size() * sizeof(CUtensorMap));
+  rc = dalloc(h, &d, sizeof(CUtensorMap));
   if (rc) return rc;
-  if (cudaMemcpy(d, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess)
-    return MK_ERR_CUDA;
-  *wd = d;
-  *mp = d + (size_t)L * 8 * sizeof(CUtensorMap);
+  if (cudaMemcpy(d, &map, sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess) return MK_ERR_CUDA;
+  *mp = d;
+  return MK_OK;
+}
+
+// the blocked copy of every layer's down projection ([E][I/8][H][8] per layer)
+int make_down_blocks(mk_handle* h, const mk_weights* w, const uint16_t** out) {
+  const mk_config& c = h->cfg;
+  const size_t per_layer = (size_t)c.n_experts * c.moe_inter * c.hidden;
+  uint16_t* d = nullptr;
+  int rc = dalloc(h, &d, per_layer * c.n_layers);
+  if (rc) return rc;
+  for (int l = 0; l < c.n_layers; l++)
+    if (relayout_down((const uint16_t*)w->w_down[l], d + per_layer * l, c.n_experts, c.hidden, c.moe_inter) !=
+        cudaSuccess)
+      return MK_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MK_ERR_CUDA;
+  *out = d;
   return MK_OK;
 }
 
@@ -379,7 +385,8 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
   TRY(dalloc(h, &p.oproj, Ls * Bs * H));
   TRY(dalloc(h, &p.moe, Ls * Bs * H));
   TRY(dalloc(h, &p.mpart, (size_t)K * (I / 8) * H));
-  TRY(make_moe_maps(h, w, p.mpart, &p.wd_maps, &p.mp_map));
+  TRY(make_moe_map(h, p.mpart, &p.mp_map));
+  TRY(make_down_blocks(h, w, &p.wd_blk));
   h->bar_words = kErrWords + (size_t)L * p.bl.per_layer;
   TRY(dalloc(h, &h->d_bars, h->bar_words));
   p.err = h->d_bars;

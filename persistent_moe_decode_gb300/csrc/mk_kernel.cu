@@ -108,6 +108,8 @@ enum : int { K_ROUTER = 0, K_QKV = 1, K_UP = 2, K_OPROJ = 3, K_DOWN = 4, K_LM = 
              K_MRED = 7 };
 // rows of one single-token GEMV chunk (one result per row in a 2048-float buffer)
 constexpr int kRowChunk = kPartFloats;
+// rows of an [H][8] down-projection block per stage (2048 x 16 bytes = one stage)
+constexpr int kDownRows = kStageBytes / 16;
 // chunk flags: first chunk of its task (P1 / FINAL run the norm first), last
 // chunk of its task (signals completion), last block of an OUT row chunk
 enum : int { FL_FIRST = 1, FL_LAST = 2, FL_CLAST = 4, FL_RTR = 8 };   // FL_RTR: the chunk ends its router rows
@@ -581,9 +583,9 @@ struct Prod {
 
   // one token: slice a0 of a1 over the routed experts' groups of 8
   // intermediate columns.  Each piece (one expert, n <= 8 groups) streams its
-  // gate rows, its up rows and then its 8 n columns of the down projection,
-  // 256 rows per stage (one box of the n-group map: whole row pieces, so the
-  // copy engine moves 16 n bytes per row request).
+  // gate rows, its up rows and then its n groups of the down projection from
+  // the blocked copy ([H][8] per group, contiguous): up to 2048 rows per
+  // stage, one bulk copy each.
   __device__ __forceinline__ bool do_up1(int a0, int a1) {
     const int H = p.H, G = p.I / 8, n_act = S.rt.n_act;
     int g0 = 0, g1 = 0;
@@ -602,7 +604,6 @@ struct Prod {
       }
     }
     if (g1 <= g0) return chunk(K_UP, FL_LAST, 0, 0, 2, H, 0, 0, 0, 0, nullptr, nullptr);
-    const uint8_t* wdm = p.wd_maps + (size_t)l * 8 * 128;
     for (int g = g0; g < g1;) {
       const int a = g / G;
       const int ge = min(min(g1, (a + 1) * G), g + 8);
@@ -627,16 +628,19 @@ struct Prod {
       const size_t eo = (size_t)e * p.I * H;
       if (!stream_rows(wptr(3) + eo, i0, i1 - i0, H)) return false;
       if (!stream_rows(wptr(4) + eo, i0, i1 - i0, H)) return false;
-      for (int r0 = 0; r0 < H; r0 += 256) {
-        uint32_t slot;
-        if (!acquire_stage(slot)) return false;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(ncb * 4096));
-          tma_load_2d(&S.stage[slot][0], wdm + (size_t)(ncb - 1) * 128, i0, e * H + r0, &S.full[slot]);
+      const uint16_t* blk = p.wd_blk + (((size_t)l * p.E + e) * G + i0 / 8) * H * 8;
+      for (int c = 0; c < ncb; c++)
+        for (int r0 = 0; r0 < H; r0 += kDownRows) {
+          const int rows = min(kDownRows, H - r0);
+          uint32_t slot;
+          if (!acquire_stage(slot)) return false;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(rows * 16));
+            bulk_g2s(&S.stage[slot][0], blk + ((size_t)c * H + r0) * 8, (uint32_t)(rows * 16), &S.full[slot]);
+          }
+          __syncwarp();
+          stage_seq++;
         }
-        __syncwarp();
-        stage_seq++;
-      }
       g = ge;
     }
     return true;
@@ -1474,43 +1478,35 @@ struct Cons {
   }
 
   // one token, after the gate/up rows of an UP piece: its n = ncb groups of
-  // columns of the down projection, 256 hidden rows of 16 n bytes per stage.
-  // Thread t takes row r0 + t and writes one partial per group:
+  // the down projection, each group's [H][8] block in stages of up to 2048
+  // rows.  Thread t takes rows t, t + 256, ... of the stage (consecutive
+  // 16-byte reads) and writes the group's partial of each:
   //   mpart[g][h] = sum_{c < 8} W_down[e][h][8 g' + c] * w_e * act[8 g' + c]
-  // Lane k starts at group (k % 8) >> (3 - tz(n)) (tz: trailing zero bits,
-  // at most 3), which puts the eight rows of a quarter-warp in distinct banks
-  // for every n.
   __device__ __forceinline__ bool down_part() {
     const int H = p.H, ncb = t[R_NROWS] / 8, g0 = t[R_REL0];
-    const int tz = min(__ffs(ncb) - 1, 3);
-    const int h0 = (lane & 7) >> (3 - tz);
-    for (int r0 = 0; r0 < H; r0 += 256) {
-      uint32_t slot;
-      if (!stage_full(slot)) return false;
-      const int row = r0 + tid;
-      if (row < H) {
-        const uint8_t* st = S.stage[slot] + tid * ncb * 16;
-        int j = h0 % ncb;
+    for (int c = 0; c < ncb; c++) {
+      float xa[8];
 #pragma unroll
-        for (int c = 0; c < 8; c++) {
-          if (c < ncb) {
-            const uint4 w = lds128(st + j * 16);
-            const float4 x0 = *(const float4*)&S.actp[8 * j];
-            const float4 x1 = *(const float4*)&S.actp[8 * j + 4];
-            float v = bf16lo(w.x) * x0.x;
-            v = fmaf(bf16hi(w.x), x0.y, v);
-            v = fmaf(bf16lo(w.y), x0.z, v);
-            v = fmaf(bf16hi(w.y), x0.w, v);
-            v = fmaf(bf16lo(w.z), x1.x, v);
-            v = fmaf(bf16hi(w.z), x1.y, v);
-            v = fmaf(bf16lo(w.w), x1.z, v);
-            v = fmaf(bf16hi(w.w), x1.w, v);
-            __stcg(p.mpart + (size_t)(g0 + j) * H + row, v);
-            j = j + 1 == ncb ? 0 : j + 1;
-          }
+      for (int j = 0; j < 8; j++) xa[j] = S.actp[8 * c + j];
+      for (int r0 = 0; r0 < H; r0 += kDownRows) {
+        const int rows = min(kDownRows, H - r0);
+        uint32_t slot;
+        if (!stage_full(slot)) return false;
+        const uint8_t* st = S.stage[slot];
+        for (int r = tid; r < rows; r += 256) {
+          const uint4 w = lds128(st + r * 16);
+          float v = bf16lo(w.x) * xa[0];
+          v = fmaf(bf16hi(w.x), xa[1], v);
+          v = fmaf(bf16lo(w.y), xa[2], v);
+          v = fmaf(bf16hi(w.y), xa[3], v);
+          v = fmaf(bf16lo(w.z), xa[4], v);
+          v = fmaf(bf16hi(w.z), xa[5], v);
+          v = fmaf(bf16lo(w.w), xa[6], v);
+          v = fmaf(bf16hi(w.w), xa[7], v);
+          __stcg(p.mpart + (size_t)(g0 + c) * H + r0 + r, v);
         }
+        stage_release(slot);
       }
-      stage_release(slot);
     }
     return true;
   }
@@ -2328,6 +2324,37 @@ int step_kernel_regs() {
 }
 
 size_t step_smem_bytes() { return kSmemBytes; }
+
+// w_down of one layer, [E][H][I] -> [E][I/8][H][8]: block (e, 32 rows, 32
+// groups) through shared memory, so both the reads (along a row) and the
+// writes (along a group's rows) are 512-byte runs
+__global__ void __launch_bounds__(256) relayout_down_kernel(const uint16_t* __restrict__ src,
+                                                            uint16_t* __restrict__ dst, int E, int H, int I) {
+  __shared__ uint4 tile[32][33];
+  const int G = I / 8;
+  const int gb = (G + 31) / 32, hb = (H + 31) / 32;
+  const int e = blockIdx.x / (hb * gb), rem = blockIdx.x % (hb * gb);
+  const int h0 = (rem / gb) * 32, g0 = (rem % gb) * 32;
+  for (int k = threadIdx.x; k < 1024; k += 256) {
+    const int r = k / 32, q = k % 32;
+    if (h0 + r < H && g0 + q < G)
+      tile[r][q] = *(const uint4*)(src + ((size_t)e * H + h0 + r) * I + (size_t)(g0 + q) * 8);
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < 1024; k += 256) {
+    const int q = k / 32, r = k % 32;
+    if (h0 + r < H && g0 + q < G)
+      *(uint4*)(dst + (((size_t)e * G + g0 + q) * H + h0 + r) * 8) = tile[r][q];
+  }
+}
+
+cudaError_t relayout_down(const uint16_t* src, uint16_t* dst, int E, int H, int I) {
+  const int G = I / 8;
+  const long long blocks = (long long)E * ((H + 31) / 32) * ((G + 31) / 32);
+  if (blocks < 1 || blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  relayout_down_kernel<<<(unsigned)blocks, 256>>>(src, dst, E, H, I);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream) {
   static bool configured = false;

@@ -150,8 +150,9 @@ struct Params {
   const uint16_t* const* w_down;
   uint16_t* const* k_pool;
   uint16_t* const* v_pool;
-  const uint8_t* wd_maps;      // [L][8] tensor maps of w_down as 2-D [E * H rows][I], boxes
-                               // of 8 n columns x 256 rows, n = 1..8 (one token: column slices)
+  const uint16_t* wd_blk;      // w_down re-laid out as [L][E][I / 8][H][8]: each 8-column group
+                               // of an expert one contiguous [H][8] block (one token: the
+                               // UP pieces' column slices stream as whole blocks)
   const uint8_t* mp_map;       // tensor map of mpart: 2-D [groups][H] fp32, boxes 32 x 256
   const uint8_t* kv_maps;      // [L][2] tensor maps (128 bytes each) of the K and V pools:
                                // 2-D [rows = pages * hkv * page_size][d], boxes of
