@@ -58,8 +58,9 @@ inline int moe_sms(const mk_config& c, int n_sm) {
 }
 
 // Attention SMs of a step: config.n_attn_claimers if set, else a share of the
-// SMs proportional to the attention's KV bytes against the routed experts'
-// gate/up/down bytes of a layer (the two branches that run side by side).
+// SMs proportional to the attention's KV bytes (weighted by 1.6) against the
+// routed experts' gate/up/down bytes of a layer (the two branches that run
+// side by side).
 // n_sm means no roles.
 int attention_sms(const mk_config& c, int n_sm, int batch, const int32_t* seq_lens);
 
