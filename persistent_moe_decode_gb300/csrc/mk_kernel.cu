@@ -999,15 +999,23 @@ struct Cons {
         h[k].w += o[k].w + m[k].w;
       }
     }
+    // the GEMVs of this layer take h * gain (in xs) and their epilogues scale
+    // by 1 / rms (S.rinv[0]): W (h g / rms) = (W (h g)) / rms, so the sum of
+    // squares is reduced while the GEMV already runs (one barrier)
     const bool keep = blockIdx.x == 0;
     float ssl = 0.f;
+    float4 hg[NI];
 #pragma unroll
     for (int k = 0; k < NI; k++) {
       const int i4 = tid + 256 * k;
+      hg[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (i4 < H4) {
         if (!final_norm) __stcg((float4*)hl + i4, h[k]);
         if (keep) __stcg((float4*)(p.hdbg + (size_t)l * Bm * H) + i4, h[k]);
         ssl += h[k].x * h[k].x + h[k].y * h[k].y + h[k].z * h[k].z + h[k].w * h[k].w;
+        hg[k] = make_float4(h[k].x * bf16lo(g[k].x), h[k].y * bf16hi(g[k].x), h[k].z * bf16lo(g[k].y),
+                            h[k].w * bf16hi(g[k].y));
+        *(float4*)&S.xs[i4 * 4] = hg[k];
       }
     }
 #pragma unroll
@@ -1018,18 +1026,18 @@ struct Cons {
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; w++) sum += S.nred[w][0];
     const float r = 1.0f / sqrtf(sum / (float)H + p.rms_eps);
+    if (tid == 0) S.rinv[0] = r;     // read by the epilogues, after their barriers
+    if (keep) {
 #pragma unroll
-    for (int k = 0; k < NI; k++) {
-      const int i4 = tid + 256 * k;
-      if (i4 < H4) {
-        const float4 x = make_float4(h[k].x * r * bf16lo(g[k].x), h[k].y * r * bf16hi(g[k].x),
-                                     h[k].z * r * bf16lo(g[k].y), h[k].w * r * bf16hi(g[k].y));
-        *(float4*)&S.xs[i4 * 4] = x;
-        __stcg((float4*)xl + i4, x);
-        if (keep) __stcg((float4*)(p.xdbg + (size_t)l * Bm * H) + i4, x);
+      for (int k = 0; k < NI; k++) {
+        const int i4 = tid + 256 * k;
+        if (i4 < H4)
+          __stcg((float4*)(p.xdbg + (size_t)l * Bm * H) + i4,
+                 make_float4(hg[k].x * r, hg[k].y * r, hg[k].z * r, hg[k].w * r));
       }
     }
-    return csync();
+    (void)xl;
+    return true;
   }
 
   __device__ __forceinline__ bool norm(int l, bool final_norm) {
@@ -1448,11 +1456,12 @@ struct Cons {
     const int nr = t[R_NROWS], row0 = t[R_ROW0];
     const size_t Bm = (size_t)p.Bmax;
     switch (kind) {
-      case K_P1: {
+      case K_P1: {   // GEMV of h * gain: scale by 1 / rms
         const int nq = t[R_NROWS1], q0 = t[R_ROW1];
+        const float r = S.rinv[0];
         for (int i = tid; i < nr + nq; i += 256) {
-          if (i < nr) __stcg(p.rlog + (size_t)l * Bm * p.E + row0 + i, res[i]);
-          else __stcg(p.qkv + (size_t)l * Bm * p.qkv_rows + q0 + i - nr, res[i]);
+          if (i < nr) __stcg(p.rlog + (size_t)l * Bm * p.E + row0 + i, res[i] * r);
+          else __stcg(p.qkv + (size_t)l * Bm * p.qkv_rows + q0 + i - nr, res[i] * r);
         }
         break;
       }
@@ -1461,8 +1470,9 @@ struct Cons {
         // the input of the piece's down-projection columns
         const int slot = S.rt.off[t[R_A]];
         const float wa = S.rt.w[0][S.rt.ent[slot] % p.topk];
+        const float r = S.rinv[0];   // GEMV of h * gain: scale by 1 / rms
         for (int i = tid; i < nr; i += 256) {
-          const float a = silu_mul(res[i], res[nr + i]);
+          const float a = silu_mul(res[i] * r, res[nr + i] * r);
           __stcg(p.abuf + ((size_t)l * Bm * p.topk + slot) * p.I + row0 + i, a);
           S.actp[i] = wa * a;
         }
@@ -1471,9 +1481,11 @@ struct Cons {
       case K_OPROJ:
         for (int i = tid; i < nr; i += 256) __stcg(p.oproj + (size_t)l * Bm * p.H + row0 + i, res[i]);
         break;
-      default:   // K_LM
-        for (int i = tid; i < nr; i += 256) p.logits[row0 + i] = res[i];
+      default: {   // K_LM: GEMV of h * gain, scale by 1 / rms
+        const float r = S.rinv[0];
+        for (int i = tid; i < nr; i += 256) p.logits[row0 + i] = res[i] * r;
         break;
+      }
     }
   }
 
