@@ -224,6 +224,10 @@ __device__ __forceinline__ void route_one(const Params& p, RouteTab& rt, int l, 
     const int e = lane + 32 * i;
     v[i] = e < E ? __ldcg(rl + e) : -INFINITY;
   }
+  // each pick: the lane's best remaining value (ties to its lower expert id),
+  // then two warp reductions on an order-preserving integer key: the largest
+  // key, and the lowest expert id holding it (-0 is taken as +0, so equal
+  // values tie exactly as in a float comparison)
   uint32_t taken = 0;
   float my_v = -INFINITY;
   int my_e = 0x7fffffff;
@@ -234,24 +238,19 @@ __device__ __forceinline__ void route_one(const Params& p, RouteTab& rt, int l, 
 #pragma unroll
     for (int i = 0; i < 8; i++) {
       const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || bi == 0x7fffffff)) {
         bv = v[i];
         bi = e;
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const uint32_t u = __float_as_uint(bv == 0.f ? 0.f : bv);
+    const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+    const uint32_t emin = __reduce_min_sync(0xffffffffu, key == kmax ? (uint32_t)bi : 0xffffffffu);
+    if ((int)(emin & 31u) == lane) taken |= 1u << (emin >> 5);
     if (lane == j) {
-      my_v = bv;
-      my_e = bi;
+      my_v = __uint_as_float((kmax & 0x80000000u) ? (kmax & 0x7fffffffu) : ~kmax);
+      my_e = (int)emin;
     }
   }
   const float top = __shfl_sync(0xffffffffu, my_v, 0);
@@ -886,19 +885,22 @@ struct Cons {
     return true;
   }
 
-  // the task's last chunk is done: bump its phase counter
-  __device__ __forceinline__ bool complete() {
+  // end of a chunk that finishes the SM's router rows (FL_RTR: release the
+  // routing wait early) and / or its task (FL_LAST: bump the phase counter):
+  // one barrier, then the releases (the block's stores, ordered before this
+  // thread by the barrier, are visible before a counter moves)
+  __device__ __forceinline__ bool finish(int flags) {
     const int op = t[R_OP], l = t[R_LAYER];
     int bar = -1;
-    if (op == OP_P1) bar = p.bl.p1;
-    else if (op == OP_UP) bar = p.bl.up;
-    else if (op == OP_OUT || op == OP_DOWN) bar = p.bl.out;
-    if (bar < 0) return csync();
+    if (flags & FL_LAST) {
+      if (op == OP_P1) bar = p.bl.p1;
+      else if (op == OP_UP) bar = p.bl.up;
+      else if (op == OP_OUT || op == OP_DOWN) bar = p.bl.out;
+    }
     if (!csync()) return false;
     if (tid == 0) {
-      // release: the block's stores (ordered before this thread by the
-      // barrier above) are visible before the counter moves
-      red_release_add(p.bars + bar_index(p, l, bar), 1u);
+      if (flags & FL_RTR) red_release_add(p.bars + bar_index(p, l, p.bl.rtr), 1u);
+      if (bar >= 0) red_release_add(p.bars + bar_index(p, l, bar), 1u);
     }
     return true;
   }
@@ -2142,9 +2144,7 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
       c.moe_write(h0, min(kOutRows, a1 - h0));
     }
   }
-  // the router rows are done: release the routing wait early
-  if (ok && (flags & FL_RTR)) ok = c.signal(bar_index(p, l, p.bl.rtr), 1);
-  if (ok && (flags & FL_LAST)) ok = c.complete();
+  if (ok && (flags & (FL_RTR | FL_LAST))) ok = c.finish(flags);
   c.save();
   return ok;
 }
@@ -2170,7 +2170,10 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
       if (split) ok = K == 2048 ? c.gemv_split<1>(res) : c.gemv_split<2>(res);
       else ok = K <= 256 ? c.gemv_row<1>(res) : K <= 768 ? c.gemv_row<3>(res)
               : K <= 2048 ? c.gemv_row<8>(res) : c.gemv_row<16>(res);
-      ok = ok && c.csync();
+      // the split path's sums are written by the threads that run the
+      // epilogue; its partial buffer is reused by the next split chunk, which
+      // the completion barrier below also orders when the task ends here
+      if (ok && !(split && (flags & FL_LAST))) ok = c.csync();
     }
     if (ok && run) {
       c.epilogue_row(res);
@@ -2180,9 +2183,7 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
     if (ok && run && kind == K_UP) ok = c.csync() && c.down_part();
   }
   if (ok && run && c.lane == 0) S.cchunk[c.warp]++;
-  // the router rows are done: release the routing wait early
-  if (ok && (flags & FL_RTR)) ok = c.signal(bar_index(p, l, p.bl.rtr), 1);
-  if (ok && (flags & FL_LAST)) ok = c.complete();
+  if (ok && (flags & (FL_RTR | FL_LAST))) ok = c.finish(flags);
   c.save();
   return ok;
 }
