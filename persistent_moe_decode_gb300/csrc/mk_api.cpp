@@ -186,12 +186,12 @@ int make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* b
   return MK_OK;
 }
 
-// one token: the tensor map of the per-group partial buffer (32 x 256 fp32)
+// one token: the tensor map of the per-group partial buffer (24 x 256 fp32)
 int make_moe_map(mk_handle* h, float* mpart, const uint8_t** mp) {
   const mk_config& c = h->cfg;
   CUtensorMap map;
   int rc = make_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, mpart, (uint64_t)c.hidden,
-                       (uint64_t)c.top_k * (c.moe_inter / 8), 32, 256);
+                       (uint64_t)c.top_k * (c.moe_inter / 8), 24, 256);   // kMredCols
   if (rc) return rc;
   uint8_t* d = nullptr;
   rc = dalloc(h, &d, sizeof(CUtensorMap));

@@ -110,6 +110,10 @@ enum : int { K_ROUTER = 0, K_QKV = 1, K_UP = 2, K_OPROJ = 3, K_DOWN = 4, K_LM = 
 constexpr int kRowChunk = kPartFloats;
 // rows of an [H][8] down-projection block per stage (2048 x 16 bytes = one stage)
 constexpr int kDownRows = kStageBytes / 16;
+// hidden rows per window of the one-token partial sums (a tensor box of
+// kMredCols x 256 fp32; 16-byte multiple; a DOWN share of up to kMredCols - 3
+// rows takes one window)
+constexpr int kMredCols = 24;
 // chunk flags: first chunk of its task (P1 / FINAL run the norm first), last
 // chunk of its task (signals completion), last block of an OUT row chunk
 enum : int { FL_FIRST = 1, FL_LAST = 2, FL_CLAST = 4, FL_RTR = 8 };   // FL_RTR: the chunk ends its router rows
@@ -716,12 +720,12 @@ struct Prod {
       }
       if (!__shfl_sync(0xffffffffu, good, 0)) return false;
       const int ng = p.topk * (p.I / 8);
-      for (int x0 = a0 & ~3; x0 < a1; x0 += 32)
+      for (int x0 = a0 & ~3; x0 < a1; x0 += kMredCols)
         for (int y0 = 0; y0 < ng; y0 += 256) {
           uint32_t slot;
           if (!acquire_stage(slot)) return false;
           if (lane == 0) {
-            mbar_arrive_expect_tx(&S.full[slot], 32u * 256u * 4u);
+            mbar_arrive_expect_tx(&S.full[slot], (uint32_t)kMredCols * 256u * 4u);
             tma_load_2d(&S.stage[slot][0], p.mp_map, x0, y0, &S.full[slot]);
           }
           __syncwarp();
@@ -1525,34 +1529,36 @@ struct Cons {
     return true;
   }
 
-  // one token, OUT: rows [a0, a1) of the experts' share of the residual
+  // one token, DOWN: rows [a0, a1) of the experts' share of the residual
   // update = the sum of every group's partial, in group order.  The partials
-  // arrive as stages of 256 groups x 32 rows (from row a0 rounded down to a
-  // multiple of 4); warp w adds groups w, w + 8, ... and the warps' sums meet
-  // in shared memory in warp order.  red: 256 floats of scratch.
+  // arrive as stages of 256 groups x kMredCols rows (from row a0 rounded down
+  // to a multiple of 4); warp w adds groups w, w + 8, ... and the warps' sums
+  // meet in shared memory in warp order.  red: 256 floats of scratch (the
+  // task's completion barrier orders its last use).
   __device__ __forceinline__ bool moe_reduce(float* red) {
     const int a0 = t[R_ROW0], a1 = a0 + t[R_NROWS], l = t[R_LAYER];
     const int ng = p.topk * (p.I / 8);
-    for (int x0 = a0 & ~3; x0 < a1; x0 += 32) {
+    for (int x0 = a0 & ~3; x0 < a1; x0 += kMredCols) {
       float s = 0.f;
       for (int y0 = 0; y0 < ng; y0 += 256) {
         uint32_t slot;
         if (!stage_full(slot)) return false;
         const float* st = (const float*)S.stage[slot];
         const int n = min(256, ng - y0);
-        for (int g = warp; g < n; g += kConsumerWarps) s += st[g * 32 + lane];
+        if (lane < kMredCols)
+          for (int g = warp; g < n; g += kConsumerWarps) s += st[g * kMredCols + lane];
         stage_release(slot);
       }
       red[warp * 32 + lane] = s;
       if (!csync()) return false;
-      if (tid < 32) {
+      if (tid < kMredCols) {
         const int h = x0 + tid;
         float v = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; w++) v += red[w * 32 + tid];
         if (h >= a0 && h < a1) __stcg(p.moe + (size_t)l * p.Bmax * p.H + h, v);
       }
-      if (!csync()) return false;
+      if (x0 + kMredCols < a1 && !csync()) return false;
     }
     return true;
   }

@@ -153,7 +153,7 @@ struct Params {
   const uint16_t* wd_blk;      // w_down re-laid out as [L][E][I / 8][H][8]: each 8-column group
                                // of an expert one contiguous [H][8] block (one token: the
                                // UP pieces' column slices stream as whole blocks)
-  const uint8_t* mp_map;       // tensor map of mpart: 2-D [groups][H] fp32, boxes 32 x 256
+  const uint8_t* mp_map;       // tensor map of mpart: 2-D [groups][H] fp32, boxes 24 x 256
   const uint8_t* kv_maps;      // [L][2] tensor maps (128 bytes each) of the K and V pools:
                                // 2-D [rows = pages * hkv * page_size][d], boxes of
                                // 64 dims x (hkv * page_size) rows, 128-byte swizzle
