@@ -2124,7 +2124,6 @@ struct Cons {
 // would cost L2 round trips.  With 216 registers per consumer thread (see
 // the register split) the union of the paths needs no spill.  The per-warp
 // pipeline counters travel through shared memory between paths.
-template <int NB>
 __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t* t) {
   Cons c(p, S, t);
   const int op = t[R_OP], kind = t[R_KIND], flags = t[R_FLAGS], l = t[R_LAYER];
@@ -2134,7 +2133,13 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
   if (ok && run && kind == K_OPROJ) ok = c.wait_counter(bar_index(p, l, p.bl.comb), p.n_comb_sms);
   if (ok && run && kind == K_DOWN) ok = c.wait_counter(bar_index(p, l, p.bl.up), p.n_up_sms);
   float* part = S.red + (S.cchunk[c.warp] & 1u) * kPartFloats;
-  if (ok && run) ok = c.gemv<NB>(part) && c.csync();
+  if (ok && run) {
+    // tokens per pass matched to the chunk (an expert's few routed tokens do
+    // not pay for eight)
+    const int nt = t[R_NT];
+    ok = (nt <= 1 ? c.gemv<1>(part) : c.gemv<8>(part)) &&
+         c.csync();
+  }
   if (ok && run) {
     c.epilogue(part);
     if (c.tid == 0) S.t_mark[2] = gtime_ns();
@@ -2251,7 +2256,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
         if constexpr (ONE) {
           ok = op_row(p, S, t);
         } else {
-          ok = op_chunk<8>(p, S, t);
+          ok = op_chunk(p, S, t);
         }
         (void)nt;
         break;
