@@ -210,6 +210,35 @@ def test_tiny_forced_split_kv_matches_oracle():
         pair.close()
 
 
+MID_SCHEDULES = (
+    [dict(n_attn_claimers=a) for a in (20, 40, 75)]
+    + [dict(n_attn_claimers=10000, wave_order=o) for o in (mk.MK_WAVES_DEFAULT, mk.MK_WAVES_INTERLEAVED)]
+    + [dict(n_attn_claimers=3, sm_cap=16), dict(n_attn_claimers=10000, sm_cap=5)]
+)
+
+
+@pytest.mark.parametrize("kw", MID_SCHEDULES, ids=lambda kw: "-".join(f"{k}{v}" for k, v in kw.items()))
+def test_mid_schedules_give_identical_logits(kw):
+    """Hidden 2048: the one-token P1 and O-proj chunks take the
+    split-contraction GEMV and the experts' down projection goes through the
+    per-group partials; neither sum order depends on the SM count, the role
+    split or the wave order, so the logits are bit-identical."""
+    wl = WORKLOADS["mid_8k"]
+    from persistent_moe_decode_gb300.runner import StepRunner
+    ref_run = StepRunner(wl, device="cuda", kv_split_tokens=256)
+    ref_run.step()
+    torch.cuda.synchronize()
+    ref_run.check_status()
+    ref = ref_run.logits.clone()
+    ref_run.close()
+    run = StepRunner(wl, device="cuda", kv_split_tokens=256, **kw)
+    run.step()
+    torch.cuda.synchronize()
+    run.check_status()
+    assert torch.equal(run.logits, ref)
+    run.close()
+
+
 def test_mid_trajectory_and_split_kv():
     wl = WORKLOADS["mid_8k"].with_(steps=4)
     pair = Pair(wl)
