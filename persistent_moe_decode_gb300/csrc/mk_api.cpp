@@ -385,6 +385,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
   TRY(dalloc(h, &p.oproj, Ls * Bs * H));
   TRY(dalloc(h, &p.moe, Ls * Bs * H));
   TRY(dalloc(h, &p.mpart, (size_t)K * (I / 8) * H));
+  TRY(dalloc(h, &p.mdown, Bs * K * H));
   TRY(make_moe_map(h, p.mpart, &p.mp_map));
   TRY(make_down_blocks(h, w, &p.wd_blk));
   h->bar_words = kErrWords + (size_t)L * p.bl.per_layer;

@@ -68,7 +68,7 @@ struct __align__(128) Smem {
                                             // layer, the attention output, the experts' hidden)
   float red[2 * kPartFloats];               // GEMV partial sums (two buffers) / attention
                                             // query fragments and merge / combine sums
-  float acc_m[kOutRows][kMaxBatch];         // DOWN row chunk (several tokens): weighted expert outputs
+  float spart[64][kConsumerWarps];          // one token, split GEMV: the warps' sums of each row
   float actp[64];                           // one token: weighted hidden values of an UP piece
   float nred[kConsumerWarps][kMaxBatch];    // norm / combine reductions
   float rinv[kMaxBatch];
@@ -93,7 +93,6 @@ struct __align__(128) Smem {
 // the dynamic shared memory is rounded up to a 1024-byte boundary (the
 // swizzled tensor copies of KV pages need it), hence the extra 1 KB
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
-static_assert(kOutRows * kMaxBatch >= 64 * kConsumerWarps, "split GEMV partials live in acc_m");
 static_assert(kSmemBytes <= 232448, "shared memory of one block exceeds the sm_103a limit");
 
 // resolved task words (written by the producer into the task ring)
@@ -103,9 +102,11 @@ enum : int {
 };
 // GEMV chunk kinds; K_P1 (router rows, then QKV rows) and K_MRED (the sum of
 // the experts' per-group partials of OUT's rows) are one-token forms, and a
-// one-token K_UP chunk also multiplies its columns of the down projection
+// one-token K_UP chunk also multiplies its columns of the down projection.
+// K_MSUM (several tokens) adds each token's k weighted expert outputs of
+// OUT's rows; it streams nothing.
 enum : int { K_ROUTER = 0, K_QKV = 1, K_UP = 2, K_OPROJ = 3, K_DOWN = 4, K_LM = 5, K_P1 = 6,
-             K_MRED = 7 };
+             K_MRED = 7, K_MSUM = 8 };
 // rows of one single-token GEMV chunk (one result per row in a 2048-float buffer)
 constexpr int kRowChunk = kPartFloats;
 // rows of an [H][8] down-projection block per stage (2048 x 16 bytes = one stage)
@@ -115,8 +116,8 @@ constexpr int kDownRows = kStageBytes / 16;
 // rows takes one window)
 constexpr int kMredCols = 24;
 // chunk flags: first chunk of its task (P1 / FINAL run the norm first), last
-// chunk of its task (signals completion), last block of an OUT row chunk
-enum : int { FL_FIRST = 1, FL_LAST = 2, FL_CLAST = 4, FL_RTR = 8 };   // FL_RTR: the chunk ends its router rows
+// chunk of its task (signals completion)
+enum : int { FL_FIRST = 1, FL_LAST = 2, FL_RTR = 8 };   // FL_RTR: the chunk ends its router rows
 
 // ---------------------------------------------------------------- errors
 __device__ __forceinline__ bool stopped(const Params& p) {
@@ -287,6 +288,7 @@ __device__ __forceinline__ void route_one(const Params& p, RouteTab& rt, int l, 
 // writes them straight into the task ring (lane 0 writes the words; no
 // per-thread arrays, which would live in local memory) and streams their
 // weight / KV stages.
+template <bool ONE>   // the batch has one token (kernel instance)
 struct Prod {
   const Params& p;
   Smem& S;
@@ -542,7 +544,7 @@ struct Prod {
 
   __device__ __forceinline__ bool do_p1_final(int a0, int a1, int b0, int b1) {
     const int H = p.H, B = p.B;
-    if (B == 1) return do_p1_final_1(a0, a1, b0, b1);
+    if (ONE) return do_p1_final_1(a0, a1, b0, b1);
     const int cr = gemv_chunk_rows(H, B);
     if (op == OP_FINAL) {
       if (a1 <= a0) return chunk(K_LM, FL_FIRST | FL_LAST, 0, 0, 1, H, B, 0, 0, 0, nullptr, nullptr);
@@ -652,7 +654,7 @@ struct Prod {
   __device__ __forceinline__ bool do_up(int a0, int a1) {
     const int H = p.H;
     if (!wait_route()) return false;
-    if (p.B == 1) return do_up1(a0, a1);
+    if (ONE) return do_up1(a0, a1);
     const int n_act = S.rt.n_act;
     int p0 = 0, p1 = 0;
     if (a0 >= 0) dshare(n_act * p.I, a1, a0, p0, p1);
@@ -660,7 +662,7 @@ struct Prod {
     int n_chunks = 0;
     for (int a = p0 / p.I; a < n_act && a * p.I < p1; a++) {
       const int i0 = max(p0 - a * p.I, 0), i1 = min(p1 - a * p.I, p.I);
-      const int cp = p.B == 1 ? kRowChunk / 2 : max(1, gemv_chunk_rows(H, S.rt.off[a + 1] - S.rt.off[a]) / 2);
+      const int cp = max(1, gemv_chunk_rows(H, S.rt.off[a + 1] - S.rt.off[a]) / 2);
       n_chunks += (i1 - i0 + cp - 1) / cp;
     }
     if (n_chunks == 0) return chunk(K_UP, FL_LAST, 0, 0, 2, H, 0, 0, 0, 0, nullptr, nullptr);
@@ -668,7 +670,7 @@ struct Prod {
       const int i0 = max(p0 - a * p.I, 0), i1 = min(p1 - a * p.I, p.I);
       const int e = S.rt.act[a];
       const int cnt = S.rt.off[a + 1] - S.rt.off[a];
-      const int cp = p.B == 1 ? kRowChunk / 2 : max(1, gemv_chunk_rows(H, cnt) / 2);
+      const int cp = max(1, gemv_chunk_rows(H, cnt) / 2);
       const size_t eo = (size_t)e * p.I * H;
       for (int c0 = i0; c0 < i1; c0 += cp) {
         n_chunks--;
@@ -680,16 +682,30 @@ struct Prod {
     return true;
   }
 
-  // OUT: O-proj rows [a0, a1) (needs no routing)
+  // OUT: O-proj rows [a0, a1) (needs no routing).  Several tokens: then the
+  // sum of each token's weighted expert outputs of the same rows (K_MSUM,
+  // after every DOWN task)
   __device__ __forceinline__ bool do_out(int a0, int a1) {
     const int B = p.B;
     const int KO = p.hq * p.d;
+    const int last = ONE ? FL_LAST : 0;
     if (a1 <= a0) return chunk(K_OPROJ, FL_LAST, 0, 0, 1, KO, B, 0, 0, 0, nullptr, nullptr);
-    const int co = B == 1 ? split_rows(KO) : gemv_chunk_rows(KO, B);
+    const int co = ONE ? split_rows(KO) : gemv_chunk_rows(KO, B);
     for (int c0 = a0; c0 < a1; c0 += co)
-      if (!chunk(K_OPROJ, c0 + co >= a1 ? FL_LAST : 0, c0, min(co, a1 - c0), 1, KO, B, 0, 0, 0, wptr(2),
+      if (!chunk(K_OPROJ, c0 + co >= a1 ? last : 0, c0, min(co, a1 - c0), 1, KO, B, 0, 0, 0, wptr(2),
                  nullptr))
         return false;
+    if (ONE) return true;
+    int32_t* w = begin();     // streams nothing
+    if (!w) return false;
+    if (lane == 0) {
+      w[R_KIND] = K_MSUM;
+      w[R_FLAGS] = FL_LAST;
+      w[R_ROW0] = a0;
+      w[R_NROWS] = a1 - a0;
+      w[R_NT] = B;
+    }
+    commit();
     return true;
   }
 
@@ -699,7 +715,7 @@ struct Prod {
   // rows per stage.
   __device__ __forceinline__ bool do_down(int a0, int a1) {
     const int H = p.H, B = p.B;
-    if (B == 1) {
+    if (ONE) {
       int32_t* w = begin();
       if (!w) return false;
       if (lane == 0) {
@@ -733,24 +749,25 @@ struct Prod {
         }
       return true;
     }
+    // several tokens: slice a0 of a1 over the routed experts' rows of the
+    // down projection (expert-major: an expert's H rows, then the next
+    // expert's); each chunk's epilogue writes its rows of every routed entry's
+    // weighted output, summed by OUT
     if (!wait_route()) return false;
     const int n_act = S.rt.n_act;
-    if (a1 <= a0 || n_act == 0) return chunk(K_DOWN, FL_LAST, 0, 0, 1, p.I, 0, 0, 0, 0, nullptr, nullptr);
-    // several tokens: row chunks of kOutRows, each expert's rows accumulated
-    // in shared memory in expert order
-    for (int h0 = a0; h0 < a1; h0 += kOutRows) {
-      const int h1 = min(a1, h0 + kOutRows);
-      const int fin = FL_CLAST | (h1 == a1 ? FL_LAST : 0);
-      for (int a = 0; a < n_act; a++) {
-        const int e = S.rt.act[a];
-        const int cnt = S.rt.off[a + 1] - S.rt.off[a];
-        const int cd = gemv_chunk_rows(p.I, cnt);
-        const uint16_t* wd = wptr(5) + (size_t)e * H * p.I;
-        for (int c0 = h0; c0 < h1; c0 += cd)
-          if (!chunk(K_DOWN, (a == n_act - 1 && c0 + cd >= h1) ? fin : 0, c0, min(cd, h1 - c0), 1, p.I, cnt,
-                     a, e, c0 - h0, wd, nullptr))
-            return false;
-      }
+    int r0 = 0, r1 = 0;
+    if (a0 >= 0) dshare(n_act * H, a1, a0, r0, r1);
+    if (r1 <= r0) return chunk(K_DOWN, FL_LAST, 0, 0, 1, p.I, 0, 0, 0, 0, nullptr, nullptr);
+    for (int a = r0 / H; a < n_act && a * H < r1; a++) {
+      const int h0 = max(r0 - a * H, 0), h1 = min(r1 - a * H, H);
+      const int e = S.rt.act[a];
+      const int cnt = S.rt.off[a + 1] - S.rt.off[a];
+      const int cd = gemv_chunk_rows(p.I, cnt);
+      const uint16_t* wd = wptr(5) + (size_t)e * H * p.I;
+      for (int c0 = h0; c0 < h1; c0 += cd)
+        if (!chunk(K_DOWN, (c0 + cd >= h1 && a * H + h1 == r1) ? FL_LAST : 0, c0, min(cd, h1 - c0), 1, p.I,
+                   cnt, a, e, 0, wd, nullptr))
+          return false;
     }
     return true;
   }
@@ -776,7 +793,7 @@ struct Prod {
         }
         case OP_ROUTE:
         case OP_COMBINE: {
-          if (op == OP_ROUTE && p.B == 1 && !route_here()) {
+          if (op == OP_ROUTE && ONE && !route_here()) {
             ok = false;
             break;
           }
@@ -826,6 +843,7 @@ struct Prod {
 // ===================================================================== consumers
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
+template <bool ONE>   // the batch has one token (kernel instance)
 struct Cons {
   const Params& p;
   Smem& S;
@@ -899,7 +917,8 @@ struct Cons {
     if (flags & FL_LAST) {
       if (op == OP_P1) bar = p.bl.p1;
       else if (op == OP_UP) bar = p.bl.up;
-      else if (op == OP_OUT || op == OP_DOWN) bar = p.bl.out;
+      else if (op == OP_OUT || (op == OP_DOWN && ONE)) bar = p.bl.out;
+      else if (op == OP_DOWN) bar = p.bl.down;
     }
     if (!csync()) return false;
     if (tid == 0) {
@@ -943,8 +962,9 @@ struct Cons {
     }
   }
 
-  // OUT and DOWN tasks of a layer: the next layer's residual is complete
-  __device__ __forceinline__ int out_target() const { return p.n_sm + p.n_down_sms; }
+  // OUT tasks of a layer (and, one token, its DOWN tasks): the next layer's
+  // residual is complete
+  __device__ __forceinline__ int out_target() const { return ONE ? p.n_sm + p.n_down_sms : p.n_sm; }
 
   // residual update of layer l, token n, float4 i4: O-proj + experts
   __device__ __forceinline__ float4 delta4(int l, int n, int i4) const {
@@ -1047,7 +1067,7 @@ struct Cons {
   }
 
   __device__ __forceinline__ bool norm(int l, bool final_norm) {
-    if (p.B == 1) return norm1(l, final_norm);
+    if (ONE) return norm1(l, final_norm);
     const int H = p.H, B = p.B, H4 = H / 4;
     const size_t Bm = (size_t)p.Bmax;
     if (l > 0 && !wait_counter(bar_index(p, l - 1, p.bl.out), out_target() + t[R_BUMP])) return false;
@@ -1087,15 +1107,6 @@ struct Cons {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ssl += __shfl_xor_sync(0xffffffffu, ssl, o);
       if (lane == 0) S.nred[warp][n] = ssl;
-      if (B == 1) {
-        // one token: keep h for the second pass in shared memory (the staging
-        // buffer is free at the start of a layer)
-#pragma unroll
-        for (int k = 0; k < NI; k++) {
-          const int i4 = tid + 256 * k;
-          if (i4 < H4) *(float4*)&S.xs[i4 * 4] = h[k];
-        }
-      }
     }
     if (!csync()) return false;
     if (tid < B) {
@@ -1109,9 +1120,7 @@ struct Cons {
       const float g0 = bf16lo(gv.x), g1 = bf16hi(gv.x), g2 = bf16lo(gv.y), g3 = bf16hi(gv.y);
       for (int n = 0; n < B; n++) {
         float4 h;
-        if (B == 1) {
-          h = *(const float4*)&S.xs[i4 * 4];
-        } else if (final_norm) {
+        if (final_norm) {
           const float4 a = __ldcg((const float4*)(hl + n * H) + i4);
           const float4 d = delta4(l - 1, n, i4);
           h = make_float4(a.x + d.x, a.y + d.y, a.z + d.z, a.w + d.w);
@@ -1120,7 +1129,6 @@ struct Cons {
         }
         const float r = S.rinv[n];
         const float4 x = make_float4(h.x * r * g0, h.y * r * g1, h.z * r * g2, h.w * r * g3);
-        if (B == 1) *(float4*)&S.xs[i4 * 4] = x;
         __stcg((float4*)(xl + n * H) + i4, x);
         if (keep) __stcg((float4*)(p.xdbg + ((size_t)l * Bm + n) * H) + i4, x);
       }
@@ -1363,7 +1371,7 @@ struct Cons {
   // chunks l, l + 32 of that range, so each warp holds only its eighth of x
   // in registers.  A stage's RB = 8 / NC rows are reduced over the lanes
   // together (transposed butterfly: 9 shuffles for 8 rows, 6 for 4); the
-  // eight warp sums of a row meet in shared memory (acc_m, [row][warp]) and
+  // eight warp sums of a row meet in shared memory (spart, [row][warp]) and
   // are added in warp order after the barrier.
   template <int NC>
   __device__ __forceinline__ bool gemv_split(float* res) {
@@ -1379,7 +1387,7 @@ struct Cons {
       xa[c][0] = a.x; xa[c][1] = a.y; xa[c][2] = a.z; xa[c][3] = a.w;
       xa[c][4] = b.x; xa[c][5] = b.y; xa[c][6] = b.z; xa[c][7] = b.w;
     }
-    float* part = &S.acc_m[0][0];
+    float* part = &S.spart[0][0];
     int rbase = 0;
     for (int g = 0; g < ngrp; g++) {
       const int nr = group_rows(g);
@@ -1598,25 +1606,27 @@ struct Cons {
         case K_OPROJ:
           __stcg(p.oproj + ((size_t)l * Bm + n) * p.H + row0 + r, v);
           break;
-        default: {   // K_DOWN: weighted by the token's routing weight
+        default: {   // K_DOWN: entry (token b, pick j), weighted by its routing weight
           const int ent = S.rt.ent[S.rt.off[t[R_A]] + n];
           const int b = ent / p.topk, j = ent % p.topk;
-          S.acc_m[t[R_REL0] + r][b] += S.rt.w[b][j] * v;
+          __stcg(p.mdown + (size_t)ent * p.H + row0 + r, S.rt.w[b][j] * v);
           break;
         }
       }
     }
   }
 
-  // DOWN row chunk done: the weighted experts' sum of rows [h0, h0 + n) of
-  // every token; the accumulators are cleared for the next row chunk
-  __device__ __forceinline__ void moe_write(int h0, int n) {
-    const int l = t[R_LAYER];
+  // several tokens, OUT: rows [row0, row0 + n) of each token's expert output,
+  // the sum of its k weighted entries in pick order (every DOWN task has
+  // written them)
+  __device__ __forceinline__ void moe_sum() {
+    const int l = t[R_LAYER], n = t[R_NROWS], row0 = t[R_ROW0], K = p.topk;
     const size_t Bm = (size_t)p.Bmax;
     for (int i = tid; i < n * p.B; i += 256) {
       const int b = i / n, r = i % n;
-      __stcg(p.moe + ((size_t)l * Bm + b) * p.H + h0 + r, S.acc_m[r][b]);
-      S.acc_m[r][b] = 0.f;
+      float s = 0.f;
+      for (int j = 0; j < K; j++) s += __ldcg(p.mdown + (size_t)(b * K + j) * p.H + row0 + r);
+      __stcg(p.moe + ((size_t)l * Bm + b) * p.H + row0 + r, s);
     }
   }
 
@@ -1627,7 +1637,7 @@ struct Cons {
     const size_t Bm = (size_t)p.Bmax;
     // one token: the producer warp has routed (the routing is in shared
     // memory before this task was handed over)
-    if (B == 1) return true;
+    if (ONE) return true;
     if (!wait_counter(bar_index(p, l, p.bl.rtr), p.n_rtr_sms)) return false;
     RouteTab& rt = S.rt;
     for (int n = warp; n < B; n += kConsumerWarps) {
@@ -2124,8 +2134,9 @@ struct Cons {
 // would cost L2 round trips.  With 216 registers per consumer thread (see
 // the register split) the union of the paths needs no spill.  The per-warp
 // pipeline counters travel through shared memory between paths.
+template <bool ONE>
 __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t* t) {
-  Cons c(p, S, t);
+  Cons<ONE> c(p, S, t);
   const int op = t[R_OP], kind = t[R_KIND], flags = t[R_FLAGS], l = t[R_LAYER];
   bool ok = true;
   if ((op == OP_P1 || op == OP_FINAL) && (flags & FL_FIRST)) ok = c.norm(l, op == OP_FINAL);
@@ -2133,26 +2144,21 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
   if (ok && run && kind == K_OPROJ) ok = c.wait_counter(bar_index(p, l, p.bl.comb), p.n_comb_sms);
   if (ok && run && kind == K_DOWN) ok = c.wait_counter(bar_index(p, l, p.bl.up), p.n_up_sms);
   float* part = S.red + (S.cchunk[c.warp] & 1u) * kPartFloats;
-  if (ok && run) {
-    // tokens per pass matched to the chunk (an expert's few routed tokens do
-    // not pay for eight)
-    const int nt = t[R_NT];
-    ok = (nt <= 1 ? c.gemv<1>(part) : c.gemv<8>(part)) &&
-         c.csync();
-  }
-  if (ok && run) {
-    c.epilogue(part);
-    if (c.tid == 0) S.t_mark[2] = gtime_ns();
-    if (c.lane == 0) S.cchunk[c.warp]++;
-  }
-  if (ok && (flags & FL_CLAST)) {
-    // the last block of a DOWN row chunk: write the experts' sum
-    ok = c.csync();
-    if (ok) {
-      const int a0 = p.tasks[(size_t)t[R_TASK] * kDescWords + F_A0];
-      const int a1 = p.tasks[(size_t)t[R_TASK] * kDescWords + F_A1];
-      const int h0 = a0 + ((t[R_ROW0] - a0) / kOutRows) * kOutRows;
-      c.moe_write(h0, min(kOutRows, a1 - h0));
+  if (kind == K_MSUM) {
+    if (ok && run) ok = c.wait_counter(bar_index(p, l, p.bl.down), p.n_down_sms);
+    if (ok && run) c.moe_sum();
+  } else {
+    if (ok && run) {
+      // tokens per pass matched to the chunk (an expert's few routed tokens do
+      // not pay for eight)
+      const int nt = t[R_NT];
+      ok = (nt <= 1 ? c.template gemv<1>(part) : c.template gemv<8>(part)) &&
+           c.csync();
+    }
+    if (ok && run) {
+      c.epilogue(part);
+      if (c.tid == 0) S.t_mark[2] = gtime_ns();
+      if (c.lane == 0) S.cchunk[c.warp]++;
     }
   }
   if (ok && (flags & (FL_RTR | FL_LAST))) ok = c.finish(flags);
@@ -2162,8 +2168,9 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
 
 // one-token chunk: one copy of the wrapper (norm, waits, epilogue,
 // completion) around the GEMV shape for the row length
+template <bool ONE>
 __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* t) {
-  Cons c(p, S, t);
+  Cons<ONE> c(p, S, t);
   const int op = t[R_OP], kind = t[R_KIND], flags = t[R_FLAGS], l = t[R_LAYER];
   bool ok = true;
   if ((op == OP_P1 || op == OP_FINAL) && (flags & FL_FIRST)) ok = c.norm(l, op == OP_FINAL);
@@ -2178,9 +2185,9 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
     if (ok && run) {
       const int K = t[R_K];
       const bool split = (kind == K_P1 || kind == K_OPROJ) && rows <= 64 && split_rows(K) == 64;
-      if (split) ok = K == 2048 ? c.gemv_split<1>(res) : c.gemv_split<2>(res);
-      else ok = K <= 256 ? c.gemv_row<1>(res) : K <= 768 ? c.gemv_row<3>(res)
-              : K <= 2048 ? c.gemv_row<8>(res) : c.gemv_row<16>(res);
+      if (split) ok = K == 2048 ? c.template gemv_split<1>(res) : c.template gemv_split<2>(res);
+      else ok = K <= 256 ? c.template gemv_row<1>(res) : K <= 768 ? c.template gemv_row<3>(res)
+              : K <= 2048 ? c.template gemv_row<8>(res) : c.template gemv_row<16>(res);
       // the split path's sums are written by the threads that run the
       // epilogue; its partial buffer is reused by the next split chunk, which
       // the completion barrier below also orders when the task ends here
@@ -2199,25 +2206,26 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
   return ok;
 }
 
+template <bool ONE>
 __device__ __forceinline__ bool op_route(const Params& p, Smem& S, const int32_t* t) {
-  Cons c(p, S, t);
+  Cons<ONE> c(p, S, t);
   const bool ok = c.route();
   c.save();
   return ok;
 }
 
-template <int D>
+template <bool ONE, int D>
 __device__ __forceinline__ bool op_attn(const Params& p, Smem& S, const int32_t* t) {
-  Cons c(p, S, t);
-  const bool ok = c.attn<D>();
+  Cons<ONE> c(p, S, t);
+  const bool ok = c.template attn<D>();
   c.save();
   return ok;
 }
 
-template <int D>
+template <bool ONE, int D>
 __device__ __forceinline__ bool op_combine(const Params& p, Smem& S, const int32_t* t) {
-  Cons c(p, S, t);
-  const bool ok = c.combine<D>();
+  Cons<ONE> c(p, S, t);
+  const bool ok = c.template combine<D>();
   c.save();
   return ok;
 }
@@ -2254,16 +2262,16 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
         // one token: whole rows per warp, by the row's length; more tokens:
         // up to eight per pass
         if constexpr (ONE) {
-          ok = op_row(p, S, t);
+          ok = op_row<true>(p, S, t);
         } else {
-          ok = op_chunk(p, S, t);
+          ok = op_chunk<false>(p, S, t);
         }
         (void)nt;
         break;
       }
-      case OP_ROUTE: ok = op_route(p, S, t); break;
-      case OP_ATTN: ok = (p.d == 128) ? op_attn<128>(p, S, t) : op_attn<64>(p, S, t); break;
-      case OP_COMBINE: ok = (p.d == 128) ? op_combine<128>(p, S, t) : op_combine<64>(p, S, t); break;
+      case OP_ROUTE: ok = op_route<ONE>(p, S, t); break;
+      case OP_ATTN: ok = (p.d == 128) ? op_attn<ONE, 128>(p, S, t) : op_attn<ONE, 64>(p, S, t); break;
+      case OP_COMBINE: ok = (p.d == 128) ? op_combine<ONE, 128>(p, S, t) : op_combine<ONE, 64>(p, S, t); break;
       default: ok = false; break;
     }
     if (p.trace && tid == 0 && n_rec < p.trace_cap) {
@@ -2309,8 +2317,6 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
     }
     mbar_init(&S.cbar, kConsumerWarps);
     mbar_init(&S.route_bar, 1);
-    for (int r = 0; r < kOutRows; r++)
-      for (int b = 0; b < kMaxBatch; b++) S.acc_m[r][b] = 0.f;
     for (int w = 0; w < kConsumerWarps; w++) {
       S.cstage[w] = S.cphase[w] = S.cchunk[w] = 0;
       S.seen_bar[w] = -1;
@@ -2326,7 +2332,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
     // registers back
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs) : "memory");
     if (wid == kConsumerWarps) {
-      Prod pr(p, S);
+      Prod<ONE> pr(p, S);
       pr.run();
     }
   } else {

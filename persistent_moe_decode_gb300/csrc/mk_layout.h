@@ -80,7 +80,6 @@ constexpr int kMaxBatch = 16;
 constexpr int kTraceWords = 16;         // words per timeline record
 constexpr int kPartFloats = 2048;       // one of the two GEMV partial-sum buffers
 constexpr int kTokPass = 8;             // tokens per GEMV pass (activations in registers)
-constexpr int kOutRows = 32;            // hidden rows per DOWN chunk (several tokens)
 constexpr int kMaxActive = 128;         // routed experts of one step (B * k <= 128)
 
 // whole rows of a [rows][K] BF16 matrix that one stage carries
@@ -105,8 +104,9 @@ struct BarLayout {
   int p1;      // P1 tasks done                                   (target n_sm)
   int up;      // UP tasks done                                   (target n_up_sms)
   int comb;    // COMBINE tasks done                              (target n_comb_sms)
-  int out;     // OUT and DOWN tasks done                         (target n_sm + n_down_sms)
+  int out;     // OUT tasks done, and one-token DOWN tasks        (target n_sm [+ n_down_sms])
   int rtr;     // P1 tasks holding router rows done               (target n_rtr_sms)
+  int down;    // several tokens: DOWN tasks done                 (target n_down_sms)
   int items;   // + b: split-KV items of sequence b done          (target: its split count)
 };
 
@@ -117,8 +117,9 @@ inline BarLayout bar_layout(int max_batch) {
   b.comb = 2;
   b.out = 3;
   b.rtr = 4;
-  b.items = 5;
-  b.per_layer = (5 + max_batch + 31) & ~31;
+  b.down = 5;
+  b.items = 6;
+  b.per_layer = (6 + max_batch + 31) & ~31;
   return b;
 }
 
@@ -197,6 +198,8 @@ struct Params {
   float* moe;        // [L][Bmax][H] weighted sum of the routed experts' outputs
   float* mpart;      // one token: [k * I / 8][H] the down projection of each 8-column
                      // group of the routed experts' hidden vectors, weighted
+  float* mdown;      // several tokens: [Bmax * k][H] the weighted down projection of each
+                     // (token, pick) entry, summed over the picks by OUT
 };
 
 }  // namespace mk

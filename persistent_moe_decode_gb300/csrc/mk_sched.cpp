@@ -167,8 +167,15 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
           case OP_COMBINE: share(units, ncomb, roles ? attn_before(s, n_sm, n_attn) : s, &lo, &hi); break;
           case OP_OUT: share(c.hidden, n_sm, s, &lo, &hi); break;
           case OP_DOWN: {
+            // one token: hidden rows (sums of the experts' partials); several:
+            // slice s of n over the routed experts' rows (like UP)
             const int slice = roles ? moe_rank(s, n_sm, n_attn) : s;
-            share(c.hidden, ndown, slice, &lo, &hi);
+            if (batch == 1) {
+              share(c.hidden, ndown, slice, &lo, &hi);
+            } else {
+              lo = slice < ndown ? slice : -1;
+              hi = ndown;
+            }
             break;
           }
           case OP_UP: {

@@ -57,7 +57,11 @@ def test_every_wave_is_covered_once_per_layer(dims, n_sm, n_attn, batch):
         out = t[t[:, F_OP] == OP_OUT]
         assert len(out) == n_sm and covered_once(out[:, [F_A0, F_A1]], H), "O-proj rows"
         down = t[t[:, F_OP] == OP_DOWN]
-        assert covered_once(down[:, [F_A0, F_A1]], H), "DOWN rows"
+        if batch == 1:
+            assert covered_once(down[:, [F_A0, F_A1]], H), "DOWN rows"
+        else:   # slices of the routed experts' rows, resolved on the device
+            n_down = int(down[0, F_A1])
+            assert sorted(down[down[:, F_A0] >= 0, F_A0].tolist()) == list(range(n_down)), "DOWN slices"
         comb = t[t[:, F_OP] == OP_COMBINE]
         assert covered_once(comb[:, [F_A0, F_A1]], batch * dims.n_q_heads), "combine units"
         up = t[t[:, F_OP] == OP_UP]
