@@ -219,13 +219,17 @@ int mk_debug_bump_wait(mk_handle* h, int layer, int delta);
 /* Task timeline of the last completed step (config.trace_records > 0):
  * HOST buffer of int32 [n_sm][trace_records][16] records
  *   {op, layer, tile or queue item, t_start_lo, t_start_hi, ready_ns, end_ns, sm,
- *    first_stage_ns, stages_done_ns, reduced_ns, 0, 0, 0, 0, 0}
+ *    first_stage_ns, stages_done_ns, reduced_ns, kind, rows, handed_ns, issued_ns,
+ *    stage_wait_ns}
  * where t_start is the %globaltimer value (ns) when the block took the task,
  * ready_ns the offset at which its inputs were ready, end_ns the offset at
  * which it signalled completion and the next three the offsets at which its
  * first stage arrived, its last stage was consumed and its partial sums were
- * reduced (equal to the start where a task has no such phase); unused records
- * have op = -1.  Copies min(bytes, size) bytes; *size_out (may be NULL) gets
+ * reduced (equal to the start where a task has no such phase); kind and rows
+ * describe the piece (a GEMV chunk kind and its row count); handed_ns and
+ * issued_ns are the (usually negative) offsets at which the streaming warp
+ * handed the piece over and issued its first copy (0: no copy), stage_wait_ns
+ * the time the block waited for its stages; unused records have op = -1.  Copies min(bytes, size) bytes; *size_out (may be NULL) gets
  * the full size. */
 int mk_read_trace(mk_handle* h, void* dst, size_t bytes, size_t* size_out);
 

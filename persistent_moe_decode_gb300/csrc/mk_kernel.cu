@@ -98,7 +98,9 @@ static_assert(kSmemBytes <= 232448, "shared memory of one block exceeds the sm_1
 // resolved task words (written by the producer into the task ring)
 enum : int {
   R_OP = 0, R_LAYER, R_TASK, R_KIND, R_FLAGS, R_ROW0, R_NROWS, R_K, R_NT, R_NBLK, R_A, R_E,
-  R_REL0, R_ITEM, R_B, R_TT0, R_TT1, R_POS, R_NST, R_U0, R_U1, R_BUMP, R_ROW1, R_NROWS1, R_NGRP
+  R_REL0, R_ITEM, R_B, R_TT0, R_TT1, R_POS, R_NST, R_U0, R_U1, R_BUMP, R_ROW1, R_NROWS1, R_NGRP,
+  R_PCOMMIT, R_PISSUE    // timeline only: %globaltimer (low word) when the producer handed the
+                         // task over and when it issued the task's first copy (0: none)
 };
 // GEMV chunk kinds; K_P1 (router rows, then QKV rows) and K_MRED (the sum of
 // the experts' per-group partials of OUT's rows) are one-token forms, and a
@@ -201,10 +203,13 @@ __device__ __forceinline__ int attn_pps(const Params& p) {
   return pb >= kStageBytes / 2 ? 1 : (kStageBytes / 2) / pb;
 }
 
-// share of slice s of n in [0, total)
+// share of slice s of n in [0, total); total * n < 2^32 for every device-side
+// share (rows or groups of the routed experts over at most a few hundred
+// slices), so 32-bit arithmetic suffices (a 64-bit division is a long
+// software sequence on the critical path)
 __device__ __forceinline__ void dshare(int total, int n, int s, int& lo, int& hi) {
-  lo = (int)((long long)total * s / n);
-  hi = (int)((long long)total * (s + 1) / n);
+  lo = (int)((uint32_t)total * (uint32_t)s / (uint32_t)n);
+  hi = (int)((uint32_t)total * (uint32_t)(s + 1) / (uint32_t)n);
 }
 
 // one token: rows of a P1 / O-proj chunk.  With K = 2048 or 4096 the
@@ -341,13 +346,22 @@ struct Prod {
 
   __device__ __forceinline__ void commit() {
     __syncwarp();
-    if (lane == 0) mbar_arrive(&S.tfull[task_seq % kTaskSlots]);
+    if (lane == 0) {
+      if (p.trace) S.task[task_seq % kTaskSlots][R_PCOMMIT] = (int32_t)(uint32_t)gtime_ns();
+      mbar_arrive(&S.tfull[task_seq % kTaskSlots]);
+    }
     task_seq++;
   }
 
   __device__ __forceinline__ bool acquire_stage(uint32_t& slot) {
     slot = stage_seq % kStages;
-    return wait_phase(p, &S.empty[slot], ((stage_seq / kStages) & 1u) ^ 1u, ti, op);
+    const bool ok = wait_phase(p, &S.empty[slot], ((stage_seq / kStages) & 1u) ^ 1u, ti, op);
+    if (p.trace && lane == 0 && task_seq > 0) {
+      // the copy is issued next (after the mbarrier's release, which orders this word)
+      int32_t* w = S.task[(task_seq - 1) % kTaskSlots];
+      if (w[R_PISSUE] == 0) w[R_PISSUE] = (int32_t)((uint32_t)gtime_ns() | 1u);
+    }
+    return ok;
   }
 
   // rows [row0, row0 + nrows) of a row-major [*, K] matrix, whole rows, one
@@ -597,10 +611,10 @@ struct Prod {
     if (a0 >= 0) {
       if (a1 >= n_act) {
         // at least one slice per expert: expert a takes slices
-        // [a * a1 / n_act, (a + 1) * a1 / n_act), so no slice spans two experts
-        int a = 0;
-        while ((long long)(a + 1) * a1 / n_act <= a0) a++;
-        const int s0 = (int)((long long)a * a1 / n_act), s1 = (int)((long long)(a + 1) * a1 / n_act);
+        // [a * a1 / n_act, (a + 1) * a1 / n_act), so no slice spans two
+        // experts; slice a0's expert is the largest a with a * a1 / n_act <= a0
+        const int a = ((a0 + 1) * n_act - 1) / a1;
+        const int s0 = a * a1 / n_act, s1 = (a + 1) * a1 / n_act;
         dshare(G, s1 - s0, a0 - s0, g0, g1);
         g0 += a * G;
         g1 += a * G;
@@ -2288,8 +2302,8 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
       for (int k = 0; k < 3; k++) rec[8 + k] = (int32_t)(S.t_mark[k] - t_start);
       rec[11] = t[R_KIND];
       rec[12] = t[R_NROWS];
-      rec[13] = t[R_NT];
-      rec[14] = t[R_FLAGS];
+      rec[13] = (int32_t)((uint32_t)t[R_PCOMMIT] - (uint32_t)t_start);
+      rec[14] = t[R_PISSUE] ? (int32_t)((uint32_t)t[R_PISSUE] - (uint32_t)t_start) : 0;
       rec[15] = (int32_t)S.t_swait;
       n_rec++;
     }
