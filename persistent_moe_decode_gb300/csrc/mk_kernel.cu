@@ -141,9 +141,11 @@ __device__ __noinline__ void report(const Params& p, uint32_t code, int task, in
 
 // Bounded wait on a shared-memory mbarrier phase, called by a whole warp.  All
 // lanes poll; lane 0 alone decides to give up (stop word or time limit) and the
-// decision is broadcast, so the warp leaves together.  false = give up.  The
-// polling loop is out of line: the fast path (phase already complete) is the
-// common case, and one shared copy of the loop keeps the kernel's code small.
+// decision is broadcast, so the warp leaves together.  false = give up; the
+// block's exit path reports a time-out (DEV_SMEM_TIMEOUT) once.  Every wait
+// site inlines this loop, so it is kept short: the give-up test runs once per
+// 256 polls and calls nothing (code that runs once per layer is fetched anew
+// each time, and a call from these paths saves many registers).
 __device__ __forceinline__ bool wait_phase_slow(const Params& p, uint64_t* bar, uint32_t parity, int task,
                                              int op, unsigned mult) {
   const unsigned long long t0 = gtime_ns();
@@ -151,16 +153,9 @@ __device__ __forceinline__ bool wait_phase_slow(const Params& p, uint64_t* bar, 
   for (uint32_t it = 1;; ++it) {
     done = done || mbar_try_wait(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
-    if ((it & 63u) == 0) {
+    if ((it & 255u) == 0) {
       int give = 0;
-      if ((threadIdx.x & 31) == 0) {
-        if (stopped(p)) {
-          give = 1;
-        } else if (gtime_ns() - t0 > mult * p.timeout_ns) {
-          report(p, DEV_SMEM_TIMEOUT, task, op, -1, 0, parity);
-          give = 1;
-        }
-      }
+      if ((threadIdx.x & 31) == 0) give = stopped(p) || gtime_ns() - t0 > mult * p.timeout_ns;
       if (__shfl_sync(0xffffffffu, give, 0)) return false;
     }
   }
@@ -375,7 +370,7 @@ struct Prod {
       if (lane == 0) {
         const uint32_t bytes = (uint32_t)(rows * K * 2);
         mbar_arrive_expect_tx(&S.full[slot], bytes);
-        bulk_g2s(&S.stage[slot][0], w + (size_t)(row0 + done) * K, bytes, &S.full[slot]);
+        bulk_g2s_hint(&S.stage[slot][0], w + (size_t)(row0 + done) * K, bytes, &S.full[slot], policy_evict_first());
       }
       __syncwarp();
       stage_seq++;
@@ -417,7 +412,8 @@ struct Prod {
           const bool is_k = lane < n;
           uint8_t* dst = &S.stage[slot][(is_k ? lane : pps + lane - n) * pb];
           for (int bx = 0; bx < nbox; bx++)
-            tma_load_2d(dst + bx * rows * 128, is_k ? km : vm, bx * 64, pg * rows, &S.full[slot]);
+            tma_load_2d_hint(dst + bx * rows * 128, is_k ? km : vm, bx * 64, pg * rows, &S.full[slot],
+                             policy_evict_first());
         }
         stage_seq++;
       }
@@ -503,56 +499,44 @@ struct Prod {
 
   // one-token P1 / FINAL: chunks of up to kRowChunk rows; a P1 chunk holds its
   // router rows and its QKV rows as two groups
+  // one token, P1: the router rows [a0, a1) first, in chunks of their own
+  // (the last one releases the router counter), then the W_qkv rows [b0, b1);
+  // FINAL: LM-head rows [a0, a1).  One loop emits every chunk (one copy of
+  // the hand-over and stream code): phase 0 walks [a0, a1), phase 1 [b0, b1).
   __device__ __forceinline__ bool do_p1_final_1(int a0, int a1, int b0, int b1) {
     const int H = p.H;
-    if (op == OP_FINAL) {
-      if (a1 <= a0) return chunk(K_LM, FL_FIRST | FL_LAST, 0, 0, 1, H, 1, 0, 0, 0, nullptr, nullptr);
-      for (int c0 = a0; c0 < a1; c0 += kRowChunk) {
-        const int c1 = min(a1, c0 + kRowChunk);
-        const int flags = (c0 == a0 ? FL_FIRST : 0) | (c1 == a1 ? FL_LAST : 0);
-        if (!chunk(K_LM, flags, c0, c1 - c0, 1, H, 1, 0, 0, 0, p.lm_head, nullptr)) return false;
-      }
-      return true;
-    }
-    // P1: the router rows [a0, a1) first, in a chunk of their own that
-    // releases the router counter, then the W_qkv rows [b0, b1)
-    if (a1 <= a0 && b1 <= b0) return chunk(K_P1, FL_FIRST | FL_LAST, 0, 0, 1, H, 1, 0, 0, 0, nullptr, nullptr);
-    const int cr = split_rows(H);
+    const bool fin = op == OP_FINAL;
+    if (fin) b1 = b0;
+    const int cr = fin ? kRowChunk : split_rows(H);
+    int ph = a1 > a0 ? 0 : 1, c0 = ph == 0 ? a0 : b0;
     bool first = true;
-    for (int c0 = a0; c0 < a1; c0 += cr) {
-      const int c1 = min(a1, c0 + cr);
-      const int flags = (first ? FL_FIRST : 0) | (c1 == a1 ? FL_RTR : 0) | (c1 == a1 && b1 <= b0 ? FL_LAST : 0);
-      if (!p1_chunk(flags, c0, c1 - c0, 0, 0)) return false;
+    do {
+      const int hi = ph == 0 ? a1 : b1;
+      const int c1 = min(hi, c0 + cr);
+      const bool end_ph = c1 >= hi;
+      const bool last = end_ph && (ph == 1 || b1 <= b0);
+      int32_t* w = begin();
+      if (!w) return false;
+      if (lane == 0) {
+        w[R_KIND] = fin ? K_LM : K_P1;
+        w[R_FLAGS] = (first ? FL_FIRST : 0) | (last ? FL_LAST : 0) | (!fin && ph == 0 && end_ph ? FL_RTR : 0);
+        w[R_ROW0] = ph == 0 ? c0 : 0;
+        w[R_NROWS] = ph == 0 ? max(c1 - c0, 0) : 0;
+        w[R_ROW1] = ph == 1 ? c0 : 0;
+        w[R_NROWS1] = ph == 1 ? max(c1 - c0, 0) : 0;
+        w[R_NBLK] = 1;
+        w[R_K] = H;
+        w[R_NT] = 1;
+      }
+      commit();
+      if (c1 > c0 && !stream_rows(fin ? p.lm_head : wptr(ph), c0, c1 - c0, H)) return false;
       first = false;
-    }
-    for (int c0 = b0; c0 < b1; c0 += cr) {
-      const int c1 = min(b1, c0 + cr);
-      const int flags = (first ? FL_FIRST : 0) | (c1 == b1 ? FL_LAST : 0);
-      if (!p1_chunk(flags, 0, 0, c0, c1 - c0)) return false;
-      first = false;
-    }
-    return true;
-  }
-
-  // one-token P1 chunk: router rows [r0, r0 + nr), then W_qkv rows [q0, q0 + nq)
-  __device__ __forceinline__ bool p1_chunk(int flags, int r0, int nr, int q0, int nq) {
-    const int H = p.H;
-    int32_t* w = begin();
-    if (!w) return false;
-    if (lane == 0) {
-      w[R_KIND] = K_P1;
-      w[R_FLAGS] = flags;
-      w[R_ROW0] = r0;
-      w[R_NROWS] = nr;
-      w[R_ROW1] = q0;
-      w[R_NROWS1] = nq;
-      w[R_NGRP] = 2;
-      w[R_K] = H;
-      w[R_NT] = 1;
-    }
-    commit();
-    if (nr > 0 && !stream_rows(wptr(0), r0, nr, H)) return false;
-    if (nq > 0 && !stream_rows(wptr(1), q0, nq, H)) return false;
+      c0 = c1;
+      if (end_ph && ph == 0) {
+        ph = 1;
+        c0 = b0;
+      }
+    } while (c0 < (ph == 0 ? a1 : b1));
     return true;
   }
 
@@ -644,22 +628,16 @@ struct Prod {
         w[R_REL0] = g;
       }
       commit();
+      // the piece's gate rows, its up rows, then each of its groups of the
+      // down projection (an [H][8] block, streamed as H rows of 8): one
+      // stream loop for all of them keeps the code short
       const size_t eo = (size_t)e * p.I * H;
-      if (!stream_rows(wptr(3) + eo, i0, i1 - i0, H)) return false;
-      if (!stream_rows(wptr(4) + eo, i0, i1 - i0, H)) return false;
       const uint16_t* blk = p.wd_blk + (((size_t)l * p.E + e) * G + i0 / 8) * H * 8;
-      for (int c = 0; c < ncb; c++)
-        for (int r0 = 0; r0 < H; r0 += kDownRows) {
-          const int rows = min(kDownRows, H - r0);
-          uint32_t slot;
-          if (!acquire_stage(slot)) return false;
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(rows * 16));
-            bulk_g2s(&S.stage[slot][0], blk + ((size_t)c * H + r0) * 8, (uint32_t)(rows * 16), &S.full[slot]);
-          }
-          __syncwarp();
-          stage_seq++;
-        }
+      for (int sg = 0; sg < 2 + ncb; sg++) {
+        const bool dn = sg >= 2;
+        const uint16_t* src = dn ? blk + (size_t)(sg - 2) * H * 8 : wptr(3 + sg) + eo;
+        if (!stream_rows(src, dn ? 0 : i0, dn ? H : i1 - i0, dn ? 8 : H)) return false;
+      }
       g = ge;
     }
     return true;
@@ -838,6 +816,9 @@ struct Prod {
       if (ok) commit();
     }
     if (!ok) {
+      // a wait gave up: a time-out, unless another block had already stopped
+      // the step (the first report wins)
+      if (lane == 0) report(p, DEV_SMEM_TIMEOUT, ti, op, -1, 0, 0);
       // stop: make sure no bulk copy of ours is still writing into shared memory
       const uint32_t n = stage_seq;
       const uint32_t first = n > (uint32_t)kStages ? n - kStages : 0u;
@@ -996,13 +977,15 @@ struct Cons {
   // one token: every load (own residual copy, the previous layer's update,
   // the gain) issued together, each thread sums the eight warp partials
   // itself (same order in every thread), x goes to the staging buffer
+  // NI: float4s per thread (H <= 1024 NI): the instance for the model's H
+  // runs, and its code is no longer than it needs to be
+  template <int NI>
   __device__ __forceinline__ bool norm1(int l, bool final_norm) {
     const int H = p.H, H4 = H / 4;
     const size_t Bm = (size_t)p.Bmax;
     float* hl = p.hloc + (size_t)blockIdx.x * Bm * H;
     float* xl = p.xloc + (size_t)blockIdx.x * Bm * H;
     const uint16_t* gain = final_norm ? p.final_norm : p.attn_norm[l];
-    constexpr int NI = 4;                       // H <= 4096: at most 4 float4 per thread
     float4 h[NI];
     uint2 g[NI];
 #pragma unroll
@@ -1081,7 +1064,10 @@ struct Cons {
   }
 
   __device__ __forceinline__ bool norm(int l, bool final_norm) {
-    if (ONE) return norm1(l, final_norm);
+    if (ONE) {
+      const int H4 = p.H / 4;
+      return H4 <= 256 ? norm1<1>(l, final_norm) : H4 <= 512 ? norm1<2>(l, final_norm) : norm1<4>(l, final_norm);
+    }
     const int H = p.H, B = p.B, H4 = H / 4;
     const size_t Bm = (size_t)p.Bmax;
     if (l > 0 && !wait_counter(bar_index(p, l - 1, p.bl.out), out_target() + t[R_BUMP])) return false;
@@ -2254,7 +2240,10 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
   int n_rec = 0;
   while (true) {
     const uint32_t slot = task_seq % kTaskSlots;
-    if (!wait_phase(p, &S.tfull[slot], (task_seq / kTaskSlots) & 1u, -1, -1)) break;
+    if (!wait_phase(p, &S.tfull[slot], (task_seq / kTaskSlots) & 1u, -1, -1)) {
+      if (tid == 0) report(p, DEV_SMEM_TIMEOUT, -1, -1, -1, 0, 0);
+      break;
+    }
     const int32_t* t = S.task[slot];
     task_seq++;
     const int op = t[R_OP];
@@ -2310,7 +2299,11 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
     // the task's words are no longer needed: hand the slot back to the producer
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.tempty[slot]);
-    if (!ok || S.abort_flag) break;
+    if (!ok || S.abort_flag) {
+      // a wait gave up (reported here as a time-out unless a report came first)
+      if (tid == 0) report(p, DEV_SMEM_TIMEOUT, t[R_TASK], op, -1, 0, 0);
+      break;
+    }
   }
 }
 
