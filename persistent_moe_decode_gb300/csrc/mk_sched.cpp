@@ -141,6 +141,21 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
     }
   }
 
+  // O-proj rows.  One token: an attention-branch SM, idle from its COMBINE
+  // until the layer ends, takes kOutAttnWeight times an expert-branch SM's
+  // share (the expert branch still sums the experts' partials first).
+  std::vector<int> o_lo(n_sm, 0), o_hi(n_sm, 0);
+  {
+    constexpr long long kOutAttnWeight = 5;
+    std::vector<long long> wo(n_sm + 1, 0);
+    for (int s = 0; s < n_sm; s++)
+      wo[s + 1] = wo[s] + ((roles && batch == 1 && is_attn_sm(s, n_sm, n_attn)) ? kOutAttnWeight : 1);
+    for (int s = 0; s < n_sm; s++) {
+      o_lo[s] = (int)(c.hidden * wo[s] / wo[n_sm]);
+      o_hi[s] = (int)(c.hidden * wo[s + 1] / wo[n_sm]);
+    }
+  }
+
   out->tasks.clear();
   out->off.assign(n_sm + 1, 0);
   for (int s = 0; s < n_sm; s++) {
@@ -165,7 +180,7 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
         switch (op) {
           case OP_P1: lo = r_lo[s]; hi = r_hi[s]; break;   // router rows; W_qkv rows below
           case OP_COMBINE: share(units, ncomb, roles ? attn_before(s, n_sm, n_attn) : s, &lo, &hi); break;
-          case OP_OUT: share(c.hidden, n_sm, s, &lo, &hi); break;
+          case OP_OUT: lo = o_lo[s]; hi = o_hi[s]; break;
           case OP_DOWN: {
             // one token: hidden rows (sums of the experts' partials); several:
             // slice s of n over the routed experts' rows (like UP)
