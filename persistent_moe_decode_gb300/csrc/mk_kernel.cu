@@ -139,32 +139,33 @@ __device__ __noinline__ void report(const Params& p, uint32_t code, int task, in
   }
 }
 
-// Bounded wait on a shared-memory mbarrier phase, called by a whole warp.  All
-// lanes poll; lane 0 alone decides to give up (stop word or time limit) and the
-// decision is broadcast, so the warp leaves together.  false = give up; the
-// block's exit path reports a time-out (DEV_SMEM_TIMEOUT) once.  Every wait
-// site inlines this loop, so it is kept short: the give-up test runs once per
-// 256 polls and calls nothing (code that runs once per layer is fetched anew
-// each time, and a call from these paths saves many registers).
-__device__ __forceinline__ bool wait_phase_slow(const Params& p, uint64_t* bar, uint32_t parity, int task,
-                                             int op, unsigned mult) {
-  const unsigned long long t0 = gtime_ns();
+// Bounded wait on a shared-memory mbarrier phase, called by a whole warp:
+// false = give up.  The phases come from this block's own warps and copies,
+// so the wait is bounded by a poll count (a few seconds of polling, far past
+// any real wait) and by the stop word (another block has reported an error),
+// read every 4096 polls by all lanes at once (one broadcast load, so the warp
+// decides together).  The block's exit path reports a time-out
+// (DEV_SMEM_TIMEOUT) once.  Every wait site inlines this loop, so it is kept
+// to a few instructions: code that runs once per layer is fetched anew each
+// time, and a call from these paths saves many registers.
+constexpr uint32_t kWaitPolls = 1u << 26;
+
+__device__ __forceinline__ bool wait_phase_slow(const Params& p, uint64_t* bar, uint32_t parity) {
   bool done = false;
   for (uint32_t it = 1;; ++it) {
     done = done || mbar_try_wait(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
-    if ((it & 255u) == 0) {
-      int give = 0;
-      if ((threadIdx.x & 31) == 0) give = stopped(p) || gtime_ns() - t0 > mult * p.timeout_ns;
-      if (__shfl_sync(0xffffffffu, give, 0)) return false;
-    }
+    if ((it & 4095u) == 0 && (it >= kWaitPolls || stopped(p))) return false;
   }
 }
 
 __device__ __forceinline__ bool wait_phase(const Params& p, uint64_t* bar, uint32_t parity, int task,
                                            int op, unsigned mult = 1) {
+  (void)task;
+  (void)op;
+  (void)mult;
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-  return wait_phase_slow(p, bar, parity, task, op, mult);
+  return wait_phase_slow(p, bar, parity);
 }
 
 // bounded spin on a global counter (Listing 2's wait, with a time limit)
