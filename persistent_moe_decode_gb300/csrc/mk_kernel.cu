@@ -2053,9 +2053,11 @@ struct Cons {
   }
 
   // ATTN_COMBINE of units [u0, u1) (unit = sequence b, query head h): merge the
-  // sequence's split-KV partials.  Warp w takes splits w, w + 8, ...; lane l
-  // dims DPL l .. DPL l + DPL - 1; the warps' sums meet in shared memory and
-  // are added in a fixed order.
+  // sequence's split-KV partials in one pass.  Warp w takes splits w, w + 8,
+  // ... (four loads in flight), lane l dims DPL l .. DPL l + DPL - 1, and keeps
+  // a running maximum: each split rescales the warp's sums to the larger
+  // maximum.  The warps' (maximum, sum, numerator) meet in shared memory and
+  // are merged in warp order.
   template <int D>
   __device__ __forceinline__ bool combine() {
     constexpr int DPL = D / 32;
@@ -2066,19 +2068,7 @@ struct Cons {
       const int g = h / grp, hh = h % grp;
       const int base = p.attn_meta[b * 2], nsplit = p.attn_meta[b * 2 + 1];
       if (!wait_counter(bar_index(p, l, p.bl.items + b), nsplit)) return false;
-      // pass 1: maximum over the splits
-      float mx = -INFINITY;
-      for (int s = tid; s < nsplit; s += 256)
-        mx = fmaxf(mx, __ldcg(p.attn_ml + (((size_t)(base + s) * hkv + g) * grp + hh) * 2));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      if (lane == 0) S.nred[warp][0] = mx;
-      if (!csync()) return false;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, S.nred[w][0]);
-      // pass 2: this warp's splits, four loads in flight
-      float num[DPL], den = 0.f;
+      float m = -INFINITY, den = 0.f, num[DPL];
 #pragma unroll
       for (int j = 0; j < DPL; j++) num[j] = 0.f;
       for (int s0 = warp; s0 < nsplit; s0 += 4 * kConsumerWarps) {
@@ -2087,43 +2077,48 @@ struct Cons {
 #pragma unroll
         for (int q = 0; q < 4; q++) {
           const int s = s0 + q * kConsumerWarps;
-          ml[q] = make_float2(-INFINITY, 0.f);
-#pragma unroll
-          for (int j = 0; j < DPL; j++) ov[q][j] = 0.f;
-          if (s < nsplit) {
-            const size_t it = ((size_t)(base + s) * hkv + g) * grp + hh;
-            ml[q] = __ldcg((const float2*)(p.attn_ml + it * 2));
-            if (DPL == 4) {
-              const float4 v = __ldcg((const float4*)(p.attn_part + it * D) + lane);
-              ov[q][0] = v.x; ov[q][1 % DPL] = v.y; ov[q][2 % DPL] = v.z; ov[q][3 % DPL] = v.w;
-            } else {
-              const float2 v = __ldcg((const float2*)(p.attn_part + it * D) + lane);
-              ov[q][0] = v.x; ov[q][1 % DPL] = v.y;
-            }
+          const size_t it = ((size_t)(base + min(s, nsplit - 1)) * hkv + g) * grp + hh;
+          ml[q] = s < nsplit ? __ldcg((const float2*)(p.attn_ml + it * 2)) : make_float2(-INFINITY, 0.f);
+          if constexpr (DPL == 4) {
+            const float4 v = __ldcg((const float4*)(p.attn_part + it * D) + lane);
+            ov[q][0] = v.x; ov[q][1 % DPL] = v.y; ov[q][2 % DPL] = v.z; ov[q][3 % DPL] = v.w;
+          } else {
+            const float2 v = __ldcg((const float2*)(p.attn_part + it * D) + lane);
+            ov[q][0] = v.x; ov[q][1 % DPL] = v.y;
           }
         }
 #pragma unroll
         for (int q = 0; q < 4; q++) {
-          const float w = (ml[q].x == -INFINITY) ? 0.f : exp2f(ml[q].x - M);
-          den += w * ml[q].y;
+          const float mn = fmaxf(m, ml[q].x);
+          const float a = m == -INFINITY ? 0.f : exp2f(m - mn);
+          const float w = ml[q].x == -INFINITY ? 0.f : exp2f(ml[q].x - mn);
+          den = den * a + w * ml[q].y;
 #pragma unroll
-          for (int j = 0; j < DPL; j++) num[j] += w * ov[q][j];
+          for (int j = 0; j < DPL; j++) num[j] = num[j] * a + w * ov[q][j];
+          m = mn;
         }
       }
       float* red = S.red;   // [warp][D]
 #pragma unroll
       for (int j = 0; j < DPL; j++) red[warp * D + lane * DPL + j] = num[j];
-      if (lane == 0) S.nred[warp][1] = den;
+      if (lane == 0) {
+        S.nred[warp][0] = m;
+        S.nred[warp][1] = den;
+      }
       if (!csync()) return false;
       if (tid < D) {
+        float M = -INFINITY;
+        for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, S.nred[w][0]);
         float sn = 0.f, sd = 0.f;
         for (int w = 0; w < kConsumerWarps; w++) {
-          sn += red[w * D + tid];
-          sd += S.nred[w][1];
+          const float mw = S.nred[w][0];
+          const float a = mw == -INFINITY ? 0.f : exp2f(mw - M);
+          sn += a * red[w * D + tid];
+          sd += a * S.nred[w][1];
         }
         __stcg(p.attn_out + ((size_t)l * Bm + b) * p.hq * D + (size_t)h * D + tid, sn / sd);
       }
-      if (!csync()) return false;
+      if (u + 1 < t[R_U1] && !csync()) return false;
     }
     return signal(bar_index(p, l, p.bl.comb), 1);
   }
