@@ -9,8 +9,9 @@
 // depends on routing (the experts' rows) are fixed as "slice s of n" and
 // resolved on the device once the routing is known.  Any order of the waves
 // in which ROUTE precedes UP precedes DOWN and ATTN precedes COMBINE precedes
-// OUT has no circular wait (every wait points at an earlier wave of the same
-// layer, or at the previous layer).
+// OUT (and, with several tokens, DOWN precedes OUT, whose expert sums wait for
+// every DOWN task) has no circular wait (every wait points at an earlier wave
+// of the same layer, or at the previous layer).
 #include "mk_sched.h"
 
 #include <algorithm>
@@ -104,10 +105,14 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
       {OP_P1, OP_ROUTE, OP_ATTN, OP_UP, OP_COMBINE, OP_DOWN, OP_OUT},
       {OP_P1, OP_ROUTE, OP_ATTN, OP_COMBINE, OP_UP, OP_DOWN, OP_OUT},
       {OP_P1, OP_ROUTE, OP_UP, OP_ATTN, OP_DOWN, OP_COMBINE, OP_OUT}};
-  // the attention branch needs no routing; the expert branch's down rows
-  // only wait for its own UP wave, so they run while attention is under way
+  // the attention branch needs no routing; several tokens: the expert
+  // branch's down rows only wait for its own UP wave, so they run while
+  // attention is under way; one token: the expert branch takes its (few)
+  // O-proj rows as soon as the attention is combined, before the sums of the
+  // experts' partials, which nothing on the SM waits for
   static const int attn_role[4] = {OP_P1, OP_ATTN, OP_COMBINE, OP_OUT};
   static const int moe_role[5] = {OP_P1, OP_ROUTE, OP_UP, OP_DOWN, OP_OUT};
+  static const int moe_role1[5] = {OP_P1, OP_ROUTE, OP_UP, OP_OUT, OP_DOWN};
 
   // P1 rows.  The router rows go, 8 rows (one stage) per SM or more if there
   // are few of them, to the first expert-branch SMs (all SMs when there are
@@ -143,10 +148,10 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
 
   // O-proj rows.  One token: an attention-branch SM, idle from its COMBINE
   // until the layer ends, takes kOutAttnWeight times an expert-branch SM's
-  // share (the expert branch still sums the experts' partials first).
+  // share.
   std::vector<int> o_lo(n_sm, 0), o_hi(n_sm, 0);
   {
-    constexpr long long kOutAttnWeight = 5;
+    constexpr long long kOutAttnWeight = 4;
     std::vector<long long> wo(n_sm + 1, 0);
     for (int s = 0; s < n_sm; s++)
       wo[s + 1] = wo[s] + ((roles && batch == 1 && is_attn_sm(s, n_sm, n_attn)) ? kOutAttnWeight : 1);
@@ -169,7 +174,7 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
       ops = attn_role;
       nops = 4;
     } else {
-      ops = moe_role;
+      ops = batch == 1 ? moe_role1 : moe_role;
       nops = 5;
     }
     std::vector<Desc> list;
