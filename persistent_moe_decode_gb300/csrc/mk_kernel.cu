@@ -1338,22 +1338,18 @@ struct Cons {
         const uint8_t* base = S.stage[slot];
         for (int rr = (warp - (rbase + done) % 8 + 8) % 8; rr < rows; rr += 8) {
           const uint8_t* wrow = base + (size_t)rr * K * 2;
-          float a0 = 0.f, a1 = 0.f;
+          float2 a = make_float2(0.f, 0.f);     // even / odd columns
 #pragma unroll
           for (int c = 0; c < NCK; c++) {
             if (c < nch && lane_on) {
               const uint4 w = lds128(wrow + (lane + 32 * c) * 16);
-              a0 = fmaf(bf16lo(w.x), xa[c][0], a0);
-              a1 = fmaf(bf16hi(w.x), xa[c][1], a1);
-              a0 = fmaf(bf16lo(w.y), xa[c][2], a0);
-              a1 = fmaf(bf16hi(w.y), xa[c][3], a1);
-              a0 = fmaf(bf16lo(w.z), xa[c][4], a0);
-              a1 = fmaf(bf16hi(w.z), xa[c][5], a1);
-              a0 = fmaf(bf16lo(w.w), xa[c][6], a0);
-              a1 = fmaf(bf16hi(w.w), xa[c][7], a1);
+              a = fma_bf2(w.x, make_float2(xa[c][0], xa[c][1]), a);
+              a = fma_bf2(w.y, make_float2(xa[c][2], xa[c][3]), a);
+              a = fma_bf2(w.z, make_float2(xa[c][4], xa[c][5]), a);
+              a = fma_bf2(w.w, make_float2(xa[c][6], xa[c][7]), a);
             }
           }
-          float v = a0 + a1;
+          float v = a.x + a.y;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
           if (lane == 0) res[rbase + done + rr] = v;
@@ -1404,18 +1400,17 @@ struct Cons {
           float a0 = 0.f, a1 = 0.f;
           if (r < rows) {
             const uint8_t* wrow = base + (size_t)r * K * 2;
+            float2 a = make_float2(0.f, 0.f);   // even / odd columns
 #pragma unroll
             for (int c = 0; c < NC; c++) {
               const uint4 w = lds128(wrow + c * 512);
-              a0 = fmaf(bf16lo(w.x), xa[c][0], a0);
-              a1 = fmaf(bf16hi(w.x), xa[c][1], a1);
-              a0 = fmaf(bf16lo(w.y), xa[c][2], a0);
-              a1 = fmaf(bf16hi(w.y), xa[c][3], a1);
-              a0 = fmaf(bf16lo(w.z), xa[c][4], a0);
-              a1 = fmaf(bf16hi(w.z), xa[c][5], a1);
-              a0 = fmaf(bf16lo(w.w), xa[c][6], a0);
-              a1 = fmaf(bf16hi(w.w), xa[c][7], a1);
+              a = fma_bf2(w.x, make_float2(xa[c][0], xa[c][1]), a);
+              a = fma_bf2(w.y, make_float2(xa[c][2], xa[c][3]), a);
+              a = fma_bf2(w.z, make_float2(xa[c][4], xa[c][5]), a);
+              a = fma_bf2(w.w, make_float2(xa[c][6], xa[c][7]), a);
             }
+            a0 = a.x;
+            a1 = a.y;
           }
           v[r] = a0 + a1;
         }
@@ -1509,6 +1504,7 @@ struct Cons {
   // rows.  Thread t takes rows t, t + 256, ... of the stage (consecutive
   // 16-byte reads) and writes the group's partial of each:
   //   mpart[g][h] = sum_{c < 8} W_down[e][h][8 g' + c] * w_e * act[8 g' + c]
+  // (even and odd c summed apart, then added)
   __device__ __forceinline__ bool down_part() {
     const int H = p.H, ncb = t[R_NROWS] / 8, g0 = t[R_REL0];
     for (int c = 0; c < ncb; c++) {
@@ -1522,15 +1518,11 @@ struct Cons {
         const uint8_t* st = S.stage[slot];
         for (int r = tid; r < rows; r += 256) {
           const uint4 w = lds128(st + r * 16);
-          float v = bf16lo(w.x) * xa[0];
-          v = fmaf(bf16hi(w.x), xa[1], v);
-          v = fmaf(bf16lo(w.y), xa[2], v);
-          v = fmaf(bf16hi(w.y), xa[3], v);
-          v = fmaf(bf16lo(w.z), xa[4], v);
-          v = fmaf(bf16hi(w.z), xa[5], v);
-          v = fmaf(bf16lo(w.w), xa[6], v);
-          v = fmaf(bf16hi(w.w), xa[7], v);
-          __stcg(p.mpart + (size_t)(g0 + c) * H + r0 + r, v);
+          float2 a = __fmul2_rn(make_float2(bf16lo(w.x), bf16hi(w.x)), make_float2(xa[0], xa[1]));
+          a = fma_bf2(w.y, make_float2(xa[2], xa[3]), a);
+          a = fma_bf2(w.z, make_float2(xa[4], xa[5]), a);
+          a = fma_bf2(w.w, make_float2(xa[6], xa[7]), a);
+          __stcg(p.mpart + (size_t)(g0 + c) * H + r0 + r, a.x + a.y);
         }
         stage_release(slot);
       }

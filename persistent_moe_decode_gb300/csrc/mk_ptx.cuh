@@ -185,6 +185,12 @@ __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v <
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 __device__ __forceinline__ float bf16f(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
 
+// a + (low, high element of the BF16 pair w) * x, as two fp32 FMAs in one
+// packed instruction (fma.rn.f32x2): a.x takes the low element, a.y the high
+__device__ __forceinline__ float2 fma_bf2(uint32_t w, float2 x, float2 a) {
+  return __ffma2_rn(make_float2(bf16lo(w), bf16hi(w)), x, a);
+}
+
 // fp32 -> bf16 bits, round to nearest even
 __device__ __forceinline__ uint16_t f2bf(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
