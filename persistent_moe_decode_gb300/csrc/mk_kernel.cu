@@ -159,11 +159,7 @@ __device__ __forceinline__ bool wait_phase_slow(const Params& p, uint64_t* bar, 
   }
 }
 
-__device__ __forceinline__ bool wait_phase(const Params& p, uint64_t* bar, uint32_t parity, int task,
-                                           int op, unsigned mult = 1) {
-  (void)task;
-  (void)op;
-  (void)mult;
+__device__ __forceinline__ bool wait_phase(const Params& p, uint64_t* bar, uint32_t parity) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   return wait_phase_slow(p, bar, parity);
 }
@@ -327,7 +323,7 @@ struct Prod {
   // reserve the next task slot, zero it and write the header; nullptr on give-up
   __device__ __forceinline__ int32_t* begin() {
     const uint32_t slot = task_seq % kTaskSlots;
-    if (!wait_phase(p, &S.tempty[slot], ((task_seq / kTaskSlots) & 1u) ^ 1u, ti, op)) return nullptr;
+    if (!wait_phase(p, &S.tempty[slot], ((task_seq / kTaskSlots) & 1u) ^ 1u)) return nullptr;
     int32_t* w = S.task[slot];
     w[lane] = 0;
     __syncwarp();
@@ -351,7 +347,7 @@ struct Prod {
 
   __device__ __forceinline__ bool acquire_stage(uint32_t& slot) {
     slot = stage_seq % kStages;
-    const bool ok = wait_phase(p, &S.empty[slot], ((stage_seq / kStages) & 1u) ^ 1u, ti, op);
+    const bool ok = wait_phase(p, &S.empty[slot], ((stage_seq / kStages) & 1u) ^ 1u);
     if (p.trace && lane == 0 && task_seq > 0) {
       // the copy is issued next (after the mbarrier's release, which orders this word)
       int32_t* w = S.task[(task_seq - 1) % kTaskSlots];
@@ -493,7 +489,7 @@ struct Prod {
   // the routing of layer l is in shared memory (written by this block's consumers)
   __device__ __forceinline__ bool wait_route() {
     if ((int)route_seen > l) return true;
-    if (!wait_phase(p, &S.route_bar, (uint32_t)l & 1u, ti, op, 2)) return false;
+    if (!wait_phase(p, &S.route_bar, (uint32_t)l & 1u)) return false;
     route_seen = l + 1;
     return true;
   }
@@ -870,7 +866,7 @@ struct Cons {
   __device__ __forceinline__ bool csync() {
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.cbar);
-    const bool ok = wait_phase(p, &S.cbar, cphase & 1u, t[R_TASK], t[R_OP], 2);
+    const bool ok = wait_phase(p, &S.cbar, cphase & 1u);
     cphase++;
     if (!ok) S.abort_flag = 1;
     return ok && !aborted();
@@ -927,7 +923,7 @@ struct Cons {
   __device__ __forceinline__ bool stage_full(uint32_t& slot) {
     slot = stage_seq % kStages;
     const unsigned long long w0 = (tid == 0 && p.trace) ? gtime_ns() : 0ull;
-    if (!wait_phase(p, &S.full[slot], (stage_seq / kStages) & 1u, t[R_TASK], t[R_OP])) {
+    if (!wait_phase(p, &S.full[slot], (stage_seq / kStages) & 1u)) {
       S.abort_flag = 1;
       return false;
     }
@@ -2228,7 +2224,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
   int n_rec = 0;
   while (true) {
     const uint32_t slot = task_seq % kTaskSlots;
-    if (!wait_phase(p, &S.tfull[slot], (task_seq / kTaskSlots) & 1u, -1, -1)) {
+    if (!wait_phase(p, &S.tfull[slot], (task_seq / kTaskSlots) & 1u)) {
       if (tid == 0) report(p, DEV_SMEM_TIMEOUT, -1, -1, -1, 0, 0);
       break;
     }

@@ -86,3 +86,43 @@ def test_router_rows_are_few_per_sm_and_on_expert_sms(dims):
     assert not attn_sms & set(p1_sm[n_router > 0].tolist())
     # an SM with router rows takes no W_qkv rows (its router chunk finishes early)
     assert np.all((p1[:, F_B1] - p1[:, F_B0])[n_router > 0] == 0)
+
+
+@pytest.mark.parametrize("batch", [1, 16])
+def test_expert_branch_orders_down_and_out(batch):
+    """Several tokens: an expert SM's DOWN precedes its OUT (OUT's per-token
+    expert sums wait for every DOWN task).  One token: OUT comes first (its
+    O-proj rows need only the attention; nothing on the SM waits for the
+    partial sums)."""
+    cfg = mk.make_config(A3B, 16, 64, 1024)
+    cfg.n_attn_claimers = 40
+    tasks, off, _ = mk.mk_plan(cfg, 152, batch)
+    checked = 0
+    for s in range(152):
+        t = tasks[off[s]:off[s + 1]]
+        layer0 = t[t[:, F_LAYER] == 0]
+        ops = layer0[:, F_OP].tolist()
+        if OP_UP not in ops:
+            continue   # attention SM
+        i_down, i_out = ops.index(OP_DOWN), ops.index(OP_OUT)
+        assert (i_out < i_down) if batch == 1 else (i_down < i_out), (s, ops)
+        checked += 1
+    assert checked == 152 - 40
+
+
+def test_one_token_oproj_rows_favour_the_attention_branch():
+    """One token: an attention SM's O-proj share is about four times an expert
+    SM's (it is idle after its COMBINE); several tokens: even shares."""
+    cfg = mk.make_config(A3B, 16, 64, 1024)
+    cfg.n_attn_claimers = 40
+    for batch, ratio in ((1, 4.0), (16, 1.0)):
+        tasks, off, _ = mk.mk_plan(cfg, 152, batch)
+        sm_of = np.repeat(np.arange(152), np.diff(off))
+        first = tasks[:, F_LAYER] == 0
+        attn_sms = set(sm_of[first & (tasks[:, F_OP] == OP_ATTN)].tolist())
+        out = tasks[first & (tasks[:, F_OP] == OP_OUT)]
+        out_sm = sm_of[first & (tasks[:, F_OP] == OP_OUT)]
+        rows = out[:, F_A1] - out[:, F_A0]
+        a = np.mean([r for r, s in zip(rows, out_sm) if s in attn_sms])
+        e = np.mean([r for r, s in zip(rows, out_sm) if s not in attn_sms])
+        assert abs(a / e - ratio) < 0.25 * ratio, (batch, a, e)
