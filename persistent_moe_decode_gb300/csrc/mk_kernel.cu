@@ -141,14 +141,16 @@ __device__ __noinline__ void report(const Params& p, uint32_t code, int task, in
 
 // Bounded wait on a shared-memory mbarrier phase, called by a whole warp:
 // false = give up.  The phases come from this block's own warps and copies,
-// so the wait is bounded by a poll count (a few seconds of polling, far past
-// any real wait) and by the stop word (another block has reported an error),
+// so the wait is bounded by a poll count (several seconds of polling: past
+// any real wait and past the counter waits' time limit, so a block waiting
+// here on a thread that waits for a counter learns of that counter's
+// time-out first) and by the stop word (another block has reported an error),
 // read every 4096 polls by all lanes at once (one broadcast load, so the warp
 // decides together).  The block's exit path reports a time-out
 // (DEV_SMEM_TIMEOUT) once.  Every wait site inlines this loop, so it is kept
 // to a few instructions: code that runs once per layer is fetched anew each
 // time, and a call from these paths saves many registers.
-constexpr uint32_t kWaitPolls = 1u << 26;
+constexpr uint32_t kWaitPolls = 1u << 28;
 
 __device__ __forceinline__ bool wait_phase_slow(const Params& p, uint64_t* bar, uint32_t parity) {
   bool done = false;
