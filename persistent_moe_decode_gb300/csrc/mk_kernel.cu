@@ -287,7 +287,8 @@ __device__ __forceinline__ void route_one(const Params& p, RouteTab& rt, int l, 
 // writes them straight into the task ring (lane 0 writes the words; no
 // per-thread arrays, which would live in local memory) and streams their
 // weight / KV stages.
-template <bool ONE>   // the batch has one token (kernel instance)
+// ONE: the batch has one token; TR: the task timeline is recorded (kernel instance)
+template <bool ONE, bool TR>
 struct Prod {
   const Params& p;
   Smem& S;
@@ -341,7 +342,7 @@ struct Prod {
   __device__ __forceinline__ void commit() {
     __syncwarp();
     if (lane == 0) {
-      if (p.trace) S.task[task_seq % kTaskSlots][R_PCOMMIT] = (int32_t)(uint32_t)gtime_ns();
+      if (TR) S.task[task_seq % kTaskSlots][R_PCOMMIT] = (int32_t)(uint32_t)gtime_ns();
       mbar_arrive(&S.tfull[task_seq % kTaskSlots]);
     }
     task_seq++;
@@ -350,7 +351,7 @@ struct Prod {
   __device__ __forceinline__ bool acquire_stage(uint32_t& slot) {
     slot = stage_seq % kStages;
     const bool ok = wait_phase(p, &S.empty[slot], ((stage_seq / kStages) & 1u) ^ 1u);
-    if (p.trace && lane == 0 && task_seq > 0) {
+    if (TR && lane == 0 && task_seq > 0) {
       // the copy is issued next (after the mbarrier's release, which orders this word)
       int32_t* w = S.task[(task_seq - 1) % kTaskSlots];
       if (w[R_PISSUE] == 0) w[R_PISSUE] = (int32_t)((uint32_t)gtime_ns() | 1u);
@@ -837,7 +838,8 @@ struct Prod {
 // ===================================================================== consumers
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
-template <bool ONE>   // the batch has one token (kernel instance)
+// ONE: the batch has one token; TR: the task timeline is recorded (kernel instance)
+template <bool ONE, bool TR>
 struct Cons {
   const Params& p;
   Smem& S;
@@ -890,7 +892,7 @@ struct Cons {
       S.seen_tgt[warp] = target;
     }
     __syncwarp();
-    if (tid == 0) S.t_ready = gtime_ns();
+    if (TR && tid == 0) S.t_ready = gtime_ns();
     return ok;
   }
 
@@ -924,12 +926,12 @@ struct Cons {
 
   __device__ __forceinline__ bool stage_full(uint32_t& slot) {
     slot = stage_seq % kStages;
-    const unsigned long long w0 = (tid == 0 && p.trace) ? gtime_ns() : 0ull;
+    const unsigned long long w0 = (TR && tid == 0) ? gtime_ns() : 0ull;
     if (!wait_phase(p, &S.full[slot], (stage_seq / kStages) & 1u)) {
       S.abort_flag = 1;
       return false;
     }
-    if (tid == 0 && p.trace) S.t_swait += gtime_ns() - w0;
+    if (TR && tid == 0) S.t_swait += gtime_ns() - w0;
     return true;
   }
 
@@ -1213,7 +1215,7 @@ struct Cons {
         const int rows = min(rps, nrows - done);
         uint32_t slot;
         if (!stage_full(slot)) return false;
-        if (tid == 0 && blk == 0 && done == 0) S.t_mark[0] = gtime_ns();
+        if (TR && tid == 0 && blk == 0 && done == 0) S.t_mark[0] = gtime_ns();
         const uint8_t* base = S.stage[slot];
         for (int pass = 0; pass < npass; pass++) {
           for (int sg0 = 0; sg0 < nsg; sg0 += NSG) {
@@ -1283,7 +1285,7 @@ struct Cons {
       }
       tile_row0 += nrows;
     }
-    if (tid == 0) S.t_mark[1] = gtime_ns();
+    if (TR && tid == 0) S.t_mark[1] = gtime_ns();
     return true;
   }
 
@@ -1332,7 +1334,7 @@ struct Cons {
         const int rows = min(rps, nr - done);
         uint32_t slot;
         if (!stage_full(slot)) return false;
-        if (tid == 0 && rbase + done == 0) S.t_mark[0] = gtime_ns();
+        if (TR && tid == 0 && rbase + done == 0) S.t_mark[0] = gtime_ns();
         const uint8_t* base = S.stage[slot];
         for (int rr = (warp - (rbase + done) % 8 + 8) % 8; rr < rows; rr += 8) {
           const uint8_t* wrow = base + (size_t)rr * K * 2;
@@ -1356,7 +1358,7 @@ struct Cons {
       }
       rbase += nr;
     }
-    if (tid == 0) S.t_mark[1] = gtime_ns();
+    if (TR && tid == 0) S.t_mark[1] = gtime_ns();
     return true;
   }
 
@@ -1390,7 +1392,7 @@ struct Cons {
         const int rows = min(RB, nr - done);
         uint32_t slot;
         if (!stage_full(slot)) return false;
-        if (tid == 0 && rbase + done == 0) S.t_mark[0] = gtime_ns();
+        if (TR && tid == 0 && rbase + done == 0) S.t_mark[0] = gtime_ns();
         const uint8_t* base = S.stage[slot] + col0 * 2;
         float v[RB];
 #pragma unroll
@@ -1447,7 +1449,7 @@ struct Cons {
       }
       rbase += nr;
     }
-    if (tid == 0) S.t_mark[1] = gtime_ns();
+    if (TR && tid == 0) S.t_mark[1] = gtime_ns();
     if (!csync()) return false;
     if (tid < rbase) {
       float v = 0.f;
@@ -1684,7 +1686,7 @@ struct Cons {
         }
       }
     }
-    if (tid == 0) S.t_mark[0] = gtime_ns();
+    if (TR && tid == 0) S.t_mark[0] = gtime_ns();
     if (!csync()) return false;
     for (int e = tid; e < E; e += 256) {
       int c = 0;
@@ -1693,7 +1695,7 @@ struct Cons {
       rt.ecount[e] = c;
     }
     if (!csync()) return false;
-    if (tid == 0) S.t_mark[1] = gtime_ns();
+    if (TR && tid == 0) S.t_mark[1] = gtime_ns();
     if (warp == 0) {
       // warp-wide exclusive scans over E <= 256 experts, 8 per lane
       int cnt[8], act[8], sc = 0, sa = 0;
@@ -1731,7 +1733,7 @@ struct Cons {
       }
     }
     if (!csync()) return false;
-    if (tid == 0) S.t_mark[2] = gtime_ns();
+    if (TR && tid == 0) S.t_mark[2] = gtime_ns();
     for (int e = tid; e < E; e += 256) {
       const int a = rt.eslot[e];
       if (a < 0) continue;
@@ -1862,7 +1864,7 @@ struct Cons {
     for (int st = 0; st < nst; st++) {
       uint32_t slot;
       if (!stage_full(slot)) return false;
-      if (tid == 0 && st == 0) S.t_mark[0] = gtime_ns();
+      if (TR && tid == 0 && st == 0) S.t_mark[0] = gtime_ns();
       for (int qi = 0; qi < pps; qi++) {
         const int page = st * pps + qi;
         if (page >= npages) break;
@@ -1965,7 +1967,7 @@ struct Cons {
       stage_release(slot);
     }
 
-    if (tid == 0) S.t_mark[1] = gtime_ns();
+    if (TR && tid == 0) S.t_mark[1] = gtime_ns();
     // running sums: add up the lanes of each head
 #pragma unroll
     for (int sh = 4; sh < 32; sh <<= 1) {
@@ -2038,7 +2040,7 @@ struct Cons {
         }
       }
     }
-    if (tid == 0) S.t_mark[2] = gtime_ns();
+    if (TR && tid == 0) S.t_mark[2] = gtime_ns();
     return signal(bar_index(p, l, p.bl.items + b), 1);
   }
 
@@ -2120,9 +2122,9 @@ struct Cons {
 // would cost L2 round trips.  With 216 registers per consumer thread (see
 // the register split) the union of the paths needs no spill.  The per-warp
 // pipeline counters travel through shared memory between paths.
-template <bool ONE>
+template <bool ONE, bool TR>
 __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t* t) {
-  Cons<ONE> c(p, S, t);
+  Cons<ONE, TR> c(p, S, t);
   const int op = t[R_OP], kind = t[R_KIND], flags = t[R_FLAGS], l = t[R_LAYER];
   bool ok = true;
   if ((op == OP_P1 || op == OP_FINAL) && (flags & FL_FIRST)) ok = c.norm(l, op == OP_FINAL);
@@ -2143,7 +2145,7 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
     }
     if (ok && run) {
       c.epilogue(part);
-      if (c.tid == 0) S.t_mark[2] = gtime_ns();
+      if (TR && c.tid == 0) S.t_mark[2] = gtime_ns();
       if (c.lane == 0) S.cchunk[c.warp]++;
     }
   }
@@ -2154,9 +2156,9 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
 
 // one-token chunk: one copy of the wrapper (norm, waits, epilogue,
 // completion) around the GEMV shape for the row length
-template <bool ONE>
+template <bool ONE, bool TR>
 __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* t) {
-  Cons<ONE> c(p, S, t);
+  Cons<ONE, TR> c(p, S, t);
   const int op = t[R_OP], kind = t[R_KIND], flags = t[R_FLAGS], l = t[R_LAYER];
   bool ok = true;
   if ((op == OP_P1 || op == OP_FINAL) && (flags & FL_FIRST)) ok = c.norm(l, op == OP_FINAL);
@@ -2181,7 +2183,7 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
     }
     if (ok && run) {
       c.epilogue_row(res);
-      if (c.tid == 0) S.t_mark[2] = gtime_ns();
+      if (TR && c.tid == 0) S.t_mark[2] = gtime_ns();
     }
     // an UP piece goes on with its columns of the down projection
     if (ok && run && kind == K_UP) ok = c.csync() && c.down_part();
@@ -2192,25 +2194,25 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
   return ok;
 }
 
-template <bool ONE>
+template <bool ONE, bool TR>
 __device__ __forceinline__ bool op_route(const Params& p, Smem& S, const int32_t* t) {
-  Cons<ONE> c(p, S, t);
+  Cons<ONE, TR> c(p, S, t);
   const bool ok = c.route();
   c.save();
   return ok;
 }
 
-template <bool ONE, int D>
+template <bool ONE, bool TR, int D>
 __device__ __forceinline__ bool op_attn(const Params& p, Smem& S, const int32_t* t) {
-  Cons<ONE> c(p, S, t);
+  Cons<ONE, TR> c(p, S, t);
   const bool ok = c.template attn<D>();
   c.save();
   return ok;
 }
 
-template <bool ONE, int D>
+template <bool ONE, bool TR, int D>
 __device__ __forceinline__ bool op_combine(const Params& p, Smem& S, const int32_t* t) {
-  Cons<ONE> c(p, S, t);
+  Cons<ONE, TR> c(p, S, t);
   const bool ok = c.template combine<D>();
   c.save();
   return ok;
@@ -2219,7 +2221,9 @@ __device__ __forceinline__ bool op_combine(const Params& p, Smem& S, const int32
 // consumer main loop: take the next resolved task, run it, record its timeline.
 // ONE: the batch has one token (one-token GEMV paths only; a separate kernel
 // instance keeps each instance's union of inlined paths within registers).
-template <bool ONE>
+// TR: the timeline is recorded (an instance of its own, so the timed
+// instances carry no clock reads).
+template <bool ONE, bool TR>
 __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
   const int tid = threadIdx.x, lane = tid & 31;
   uint32_t task_seq = 0;
@@ -2234,8 +2238,8 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
     task_seq++;
     const int op = t[R_OP];
     if (op == OP_END) break;
-    const unsigned long long t_start = gtime_ns();
-    if (tid == 0) {
+    const unsigned long long t_start = TR ? gtime_ns() : 0ull;
+    if (TR && tid == 0) {
       S.t_ready = t_start;
       S.t_mark[0] = S.t_mark[1] = S.t_mark[2] = S.t_mark[3] = t_start;
       S.t_swait = 0;
@@ -2251,19 +2255,19 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
         // one token: whole rows per warp, by the row's length; more tokens:
         // up to eight per pass
         if constexpr (ONE) {
-          ok = op_row<true>(p, S, t);
+          ok = op_row<true, TR>(p, S, t);
         } else {
-          ok = op_chunk<false>(p, S, t);
+          ok = op_chunk<false, TR>(p, S, t);
         }
         (void)nt;
         break;
       }
-      case OP_ROUTE: ok = op_route<ONE>(p, S, t); break;
-      case OP_ATTN: ok = (p.d == 128) ? op_attn<ONE, 128>(p, S, t) : op_attn<ONE, 64>(p, S, t); break;
-      case OP_COMBINE: ok = (p.d == 128) ? op_combine<ONE, 128>(p, S, t) : op_combine<ONE, 64>(p, S, t); break;
+      case OP_ROUTE: ok = op_route<ONE, TR>(p, S, t); break;
+      case OP_ATTN: ok = (p.d == 128) ? op_attn<ONE, TR, 128>(p, S, t) : op_attn<ONE, TR, 64>(p, S, t); break;
+      case OP_COMBINE: ok = (p.d == 128) ? op_combine<ONE, TR, 128>(p, S, t) : op_combine<ONE, TR, 64>(p, S, t); break;
       default: ok = false; break;
     }
-    if (p.trace && tid == 0 && n_rec < p.trace_cap) {
+    if (TR && tid == 0 && n_rec < p.trace_cap) {
       const unsigned long long t_end = gtime_ns();
       int32_t* rec = p.trace + ((size_t)blockIdx.x * p.trace_cap + n_rec) * kTraceWords;
       rec[0] = op;
@@ -2293,7 +2297,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
   }
 }
 
-template <bool ONE>
+template <bool ONE, bool TR>
 __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_constant__ Params p) {
   static_assert(kThreads == 384 && kLaunchRegs == 168, "register split assumes 384 threads x 168");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -2325,25 +2329,34 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
     // registers back
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs) : "memory");
     if (wid == kConsumerWarps) {
-      Prod<ONE> pr(p, S);
+      Prod<ONE, TR> pr(p, S);
       pr.run();
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs) : "memory");
-    consumer_loop<ONE>(p, S);
+    consumer_loop<ONE, TR>(p, S);
   }
 }
 
-// registers per thread both kernel instances were built with (the split
-// above needs kLaunchRegs); -1 if they differ or cannot be read
+// the four kernel instances: (one token, several) x (timeline off, on)
+static const void* const kStepKernels[4] = {
+    (const void*)mk_step_kernel<false, false>, (const void*)mk_step_kernel<true, false>,
+    (const void*)mk_step_kernel<false, true>, (const void*)mk_step_kernel<true, true>};
+
+// registers per thread every kernel instance was built with (the split above
+// needs kLaunchRegs); -1 if they differ or cannot be read
 int step_kernel_regs() {
-  cudaFuncAttributes a, b;
-  if (cudaFuncGetAttributes(&a, mk_step_kernel<true>) != cudaSuccess ||
-      cudaFuncGetAttributes(&b, mk_step_kernel<false>) != cudaSuccess) {
-    cudaGetLastError();
-    return -1;
+  int regs = -1;
+  for (int i = 0; i < 4; i++) {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, kStepKernels[i]) != cudaSuccess) {
+      cudaGetLastError();
+      return -1;
+    }
+    if (i > 0 && a.numRegs != regs) return -1;
+    regs = a.numRegs;
   }
-  return a.numRegs == b.numRegs ? a.numRegs : -1;
+  return regs;
 }
 
 size_t step_smem_bytes() { return kSmemBytes; }
@@ -2382,12 +2395,11 @@ cudaError_t relayout_down(const uint16_t* src, uint16_t* dst, int E, int H, int 
 cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(mk_step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(mk_step_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
+    for (int i = 0; i < 4; i++) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(kStepKernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+      if (e != cudaSuccess) return e;
+    }
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
@@ -2400,8 +2412,9 @@ cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return p.B == 1 ? cudaLaunchKernelEx(&cfg, mk_step_kernel<true>, p)
-                  : cudaLaunchKernelEx(&cfg, mk_step_kernel<false>, p);
+  const void* k = kStepKernels[(p.B == 1 ? 1 : 0) + (p.trace != nullptr ? 2 : 0)];
+  void* args[1] = {(void*)&p};
+  return cudaLaunchKernelExC(&cfg, k, args);
 }
 
 }  // namespace mk
