@@ -68,7 +68,7 @@ struct __align__(128) Smem {
                                             // layer, the attention output, the experts' hidden)
   float red[2 * kPartFloats];               // GEMV partial sums (two buffers) / attention
                                             // query fragments and merge / combine sums
-  float spart[64][kConsumerWarps];          // one token, split GEMV: the warps' sums of each row
+  float spart[128][kConsumerWarps];         // one token, split GEMV: the warps' sums of each row
   float actp[64];                           // one token: weighted hidden values of an UP piece
   float nred[kConsumerWarps][kMaxBatch];    // norm / combine reductions
   float rinv[kMaxBatch];
@@ -1362,8 +1362,9 @@ struct Cons {
     return true;
   }
 
-  // one token, few rows per warp (P1 and O-proj chunks of at most 64 rows, K
-  // 2048 or 4096): the contraction is split over the warps instead of the
+  // one token, few rows per warp (P1 and O-proj chunks of at most 64 rows,
+  // UP pieces of at most 64 + 64; K 2048 or 4096): the contraction is split
+  // over the warps instead of the
   // rows.  Warp w takes columns [w K / 8, (w + 1) K / 8), lane l the 8-column
   // chunks l, l + 32 of that range, so each warp holds only its eighth of x
   // in registers.  A stage's RB = 8 / NC rows are reduced over the lanes
@@ -2172,14 +2173,17 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
     if (ok && run && kind == K_OPROJ) ok = c.wait_counter(bar_index(p, l, p.bl.comb), p.n_comb_sms) && c.stage_x();
     if (ok && run) {
       const int K = t[R_K];
-      const bool split = (kind == K_P1 || kind == K_OPROJ) && rows <= 64 && split_rows(K) == 64;
+      // P1, O-proj and UP chunks (an UP piece's gate rows and up rows, at most
+      // 64 each) share the split GEMV: one code path for the layer's GEMVs
+      const bool split = (kind == K_P1 || kind == K_OPROJ || kind == K_UP) && rows <= 64 && split_rows(K) == 64;
       if (split) ok = K == 2048 ? c.template gemv_split<1>(res) : c.template gemv_split<2>(res);
       else ok = K <= 256 ? c.template gemv_row<1>(res) : K <= 768 ? c.template gemv_row<3>(res)
               : K <= 2048 ? c.template gemv_row<8>(res) : c.template gemv_row<16>(res);
       // the split path's sums are written by the threads that run the
-      // epilogue; its partial buffer is reused by the next split chunk, which
-      // the completion barrier below also orders when the task ends here
-      if (ok && !(split && (flags & FL_LAST))) ok = c.csync();
+      // epilogue (except UP's, whose epilogue pairs row i with row nr + i);
+      // its partial buffer is reused by the next split chunk, which the
+      // completion barrier below also orders when the task ends here
+      if (ok && !(split && (flags & FL_LAST) && kind != K_UP)) ok = c.csync();
     }
     if (ok && run) {
       c.epilogue_row(res);
