@@ -501,13 +501,15 @@ struct Prod {
   // router rows and its QKV rows as two groups
   // one token, P1: the router rows [a0, a1) first, in chunks of their own
   // (the last one releases the router counter), then the W_qkv rows [b0, b1);
-  // FINAL: LM-head rows [a0, a1).  One loop emits every chunk (one copy of
-  // the hand-over and stream code): phase 0 walks [a0, a1), phase 1 [b0, b1).
-  __device__ __forceinline__ bool do_p1_final_1(int a0, int a1, int b0, int b1) {
-    const int H = p.H;
-    const bool fin = op == OP_FINAL;
-    if (fin) b1 = b0;
+  // FINAL: LM-head rows [a0, a1); OUT: O-proj rows [a0, a1).  One loop emits
+  // every chunk (one copy of the hand-over and stream code): phase 0 walks
+  // [a0, a1), phase 1 [b0, b1).
+  __device__ __forceinline__ bool do_rows1(int a0, int a1, int b0, int b1) {
+    const bool fin = op == OP_FINAL, out = op == OP_OUT;
+    const int H = out ? p.hq * p.d : p.H;         // row length
+    if (fin || out) b1 = b0;
     const int cr = fin ? kRowChunk : split_rows(H);
+    const uint16_t* m0 = fin ? p.lm_head : wptr(out ? 2 : 0);
     int ph = a1 > a0 ? 0 : 1, c0 = ph == 0 ? a0 : b0;
     bool first = true;
     do {
@@ -518,8 +520,8 @@ struct Prod {
       int32_t* w = begin();
       if (!w) return false;
       if (lane == 0) {
-        w[R_KIND] = fin ? K_LM : K_P1;
-        w[R_FLAGS] = (first ? FL_FIRST : 0) | (last ? FL_LAST : 0) | (!fin && ph == 0 && end_ph ? FL_RTR : 0);
+        w[R_KIND] = fin ? K_LM : out ? K_OPROJ : K_P1;
+        w[R_FLAGS] = (first ? FL_FIRST : 0) | (last ? FL_LAST : 0) | (op == OP_P1 && ph == 0 && end_ph ? FL_RTR : 0);
         w[R_ROW0] = ph == 0 ? c0 : 0;
         w[R_NROWS] = ph == 0 ? max(c1 - c0, 0) : 0;
         w[R_ROW1] = ph == 1 ? c0 : 0;
@@ -529,7 +531,7 @@ struct Prod {
         w[R_NT] = 1;
       }
       commit();
-      if (c1 > c0 && !stream_rows(fin ? p.lm_head : wptr(ph), c0, c1 - c0, H)) return false;
+      if (c1 > c0 && !stream_rows(ph == 0 ? m0 : wptr(1), c0, c1 - c0, H)) return false;
       first = false;
       c0 = c1;
       if (end_ph && ph == 0) {
@@ -542,7 +544,7 @@ struct Prod {
 
   __device__ __forceinline__ bool do_p1_final(int a0, int a1, int b0, int b1) {
     const int H = p.H, B = p.B;
-    if (ONE) return do_p1_final_1(a0, a1, b0, b1);
+    if (ONE) return do_rows1(a0, a1, b0, b1);
     const int cr = gemv_chunk_rows(H, B);
     if (op == OP_FINAL) {
       if (a1 <= a0) return chunk(K_LM, FL_FIRST | FL_LAST, 0, 0, 1, H, B, 0, 0, 0, nullptr, nullptr);
@@ -802,7 +804,7 @@ struct Prod {
         }
         case OP_ATTN: ok = do_attn(); break;
         case OP_UP: ok = do_up(a0, a1); break;
-        case OP_OUT: ok = do_out(a0, a1); break;
+        case OP_OUT: ok = ONE ? do_rows1(a0, a1, 0, 0) : do_out(a0, a1); break;
         case OP_DOWN: ok = do_down(a0, a1); break;
         default:
           if (lane == 0) report(p, DEV_BAD_OP, ti, op, -1, 0, 0);
