@@ -6,9 +6,11 @@
  * step and walks a host-built per-SM task list ("Inside the megakernel serving
  * engine for North Mini Code", §What is a Megakernel, Fig 2).  Dependencies
  * between tiles are global-memory counters that producers increment and
- * consumers spin on (§Barriers, Listing 2); attention and expert tiles whose
- * count depends on the live sequence lengths and on routing sit in shared
- * queues drained by claimer tasks (§The task scheduler, the dynamic part).
+ * consumers spin on (§Barriers, Listing 2).  Work whose size depends on the
+ * live sequence lengths or on the routing is cut into equal shares: the
+ * split-KV items on the host, the routed experts' rows on the device once the
+ * routing is known (the pages drain such tiles from shared queues; §The task
+ * scheduler, the dynamic part).
  *
  * The host side mirrors the pages' decode service loop (§The serving engine
  * around the kernel: update_kv_page_tables, clear_scratch_and_barriers,

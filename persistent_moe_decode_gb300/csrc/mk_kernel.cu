@@ -13,33 +13,40 @@
 //    partial results; the MoE tiles indexed by the routing result.
 //
 // GB300 design (not the pages' H100 one):
-//  - block = 8 consumer warps + 1 producer warp.  The producer resolves the
-//    task list (attention items, the routed experts' rows) and streams every
-//    weight / KV byte HBM -> shared memory with 1-D bulk async copies into a
-//    6-stage ring of 32 KB stages guarded by mbarriers.  The ring runs ahead
+//  - block = 8 consumer warps + 1 producer warp (setmaxnreg 216 / 72).  The
+//    producer resolves the task list (attention items, the routed experts'
+//    rows) and streams every weight / KV byte HBM -> shared memory into a
+//    5-stage ring of 32 KB stages guarded by mbarriers: 1-D bulk copies of
+//    whole weight rows, 2-D tensor copies (128-byte swizzle) of KV pages, all
+//    with an evict-first L2 policy (each of those bytes is read once a step;
+//    the kernel's code and activations stay in L2).  The ring runs ahead
 //    across task boundaries, so a task that waits for its activations
 //    already has its weights in flight.
-//  - every SM takes an equal share of every phase of a layer (rows of
-//    [W_router; W_qkv], pages of the KV, (gate, up) row pairs of the routed
-//    experts, query heads to merge, hidden rows of O-proj + down), so all SMs
-//    stream for the whole layer.  The attention's KV pages depend on nothing
-//    computed in the step and stream while the routing is still open.
-//  - GEMV: a stage is whole contiguous weight rows moved by ONE bulk copy; the
-//    warps split each row into 256-column segments, multiply on the CUDA cores
-//    in fp32 against fp32 activations held in registers and reduce with warp
-//    shuffles; segments are summed in a fixed order, fused with the epilogue.
+//  - roles: per step the SMs split into an attention branch (P1, ATTN,
+//    COMBINE, OUT) and an expert branch (P1, ROUTE, UP, DOWN, OUT) of the
+//    parallel layer; every SM of a branch takes an equal share of each of
+//    its waves (one token: an attention SM takes 4 times an expert SM's
+//    O-proj rows).
+//  - GEMV, one token: P1, O-proj and UP chunks split the contraction over the
+//    warps (x in registers, a transposed butterfly per stage, the warps' sums
+//    in a fixed order); an UP piece also multiplies its columns of the down
+//    projection, one fp32 partial per 8-column group, summed by the DOWN
+//    wave.  Several tokens: 256-column segments per warp, up to eight tokens
+//    per pass, fixed-order segment sums.  CUDA cores, fp32 (packed FMAs).
 //  - the residual add + RMSNorm is computed by every SM for itself at the
 //    start of each layer (its own copy of the residual stream), so no SM waits
-//    for a norm task; the routing (top-k, per-expert grouping) likewise.
+//    for a norm task; the routing likewise (one token: by each expert SM's
+//    producer warp).
 //  - attention: one item = one sequence, all KV heads, a run of 16-token
-//    pages.  QK^T on the tensor cores with the RoPE'd fp32 query split into
-//    BF16 high + low halves (kept in shared memory), online softmax in fp32,
-//    PV on the CUDA cores.  The item holding the new token applies RoPE to
-//    its key, patches K/V into the staged page and writes them to the cache.
-//  - every wait has a %globaltimer limit (the consumer warps' own barrier is
-//    an mbarrier with a bounded wait, not bar.sync); on expiry the block
-//    records the error, sets a global stop word that every other wait polls,
-//    drains its own in-flight copies and returns.
+//    pages.  S^T = K Q^T and O^T += V^T P^T on the tensor cores (mma.sync,
+//    BF16 high + low halves of the fp32 query and probabilities), online
+//    softmax in fp32.  The item holding the new token applies RoPE to its
+//    key, patches K/V into the staged page and writes them to the cache.
+//  - bounded waits: counter waits have a %globaltimer limit; shared-memory
+//    waits (the consumer warps' own barrier is an mbarrier, not bar.sync) a
+//    poll count and the stop word.  On expiry the block records the error,
+//    sets a global stop word that every other wait checks, drains its own
+//    in-flight copies and returns.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
