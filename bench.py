@@ -133,9 +133,12 @@ def step_bytes(dims, routing_idx, keys_per_seq):
 
 class CpuSample:
     """The CPU oracle on a bounded sample of one step: layers [0, n) at the full
-    shapes and 1/lm_frac of the LM-head rows, extrapolated to a whole token."""
+    shapes and 1/lm_frac of the LM-head rows, extrapolated to a whole step.
 
-    def __init__(self, model, k_pool, v_pool, batch, n_layers_sample: int, lm_frac: int = 8):
+    ``state`` = (tokens, seq_lens, page_tables) of a step that was scheduled
+    (every sequence owns the page its new token lands in)."""
+
+    def __init__(self, model, k_pool, v_pool, state, wl, n_layers_sample: int, lm_frac: int = 8):
         import dataclasses
 
         import oracle
@@ -151,39 +154,56 @@ class CpuSample:
         vp = bf16_bits(v_pool[:n].cpu().contiguous()).copy()
         self.oracle = oracle
         self.orc = oracle.Oracle({**dataclasses.asdict(d), "n_layers": n}, w, kp, vp)
-        self.d, self.n, self.lm_frac, self.batch = d, n, lm_frac, batch
-        B = batch.wl.batch
-        self.h0 = oracle.bf16_to_f64(w["embed"][batch.tokens[:B]])
+        self.d, self.n, self.lm_frac, self.wl = d, n, lm_frac, wl
+        tokens, lens, pt = state
+        self.B = len(tokens)
+        self.lens = np.ascontiguousarray(lens, dtype=np.int32).copy()
+        self.pt = np.ascontiguousarray(pt, dtype=np.int32).copy()
+        self.h0 = oracle.bf16_to_f64(w["embed"][np.asarray(tokens)])
         self.lm = w["lm_head"][:d.vocab // lm_frac]
 
     def time_token(self) -> float:
         """Seconds the oracle needs per decode step of the whole batch."""
-        B = self.batch.wl.batch
         t0 = time.perf_counter()
-        self.orc.run_layers(0, self.n, self.h0, self.batch.seq_lens[:B], self.batch.page_tables[:B])
+        self.orc.run_layers(0, self.n, self.h0, self.lens, self.pt)
         t1 = time.perf_counter()
         self.oracle.matvec(self.lm, self.h0)
         t2 = time.perf_counter()
         return (t1 - t0) * (self.d.n_layers / self.n) + (t2 - t1) * self.lm_frac
 
     def describe(self, reps: int) -> str:
-        return (f"layers 0..{self.n - 1} of one decode step at the full shapes (context "
-                f"{int(self.batch.seq_lens[0])}, batch {self.batch.wl.batch}) plus 1/{self.lm_frac} of "
-                f"the LM-head rows, {reps} repetitions, extrapolated to {self.d.n_layers} layers and "
-                f"the whole LM head")
+        ctx = f"context {int(self.lens[0])}" if self.B == 1 else \
+            f"contexts {int(self.lens.min())}..{int(self.lens.max())}"
+        return (f"layers 0..{self.n - 1} of one decode step of {self.wl.name} at the full shapes "
+                f"({ctx}, batch {self.B}) plus 1/{self.lm_frac} of the LM-head rows, {reps} "
+                f"repetitions, extrapolated to {self.d.n_layers} layers and the whole LM head")
 
     def measure(self, min_seconds: float) -> dict:
-        B = self.batch.wl.batch
         ts, t_start = [], time.perf_counter()
         while not ts or time.perf_counter() - t_start < min_seconds:
             ts.append(self.time_token())
-        return {"value": B / float(np.median(ts)), "unit": "tok/s", "cores": self.oracle.get_threads(),
+        return {"value": self.B / float(np.median(ts)), "unit": "tok/s", "cores": self.oracle.get_threads(),
                 "kind": "oracle", "sample": self.describe(len(ts)),
                 "seconds": round(time.perf_counter() - t_start, 2)}
 
 
+def snapshot(batch):
+    """(tokens, seq_lens, page_tables) of the batch's next step, pages present."""
+    batch.prepare_step()
+    B = batch.wl.batch
+    return batch.tokens[:B].copy(), batch.seq_lens[:B].copy(), batch.page_tables[:B].copy()
+
+
+def context_of(lens) -> int | str:
+    return int(lens[0]) if len(lens) == 1 else "ragged"
+
+
 def run_reference(args, wl):
-    """Reference arm: the CPU oracle as it stands, one bounded sample per step."""
+    """Reference arm: the CPU oracle as it stands, one bounded sample per step.
+
+    The batch goes through the same warm-up steps as the GPU arm (bookkeeping
+    only: tokens, lengths, pages, churn), so the timed steps start at the same
+    context."""
     from persistent_moe_decode_gb300.synth import DecodeBatch, make_kv_pools, make_model
     d = wl.dims
     n = min(args.ref_layers, d.n_layers)
@@ -192,18 +212,28 @@ def run_reference(args, wl):
     batch = DecodeBatch(wl)
     kp, vp = make_kv_pools(small, batch.num_pages, wl.kv_std, wl.seed, "cpu")
     model.dims = d
-    cs = CpuSample(model, kp, vp, batch, n)
+    rng = np.random.default_rng(1234)
+    B = wl.batch
+
+    def advance():
+        batch.advance(rng.integers(0, d.vocab, size=B).astype(np.int32))
+        if wl.churn:
+            batch.churn()
+
     for _ in range(args.warmup):
-        cs.time_token()
+        advance()
+    state = snapshot(batch)
+    cs = CpuSample(model, kp, vp, state, wl, n)
+    cs.time_token()                       # untimed: first touch of the host arrays
     t_all = time.perf_counter()
     secs = [cs.time_token() for _ in range(args.steps)]
     wall = time.perf_counter() - t_all
-    v = wl.batch * args.steps / float(np.sum(secs))
+    v = B * args.steps / float(np.sum(secs))
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * float(np.mean(secs)),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": wl.name, "batch": wl.batch, "context": int(batch.seq_lens[0]),
+            "config": {"workload": wl.name, "batch": B, "context": context_of(state[1]),
                        "layers": d.n_layers, "l2": "inputs larger than L2"},
             "cpu_baseline": {"value": v, "unit": "tok/s", "kind": "oracle",
                              "cores": cs.oracle.get_threads(), "sample": cs.describe(args.steps)},
@@ -212,16 +242,105 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def device_timed(run, wl, args, stream, tok_seq, dist=None, clocks=None):
+    """Warm-up, then K steps timed with CUDA events on the launching stream.
+
+    Returns (elapsed ms over the K steps, mean kernel ms, the state of the first
+    timed step, the keys attended per sequence in the last timed step, the
+    clocks sampled during the timed steps).  The
+    churn bookkeeping between steps stays in the loop; the joining sequences'
+    pages keep the random K/V they hold (no random-number kernels in the loop)."""
+    import torch
+    for i in range(args.warmup):
+        run.schedule(stream)
+        run.launch(stream)
+        run.advance(tok_seq[i], refill=False)
+    torch.cuda.synchronize()
+    run.check_status()
+    state = snapshot(run.batch)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if clocks:
+        clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    keys = None
+    for i in range(args.steps):
+        run.schedule(stream)
+        ev[i][0].record(stream)
+        run.launch(stream)
+        ev[i][1].record(stream)
+        keys = (run.batch.seq_lens + 1).copy()
+        run.advance(tok_seq[args.warmup + i], refill=False)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    run.check_status()
+    elapsed_ms = t0.elapsed_time(t1)
+    kern_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    return elapsed_ms, kern_ms, state, keys, clk
+
+
+def roofline_of(run, wl, kern_ms, keys, traffic_key):
+    idx, _ = run.dec.routing()
+    bytes_step = step_bytes(wl.dims, idx, keys)
+    peak, peak_kind = load_peaks()
+    achieved = bytes_step / (kern_ms / 1000.0) / 1e9
+    return bytes_step, {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                        "frac": achieved / peak, "peak_kind": peak_kind,
+                        "traffic": load_traffic(traffic_key),
+                        "algorithmic_bytes_per_step": bytes_step, "kernel_ms": kern_ms,
+                        "kernel": "mk_step_kernel (persistent, one block per SM)"}
+
+
+def e2e_timed(run, wl, args, stream, world):
+    """The same metric end to end through the C ABI: per step the host arrays
+    go up (schedule), the step runs, the logits come back to pinned host
+    memory and the host picks the next tokens (greedy)."""
+    import torch
+    from persistent_moe_decode_gb300 import mk
+    B = wl.batch
+    host_logits = torch.empty(B, wl.dims.vocab, dtype=torch.float32, pin_memory=True)
+    for i in range(3):
+        run.step(stream)
+        host_logits.copy_(run.logits, non_blocking=True)
+        torch.cuda.synchronize()
+        run.advance(host_logits.numpy().argmax(1).astype(np.int32), refill=False)
+    torch.cuda.synchronize()
+    h2d = d2h = 0
+    ts = time.perf_counter()
+    for i in range(args.steps):
+        run.step(stream)
+        h2d += mk.mk_step_upload_bytes(run.dec.h, B)
+        host_logits.copy_(run.logits, non_blocking=True)
+        torch.cuda.synchronize()
+        d2h += host_logits.numel() * 4
+        run.advance(host_logits.numpy().argmax(1).astype(np.int32), refill=False)
+    te = time.perf_counter()
+    run.check_status()
+    return {"value": B * args.steps * world / (te - ts), "unit": "tok/s",
+            "h2d_bytes_per_step": int(h2d // args.steps), "d2h_bytes_per_step": int(d2h // args.steps)}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="a3b_8k")
+    ap.add_argument("--workload", default="a3b_8k",
+                    help="a3b_8k (default), a3b_b16, a3b_256k, mid_8k, tiny")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=0, help="profiling: run only the first L layers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-b16", action="store_true",
+                    help="a3b_8k: skip the batch-16 line measured on the same model")
     ap.add_argument("--ref-layers", type=int, default=2)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
@@ -250,7 +369,6 @@ def main():
 
     from persistent_moe_decode_gb300 import build
     build.build()
-    from persistent_moe_decode_gb300 import mk
     from persistent_moe_decode_gb300.runner import StepRunner
 
     dims = wl.dims
@@ -258,112 +376,65 @@ def main():
     stream = torch.cuda.current_stream()
     B = wl.batch
     rng = np.random.default_rng(1234 + rank)
-    total = args.warmup + args.steps
-    tok_seq = rng.integers(0, dims.vocab, size=(total, B)).astype(np.int32)
+    tok_seq = rng.integers(0, dims.vocab, size=(args.warmup + args.steps, B)).astype(np.int32)
 
-    # ---- device-timed loop: inputs resident, tokens drawn ahead of time
-    def one_step(i):
-        run.schedule(stream)
-        run.launch(stream)
-
-    for i in range(args.warmup):
-        one_step(i)
-        run.advance(tok_seq[i])
-    torch.cuda.synchronize()
-    run.check_status()
-    keys0 = (run.batch.seq_lens + 1).copy()
-
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    clocks = ClockSampler(local)
-    clocks.start()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    keys = []
-    for i in range(args.steps):
-        run.schedule(stream)
-        ev[i][0].record(stream)
-        run.launch(stream)
-        ev[i][1].record(stream)
-        keys.append((run.batch.seq_lens + 1).copy())
-        run.advance(tok_seq[args.warmup + i])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    clk = clocks.stop()
-    run.check_status()
-    elapsed_ms = t0.elapsed_time(t1)
-    kern_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    elapsed_ms, kern_ms, state, keys, clk = device_timed(run, wl, args, stream, tok_seq, dist,
+                                                         ClockSampler(local))
     if dist:
         tt = torch.tensor([elapsed_ms], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         elapsed_ms = float(tt.item())
     tok_s = B * args.steps * world / (elapsed_ms / 1000.0)
+    traffic_key = wl.name if not args.layers else f"{wl.name}:L{args.layers}"
+    bytes_step, roof = roofline_of(run, wl, kern_ms, keys, traffic_key)
 
-    # bytes: routing of the last step (B = 1: always top_k distinct experts per layer)
-    idx, _ = run.dec.routing()
-    bytes_step = step_bytes(dims, idx, keys[-1])
-    peak, peak_kind = load_peaks()
-    achieved = bytes_step / (kern_ms / 1000.0) / 1e9
-
-    # ---- end-to-end through the C ABI with host buffers
-    e2e = None
-    if not args.no_e2e:
-        host_logits = torch.empty(B, dims.vocab, dtype=torch.float32, pin_memory=True)
-        for i in range(3):
-            run.step(stream)
-            host_logits.copy_(run.logits, non_blocking=True)
-            torch.cuda.synchronize()
-            run.advance(host_logits.numpy().argmax(1).astype(np.int32))
-        torch.cuda.synchronize()
-        h2d = d2h = 0
-        ts = time.perf_counter()
-        for i in range(args.steps):
-            run.step(stream)
-            h2d += mk.mk_step_upload_bytes(run.dec.h, B)
-            host_logits.copy_(run.logits, non_blocking=True)
-            torch.cuda.synchronize()
-            d2h += host_logits.numel() * 4
-            run.advance(host_logits.numpy().argmax(1).astype(np.int32))
-        te = time.perf_counter()
-        run.check_status()
-        e2e = {"value": B * args.steps * world / (te - ts), "unit": "tok/s",
-               "h2d_bytes_per_step": int(h2d // args.steps), "d2h_bytes_per_step": int(d2h // args.steps)}
+    e2e = None if args.no_e2e else e2e_timed(run, wl, args, stream, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
-            cpu = CpuSample(run.model, run.k_pool, run.v_pool, run.batch,
-                            min(4, dims.n_layers)).measure(args.cpu_seconds)
+            cpu = CpuSample(run.model, run.k_pool, run.v_pool, state, wl,
+                            min(4 if B == 1 else 2, dims.n_layers)).measure(args.cpu_seconds)
         except Exception as e:  # report, do not hide
             cpu = {"value": None, "error": repr(e)}
 
-    traffic = load_traffic(wl.name if not args.layers else f"{wl.name}:L{args.layers}")
+    # the metric names batch 1 and batch 16: with the 30B/3.3B model at batch 1,
+    # the batch-16 continuous-batching workload runs on the same weights
+    b16 = None
+    if wl.name == "a3b_8k" and not args.layers and not args.no_b16:
+        wl16 = WORKLOADS["a3b_b16"]
+        run16 = StepRunner(wl16.with_(seed=wl16.seed + rank), device=f"cuda:{local}", model=run.model)
+        tok16 = rng.integers(0, dims.vocab, size=(args.warmup + args.steps, 16)).astype(np.int32)
+        a16 = argparse.Namespace(**{**vars(args), "steps": min(args.steps, 20)})
+        el16, kern16, st16, keys16, clk16 = device_timed(run16, wl16, a16, stream, tok16, dist,
+                                                         ClockSampler(local))
+        bytes16, roof16 = roofline_of(run16, wl16, kern16, keys16, wl16.name)
+        b16 = {"workload": wl16.name, "batch": 16, "steps": a16.steps,
+               "value": 16 * a16.steps * world / (el16 / 1000.0), "unit": "tok/s",
+               "ms_per_step": el16 / a16.steps,
+               "contexts": f"{int(st16[1].min())}..{int(st16[1].max())} at the first timed step",
+               "roofline": roof16, "clocks": clk16}
+        run16.close()
+
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name + (f" (first {args.layers} layers)" if args.layers else ""),
-                   "batch": B, "context": int(keys0[0] - 1) if B == 1 else "ragged",
+                   "batch": B, "context": context_of(state[1]),
+                   "context_note": "cached tokens at the first timed step",
                    "layers": dims.n_layers,
                    "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB read per step)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "sol_frac": {"of_measured_hbm": achieved / peak, "of_nominal_8tbs": achieved / 8000.0},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": traffic,
-                     "algorithmic_bytes_per_step": bytes_step, "kernel_ms": kern_ms,
-                     "kernel": "mk_step_kernel (persistent, one block per SM)"},
+        "sol_frac": {"of_measured_hbm": roof["frac"], "of_nominal_8tbs": roof["achieved"] / 8000.0},
+        "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clk,
     }
+    if b16 is not None:
+        line["batch16"] = b16
     if rank == 0:
         print(json.dumps(line), flush=True)
     run.close()

@@ -50,13 +50,19 @@ class StepRunner:
     def greedy(self) -> np.ndarray:
         return self.logits.argmax(dim=1).to(torch.int32).cpu().numpy()
 
-    def advance(self, next_tokens) -> tuple[int, list[int]] | None:
-        """Append the step's token; with churn, retire one sequence and admit one."""
+    def advance(self, next_tokens, refill: bool = True) -> tuple[int, list[int]] | None:
+        """Append the step's token; with churn, retire one sequence and admit one.
+
+        ``refill`` draws fresh K/V for the joining sequence's pages (input
+        synthesis).  Without it the pages keep the random K/V they already hold
+        (a retired sequence's), which is as good a synthetic prefix and keeps
+        the random-number kernels out of a timed loop."""
         self.batch.advance(next_tokens)
         self.step_index += 1
         if self.wl.churn:
             slot, pages = self.batch.churn()
-            refill_pages(self.k_pool, self.v_pool, pages, self.wl.kv_std, self.seed, self.step_index)
+            if refill:
+                refill_pages(self.k_pool, self.v_pool, pages, self.wl.kv_std, self.seed, self.step_index)
             return slot, pages
         return None
 

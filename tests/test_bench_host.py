@@ -1,0 +1,44 @@
+"""Host-side pieces of bench.py, without a GPU.
+
+The CPU baseline inside the measured line must time the oracle on a step
+whose pages are all present: after ``advance()`` the next token can land on a
+page the batch has not taken yet, and only ``prepare_step()`` takes it.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import bench
+from persistent_moe_decode_gb300.configs import WORKLOADS
+from persistent_moe_decode_gb300.synth import DecodeBatch, make_kv_pools, make_model
+
+
+@pytest.fixture(scope="module")
+def tiny_inputs(oracle_lib):
+    wl = WORKLOADS["tiny"].with_(context=63)     # the first advance crosses a page boundary
+    model = make_model(wl.dims, wl.seed, "cpu")
+    batch = DecodeBatch(wl)
+    kp, vp = make_kv_pools(wl.dims, batch.num_pages, wl.kv_std, wl.seed, "cpu")
+    return wl, model, batch, kp, vp
+
+
+def test_cpu_sample_after_advance_on_a_page_boundary(tiny_inputs):
+    wl, model, batch, kp, vp = tiny_inputs
+    batch.advance(np.array([5], dtype=np.int32))
+    assert int(batch.seq_lens[0]) == 64
+    # the page of position 64 is not taken yet: the oracle refuses the step
+    raw = (batch.tokens.copy(), batch.seq_lens.copy(), batch.page_tables.copy())
+    with pytest.raises(RuntimeError, match="-2"):
+        bench.CpuSample(model, kp, vp, raw, wl, 2).time_token()
+    state = bench.snapshot(batch)
+    assert state[2][0, 64 // 16] >= 0
+    cs = bench.CpuSample(model, kp, vp, state, wl, 2)
+    assert cs.time_token() > 0.0
+    out = cs.measure(0.0)
+    assert out["value"] > 0 and out["cores"] >= 1 and "context 64" in out["sample"]
+
+
+def test_context_reported_the_same_way_in_both_arms():
+    assert bench.context_of(np.array([8197])) == 8197
+    assert bench.context_of(np.array([1, 2])) == "ragged"

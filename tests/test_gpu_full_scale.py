@@ -1,19 +1,24 @@
-"""Parity at the full 30B-total / 3.3B-active sizes, in the launch configuration
-the benchmark times (all SMs, default schedule, one step).
+"""Parity at the full sizes of the benchmark workloads, in the launch
+configuration the benchmark times (all SMs, the per-step schedule), over
+teacher-forced trajectories against the whole-model CPU oracle:
 
-A whole 48-layer step is too slow for the fp64 oracle in a test, so the step is
-checked on what the oracle can compute one piece at a time:
-  - sampled layers, teacher-forced: the oracle runs layer l from the GPU's
-    residual entering it (same weights, same KV cache, same new token) and the
-    residual leaving it must agree with the GPU's; the routed expert sets of
-    that layer must be equal wherever the oracle's k-th / (k+1)-th router gap
-    exceeds 1e-3;
-  - the LM head over the whole vocabulary from the GPU's final residual:
-    logits within max-abs 2e-2 and relative L2 1e-2, greedy token equal.
+  mid_8k    8 layers, batch 1, 8K context: all 32 steps;
+  a3b_8k    30B-total / 3.3B-active, batch 1, 8K context: 16 steps;
+  a3b_b16   the same model, 16 ragged sequences, one retiring and one joining
+            on fresh random pages every step: 8 steps;
+  a3b_256k  the same model, batch 1, 256K context: 2 steps.
+
+Every step: logits max-abs <= 2e-2 and relative L2 <= 1e-2 over the whole
+vocabulary of every sequence, routed expert sets equal on every (layer,
+sequence) where the oracle's k-th / (k+1)-th router gap exceeds 1e-3, greedy
+tokens equal on >= 99 % of steps.  On the first step the residual entering
+every layer is also compared with the oracle's (whole-model propagation, no
+teacher forcing inside the step).
 """
 from __future__ import annotations
 
-import dataclasses
+import gc
+import time
 
 import numpy as np
 import pytest
@@ -22,11 +27,11 @@ import torch
 import oracle
 from persistent_moe_decode_gb300 import mk
 from persistent_moe_decode_gb300.configs import WORKLOADS
-from persistent_moe_decode_gb300.synth import bf16_bits
+from tests._pair import Pair, run_trajectory
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-GAP = 1e-3
+STEPS = {"mid_8k": 32, "a3b_8k": 16, "a3b_b16": 8, "a3b_256k": 2}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -38,72 +43,33 @@ def built():
     oracle.build()
 
 
-def host(t) -> np.ndarray:
-    return bf16_bits(t.cpu().contiguous())
-
-
-def layer_oracle(run, l):
-    """An oracle over layer l alone (weights and KV pools of that layer)."""
-    d = run.dims
-    m = run.model
-    w = {n: host(getattr(m, n)[l:l + 1]) for n in oracle.Oracle.PER_LAYER}
-    # embedding, LM head and final norm are not used by run_layers: small stand-ins
-    w["embed"] = np.zeros((1, d.hidden), dtype=np.uint16)
-    w["lm_head"] = np.zeros((1, d.hidden), dtype=np.uint16)
-    w["final_norm"] = np.zeros(d.hidden, dtype=np.uint16)
-    kp = host(run.k_pool[l:l + 1]).copy()
-    vp = host(run.v_pool[l:l + 1]).copy()
-    return oracle.Oracle({**dataclasses.asdict(d), "n_layers": 1}, w, kp, vp)
-
-
-@pytest.mark.parametrize("name", ["a3b_8k", "a3b_b16", "a3b_256k"])
-def test_full_size_step_matches_oracle_on_sampled_layers_and_lm_head(name):
-    from persistent_moe_decode_gb300.runner import StepRunner
+@pytest.mark.parametrize("name", list(STEPS))
+def test_full_size_trajectory_matches_the_oracle(name):
     wl = WORKLOADS[name]
     d = wl.dims
-    run = StepRunner(wl, device="cuda")
+    steps = STEPS[name]
+    t0 = time.time()
+    pair = Pair(wl.with_(steps=max(steps, 1)))
+    B = wl.batch
+
+    def residuals(s, gpu, ref, tr):
+        if s != 0:
+            return
+        dec = pair.run.dec
+        for l in range(d.n_layers + 1):
+            h = np.frombuffer(dec.scratch(mk.MK_SCRATCH_H, l), dtype=np.float32).reshape(B, d.hidden)
+            want = tr["h_in"][l]
+            scale = max(1.0, float(np.abs(want).max()))
+            err = float(np.abs(h - want).max())
+            assert err <= 1e-3 * scale, f"{name}: residual entering layer {l}: max-abs {err:.3e}"
+
     try:
-        b = run.batch
-        b.prepare_step()
-        lens, pt = b.seq_lens.copy(), b.page_tables.copy()
-        run.dec.schedule(b.tokens, b.page_tables, b.seq_lens, seq_ids=b.seq_ids)
-        run.launch()
-        torch.cuda.synchronize()
-        run.check_status()
-        B = wl.batch
-        dec = run.dec
-        idx_gpu, _ = dec.routing()
-
-        def scratch(kind, l, width):
-            return np.frombuffer(dec.scratch(kind, l), dtype=np.float32).reshape(B, width).astype(np.float64)
-
-        for l in (0, d.n_layers // 2, d.n_layers - 1):
-            h_in = scratch(mk.MK_SCRATCH_H, l, d.hidden)
-            h_out = scratch(mk.MK_SCRATCH_H, l + 1, d.hidden)
-            orc = layer_oracle(run, l)
-            ref = orc.run_layers(0, 1, h_in, lens, pt)
-            scale = max(1.0, float(np.abs(ref).max()))
-            err = float(np.abs(h_out - ref).max())
-            assert err <= 2e-3 * scale, f"{name} layer {l}: residual max-abs {err:.3e} (scale {scale:.2f})"
-            # routing of the layer: the oracle's own router logits from its own norm
-            x = np.stack([oracle.rmsnorm(h_in[i], orc.w["attn_norm"][0], d.rms_eps) for i in range(B)])
-            for i in range(B):
-                r = oracle.matvec(orc.w["w_router"][0], x[i])
-                idx, _, gap = oracle.route(r, d.top_k)
-                if gap > GAP:
-                    assert set(idx_gpu[l, i].tolist()) == set(idx.tolist()), (name, l, i)
-        # the whole LM head from the GPU's final residual
-        h_f = scratch(mk.MK_SCRATCH_H, d.n_layers, d.hidden)
-        lm = host(run.model.lm_head)
-        g_f = host(run.model.final_norm)
-        xf = np.stack([oracle.rmsnorm(h_f[i], g_f, d.rms_eps) for i in range(B)])
-        ref = oracle.matvec(lm, xf).reshape(B, -1)
-        gpu = run.logits.double().cpu().numpy()
-        err = float(np.abs(gpu - ref).max())
-        rel = float(np.linalg.norm(gpu - ref) / np.linalg.norm(ref))
-        assert err <= 2e-2 and rel <= 1e-2, f"{name}: logits max-abs {err:.3e} rel-L2 {rel:.3e}"
-        assert np.array_equal(gpu.argmax(1), ref.argmax(1))
+        exempt, compared, agree = run_trajectory(pair, steps, on_step=residuals)
+        assert compared > 0
+        print(f"\n{name}: {steps} steps, argmax agreed on {agree}, routing sets compared {compared}, "
+              f"exempt by the gap rule {exempt}, {time.time() - t0:.0f} s")
     finally:
-        run.close()
-        del run
+        pair.close()
+        del pair
+        gc.collect()
         torch.cuda.empty_cache()

@@ -19,15 +19,10 @@ import torch
 import oracle
 from persistent_moe_decode_gb300 import mk
 from persistent_moe_decode_gb300.configs import WORKLOADS
-from tests._util import dims_dict, host_pool, host_weights
+from tests._pair import Pair, check_logits, check_routing, run_trajectory
+from tests._util import host_pool
 
 pytestmark = pytest.mark.gpu
-
-MAX_ABS, REL_L2, GAP = 2e-2, 1e-2, 1e-3
-
-
-def oracle_flags(batch: int) -> int:
-    return 0
 
 
 def rope_np(qkv_row, dims, pos):
@@ -48,72 +43,6 @@ def built():
     from persistent_moe_decode_gb300 import build
     build.build()
     oracle.build()
-
-
-class Pair:
-    """GPU runner + oracle over the same inputs."""
-
-    def __init__(self, wl, **cfg_kw):
-        from persistent_moe_decode_gb300.runner import StepRunner
-        self.wl = wl
-        self.run = StepRunner(wl, device="cuda", **cfg_kw)
-        self.orc = oracle.Oracle(dims_dict(wl.dims), host_weights(self.run.model),
-                                 host_pool(self.run.k_pool), host_pool(self.run.v_pool))
-
-    def step(self, trace=False):
-        b = self.run.batch
-        b.prepare_step()
-        tokens, lens, pt = b.tokens.copy(), b.seq_lens.copy(), b.page_tables.copy()
-        self.run.step()
-        torch.cuda.synchronize()
-        self.run.check_status()
-        gpu = self.run.logits.double().cpu().numpy()
-        out = self.orc.decode_step(tokens, lens, pt, flags=oracle_flags(self.wl.batch), trace=trace)
-        ref, tr = (out if trace else (out, None))
-        return gpu, ref, tr
-
-    def advance(self, tokens):
-        ch = self.run.advance(tokens)
-        if ch is not None:        # mirror the refilled pages into the oracle's pools
-            slot, pages = ch
-            idx = torch.as_tensor(pages, dtype=torch.long, device=self.run.k_pool.device)
-            self.orc.k_pool[:, pages] = host_pool(self.run.k_pool[:, idx])
-            self.orc.v_pool[:, pages] = host_pool(self.run.v_pool[:, idx])
-
-    def close(self):
-        self.run.close()
-
-
-def check_logits(gpu, ref, where=""):
-    err = np.abs(gpu - ref).max()
-    rel = np.linalg.norm(gpu - ref) / np.linalg.norm(ref)
-    assert np.all(np.isfinite(gpu)), f"{where}: non-finite logits"
-    assert err <= MAX_ABS and rel <= REL_L2, f"{where}: max-abs {err:.3e} rel-L2 {rel:.3e}"
-    return err, rel
-
-
-def check_routing(pair, tr):
-    idx, _ = pair.run.dec.routing()
-    ok = tr["gap"] > GAP
-    for l in range(idx.shape[0]):
-        for b in range(idx.shape[1]):
-            if ok[l, b]:
-                assert set(idx[l, b]) == set(tr["idx"][l, b]), (l, b, idx[l, b], tr["idx"][l, b])
-    return int((~ok).sum())
-
-
-def run_trajectory(pair, steps, trace_every=1):
-    agree, exempt = 0, 0
-    for s in range(steps):
-        gpu, ref, tr = pair.step(trace=(s % trace_every == 0))
-        check_logits(gpu, ref, f"step {s}")
-        if tr is not None:
-            exempt += check_routing(pair, tr)
-        g_tok, r_tok = gpu.argmax(1), ref.argmax(1)
-        agree += int((g_tok == r_tok).all())
-        pair.advance(g_tok.astype(np.int32))
-    assert agree >= 0.99 * steps or steps - agree <= 0, f"argmax agreed on {agree}/{steps} steps"
-    return exempt
 
 
 def test_tiny_intermediates_match_layer_by_layer():
