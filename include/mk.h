@@ -115,7 +115,7 @@ typedef struct {
  *   w_o[l]           [H][hq d]
  *   w_router[l]      [E][H]
  *   w_gate[l], w_up[l]  [E][I][H]
- *   w_down[l]        [E][H][I]
+ *   w_down[l]        [E][H][I]          (read once, at mk_create: see there)
  *   k_pool[l], v_pool[l]  [num_kv_pages][hkv][page_size][d]  (written: the
  *                    step stores its new K/V, post-RoPE, at position seq_len)
  * Every pointer must be 16-byte aligned.
@@ -152,6 +152,16 @@ typedef struct mk_handle mk_handle;
  * Validates cfg (MK_ERR_BAD_CONFIG), copies the per-layer pointer arrays,
  * allocates the library-owned device state (counters, activations scratch,
  * queues, task lists: MK_ERR_OOM on failure) and builds the per-layer waves.
+ *
+ * Weight snapshot: mk_create also copies every layer's w_down into a
+ * library-owned device array in a blocked layout, [L][E][I / 8][H][8] BF16
+ * (each 8-column group of an expert's down projection contiguous), and the
+ * decode step reads that copy, not w_down.  It costs L * E * I * H * 2 bytes
+ * of device memory (19.3 GB for L = 48, E = 128, I = 768, H = 2048), counted
+ * in mk_device_bytes, and is made with a device-wide synchronize before
+ * mk_create returns.  Changes the caller makes to w_down after mk_create are
+ * therefore NOT seen by later steps: destroy and re-create the handle to pick
+ * them up.  Every other weight and both KV pools are read in place.
  * On success *out owns that state until mk_destroy. */
 int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out);
 
@@ -239,25 +249,34 @@ int mk_read_trace(mk_handle* h, void* dst, size_t bytes, size_t* size_out);
  * mk_decode_step_static (256 KB per device). */
 #define MK_STATIC_COUNTER_WORDS 65536
 
-/* mk_decode_step with the step's counters, queue claim heads and error words
- * in a fixed device array of MK_STATIC_COUNTER_WORDS words instead of the
- * handle's own; the pages describe no such variant (their host loop clears
- * and reuses one scratch area per engine).  The call allocates nothing: the
- * schedule for the batch is the one mk_schedule_step built, and the words the
- * step uses are cleared to zero on `stream` before the launch.  After the
- * kernel, the error words are copied on `stream` into the handle's own error
- * block, so mk_step_status reports this step as usual.  Same results as
- * mk_decode_step for the same scheduled batch.
- * Errors: MK_ERR_BAD_CONFIG if the handle needs more counter words than the
- * array holds (32 + n_layers * a per-layer block of 32 words),
- * MK_ERR_NOT_SCHEDULED, MK_ERR_BAD_ARG (NULL logits, or the current device is
- * not the handle's), MK_ERR_CUDA.
- * One array serves every handle on a device: two calls of this function whose
- * executions overlap (other streams, other handles, other threads) share the
- * counters and corrupt each other's step; serialise them.  mk_decode_step
- * does not touch the array.  The first call on a device looks up the array's
- * address and sets the kernel's shared-memory limit; make that first call
- * outside any stream capture. */
+/* mk_decode_step for callers that may not allocate device memory while they
+ * run a step: a real-time serving loop that must not take the allocator's
+ * locks or meet an out-of-memory failure between steps, or a host runtime
+ * that owns every device allocation itself and forbids its plug-ins to call
+ * cudaMalloc.  The paper has no counterpart of this call.
+ *
+ * mk_decode_step keeps the step's counters, queue claim heads and error words
+ * in device memory the handle allocated; this call keeps them instead in one
+ * file-scope device array of MK_STATIC_COUNTER_WORDS 32-bit words that the
+ * library holds on every device where it is loaded, until the process exits.
+ * It calls no allocating routine: the schedule is the one mk_schedule_step
+ * built, the words the step uses are cleared to zero on `stream` before the
+ * kernel, and after it the error words are copied on `stream` into the
+ * handle's own error block, so mk_step_status reports the step as usual.
+ * The results are the same as those of mk_decode_step for the same batch.
+ *
+ * Limit: a handle needs 32 + n_layers * round_up(6 + max_batch, 32) words;
+ * with max_batch <= 16 that is 32 words per layer, so up to 2,047 layers fit.
+ * A larger need returns MK_ERR_BAD_CONFIG.  Other errors: MK_ERR_NOT_SCHEDULED, MK_ERR_BAD_ARG
+ * (NULL logits, or the current device is not the handle's), MK_ERR_CUDA.
+ *
+ * Sharing: every handle on a device uses the same array, and it keeps what
+ * the last call left in it.  Two calls whose kernels overlap on the GPU
+ * (other streams, other handles, other threads) race on it and corrupt each
+ * other's step: serialise them.  mk_decode_step does not touch the array.
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and sets the kernel's
+ * shared-memory limit there; make that first call before any stream capture. */
 int mk_decode_step_static(mk_handle* h, float* logits, void* stream);
 
 /* Library-owned device bytes (counters, scratch, queues, task lists). */
