@@ -222,6 +222,24 @@ int mk_read_scratch(mk_handle* h, int which, int layer, void* dst, size_t bytes,
 int mk_plan(const mk_config* cfg, int n_sm, int batch, int32_t* tasks, int32_t* offsets,
             int* n_tasks_out, int* n_barriers_out);
 
+/* The whole host schedule of one step, as mk_schedule_step builds it for the
+ * lengths seq_lens [batch] (HOST array): the attention-branch size, the
+ * split-KV items and the per-SM task lists, for checking the scheduler and
+ * its counter accounting without a GPU.  Host-only; needs no device.
+ *   info      int32 [9]: n_tasks, n_items, attention SMs, then the SM counts
+ *             the kernel takes as counter targets (COMBINE, UP, DOWN and
+ *             router-row SMs), the split-KV chunk (tokens; 0 = balanced page
+ *             runs), counter words; always written
+ *   tasks     int32 [n_tasks][32] descriptors, SM-major; task_off [n_sm + 1]
+ *   items     int32 [n_items][8] split-KV items (sequence, split index, split
+ *             count, first key, end key, first item of the sequence, new
+ *             token's position, 0); item_off [n_sm + 1] items of each SM
+ *   meta      int32 [batch][2]: first item and split count of each sequence
+ * Any of tasks .. meta may be NULL (call once with NULL to size them).
+ * Errors: MK_ERR_BAD_ARG, MK_ERR_BATCH_TOO_LARGE, MK_ERR_BAD_CONFIG. */
+int mk_plan_step(const mk_config* cfg, int n_sm, int batch, const int32_t* seq_lens, int32_t* info,
+                 int32_t* tasks, int32_t* task_off, int32_t* items, int32_t* item_off, int32_t* meta);
+
 /* Testing aid for the device timeout path: add `delta` to the wait target of
  * the norm task of `layer` in the cached schedules, so that its counter wait
  * can never complete and runs out after config.timeout_ms (the kernel then

@@ -186,6 +186,57 @@ int make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* b
   return MK_OK;
 }
 
+// One token: a weight matrix [rows][K] (K = 2048 or 4096) viewed as 3-D
+// [K / 64][rows][64] BF16 (strides: K * 2 bytes per row, 128 bytes per column
+// block), boxes of every column block x (32768 / (2 K)) rows x 64 columns,
+// 128-byte swizzle: one stage of whole rows per copy.
+int make_row_map(CUtensorMap* m, const void* base, uint64_t rows, int K) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return MK_ERR_CUDA;
+  const cuuint64_t dims[3] = {64, rows, (cuuint64_t)(K / 64)};
+  const cuuint64_t strides[2] = {(cuuint64_t)K * 2, 128};
+  const cuuint32_t box[3] = {64, (cuuint32_t)(32768 / (2 * K)), (cuuint32_t)(K / 64)};
+  const cuuint32_t es[3] = {1, 1, 1};
+  if (rows >= (1ull << 32) || !aligned16(base)) return MK_ERR_BAD_ARG;
+  if (enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MK_ERR_BAD_ARG;
+  return MK_OK;
+}
+
+// the one-token tensor maps of every layer's router, W_qkv, W_o, gate and up
+// matrices and of the LM head (W_MAP_* order); none when the hidden size does
+// not take the tensor-core path
+int make_weight_maps(mk_handle* h, const mk_weights* w, const uint8_t** out) {
+  const mk_config& c = h->cfg;
+  *out = nullptr;
+  const int H = c.hidden, KO = c.n_q_heads * c.head_dim, L = c.n_layers;
+  if (!rotated_rows(H)) return MK_OK;
+  if (!rotated_rows(KO)) return MK_ERR_BAD_CONFIG;   // both GEMV paths in one layer are not built
+  std::vector<CUtensorMap> maps((size_t)W_MAPS_PER_LAYER * L + 1);
+  const uint64_t qrows = (uint64_t)(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  const uint64_t erows = (uint64_t)c.n_experts * c.moe_inter;
+  for (int l = 0; l < L; l++) {
+    CUtensorMap* m = &maps[(size_t)W_MAPS_PER_LAYER * l];
+    int rc = make_row_map(&m[W_MAP_ROUTER], w->w_router[l], (uint64_t)c.n_experts, H);
+    if (!rc) rc = make_row_map(&m[W_MAP_QKV], w->w_qkv[l], qrows, H);
+    if (!rc) rc = make_row_map(&m[W_MAP_O], w->w_o[l], (uint64_t)H, KO);
+    if (!rc) rc = make_row_map(&m[W_MAP_GATE], w->w_gate[l], erows, H);
+    if (!rc) rc = make_row_map(&m[W_MAP_UP], w->w_up[l], erows, H);
+    if (rc) return rc;
+  }
+  int rc = make_row_map(&maps.back(), w->lm_head, (uint64_t)c.vocab, H);
+  if (rc) return rc;
+  uint8_t* d = nullptr;
+  rc = dalloc(h, &d, maps.size() * sizeof(CUtensorMap));
+  if (rc) return rc;
+  if (cudaMemcpy(d, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess)
+    return MK_ERR_CUDA;
+  *out = d;
+  return MK_OK;
+}
+
 // one token: the tensor map of the per-group partial buffer (24 x 256 fp32)
 int make_moe_map(mk_handle* h, float* mpart, const uint8_t** mp) {
   const mk_config& c = h->cfg;
@@ -295,6 +346,39 @@ int mk_plan(const mk_config* cfg, int n_sm, int batch, int32_t* tasks, int32_t* 
   return MK_OK;
 }
 
+int mk_plan_step(const mk_config* cfg, int n_sm, int batch, const int32_t* seq_lens, int32_t* info,
+                 int32_t* tasks, int32_t* task_off, int32_t* items, int32_t* item_off, int32_t* meta) {
+  if (!cfg || !seq_lens || !info || n_sm < 1) return MK_ERR_BAD_ARG;
+  if (batch < 1 || batch > cfg->max_batch) return MK_ERR_BATCH_TOO_LARGE;
+  mk_config c = *cfg;
+  if (c.max_attn_items == 0) c.max_attn_items = 8192;
+  for (int b = 0; b < batch; b++)
+    if (seq_lens[b] < 0) return MK_ERR_BAD_ARG;
+  // the same three calls mk_schedule_step makes
+  const int na = attention_sms(c, n_sm, batch, seq_lens);
+  std::vector<int32_t> it, so, me;
+  const int split = split_kv(c, n_sm, na, batch, seq_lens, &it, &so, &me);
+  if (split < 0) return MK_ERR_BAD_CONFIG;
+  Plan plan;
+  int rc = build_plan(c, n_sm, batch, na, &plan);
+  if (rc) return rc;
+  info[0] = (int32_t)(plan.tasks.size() / kDescWords);
+  info[1] = (int32_t)(it.size() / 8);
+  info[2] = na;
+  info[3] = plan.n_comb_sms;
+  info[4] = plan.n_up_sms;
+  info[5] = plan.n_down_sms;
+  info[6] = plan.n_rtr_sms;
+  info[7] = split;
+  info[8] = plan.n_bars;
+  if (tasks) memcpy(tasks, plan.tasks.data(), plan.tasks.size() * 4);
+  if (task_off) memcpy(task_off, plan.off.data(), plan.off.size() * 4);
+  if (items) memcpy(items, it.data(), it.size() * 4);
+  if (item_off) memcpy(item_off, so.data(), so.size() * 4);
+  if (meta) memcpy(meta, me.data(), me.size() * 4);
+  return MK_OK;
+}
+
 void mk_destroy(mk_handle* h) {
   if (!h) return;
   cudaDeviceSynchronize();
@@ -367,6 +451,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
   TRY(upload_ptrs(h, (const void* const*)w->k_pool, L, (const void* const**)&p.k_pool));
   TRY(upload_ptrs(h, (const void* const*)w->v_pool, L, (const void* const**)&p.v_pool));
   TRY(make_kv_maps(h, w, &p.kv_maps));
+  TRY(make_weight_maps(h, w, &p.w_maps));
 
   const size_t Ls = (size_t)L, Bs = (size_t)Bm, Ns = (size_t)h->n_sm;
   p.max_attn_items = c.max_attn_items;

@@ -51,6 +51,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "mk_layout.h"
 #include "mk_ptx.cuh"
 
@@ -213,12 +215,10 @@ __device__ __forceinline__ void dshare(int total, int n, int s, int& lo, int& hi
   hi = (int)((uint32_t)total * (uint32_t)(s + 1) / (uint32_t)n);
 }
 
-// one token: rows of a P1 / O-proj chunk.  With K = 2048 or 4096 the
-// consumers split the contraction over the warps and hold at most 64 rows'
-// partial sums, so every chunk (whatever the SM count) takes that path.
-__device__ __forceinline__ int split_rows(int K) {
-  return (K % 2048 == 0 && K <= 4096) ? 64 : kRowChunk;
-}
+// one token: rows of a GEMV chunk.  Rows of 2048 or 4096 columns go to the
+// tensor cores, whose per-warp partial sums of a chunk fill one kMmaRows x 8
+// buffer; other row lengths go whole to one warp each.
+__device__ __forceinline__ int one_rows(int K) { return rotated_rows(K) ? kMmaRows : kRowChunk; }
 
 // One token: top-k of the router logits of layer l, softmax weights over the
 // picks (the top-k of the softmax = the top-k of the logits; ties to the lower
@@ -367,22 +367,38 @@ struct Prod {
   }
 
   // rows [row0, row0 + nrows) of a row-major [*, K] matrix, whole rows, one
-  // bulk copy per stage
-  __device__ __forceinline__ bool stream_rows(const uint16_t* w, int row0, int nrows, int K) {
+  // copy per stage: a 1-D bulk copy, or (one token, rows of 2048 or 4096
+  // columns) a 3-D tensor copy through the matrix's map, which lands the
+  // stage swizzled for the tensor-core GEMV (a whole box: rows past a short
+  // last stage are copied too, or zero-filled past the matrix)
+  __device__ __forceinline__ bool stream_rows(const uint16_t* w, int row0, int nrows, int K,
+                                              const uint8_t* map = nullptr) {
     const int rps = rows_per_stage(K);
+    const bool rot = ONE && rotated_rows(K);
     for (int done = 0; done < nrows; done += rps) {
       const int rows = min(rps, nrows - done);
       uint32_t slot;
       if (!acquire_stage(slot)) return false;
       if (lane == 0) {
-        const uint32_t bytes = (uint32_t)(rows * K * 2);
-        mbar_arrive_expect_tx(&S.full[slot], bytes);
-        bulk_g2s_hint(&S.stage[slot][0], w + (size_t)(row0 + done) * K, bytes, &S.full[slot], policy_evict_first());
+        if (rot) {
+          mbar_arrive_expect_tx(&S.full[slot], (uint32_t)kStageBytes);
+          tma_load_3d_hint(&S.stage[slot][0], map, 0, row0 + done, 0, &S.full[slot], policy_evict_first());
+        } else {
+          const uint32_t bytes = (uint32_t)(rows * K * 2);
+          mbar_arrive_expect_tx(&S.full[slot], bytes);
+          bulk_g2s_hint(&S.stage[slot][0], w + (size_t)(row0 + done) * K, bytes, &S.full[slot],
+                        policy_evict_first());
+        }
       }
       __syncwarp();
       stage_seq++;
     }
     return true;
+  }
+
+  // one token: the tensor map of matrix `which` (W_MAP_*) of the current layer
+  __device__ __forceinline__ const uint8_t* wmap(int which) const {
+    return p.w_maps + ((size_t)W_MAPS_PER_LAYER * l + which) * 128;
   }
 
   // pages [pg0, pg0 + npages) of sequence b, all KV heads: K pages then V
@@ -515,8 +531,12 @@ struct Prod {
     const bool fin = op == OP_FINAL, out = op == OP_OUT;
     const int H = out ? p.hq * p.d : p.H;         // row length
     if (fin || out) b1 = b0;
-    const int cr = fin ? kRowChunk : split_rows(H);
+    const int cr = one_rows(H);
     const uint16_t* m0 = fin ? p.lm_head : wptr(out ? 2 : 0);
+    const bool rot = rotated_rows(H);
+    const uint8_t* map0 = !rot ? nullptr : fin ? p.w_maps + (size_t)W_MAPS_PER_LAYER * p.L * 128
+                                             : wmap(out ? W_MAP_O : W_MAP_ROUTER);
+    const uint8_t* map1 = rot ? wmap(W_MAP_QKV) : nullptr;
     int ph = a1 > a0 ? 0 : 1, c0 = ph == 0 ? a0 : b0;
     bool first = true;
     do {
@@ -538,7 +558,7 @@ struct Prod {
         w[R_NT] = 1;
       }
       commit();
-      if (c1 > c0 && !stream_rows(ph == 0 ? m0 : wptr(1), c0, c1 - c0, H)) return false;
+      if (c1 > c0 && !stream_rows(ph == 0 ? m0 : wptr(1), c0, c1 - c0, H, ph == 0 ? map0 : map1)) return false;
       first = false;
       c0 = c1;
       if (end_ph && ph == 0) {
@@ -645,7 +665,10 @@ struct Prod {
       for (int sg = 0; sg < 2 + ncb; sg++) {
         const bool dn = sg >= 2;
         const uint16_t* src = dn ? blk + (size_t)(sg - 2) * H * 8 : wptr(3 + sg) + eo;
-        if (!stream_rows(src, dn ? 0 : i0, dn ? H : i1 - i0, dn ? 8 : H)) return false;
+        // gate / up rows through their maps: rows of the [E I][H] matrix
+        if (!stream_rows(src, dn ? 0 : (rotated_rows(H) ? e * p.I : 0) + i0, dn ? H : i1 - i0, dn ? 8 : H,
+                         dn || !rotated_rows(H) ? nullptr : wmap(sg == 0 ? W_MAP_GATE : W_MAP_UP)))
+          return false;
       }
       g = ge;
     }
@@ -691,7 +714,7 @@ struct Prod {
     const int KO = p.hq * p.d;
     const int last = ONE ? FL_LAST : 0;
     if (a1 <= a0) return chunk(K_OPROJ, FL_LAST, 0, 0, 1, KO, B, 0, 0, 0, nullptr, nullptr);
-    const int co = ONE ? split_rows(KO) : gemv_chunk_rows(KO, B);
+    const int co = ONE ? one_rows(KO) : gemv_chunk_rows(KO, B);
     for (int c0 = a0; c0 < a1; c0 += co)
       if (!chunk(K_OPROJ, c0 + co >= a1 ? last : 0, c0, min(co, a1 - c0), 1, KO, B, 0, 0, 0, wptr(2),
                  nullptr))
@@ -1371,91 +1394,83 @@ struct Cons {
     return true;
   }
 
-  // one token, few rows per warp (P1 and O-proj chunks of at most 64 rows,
-  // UP pieces of at most 64 + 64; K 2048 or 4096): the contraction is split
-  // over the warps instead of the
-  // rows.  Warp w takes columns [w K / 8, (w + 1) K / 8), lane l the 8-column
-  // chunks l, l + 32 of that range, so each warp holds only its eighth of x
-  // in registers.  A stage's RB = 8 / NC rows are reduced over the lanes
-  // together (transposed butterfly: 9 shuffles for 8 rows, 6 for 4); the
-  // eight warp sums of a row meet in shared memory (spart, [row][warp]) and
-  // are added in warp order after the barrier.
-  template <int NC>
-  __device__ __forceinline__ bool gemv_split(float* res) {
-    constexpr int RB = 8 / NC;                    // rows per stage (32 KB of 2 K-byte rows)
-    const int K = t[R_K];
+  // one token, rows of K = 2048 NH columns on the tensor cores (mma.sync
+  // m16n8k16, BF16 in, fp32 accumulate).  A stage holds R = 8 / NH rows as
+  // [K / 64 column blocks][R rows][64 columns], swizzled (rotated_rows).  Warp
+  // w takes column blocks [4 NH w, 4 NH w + 4 NH) of every row, cut into
+  // P = 2 NH parts of two blocks: the MMA's M side is (row m % R, part m / R),
+  // its K side 16 columns of that part, its N side the activation: column
+  // n = 2 j + t holds the BF16 high (t = 0) or low (t = 1) half of x over part
+  // j, so every product keeps about 16 bits of x.  C[m][n] is the part's dot
+  // product where n matches m's part; the lanes holding a row's parts are
+  // added (quad shuffles; with R = 4 also the two quads of a row), and the
+  // eight warp sums of a row meet in shared memory (spart, [row][warp]),
+  // added in warp order after the barrier.  With R = 4 the parts take every
+  // other block (parts 2 q and 2 q + 1 differ in block parity) so that the
+  // eight rows of an ldmatrix tile lie in distinct 128-byte lines mod 8.
+  template <int NH>
+  __device__ __forceinline__ int mma_block(int j, int t) const {
+    return NH == 1 ? 4 * warp + 2 * j + t : 8 * warp + 4 * (j >> 1) + 2 * t + (j & 1);
+  }
+
+  template <int NH>
+  __device__ __forceinline__ bool gemv_mma(float* res) {
+    constexpr int R = 8 / NH;                     // rows per stage
     const int ngrp = row_groups();
-    const int col0 = warp * (K / 8) + lane * 8;
-    float xa[NC][8];
+    // B fragments (x as k x n) for the 8 k-steps of the warp's parts: lane
+    // (gl, cq) holds column n = gl, rows 2 cq, 2 cq + 1 and 8 + 2 cq, 9 + 2 cq
+    uint32_t xb[8][2];
+    {
+      const int j = gl >> 1, lo = gl & 1;
+      const bool on = j < 2 * NH;
 #pragma unroll
-    for (int c = 0; c < NC; c++) {
-      const float4 a = *(const float4*)(S.xs + col0 + 256 * c);
-      const float4 b = *(const float4*)(S.xs + col0 + 256 * c + 4);
-      xa[c][0] = a.x; xa[c][1] = a.y; xa[c][2] = a.z; xa[c][3] = a.w;
-      xa[c][4] = b.x; xa[c][5] = b.y; xa[c][6] = b.z; xa[c][7] = b.w;
+      for (int s = 0; s < 8; s++) {
+        const float* xs = S.xs + mma_block<NH>(j, s >> 2) * 64 + (s & 3) * 16 + 2 * cq;
+#pragma unroll
+        for (int hf = 0; hf < 2; hf++) {
+          float2 v = on ? *(const float2*)(xs + hf * 8) : make_float2(0.f, 0.f);
+          if (lo) v = make_float2(v.x - bf16f(f2bf(v.x)), v.y - bf16f(f2bf(v.y)));
+          xb[s][hf] = pack_bf2(v.x, v.y);
+        }
+      }
     }
+    // ldmatrix rows of this lane: tile i = lane / 8 holds M rows (i & 1) * 8 +
+    // 0..7, columns 8 (i >> 1) .. + 7 of the k-step; lane & 7 is the M row
+    uint32_t aoff[8];
+    {
+      const int m = ((lane >> 3) & 1) * 8 + (lane & 7), r = m % R, j = m / R, kh = lane >> 4;
+#pragma unroll
+      for (int s = 0; s < 8; s++) {
+        const int line = mma_block<NH>(j, s >> 2) * R + r;
+        aoff[s] = (uint32_t)(line * 128 + ((((s & 3) * 2 + kh) ^ (line & 7)) << 4));
+      }
+    }
+    // C entries this lane keeps: M row gl is part gl / R, row gl + 8 part (gl + 8) / R
+    const int j0 = gl / R, j1 = (gl + 8) / R;
     float* part = &S.spart[0][0];
     int rbase = 0;
     for (int g = 0; g < ngrp; g++) {
       const int nr = group_rows(g);
-      for (int done = 0; done < nr; done += RB) {
-        const int rows = min(RB, nr - done);
+      for (int done = 0; done < nr; done += R) {
+        const int rows = min(R, nr - done);
         uint32_t slot;
         if (!stage_full(slot)) return false;
         if (TR && tid == 0 && rbase + done == 0) S.t_mark[0] = gtime_ns();
-        const uint8_t* base = S.stage[slot] + col0 * 2;
-        float v[RB];
+        const uint8_t* base = S.stage[slot];
+        float ca[4] = {0.f, 0.f, 0.f, 0.f}, cc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int r = 0; r < RB; r++) {
-          float a0 = 0.f, a1 = 0.f;
-          if (r < rows) {
-            const uint8_t* wrow = base + (size_t)r * K * 2;
-            float2 a = make_float2(0.f, 0.f);   // even / odd columns
-#pragma unroll
-            for (int c = 0; c < NC; c++) {
-              const uint4 w = lds128(wrow + c * 512);
-              a = fma_bf2(w.x, make_float2(xa[c][0], xa[c][1]), a);
-              a = fma_bf2(w.y, make_float2(xa[c][2], xa[c][3]), a);
-              a = fma_bf2(w.z, make_float2(xa[c][4], xa[c][5]), a);
-              a = fma_bf2(w.w, make_float2(xa[c][6], xa[c][7]), a);
-            }
-            a0 = a.x;
-            a1 = a.y;
-          }
-          v[r] = a0 + a1;
+        for (int s = 0; s < 8; s++) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(a0, a1, a2, a3, base + aoff[s]);
+          mma_bf16((s & 1) ? cc : ca, a0, a1, a2, a3, xb[s][0], xb[s][1]);
         }
         stage_release(slot);
-        // transposed butterfly: each step halves the values a lane holds
-        float u[4];
-        if (RB == 8) {
-          const bool h = lane & 16;
-#pragma unroll
-          for (int j = 0; j < 4; j++) u[j] = (h ? v[j + 4] : v[j]) + __shfl_xor_sync(0xffffffffu, h ? v[j] : v[j + 4], 16);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; j++) u[j] = v[j % RB];
-        }
-        float w2[2];
-        {
-          const int o = RB == 8 ? 8 : 16;
-          const bool h = lane & o;
-#pragma unroll
-          for (int j = 0; j < 2; j++) w2[j] = (h ? u[j + 2] : u[j]) + __shfl_xor_sync(0xffffffffu, h ? u[j] : u[j + 2], o);
-        }
-        float q;
-        {
-          const int o = RB == 8 ? 4 : 8;
-          const bool h = lane & o;
-          q = (h ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, h ? w2[0] : w2[1], o);
-        }
-        // RB = 8: lane l now holds row (l >> 2) & 7 over lanes with equal l & 3;
-        // RB = 4: row (l >> 3) & 3 over lanes with equal l & 7
-        if (RB == 4) q += __shfl_xor_sync(0xffffffffu, q, 4);
-        q += __shfl_xor_sync(0xffffffffu, q, 2);
-        q += __shfl_xor_sync(0xffffffffu, q, 1);
-        const int row = RB == 8 ? (lane >> 2) & 7 : (lane >> 3) & 3;
-        if ((lane & (RB == 8 ? 3 : 7)) == 0 && row < rows)
-          part[(rbase + done + row) * kConsumerWarps + warp] = q;
+        float v = (cq == j0 ? (ca[0] + cc[0]) + (ca[1] + cc[1]) : 0.f) +
+                  (cq == j1 ? (ca[2] + cc[2]) + (ca[3] + cc[3]) : 0.f);
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if (R == 4) v += __shfl_xor_sync(0xffffffffu, v, 16);
+        if (cq == 0 && gl < rows) part[(rbase + done + gl) * kConsumerWarps + warp] = v;
       }
       rbase += nr;
     }
@@ -2182,15 +2197,16 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
     if (ok && run && kind == K_OPROJ) ok = c.wait_counter(bar_index(p, l, p.bl.comb), p.n_comb_sms) && c.stage_x();
     if (ok && run) {
       const int K = t[R_K];
-      // P1, O-proj and UP chunks (an UP piece's gate rows and up rows, at most
-      // 64 each) share the split GEMV: one code path for the layer's GEMVs
-      const bool split = (kind == K_P1 || kind == K_OPROJ || kind == K_UP) && rows <= 64 && split_rows(K) == 64;
-      if (split) ok = K == 2048 ? c.template gemv_split<1>(res) : c.template gemv_split<2>(res);
+      // rows of 2048 or 4096 columns (every chunk kind: P1, O-proj, an UP
+      // piece's gate and up rows, LM head) on the tensor cores: one code path
+      // for the layer's GEMVs
+      const bool split = rotated_rows(K);
+      if (split) ok = K == 2048 ? c.template gemv_mma<1>(res) : c.template gemv_mma<2>(res);
       else ok = K <= 256 ? c.template gemv_row<1>(res) : K <= 768 ? c.template gemv_row<3>(res)
               : K <= 2048 ? c.template gemv_row<8>(res) : c.template gemv_row<16>(res);
-      // the split path's sums are written by the threads that run the
+      // the tensor-core path's sums are written by the threads that run the
       // epilogue (except UP's, whose epilogue pairs row i with row nr + i);
-      // its partial buffer is reused by the next split chunk, which the
+      // its partial buffer is reused by the next chunk, which the
       // completion barrier below also orders when the task ends here
       if (ok && !(split && (flags & FL_LAST) && kind != K_UP)) ok = c.csync();
     }
@@ -2405,16 +2421,26 @@ cudaError_t relayout_down(const uint16_t* src, uint16_t* dst, int E, int H, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    for (int i = 0; i < 4; i++) {
-      const cudaError_t e =
-          cudaFuncSetAttribute(kStepKernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-      if (e != cudaSuccess) return e;
-    }
-    configured = true;
+// the dynamic shared-memory limit is a per-device attribute of each kernel:
+// set once on every device that launches the step
+cudaError_t configure_step_kernels() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<bool> configured[kMaxDev];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDev && configured[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  for (int i = 0; i < 4; i++) {
+    e = cudaFuncSetAttribute(kStepKernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
   }
+  if (dev >= 0 && dev < kMaxDev) configured[dev].store(true, std::memory_order_release);
+  return cudaSuccess;
+}
+
+cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream) {
+  const cudaError_t ce = configure_step_kernels();
+  if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_sm);
   cfg.blockDim = dim3(kThreads);

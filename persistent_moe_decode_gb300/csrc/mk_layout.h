@@ -88,6 +88,20 @@ MK_HD inline int rows_per_stage(int K) {
   return r > 0 ? r : 1;
 }
 
+// One token: weight rows of 2048 or 4096 columns are multiplied on the tensor
+// cores.  A stage of such rows arrives as ONE 3-D tensor copy of the matrix
+// viewed as [K / 64 column blocks][rows][64 columns] (box: all column blocks x
+// R = 32768 / (2 K) rows x 64 columns) with 128-byte swizzle: column block cb
+// of row r is the 128-byte line cb R + r of the stage, its 16-byte chunk c
+// stored at chunk c ^ (line & 7), so the eight rows an ldmatrix reads at one
+// column fall in distinct banks.  Row shares of such matrices are multiples
+// of 8 rows where the host chooses them, so a stage copies no row it does not
+// use.
+MK_HD inline bool rotated_rows(int K) { return K == 2048 || K == 4096; }
+constexpr int kMmaRows = 128;           // rows of one tensor-core GEMV chunk (one partial buffer)
+// tensor maps of the one-token weight matrices, per layer (W_MAP_* + 5 l), then the LM head
+enum : int { W_MAP_ROUTER = 0, W_MAP_QKV = 1, W_MAP_O = 2, W_MAP_GATE = 3, W_MAP_UP = 4, W_MAPS_PER_LAYER = 5 };
+
 // GEMV contraction segments: 256 columns (32 lanes x 8), or all of K below that
 MK_HD inline int gemv_nseg(int K) { return K < 256 ? 1 : K / 256; }
 
@@ -155,6 +169,9 @@ struct Params {
                                // of an expert one contiguous [H][8] block (one token: the
                                // UP pieces' column slices stream as whole blocks)
   const uint8_t* mp_map;       // tensor map of mpart: 2-D [groups][H] fp32, boxes 24 x 256
+  const uint8_t* w_maps;       // one token, rows of 2048 / 4096 columns: [5 L + 1] tensor maps
+                               // (W_MAP_*; the last the LM head), 3-D views described above
+                               // (nullptr when the model's rows take the other GEMV path)
   const uint8_t* kv_maps;      // [L][2] tensor maps (128 bytes each) of the K and V pools:
                                // 2-D [rows = pages * hkv * page_size][d], boxes of
                                // 64 dims x (hkv * page_size) rows, 128-byte swizzle

@@ -94,6 +94,17 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const void* map, int
       : "memory");
 }
 
+// 3-D tiled tensor copy global -> shared with an L2 cache policy; x is the
+// innermost coordinate
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const void* map, int x, int y, int z, uint64_t* bar,
+                                                 uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
 // orders this thread's earlier (acquired) view of global memory before its
 // later async-proxy (bulk copy) reads
 __device__ __forceinline__ void fence_proxy_async_global() {

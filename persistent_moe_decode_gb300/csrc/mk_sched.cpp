@@ -124,7 +124,7 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
   std::vector<int> r_lo(n_sm, 0), r_hi(n_sm, 0), q_lo(n_sm, 0), q_hi(n_sm, 0);
   {
     const int cand = roles ? n_sm - n_attn : n_sm;               // >= 1
-    const int per = std::max(8, (c.n_experts + cand - 1) / cand);
+    const int per = (std::max(8, (c.n_experts + cand - 1) / cand) + 7) / 8 * 8;
     int next = 0;
     for (int s = 0; s < n_sm && next < c.n_experts; s++) {
       if (roles && is_attn_sm(s, n_sm, n_attn)) continue;
@@ -140,9 +140,12 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
         // router SMs take no W_qkv rows, unless every SM holds router rows
         wq[s + 1] = wq[s] + ((pass == 0 && r_hi[s] > r_lo[s]) ? 0 : (hi - lo));
       }
+    // in whole groups of 8 rows (one tensor-core stage of 2048-column rows)
+    // where the row count allows it
+    const long long qg = qrows % 8 == 0 ? 8 : 1;
     for (int s = 0; s < n_sm; s++) {
-      q_lo[s] = wq[n_sm] > 0 ? (int)(qrows * wq[s] / wq[n_sm]) : 0;
-      q_hi[s] = wq[n_sm] > 0 ? (int)(qrows * wq[s + 1] / wq[n_sm]) : 0;
+      q_lo[s] = wq[n_sm] > 0 ? (int)(qg * (qrows / qg * wq[s] / wq[n_sm])) : 0;
+      q_hi[s] = wq[n_sm] > 0 ? (int)(qg * (qrows / qg * wq[s + 1] / wq[n_sm])) : 0;
     }
   }
 
@@ -155,9 +158,10 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
     std::vector<long long> wo(n_sm + 1, 0);
     for (int s = 0; s < n_sm; s++)
       wo[s + 1] = wo[s] + ((roles && batch == 1 && is_attn_sm(s, n_sm, n_attn)) ? kOutAttnWeight : 1);
+    const long long og = c.hidden % 8 == 0 ? 8 : 1;   // whole groups of 8 rows
     for (int s = 0; s < n_sm; s++) {
-      o_lo[s] = (int)(c.hidden * wo[s] / wo[n_sm]);
-      o_hi[s] = (int)(c.hidden * wo[s + 1] / wo[n_sm]);
+      o_lo[s] = (int)(og * (c.hidden / og * wo[s] / wo[n_sm]));
+      o_hi[s] = (int)(og * (c.hidden / og * wo[s + 1] / wo[n_sm]));
     }
   }
 
@@ -216,8 +220,11 @@ int build_plan(const mk_config& c, int n_sm, int batch, int n_attn, Plan* out, i
       }
     }
     {
+      // LM-head rows in whole groups of 8 (the last SM also takes the vocabulary's tail)
       int lo, hi;
-      share(c.vocab, n_sm, s, &lo, &hi);
+      share(c.vocab / 8, n_sm, s, &lo, &hi);
+      lo *= 8;
+      hi = s == n_sm - 1 ? c.vocab : hi * 8;
       Desc t = task(OP_FINAL, L, lo, hi);
       if (L == bump_layer) t[F_BUMP] = bump;
       list.push_back(t);

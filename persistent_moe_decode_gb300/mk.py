@@ -36,7 +36,7 @@ MK_WAVES_DEFAULT, MK_WAVES_ATTN_FIRST, MK_WAVES_INTERLEAVED = 0, 1, 2
 EXPORTS = ("mk_create", "mk_schedule_step", "mk_decode_step", "mk_step_status", "mk_get_routing",
            "mk_read_scratch", "mk_plan", "mk_debug_bump_wait", "mk_device_bytes", "mk_num_sms",
            "mk_step_upload_bytes", "mk_destroy", "mk_strerror", "mk_abi_version", "mk_read_trace",
-           "mk_decode_step_static")
+           "mk_decode_step_static", "mk_plan_step")
 
 
 class mk_config(C.Structure):
@@ -93,6 +93,7 @@ def lib():
             L.mk_read_scratch.argtypes = [vp, i32, i32, vp, C.c_size_t, C.POINTER(C.c_size_t)]
             L.mk_plan.argtypes = [C.POINTER(mk_config), i32, i32, vp, vp, C.POINTER(i32),
                                   C.POINTER(i32)]
+            L.mk_plan_step.argtypes = [C.POINTER(mk_config), i32, i32, vp, vp, vp, vp, vp, vp, vp]
             L.mk_debug_bump_wait.argtypes = [vp, i32, i32]
             L.mk_read_trace.argtypes = [vp, vp, C.c_size_t, C.POINTER(C.c_size_t)]
             L.mk_device_bytes.argtypes = [vp]
@@ -193,6 +194,27 @@ def mk_plan(cfg: mk_config, n_sm: int, batch: int):
     _check(lib().mk_plan(C.byref(cfg), int(n_sm), int(batch), _ptr(tasks), _ptr(off), None, None),
            "mk_plan")
     return tasks, off, n_bars.value
+
+
+def mk_plan_step(cfg: mk_config, n_sm: int, batch: int, seq_lens) -> dict:
+    """The host schedule of one step (see include/mk.h): task lists, split-KV
+    items and the counter-target SM counts."""
+    sl = _i32(seq_lens)
+    info = np.zeros(9, dtype=np.int32)
+    _check(lib().mk_plan_step(C.byref(cfg), int(n_sm), int(batch), _ptr(sl), _ptr(info), None, None,
+                              None, None, None), "mk_plan_step")
+    n_tasks, n_items = int(info[0]), int(info[1])
+    tasks = np.zeros((n_tasks, 32), dtype=np.int32)
+    task_off = np.zeros(n_sm + 1, dtype=np.int32)
+    items = np.zeros((max(n_items, 1), 8), dtype=np.int32)
+    item_off = np.zeros(n_sm + 1, dtype=np.int32)
+    meta = np.zeros((batch, 2), dtype=np.int32)
+    _check(lib().mk_plan_step(C.byref(cfg), int(n_sm), int(batch), _ptr(sl), _ptr(info), _ptr(tasks),
+                              _ptr(task_off), _ptr(items), _ptr(item_off), _ptr(meta)), "mk_plan_step")
+    return {"tasks": tasks, "task_off": task_off, "items": items[:n_items], "item_off": item_off,
+            "meta": meta, "n_attn": int(info[2]), "n_comb_sms": int(info[3]), "n_up_sms": int(info[4]),
+            "n_down_sms": int(info[5]), "n_rtr_sms": int(info[6]), "split": int(info[7]),
+            "n_bars": int(info[8])}
 
 
 def mk_read_trace(h) -> np.ndarray:
