@@ -263,6 +263,23 @@ int mk_debug_bump_wait(mk_handle* h, int layer, int delta);
  * the full size. */
 int mk_read_trace(mk_handle* h, void* dst, size_t bytes, size_t* size_out);
 
+/* Integer results of the last completed step, for exact checks; recorded
+ * only when the handle keeps the task timeline (config.trace_records > 0),
+ * else MK_ERR_BAD_CONFIG.  Copies min(bytes, size) bytes to the HOST buffer
+ * dst; *size_out (may be NULL) gets the full size.
+ *   MK_DEBUG_ROUTE_GROUPS  int32 [L][386]: block 0's grouping of each layer's
+ *       routing: n_act; the routed experts ascending (128 slots); the first
+ *       grouped slot of each (129 slots, the last = the entry count); the
+ *       grouped entries b * top_k + j, tokens ascending within an expert
+ *       (128 slots); unused slots -1
+ *   MK_DEBUG_PAGE_GATHER   int32 [batch][max_pages_per_seq]: the physical
+ *       page the attention streamed for each logical page in layer 0, -1 for
+ *       pages past the sequence
+ *   MK_DEBUG_NEW_SLOT      int32 [batch]: the cache slot page * page_size +
+ *       row where layer 0 wrote each sequence's new K/V */
+enum mk_debug { MK_DEBUG_ROUTE_GROUPS = 0, MK_DEBUG_PAGE_GATHER = 1, MK_DEBUG_NEW_SLOT = 2 };
+int mk_read_debug(mk_handle* h, int which, void* dst, size_t bytes, size_t* size_out);
+
 /* Words of the fixed device-resident counter block used by
  * mk_decode_step_static (256 KB per device). */
 #define MK_STATIC_COUNTER_WORDS 65536
@@ -296,6 +313,64 @@ int mk_read_trace(mk_handle* h, void* dst, size_t bytes, size_t* size_out);
  * (cudaGetSymbolAddress, with that device current) and sets the kernel's
  * shared-memory limit there; make that first call before any stream capture. */
 int mk_decode_step_static(mk_handle* h, float* logits, void* stream);
+
+/* ---------------------------------------------------------------------
+ * Decode service ("Inside the megakernel serving engine for North Mini
+ * Code", §The serving engine around the kernel: the host loop and its
+ * park / resume rule).  A loop thread owns the handle and, per step:
+ * retires the requests that have all their tokens and admits waiting ones
+ * into the free slots (only between steps: the kernel never sees a batch
+ * half updated), builds the page tables and lengths of the live slots,
+ * schedules the step for the longest live context (mk_schedule_step),
+ * launches it, picks every sequence's greedy token on the device (largest
+ * logit, ties to the lowest index) and feeds it to the next step on the
+ * device.  The host records the tokens from small asynchronous copies, a few
+ * steps later.  The loop parks when it has run the steps asked for and
+ * resumes on mk_service_run.  Requests finish after max_new_tokens tokens.
+ *
+ * While a service exists it is the only user of its handle: make no other
+ * call on the handle (except mk_destroy after mk_service_destroy).  The
+ * service functions are thread-safe.
+ */
+typedef struct mk_service mk_service;
+
+/* Start the loop thread on the handle's device (must be current).  logits:
+ * DEVICE fp32 [max_batch][V] the caller owns; each step writes its live
+ * sequences' logits there, position i = the i-th live slot.  Errors:
+ * MK_ERR_BAD_ARG, MK_ERR_OOM. */
+int mk_service_create(mk_handle* h, float* logits, mk_service** out);
+
+/* Queue a request: a sequence whose first cached_len tokens are already in
+ * the KV pools, on the caller's physical pages pages[0 .. n_pages) (HOST
+ * array, copied) in logical order, covering every position the request will
+ * write (n_pages * page_size >= cached_len + max_new_tokens); first_token is
+ * its next input token.  The pages stay the caller's; it may reuse them once
+ * the request is done.  *id_out gets the request id.  Errors: MK_ERR_BAD_ARG,
+ * MK_ERR_BAD_PAGE. */
+int mk_service_submit(mk_service* s, const int32_t* pages, int n_pages, int cached_len, int32_t first_token,
+                      int max_new_tokens, int64_t* id_out);
+
+/* Ask the loop for n_steps more steps (resume it if parked); returns at once.
+ * Returns the sticky error of an earlier step, if any. */
+int mk_service_run(mk_service* s, int n_steps);
+
+/* Block until the loop has run every step asked for and parked (the stream
+ * synchronised, every token recorded); returns MK_OK or the first error (a
+ * failed call or the device status of the last step). */
+int mk_service_wait(mk_service* s);
+
+/* The tokens request `id` has generated so far (HOST int32, up to cap), their
+ * count and whether the request is done.  Call after mk_service_wait for a
+ * complete record. */
+int mk_service_result(mk_service* s, int64_t id, int32_t* tokens, int cap, int* n_out, int* done);
+
+/* The last step's batch, position by position (HOST arrays of max_batch, any
+ * may be NULL): request ids, cached lengths before the step, input tokens;
+ * *batch gets its size.  Call after mk_service_wait. */
+int mk_service_batch(mk_service* s, int64_t* ids, int32_t* seq_lens, int32_t* tokens, int* batch);
+
+/* Stop the loop (after the step in flight) and free the service. */
+void mk_service_destroy(mk_service* s);
 
 /* Library-owned device bytes (counters, scratch, queues, task lists). */
 size_t mk_device_bytes(const mk_handle* h);

@@ -35,7 +35,8 @@ def _cuda_home() -> str:
 
 
 def _sources():
-    return [os.path.join(CSRC, f) for f in ("mk_kernel.cu", "mk_static.cu", "mk_sched.cpp", "mk_api.cpp")]
+    return [os.path.join(CSRC, f) for f in ("mk_kernel.cu", "mk_static.cu", "mk_service.cu", "mk_sched.cpp",
+                                             "mk_api.cpp")]
 
 
 def _deps():

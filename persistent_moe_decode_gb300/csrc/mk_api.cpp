@@ -84,6 +84,8 @@ struct mk_handle {
   size_t bar_words = 0;
   int32_t* d_trace = nullptr;
   size_t trace_words = 0;
+  int32_t* d_dbg = nullptr;
+  size_t dbg_words = 0;
 };
 
 namespace {
@@ -489,6 +491,9 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
     TRY(dalloc(h, &h->d_trace, h->trace_words));
     p.trace = h->d_trace;
     p.trace_cap = c.trace_records;
+    h->dbg_words = (size_t)L * kDbgRouteWords + Bs * c.max_pages_per_seq + Bs;
+    TRY(dalloc(h, &h->d_dbg, h->dbg_words));
+    p.dbg = h->d_dbg;
   }
   if (cudaMemset(h->d_bars, 0, h->bar_words * 4) != cudaSuccess) { mk_destroy(h); return MK_ERR_CUDA; }
   h->step_bytes_cap = step_upload_bytes(c, h->n_sm, Bm, c.max_attn_items);
@@ -618,7 +623,8 @@ int mk_decode_step(mk_handle* h, float* logits, void* stream) {
   if (rc) return rc;
   cudaStream_t sm = (cudaStream_t)stream;
   if (cudaMemsetAsync(h->d_bars, 0, h->bar_words * 4, sm) != cudaSuccess) return MK_ERR_CUDA;
-  if (h->d_trace && cudaMemsetAsync(h->d_trace, 0xff, h->trace_words * 4, sm) != cudaSuccess)
+  if (h->d_trace && (cudaMemsetAsync(h->d_trace, 0xff, h->trace_words * 4, sm) != cudaSuccess ||
+                     cudaMemsetAsync(h->d_dbg, 0xff, h->dbg_words * 4, sm) != cudaSuccess))
     return MK_ERR_CUDA;
   const Params p = step_params(h, *plan, logits);
   if (launch_step(p, h->n_sm, sm) != cudaSuccess) {
@@ -645,7 +651,8 @@ int mk_decode_step_static(mk_handle* h, float* logits, void* stream) {
   if (rc) return rc;
   cudaStream_t sm = (cudaStream_t)stream;
   if (cudaMemsetAsync(ctr, 0, h->bar_words * 4, sm) != cudaSuccess) return MK_ERR_CUDA;
-  if (h->d_trace && cudaMemsetAsync(h->d_trace, 0xff, h->trace_words * 4, sm) != cudaSuccess)
+  if (h->d_trace && (cudaMemsetAsync(h->d_trace, 0xff, h->trace_words * 4, sm) != cudaSuccess ||
+                     cudaMemsetAsync(h->d_dbg, 0xff, h->dbg_words * 4, sm) != cudaSuccess))
     return MK_ERR_CUDA;
   Params p = step_params(h, it->second, logits);
   p.err = ctr;
@@ -744,6 +751,27 @@ int mk_read_trace(mk_handle* h, void* dst, size_t bytes, size_t* size_out) {
   return MK_OK;
 }
 
+int mk_read_debug(mk_handle* h, int which, void* dst, size_t bytes, size_t* size_out) {
+  if (!h) return MK_ERR_BAD_ARG;
+  if (!h->d_dbg) return MK_ERR_BAD_CONFIG;
+  if (h->last_batch < 1) return MK_ERR_NOT_SCHEDULED;
+  const mk_config& c = h->cfg;
+  const size_t route = (size_t)c.n_layers * kDbgRouteWords, pages = (size_t)c.max_batch * c.max_pages_per_seq;
+  size_t off = 0, words = 0;
+  switch (which) {
+    case MK_DEBUG_ROUTE_GROUPS: off = 0; words = route; break;
+    case MK_DEBUG_PAGE_GATHER: off = route; words = (size_t)h->last_batch * c.max_pages_per_seq; break;
+    case MK_DEBUG_NEW_SLOT: off = route + pages; words = (size_t)h->last_batch; break;
+    default: return MK_ERR_BAD_ARG;
+  }
+  if (size_out) *size_out = words * 4;
+  if (dst && cudaMemcpy(dst, h->d_dbg + off, std::min(bytes, words * 4), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  return MK_OK;
+}
+
 int mk_debug_bump_wait(mk_handle* h, int layer, int delta) {
   if (!h || layer < 0 || layer > h->cfg.n_layers) return MK_ERR_BAD_ARG;
   cudaDeviceSynchronize();
@@ -752,6 +780,18 @@ int mk_debug_bump_wait(mk_handle* h, int layer, int delta) {
   free_plans(h);
   return MK_OK;
 }
+
+}  // extern "C"
+
+namespace mk {
+// for the decode service (same library): the step's device token buffer and
+// the handle's config and device
+int32_t* handle_tokens(mk_handle* h) { return h->d_tokens; }
+const mk_config* handle_config(const mk_handle* h) { return &h->cfg; }
+int handle_device(const mk_handle* h) { return h->device; }
+}  // namespace mk
+
+extern "C" {
 
 size_t mk_device_bytes(const mk_handle* h) { return h ? h->dev_bytes : 0; }
 int mk_num_sms(const mk_handle* h) { return h ? h->n_sm : 0; }

@@ -422,6 +422,8 @@ struct Prod {
       for (int q = 0; q < cn; q += pps) {
         const int n = min(pps, cn - q);
         const int pg = __shfl_sync(0xffffffffu, id, q + (lane % n));
+        if (TR && p.dbg && l == 0 && lane < n)
+          p.dbg[(size_t)p.L * kDbgRouteWords + (size_t)b * p.max_pages + pg0 + c0 + q + lane] = pg;
         const bool bad = (lane < 2 * n) && (pg < 0 || pg >= p.num_pages);
         if (__any_sync(0xffffffffu, bad)) {
           if (bad) report(p, DEV_BAD_PAGE, ti, OP_ATTN, -1, (uint32_t)pg, (uint32_t)p.num_pages);
@@ -509,6 +511,16 @@ struct Prod {
     if (!warp_spin(bar_index(p, l, p.bl.rtr), (uint32_t)p.n_rtr_sms)) return false;
     route_one(p, S.rt, l, lane, blockIdx.x == 0);
     route_seen = l + 1;
+    if (TR && p.dbg && blockIdx.x == 0) {
+      int32_t* d = p.dbg + (size_t)l * kDbgRouteWords;
+      const int n = S.rt.n_act;
+      if (lane == 0) d[0] = n;
+      for (int i = lane; i < n; i += 32) {
+        d[1 + i] = S.rt.act[i];
+        d[1 + kMaxActive + 1 + kMaxActive + i] = S.rt.ent[i];
+      }
+      for (int i = lane; i <= n; i += 32) d[1 + kMaxActive + i] = S.rt.off[i];
+    }
     return true;
   }
 
@@ -1768,6 +1780,14 @@ struct Cons {
           if (rt.idx[n][j] == e) rt.ent[i++] = n * K + j;
     }
     if (!csync()) return false;
+    if (TR && p.dbg && blockIdx.x == 0) {
+      int32_t* d = p.dbg + (size_t)l * kDbgRouteWords;
+      const int n = rt.n_act;
+      if (tid == 0) d[0] = n;
+      for (int i = tid; i < n; i += 256) d[1 + i] = rt.act[i];
+      for (int i = tid; i <= n; i += 256) d[1 + kMaxActive + i] = rt.off[i];
+      for (int i = tid; i < rt.off[n]; i += 256) d[1 + kMaxActive + 1 + kMaxActive + i] = rt.ent[i];
+    }
     if (tid == 0) mbar_arrive(&S.route_bar);   // the producer may now resolve the experts
     return true;
   }
@@ -1906,6 +1926,8 @@ struct Cons {
           const float* krw = qraw + (size_t)(hq + g) * D;
           const float* vrw = qraw + (size_t)(hq + hkv + g) * D;
           const int pg = p.page_tables[(size_t)b * p.max_pages + pos / P];
+          if (TR && p.dbg && l == 0 && g == 0 && lane == 0)
+            p.dbg[(size_t)p.L * kDbgRouteWords + (size_t)p.Bmax * p.max_pages + b] = pg * P + row;
           uint16_t* kcache = p.k_pool[l] + (((size_t)pg * hkv + g) * P + row) * D;
           uint16_t* vcache = p.v_pool[l] + (((size_t)pg * hkv + g) * P + row) * D;
           const int r = g * P + row;

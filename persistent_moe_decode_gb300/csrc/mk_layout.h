@@ -81,6 +81,7 @@ constexpr int kTraceWords = 16;         // words per timeline record
 constexpr int kPartFloats = 2048;       // one of the two GEMV partial-sum buffers
 constexpr int kTokPass = 8;             // tokens per GEMV pass (activations in registers)
 constexpr int kMaxActive = 128;         // routed experts of one step (B * k <= 128)
+constexpr int kDbgRouteWords = 1 + kMaxActive + (kMaxActive + 1) + kMaxActive;   // 386
 
 // whole rows of a [rows][K] BF16 matrix that one stage carries
 MK_HD inline int rows_per_stage(int K) {
@@ -197,6 +198,11 @@ struct Params {
   unsigned long long timeout_ns;
   int32_t* trace;      // [n_sm][trace_cap][kTraceWords] task timeline (nullptr: off)
   int trace_cap;
+  int32_t* dbg;        // with the timeline: integer results for exact checks (nullptr: off)
+                       //   [L][kDbgRouteWords] block 0's grouping of each layer's routing:
+                       //     n_act, act[128], off[129], ent[128];
+                       //   then [Bmax][max_pages] the physical pages layer 0 streamed;
+                       //   then [Bmax] the cache slot (page * P + row) of each new token
   // scratch; per-layer strides use Bmax; activations are fp32
   float* hloc;       // [n_sm][Bmax][H]  each SM's own copy of the residual stream
   float* xloc;       // [n_sm][Bmax][H]  each SM's own normalised layer input

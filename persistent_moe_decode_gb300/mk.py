@@ -31,12 +31,15 @@ MK_ERR_DEVICE = -9
 MK_WAVES_DEFAULT, MK_WAVES_ATTN_FIRST, MK_WAVES_INTERLEAVED = 0, 1, 2
 (MK_SCRATCH_H, MK_SCRATCH_X, MK_SCRATCH_QKV, MK_SCRATCH_ATTN, MK_SCRATCH_ROUTER,
  MK_SCRATCH_OPROJ, MK_SCRATCH_MOE) = range(7)
+MK_DEBUG_ROUTE_GROUPS, MK_DEBUG_PAGE_GATHER, MK_DEBUG_NEW_SLOT = range(3)
 
 # every symbol include/mk.h declares
 EXPORTS = ("mk_create", "mk_schedule_step", "mk_decode_step", "mk_step_status", "mk_get_routing",
            "mk_read_scratch", "mk_plan", "mk_debug_bump_wait", "mk_device_bytes", "mk_num_sms",
            "mk_step_upload_bytes", "mk_destroy", "mk_strerror", "mk_abi_version", "mk_read_trace",
-           "mk_decode_step_static", "mk_plan_step")
+           "mk_decode_step_static", "mk_plan_step", "mk_read_debug", "mk_service_create",
+           "mk_service_submit", "mk_service_run", "mk_service_wait", "mk_service_result",
+           "mk_service_batch", "mk_service_destroy")
 
 
 class mk_config(C.Structure):
@@ -96,6 +99,15 @@ def lib():
             L.mk_plan_step.argtypes = [C.POINTER(mk_config), i32, i32, vp, vp, vp, vp, vp, vp, vp]
             L.mk_debug_bump_wait.argtypes = [vp, i32, i32]
             L.mk_read_trace.argtypes = [vp, vp, C.c_size_t, C.POINTER(C.c_size_t)]
+            L.mk_read_debug.argtypes = [vp, i32, vp, C.c_size_t, C.POINTER(C.c_size_t)]
+            L.mk_service_create.argtypes = [vp, vp, C.POINTER(vp)]
+            L.mk_service_submit.argtypes = [vp, vp, i32, i32, i32, i32, C.POINTER(C.c_int64)]
+            L.mk_service_run.argtypes = [vp, i32]
+            L.mk_service_wait.argtypes = [vp]
+            L.mk_service_result.argtypes = [vp, C.c_int64, vp, i32, C.POINTER(i32), C.POINTER(i32)]
+            L.mk_service_batch.argtypes = [vp, vp, vp, vp, C.POINTER(i32)]
+            L.mk_service_destroy.argtypes = [vp]
+            L.mk_service_destroy.restype = None
             L.mk_device_bytes.argtypes = [vp]
             L.mk_device_bytes.restype = C.c_size_t
             L.mk_num_sms.argtypes = [vp]
@@ -225,6 +237,14 @@ def mk_read_trace(h) -> np.ndarray:
     return out.reshape(-1, 16)
 
 
+def mk_read_debug(h, which: int) -> np.ndarray:
+    size = C.c_size_t(0)
+    _check(lib().mk_read_debug(h, int(which), None, 0, C.byref(size)), "mk_read_debug")
+    out = np.empty(size.value // 4, dtype=np.int32)
+    _check(lib().mk_read_debug(h, int(which), _ptr(out), size.value, None), "mk_read_debug")
+    return out
+
+
 def mk_debug_bump_wait(h, layer: int, delta: int) -> int:
     return _check(lib().mk_debug_bump_wait(h, int(layer), int(delta)), "mk_debug_bump_wait")
 
@@ -244,6 +264,50 @@ def mk_step_upload_bytes(h, batch: int) -> int:
 def mk_destroy(h) -> None:
     if h:
         lib().mk_destroy(h)
+
+
+def mk_service_create(h, logits_ptr: int):
+    s = C.c_void_p()
+    _check(lib().mk_service_create(h, C.c_void_p(int(logits_ptr)), C.byref(s)), "mk_service_create")
+    return s
+
+
+def mk_service_submit(s, pages, cached_len: int, first_token: int, max_new_tokens: int) -> int:
+    pg = _i32(pages)
+    rid = C.c_int64(0)
+    _check(lib().mk_service_submit(s, _ptr(pg), int(pg.size), int(cached_len), int(first_token),
+                                   int(max_new_tokens), C.byref(rid)), "mk_service_submit")
+    return int(rid.value)
+
+
+def mk_service_run(s, n_steps: int) -> int:
+    return _check(lib().mk_service_run(s, int(n_steps)), "mk_service_run")
+
+
+def mk_service_wait(s) -> int:
+    return _check(lib().mk_service_wait(s), "mk_service_wait")
+
+
+def mk_service_result(s, rid: int, cap: int = 4096):
+    out = np.empty(cap, dtype=np.int32)
+    n, done = C.c_int(0), C.c_int(0)
+    _check(lib().mk_service_result(s, C.c_int64(rid), _ptr(out), int(cap), C.byref(n), C.byref(done)),
+           "mk_service_result")
+    return out[:min(n.value, cap)].copy(), bool(done.value)
+
+
+def mk_service_batch(s, max_batch: int):
+    ids = np.zeros(max_batch, dtype=np.int64)
+    lens = np.zeros(max_batch, dtype=np.int32)
+    toks = np.zeros(max_batch, dtype=np.int32)
+    b = C.c_int(0)
+    _check(lib().mk_service_batch(s, _ptr(ids), _ptr(lens), _ptr(toks), C.byref(b)), "mk_service_batch")
+    return ids[:b.value].copy(), lens[:b.value].copy(), toks[:b.value].copy()
+
+
+def mk_service_destroy(s) -> None:
+    if s:
+        lib().mk_service_destroy(s)
 
 
 # ---------------------------------------------------------- convenience
