@@ -341,6 +341,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-b16", action="store_true",
                     help="a3b_8k: skip the batch-16 line measured on the same model")
+    ap.add_argument("--waves", default=None, choices=["default", "attn_first", "interleaved"],
+                    help="schedule ablation: every SM runs every phase in this wave order (no roles)")
+    ap.add_argument("--attn-sms", type=int, default=0,
+                    help="schedule ablation: SMs on the attention branch (0 = chosen per step)")
+    ap.add_argument("--kv-split", type=int, default=0,
+                    help="schedule ablation: split-KV chunk in tokens (0 = one run per attention SM)")
+    ap.add_argument("--moe-depth", type=int, default=0,
+                    help="schedule ablation: stages an expert-branch SM keeps in flight (0 = per step)")
     ap.add_argument("--ref-layers", type=int, default=2)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
@@ -372,7 +380,19 @@ def main():
     from persistent_moe_decode_gb300.runner import StepRunner
 
     dims = wl.dims
-    run = StepRunner(wl.with_(seed=wl.seed + rank), device=f"cuda:{local}")
+    sched = {}
+    if args.waves:
+        from persistent_moe_decode_gb300 import mk
+        sched["n_attn_claimers"] = 1 << 20
+        sched["wave_order"] = {"default": mk.MK_WAVES_DEFAULT, "attn_first": mk.MK_WAVES_ATTN_FIRST,
+                               "interleaved": mk.MK_WAVES_INTERLEAVED}[args.waves]
+    elif args.attn_sms:
+        sched["n_attn_claimers"] = args.attn_sms
+    if args.kv_split:
+        sched["kv_split_tokens"] = args.kv_split
+    if args.moe_depth:
+        sched["moe_stage_depth"] = args.moe_depth
+    run = StepRunner(wl.with_(seed=wl.seed + rank), device=f"cuda:{local}", **sched)
     stream = torch.cuda.current_stream()
     B = wl.batch
     rng = np.random.default_rng(1234 + rank)
@@ -401,7 +421,7 @@ def main():
     # the metric names batch 1 and batch 16: with the 30B/3.3B model at batch 1,
     # the batch-16 continuous-batching workload runs on the same weights
     b16 = None
-    if wl.name == "a3b_8k" and not args.layers and not args.no_b16:
+    if wl.name == "a3b_8k" and not args.layers and not args.no_b16 and not sched:
         wl16 = WORKLOADS["a3b_b16"]
         run16 = StepRunner(wl16.with_(seed=wl16.seed + rank), device=f"cuda:{local}", model=run.model)
         tok16 = rng.integers(0, dims.vocab, size=(args.warmup + args.steps, 16)).astype(np.int32)
@@ -425,7 +445,11 @@ def main():
                    "context_note": "cached tokens at the first timed step",
                    "layers": dims.n_layers,
                    "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB read per step)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "schedule": ({"waves": args.waves} if args.waves else
+                                {"attention_sms": args.attn_sms or "per step"})
+                               | ({"kv_split_tokens": args.kv_split} if args.kv_split else {})
+                               | ({"moe_stage_depth": args.moe_depth} if args.moe_depth else {})},
         "sol_frac": {"of_measured_hbm": roof["frac"], "of_nominal_8tbs": roof["achieved"] / 8000.0},
         "roofline": roof,
         "cpu_baseline": cpu,

@@ -102,6 +102,12 @@ typedef struct {
   int sm_cap;             /* use at most this many SMs; 0 = all                  */
   int timeout_ms;         /* device spin limit per wait; 0 = 2000                */
   int trace_records;      /* per-SM task timeline records kept; 0 = tracing off  */
+  int moe_stage_depth;    /* batch 1: weight stages an expert-branch SM keeps in
+                             flight (1..5); 0 = chosen per step: 3 when the
+                             expert branch has more SMs than the attention
+                             branch (its streams would otherwise take HBM
+                             bandwidth from the attention branch, which is on
+                             the critical path), else 5                      */
 } mk_config;
 
 /*

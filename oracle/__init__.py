@@ -86,6 +86,9 @@ def lib():
             L.orc_decode_step.argtypes = [C.POINTER(_Dims), C.POINTER(_Model), i32, vp, vp, vp,
                                           i32, C.c_uint, vp, C.POINTER(_Trace)]
             L.orc_decode_step.restype = i32
+            L.orc_decode_step_forced.argtypes = [C.POINTER(_Dims), C.POINTER(_Model), i32, vp, vp, vp,
+                                                 i32, C.c_uint, vp, vp, vp, C.POINTER(_Trace)]
+            L.orc_decode_step_forced.restype = i32
             L.orc_run_layers.argtypes = [C.POINTER(_Dims), C.POINTER(_Model), i32, i32, i32,
                                          vp, vp, i32, C.c_uint, vp]
             L.orc_run_layers.restype = i32
@@ -243,7 +246,10 @@ class Oracle:
                       _p(w), int(flags), _p(out))
         return out
 
-    def decode_step(self, tokens, seq_lens, page_tables, flags: int = 0, trace: bool = False):
+    def decode_step(self, tokens, seq_lens, page_tables, flags: int = 0, trace: bool = False,
+                    force=None):
+        """One step; ``force`` = (idx int32 [L, B, k], mask bool [L, B]) imposes
+        those experts where mask is set (orc_decode_step_forced)."""
         d = self.dims
         B = len(tokens)
         L, H, E, K = d["n_layers"], d["hidden"], d["n_experts"], d["top_k"]
@@ -263,9 +269,17 @@ class Oracle:
                    "gap": np.zeros((L, B)), "moe": np.zeros((L, B, H)),
                    "xf": np.zeros((B, H))}
             tr = _Trace(**{n: a.ctypes.data for n, a in out.items()})
-        rc = lib().orc_decode_step(C.byref(self._dm), C.byref(self._m), B, _p(tok), _p(sl),
-                                   _p(pt), pt.shape[1], int(flags), _p(logits),
-                                   C.byref(tr) if tr is not None else None)
+        if force is not None:
+            fidx = np.ascontiguousarray(force[0], dtype=np.int32)
+            fmask = np.ascontiguousarray(force[1], dtype=np.uint8)
+            assert fidx.shape == (L, B, K) and fmask.shape == (L, B)
+            rc = lib().orc_decode_step_forced(C.byref(self._dm), C.byref(self._m), B, _p(tok), _p(sl),
+                                              _p(pt), pt.shape[1], int(flags), _p(fidx), _p(fmask),
+                                              _p(logits), C.byref(tr) if tr is not None else None)
+        else:
+            rc = lib().orc_decode_step(C.byref(self._dm), C.byref(self._m), B, _p(tok), _p(sl),
+                                       _p(pt), pt.shape[1], int(flags), _p(logits),
+                                       C.byref(tr) if tr is not None else None)
         if rc != 0:
             raise RuntimeError(f"orc_decode_step failed: {rc}")
         return (logits, out) if trace else logits

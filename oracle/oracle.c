@@ -218,9 +218,16 @@ void orc_moe(const orc_dims* dm, const orc_model* m, int layer, const double* x,
 /* ----------------------------------------------------- one layer, batch */
 typedef struct { double *x, *qkv, *att, *ap, *rl, *mo, *wt; int32_t* idx; } layer_bufs;
 
+/* Routing imposed from outside (for comparing with an implementation that
+ * decided a near tie the other way): where force[l * B + b] is set, token b
+ * of layer l uses the experts force_idx[(l * B + b) * k + j] instead of its
+ * own top-k, with the routing weights renormalised over them as usual. */
+typedef struct { const int32_t* idx; const uint8_t* mask; } orc_force;
+
 static int layer_body(const orc_dims* dm, const orc_model* m, int l, int B,
                       const int32_t* seq_lens, const int32_t* page_tables, int max_pages,
-                      unsigned flags, double* h, orc_trace* tr, const layer_bufs* bf) {
+                      unsigned flags, double* h, orc_trace* tr, const layer_bufs* bf,
+                      const orc_force* fr) {
   const int H = dm->hidden, hq = dm->n_q_heads, hkv = dm->n_kv_heads, d = dm->head_dim;
   const int E = dm->n_experts, K = dm->top_k, P = dm->page_size, L = dm->n_layers;
   const int QD = hq * d, R = (hq + 2 * hkv) * d, grp = hq / hkv;
@@ -296,6 +303,22 @@ static int layer_body(const orc_dims* dm, const orc_model* m, int l, int B,
     double gap;
     orc_route(E, K, rl + (size_t)b * E, idx + (size_t)b * K, wt + (size_t)b * K, &gap);
     if (tr && tr->gap) tr->gap[(size_t)l * B + b] = gap;
+    if (fr && fr->mask[(size_t)l * B + b]) {
+      /* the imposed experts; weights p_j / sum of p over them, p = softmax of
+       * the logits (the same operations as orc_route's) */
+      const double* r = rl + (size_t)b * E;
+      const int32_t* fi = fr->idx + ((size_t)l * B + b) * K;
+      double mx = -INFINITY, den = 0.0, sel = 0.0;
+      for (int e = 0; e < E; e++) if (r[e] > mx) mx = r[e];
+      for (int e = 0; e < E; e++) den += exp(r[e] - mx);
+      for (int j = 0; j < K; j++) {
+        if (fi[j] < 0 || fi[j] >= E) return ORC_ERR_ARG;
+        idx[(size_t)b * K + j] = fi[j];
+        wt[(size_t)b * K + j] = exp(r[fi[j]] - mx) / den;
+        sel += wt[(size_t)b * K + j];
+      }
+      for (int j = 0; j < K; j++) wt[(size_t)b * K + j] /= sel;
+    }
     orc_moe(dm, m, l, x + (size_t)b * H, K, idx + (size_t)b * K, wt + (size_t)b * K, flags,
             mo + (size_t)b * H);
   }
@@ -313,7 +336,7 @@ static int layer_body(const orc_dims* dm, const orc_model* m, int l, int B,
 
 static int layer_forward(const orc_dims* dm, const orc_model* m, int l, int B,
                          const int32_t* seq_lens, const int32_t* page_tables, int max_pages,
-                         unsigned flags, double* h, orc_trace* tr) {
+                         unsigned flags, double* h, orc_trace* tr, const orc_force* fr) {
   const int H = dm->hidden, QD = dm->n_q_heads * dm->head_dim;
   const int R = (dm->n_q_heads + 2 * dm->n_kv_heads) * dm->head_dim;
   layer_bufs bf;
@@ -327,7 +350,7 @@ static int layer_forward(const orc_dims* dm, const orc_model* m, int l, int B,
   bf.wt = (double*)malloc(sizeof(double) * (size_t)B * dm->top_k);
   int rc = ORC_ERR_NOMEM;
   if (bf.x && bf.qkv && bf.att && bf.ap && bf.rl && bf.mo && bf.idx && bf.wt)
-    rc = layer_body(dm, m, l, B, seq_lens, page_tables, max_pages, flags, h, tr, &bf);
+    rc = layer_body(dm, m, l, B, seq_lens, page_tables, max_pages, flags, h, tr, &bf, fr);
   free(bf.x); free(bf.qkv); free(bf.att); free(bf.ap); free(bf.rl); free(bf.mo);
   free(bf.idx); free(bf.wt);
   return rc;
@@ -348,7 +371,7 @@ int orc_run_layers(const orc_dims* dm, const orc_model* m, int l0, int l1, int b
                    unsigned flags, double* h) {
   if (check_dims(dm) != ORC_OK || batch <= 0 || l0 < 0 || l1 > dm->n_layers) return ORC_ERR_ARG;
   for (int l = l0; l < l1; l++) {
-    int rc = layer_forward(dm, m, l, batch, seq_lens, page_tables, max_pages, flags, h, NULL);
+    int rc = layer_forward(dm, m, l, batch, seq_lens, page_tables, max_pages, flags, h, NULL, NULL);
     if (rc != ORC_OK) return rc;
   }
   return ORC_OK;
@@ -357,10 +380,14 @@ int orc_run_layers(const orc_dims* dm, const orc_model* m, int l0, int l1, int b
 /* -------------------------------------------------- one decode step
  * h = embed[token]; for every layer the parallel block above; then
  * logits = W_lm RMSNorm(h; g_f). */
-int orc_decode_step(const orc_dims* dm, const orc_model* m, int batch, const int32_t* tokens,
-                    const int32_t* seq_lens, const int32_t* page_tables, int max_pages,
-                    unsigned flags, double* logits, orc_trace* trace) {
+int orc_decode_step_forced(const orc_dims* dm, const orc_model* m, int batch, const int32_t* tokens,
+                           const int32_t* seq_lens, const int32_t* page_tables, int max_pages,
+                           unsigned flags, const int32_t* force_idx, const uint8_t* force_mask,
+                           double* logits, orc_trace* trace) {
   if (check_dims(dm) != ORC_OK || batch <= 0) return ORC_ERR_ARG;
+  if ((force_idx == NULL) != (force_mask == NULL)) return ORC_ERR_ARG;
+  orc_force fr = {force_idx, force_mask};
+  const orc_force* frp = force_idx ? &fr : NULL;
   const int H = dm->hidden, V = dm->vocab;
   double* h = (double*)malloc(sizeof(double) * (size_t)batch * H);
   double* xf = (double*)malloc(sizeof(double) * (size_t)batch * H);
@@ -372,7 +399,7 @@ int orc_decode_step(const orc_dims* dm, const orc_model* m, int batch, const int
     for (int i = 0; i < H; i++) h[(size_t)b * H + i] = orc_bf16_to_double(er[i]);
   }
   for (int l = 0; l < dm->n_layers; l++) {
-    rc = layer_forward(dm, m, l, batch, seq_lens, page_tables, max_pages, flags, h, trace);
+    rc = layer_forward(dm, m, l, batch, seq_lens, page_tables, max_pages, flags, h, trace, frp);
     if (rc != ORC_OK) goto out;
   }
   for (int b = 0; b < batch; b++) {
@@ -385,4 +412,11 @@ int orc_decode_step(const orc_dims* dm, const orc_model* m, int batch, const int
 out:
   free(h); free(xf);
   return rc;
+}
+
+int orc_decode_step(const orc_dims* dm, const orc_model* m, int batch, const int32_t* tokens,
+                    const int32_t* seq_lens, const int32_t* page_tables, int max_pages,
+                    unsigned flags, double* logits, orc_trace* trace) {
+  return orc_decode_step_forced(dm, m, batch, tokens, seq_lens, page_tables, max_pages, flags, NULL, NULL,
+                                logits, trace);
 }

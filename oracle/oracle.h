@@ -98,6 +98,16 @@ int orc_decode_step(const orc_dims* dm, const orc_model* m, int batch, const int
                     const int32_t* seq_lens, const int32_t* page_tables, int max_pages,
                     unsigned flags, double* logits, orc_trace* trace);
 
+/* orc_decode_step with routing imposed where force_mask [L][B] is non-zero:
+ * token b of layer l then uses the experts force_idx [L][B][k] (instead of its
+ * own top-k), its weights renormalised over them.  Both NULL = orc_decode_step.
+ * For comparing with an implementation that decided a near tie (a k-th /
+ * (k+1)-th router gap within its rounding) the other way. */
+int orc_decode_step_forced(const orc_dims* dm, const orc_model* m, int batch, const int32_t* tokens,
+                           const int32_t* seq_lens, const int32_t* page_tables, int max_pages,
+                           unsigned flags, const int32_t* force_idx, const uint8_t* force_mask,
+                           double* logits, orc_trace* trace);
+
 /* Subset of the step used to time the oracle on a bounded sample: runs layers
  * [l0, l1) on the residual h [B][H] in place (no embedding, no LM head). */
 int orc_run_layers(const orc_dims* dm, const orc_model* m, int l0, int l1, int batch,

@@ -100,6 +100,9 @@ WORKLOADS = {
                         ragged=(1024, 32768), churn=True, join_context=1024),
     # same model, batch 1 at 256K cached tokens, 32 steps
     "a3b_256k": Workload("a3b_256k", A3B, batch=1, context=262144, steps=32),
+    # the same model at batch 2 and 4, 8K context each (the schedule ablation)
+    "a3b_8k_b2": Workload("a3b_8k_b2", A3B, batch=2, context=8192, steps=128),
+    "a3b_8k_b4": Workload("a3b_8k_b4", A3B, batch=4, context=8192, steps=128),
     # small multi-sequence cases for the parity tests: ragged contexts with
     # churn, one token pass (5 sequences) and two passes (12, 16 sequences)
     "tiny_b5": Workload("tiny_b5", TINY, batch=5, context=0, steps=6, ragged=(10, 300),
@@ -108,6 +111,12 @@ WORKLOADS = {
                          churn=True, join_context=17),
     "mid_b16": Workload("mid_b16", MID, batch=16, context=0, steps=3, ragged=(64, 2048),
                         churn=True, join_context=100),
+    # few sequences (the tensor-core GEMVs of dense rows with up to 8 / 4 tokens):
+    # the mid model at batch 4, the 30B/3.3B shape cut to 4 layers at batch 3
+    "mid_b4": Workload("mid_b4", MID, batch=4, context=0, steps=3, ragged=(64, 2048),
+                       churn=True, join_context=100),
+    "a3b4_b3": Workload("a3b4_b3", replace(A3B, n_layers=4), batch=3, context=0, steps=3,
+                        ragged=(200, 1500), churn=True, join_context=100),
 }
 
 

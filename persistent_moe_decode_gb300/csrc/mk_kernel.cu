@@ -310,8 +310,14 @@ struct Prod {
   const uint16_t* cur = nullptr;
   const uint16_t* nxt = nullptr;
   int ptr_layer = -1;
+  // stages this SM keeps in flight: the whole ring, or moe_depth on an SM
+  // without attention items (the expert branch)
+  uint32_t depth = kStages;
 
-  __device__ __forceinline__ Prod(const Params& pp, Smem& ss) : p(pp), S(ss), lane(threadIdx.x & 31) {}
+  __device__ __forceinline__ Prod(const Params& pp, Smem& ss) : p(pp), S(ss), lane(threadIdx.x & 31) {
+    if (ONE && p.attn_sm_off[blockIdx.x] == p.attn_sm_off[blockIdx.x + 1] && p.moe_depth > 0)
+      depth = (uint32_t)min(p.moe_depth, kStages);
+  }
 
   __device__ __forceinline__ const uint16_t* load_ptr(int layer) const {
     if (layer >= p.L || lane >= 6) return nullptr;
@@ -357,7 +363,14 @@ struct Prod {
 
   __device__ __forceinline__ bool acquire_stage(uint32_t& slot) {
     slot = stage_seq % kStages;
-    const bool ok = wait_phase(p, &S.empty[slot], ((stage_seq / kStages) & 1u) ^ 1u);
+    bool ok = wait_phase(p, &S.empty[slot], ((stage_seq / kStages) & 1u) ^ 1u);
+    // an expert-branch SM keeps at most moe_depth stages in flight: stage
+    // stage_seq - moe_depth must have been consumed (its slot's phase of that
+    // round has completed)
+    if (ONE && ok && depth < (uint32_t)kStages && stage_seq >= depth) {
+      const uint32_t n = stage_seq - depth;
+      ok = wait_phase(p, &S.empty[n % kStages], (n / kStages) & 1u);
+    }
     if (TR && lane == 0 && task_seq > 0) {
       // the copy is issued next (after the mbarrier's release, which orders this word)
       int32_t* w = S.task[(task_seq - 1) % kTaskSlots];
@@ -371,18 +384,22 @@ struct Prod {
   // columns) a 3-D tensor copy through the matrix's map, which lands the
   // stage swizzled for the tensor-core GEMV (a whole box: rows past a short
   // last stage are copied too, or zero-filled past the matrix)
+  // (map_row0: the first row's index in the map, when it differs from row0;
+  // box_rows: rows of one box, 0 = a full 32 KB stage of rows)
   __device__ __forceinline__ bool stream_rows(const uint16_t* w, int row0, int nrows, int K,
-                                              const uint8_t* map = nullptr) {
-    const int rps = rows_per_stage(K);
-    const bool rot = ONE && rotated_rows(K);
+                                              const uint8_t* map = nullptr, int map_row0 = -1,
+                                              int box_rows = 0) {
+    const bool rot = map != nullptr;
+    const int rps = rot && box_rows > 0 ? box_rows : rows_per_stage(K);
+    const int mrow0 = map_row0 >= 0 ? map_row0 : row0;
     for (int done = 0; done < nrows; done += rps) {
       const int rows = min(rps, nrows - done);
       uint32_t slot;
       if (!acquire_stage(slot)) return false;
       if (lane == 0) {
         if (rot) {
-          mbar_arrive_expect_tx(&S.full[slot], (uint32_t)kStageBytes);
-          tma_load_3d_hint(&S.stage[slot][0], map, 0, row0 + done, 0, &S.full[slot], policy_evict_first());
+          mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(rps * K * 2));
+          tma_load_3d_hint(&S.stage[slot][0], map, 0, mrow0 + done, 0, &S.full[slot], policy_evict_first());
         } else {
           const uint32_t bytes = (uint32_t)(rows * K * 2);
           mbar_arrive_expect_tx(&S.full[slot], bytes);
@@ -448,7 +465,9 @@ struct Prod {
 
   // one GEMV chunk of nblk blocks x nrows rows: publish, then stream each block
   __device__ __forceinline__ bool chunk(int kind, int flags, int row0, int nrows, int nblk, int K, int nt,
-                                        int a, int e, int rel0, const uint16_t* w0, const uint16_t* w1) {
+                                        int a, int e, int rel0, const uint16_t* w0, const uint16_t* w1,
+                                        const uint8_t* m0 = nullptr, const uint8_t* m1 = nullptr,
+                                        int map_row0 = -1, int box_rows = 0) {
     int32_t* w = begin();
     if (!w) return false;
     if (lane == 0) {
@@ -464,20 +483,27 @@ struct Prod {
       w[R_REL0] = rel0;
     }
     commit();
-    if (nrows > 0 && !stream_rows(w0, row0, nrows, K)) return false;
-    if (nblk > 1 && nrows > 0 && !stream_rows(w1, row0, nrows, K)) return false;
+    if (nrows > 0 && !stream_rows(w0, row0, nrows, K, m0, map_row0, box_rows)) return false;
+    if (nblk > 1 && nrows > 0 && !stream_rows(w1, row0, nrows, K, m1, map_row0, box_rows)) return false;
     return true;
   }
 
-  // rows [lo, hi) of w in chunks of cr; `first` / `last` mark the task's ends
+  // rows [lo, hi) of w in chunks of cr; `first` / `last` mark the task's ends;
+  // map: the matrix's tensor map when the chunks go to the tensor cores
   __device__ __forceinline__ bool rows_task(int kind, const uint16_t* w, int lo, int hi, int cr, int K,
-                                            int nt, bool first, bool last, int last_extra = 0) {
+                                            int nt, bool first, bool last, int last_extra = 0,
+                                            const uint8_t* map = nullptr) {
     for (int c0 = lo; c0 < hi; c0 += cr) {
       const int flags = (first && c0 == lo ? FL_FIRST : 0) | (last && c0 + cr >= hi ? FL_LAST : 0) |
                         (c0 + cr >= hi ? last_extra : 0);
-      if (!chunk(kind, flags, c0, min(cr, hi - c0), 1, K, nt, 0, 0, 0, w, nullptr)) return false;
+      if (!chunk(kind, flags, c0, min(cr, hi - c0), 1, K, nt, 0, 0, 0, w, nullptr, map)) return false;
     }
     return true;
+  }
+
+  // several tokens: the tensor map of matrix `which` when its rows go to the tensor cores
+  __device__ __forceinline__ const uint8_t* mmap(int which, int K) const {
+    return (p.w_maps && mma_multi_rows(K, p.B)) ? wmap(which) : nullptr;
   }
 
   // bounded spin of the whole warp on a global counter; every lane's load is
@@ -587,14 +613,17 @@ struct Prod {
     const int cr = gemv_chunk_rows(H, B);
     if (op == OP_FINAL) {
       if (a1 <= a0) return chunk(K_LM, FL_FIRST | FL_LAST, 0, 0, 1, H, B, 0, 0, 0, nullptr, nullptr);
-      return rows_task(K_LM, p.lm_head, a0, a1, cr, H, B, true, true);
+      const uint8_t* lm = (p.w_maps && mma_multi_rows(H, B)) ? p.w_maps + (size_t)W_MAPS_PER_LAYER * p.L * 128
+                                                              : nullptr;
+      return rows_task(K_LM, p.lm_head, a0, a1, cr, H, B, true, true, 0, lm);
     }
     // P1: router rows [a0, a1) (the last of their chunks releases the router
     // counter), then W_qkv rows [b0, b1)
     const int r0 = a0, r1 = a1, q0 = b0, q1 = b1;
     if (r1 <= r0 && q1 <= q0) return chunk(K_ROUTER, FL_FIRST | FL_LAST, 0, 0, 1, H, B, 0, 0, 0, nullptr, nullptr);
-    if (r1 > r0 && !rows_task(K_ROUTER, wptr(0), r0, r1, cr, H, B, true, q1 <= q0, FL_RTR)) return false;
-    if (q1 > q0 && !rows_task(K_QKV, wptr(1), q0, q1, cr, H, B, r1 <= r0, true)) return false;
+    if (r1 > r0 && !rows_task(K_ROUTER, wptr(0), r0, r1, cr, H, B, true, q1 <= q0, FL_RTR, mmap(W_MAP_ROUTER, H)))
+      return false;
+    if (q1 > q0 && !rows_task(K_QKV, wptr(1), q0, q1, cr, H, B, r1 <= r0, true, 0, mmap(W_MAP_QKV, H))) return false;
     return true;
   }
 
@@ -708,10 +737,13 @@ struct Prod {
       const int cnt = S.rt.off[a + 1] - S.rt.off[a];
       const int cp = max(1, gemv_chunk_rows(H, cnt) / 2);
       const size_t eo = (size_t)e * p.I * H;
+      const bool mma = p.w_maps && mma_multi_rows(H, cnt);
+      const uint8_t* mg = mma ? wmap(W_MAP_GATE) : nullptr;
+      const uint8_t* mu = mma ? wmap(W_MAP_UP) : nullptr;
       for (int c0 = i0; c0 < i1; c0 += cp) {
         n_chunks--;
         if (!chunk(K_UP, n_chunks == 0 ? FL_LAST : 0, c0, min(cp, i1 - c0), 2, H, cnt, a, e, 0,
-                   wptr(3) + eo, wptr(4) + eo))
+                   wptr(3) + eo, wptr(4) + eo, mg, mu, e * p.I + c0))
           return false;
       }
     }
@@ -726,10 +758,13 @@ struct Prod {
     const int KO = p.hq * p.d;
     const int last = ONE ? FL_LAST : 0;
     if (a1 <= a0) return chunk(K_OPROJ, FL_LAST, 0, 0, 1, KO, B, 0, 0, 0, nullptr, nullptr);
-    const int co = ONE ? one_rows(KO) : gemv_chunk_rows(KO, B);
+    // (several tokens through the tensor cores: one partial per (row, warp,
+    // token), at most kPartFloats of them per chunk)
+    const uint8_t* mo = ONE ? nullptr : mmap(W_MAP_O, KO);
+    const int co = ONE ? one_rows(KO) : mo ? kPartFloats / (kConsumerWarps * B) : gemv_chunk_rows(KO, B);
     for (int c0 = a0; c0 < a1; c0 += co)
       if (!chunk(K_OPROJ, c0 + co >= a1 ? last : 0, c0, min(co, a1 - c0), 1, KO, B, 0, 0, 0, wptr(2),
-                 nullptr))
+                 nullptr, mo))
         return false;
     if (ONE) return true;
     int32_t* w = begin();     // streams nothing
@@ -798,11 +833,16 @@ struct Prod {
       const int h0 = max(r0 - a * H, 0), h1 = min(r1 - a * H, H);
       const int e = S.rt.act[a];
       const int cnt = S.rt.off[a + 1] - S.rt.off[a];
-      const int cd = gemv_chunk_rows(p.I, cnt);
+      // tensor cores: one fp32 partial per (row, warp, token) in the chunk's buffer
+      const bool mma = p.wd_maps != nullptr;
+      const int cd = mma ? max(kDownBoxRows, min(512, kPartFloats / (kConsumerWarps * cnt)) / kDownBoxRows *
+                                                 kDownBoxRows)
+                         : gemv_chunk_rows(p.I, cnt);
       const uint16_t* wd = wptr(5) + (size_t)e * H * p.I;
+      const uint8_t* md = mma ? p.wd_maps + (size_t)l * 128 : nullptr;
       for (int c0 = h0; c0 < h1; c0 += cd)
         if (!chunk(K_DOWN, (c0 + cd >= h1 && a * H + h1 == r1) ? FL_LAST : 0, c0, min(cd, h1 - c0), 1, p.I,
-                   cnt, a, e, 0, wd, nullptr))
+                   cnt, a, e, 0, wd, nullptr, md, nullptr, e * H + c0, kDownBoxRows))
           return false;
     }
     return true;
@@ -1333,6 +1373,159 @@ struct Cons {
     return true;
   }
 
+  // -------------------------------- several tokens, expert chunks, tensor cores
+  // Both write one fp32 partial per (row, warp, token) to part[(row * 8 +
+  // warp) * nt + token]: the epilogue adds a row's eight warp partials in warp
+  // order (as it adds the CUDA-core path's segment partials).
+  //
+  // Rows of K = 2048 NH columns with nt <= 8 / NH tokens (dense rows, or an
+  // expert's gate and up rows: R_NBLK groups), stages as in the one-token
+  // GEMV (R = 8 / NH rows x every column block, swizzled): the M side is
+  // (row m % R, part m / R) of the warp's 256 NH columns in P = 2 NH parts,
+  // the N side column n = 8 q + g of n-tile q holds token q (8 / (4 NH))
+  // + g / (4 NH), part (g / 2) % P, high or low half g % 2 of x.  C[m][n] is
+  // kept where the parts match; the lanes holding a token's parts of a row
+  // are added (quad shuffles; with R = 4 also the two quads of a row).
+  template <int NH>
+  __device__ __forceinline__ bool gemv_mma_multi(float* part) {
+    constexpr int R = 8 / NH, TPT = 2 / NH;       // rows per stage, tokens per n-tile
+    const int nt = t[R_NT], nr = t[R_NROWS], nblk = t[R_NBLK];
+    const int nq = (nt + TPT - 1) / TPT;          // n-tiles in use (<= 4)
+    uint32_t xb[4][8][2];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      const int tk = q * TPT + gl / (4 * NH), j = (gl >> 1) & (2 * NH - 1), lo = gl & 1;
+      const bool on = q < nq && tk < nt;
+      const float* xr = on ? xrow(tk) : nullptr;
+#pragma unroll
+      for (int s = 0; s < 8; s++)
+#pragma unroll
+        for (int hf = 0; hf < 2; hf++) {
+          float2 v = make_float2(0.f, 0.f);
+          if (on) v = __ldcg((const float2*)(xr + mma_block<NH>(j, s >> 2) * 64 + (s & 3) * 16 + hf * 8 + 2 * cq));
+          if (lo) v = make_float2(v.x - bf16f(f2bf(v.x)), v.y - bf16f(f2bf(v.y)));
+          xb[q][s][hf] = pack_bf2(v.x, v.y);
+        }
+    }
+    uint32_t aoff[8];
+    {
+      const int m = ((lane >> 3) & 1) * 8 + (lane & 7), kh = lane >> 4;
+#pragma unroll
+      for (int s = 0; s < 8; s++) {
+        const int line = mma_block<NH>(m / R, s >> 2) * R + (m % R);
+        aoff[s] = (uint32_t)(line * 128 + ((((s & 3) * 2 + kh) ^ (line & 7)) << 4));
+      }
+    }
+    // this lane's part of the n-tile's columns 2 cq, 2 cq + 1, and the parts of
+    // its M rows g (part g / R) and g + 8 (part (g + 8) / R)
+    const int pc = cq & (2 * NH - 1), j0 = gl / R, j1 = (gl + 8) / R;
+    for (int blk = 0; blk < nblk; blk++) {
+      for (int done = 0; done < nr; done += R) {
+        const int rows = min(R, nr - done);
+        uint32_t slot;
+        if (!stage_full(slot)) return false;
+        if (TR && tid == 0 && blk == 0 && done == 0) S.t_mark[0] = gtime_ns();
+        const uint8_t* base = S.stage[slot];
+        float c[4][4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) c[q][0] = c[q][1] = c[q][2] = c[q][3] = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; s++) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(a0, a1, a2, a3, base + aoff[s]);
+#pragma unroll
+          for (int q = 0; q < 4; q++)
+            if (q < nq) mma_bf16(c[q], a0, a1, a2, a3, xb[q][s][0], xb[q][s][1]);
+        }
+        stage_release(slot);
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+          if (q >= nq) break;
+          float v = (pc == j0 ? c[q][0] + c[q][1] : 0.f) + (pc == j1 ? c[q][2] + c[q][3] : 0.f);
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          if (NH == 2) {
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+          }
+          // NH = 1: lanes cq = 0, 2 hold tokens 2 q, 2 q + 1 of row g; NH = 2:
+          // lane cq = 0 of quads g < 4 holds token q of row g
+          const int tk = q * TPT + (NH == 1 ? (cq >> 1) : 0);
+          const bool writer = NH == 1 ? !(cq & 1) : (cq == 0 && gl < R);
+          if (writer && gl < rows && tk < nt)
+            part[((blk * nr + done + gl) * kConsumerWarps + warp) * nt + tk] = v;
+        }
+      }
+    }
+    if (TR && tid == 0) S.t_mark[1] = gtime_ns();
+    return true;
+  }
+
+  // Down rows of an expert (K = I, a multiple of 128 up to 1024), stages of 16
+  // rows x every column block (swizzled, line 16 cb + r): the M side is the 16
+  // rows, the K side the warp's I / 8 columns, the N side column n = 8 q + g
+  // holds token 4 q + g / 2, high or low half g % 2 of its hidden vector.
+  __device__ __forceinline__ bool gemv_mma_down(float* part) {
+    const int K = t[R_K], nt = t[R_NT], nr = t[R_NROWS];
+    const int ks = K >> 7;                        // k-steps per warp (<= 8)
+    const int nq = (nt + 3) >> 2;                 // n-tiles: four tokens each
+    const int col0 = warp * (K >> 3);
+    uint32_t xb[4][8][2];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      const int tk = 4 * q + (gl >> 1), lo = gl & 1;
+      const bool on = q < nq && tk < nt;
+      const float* xr = on ? xrow(tk) : nullptr;
+#pragma unroll
+      for (int s = 0; s < 8; s++)
+#pragma unroll
+        for (int hf = 0; hf < 2; hf++) {
+          float2 v = make_float2(0.f, 0.f);
+          if (on && s < ks) v = __ldcg((const float2*)(xr + col0 + 16 * s + 8 * hf + 2 * cq));
+          if (lo) v = make_float2(v.x - bf16f(f2bf(v.x)), v.y - bf16f(f2bf(v.y)));
+          xb[q][s][hf] = pack_bf2(v.x, v.y);
+        }
+    }
+    uint32_t aoff[8];
+    {
+      const int m = ((lane >> 3) & 1) * 8 + (lane & 7), kh = lane >> 4;
+#pragma unroll
+      for (int s = 0; s < 8; s++) {
+        const int col = col0 + 16 * s + 8 * kh;
+        const int line = (col >> 6) * kDownBoxRows + m;
+        aoff[s] = (uint32_t)(line * 128 + ((((col & 63) >> 3) ^ (line & 7)) << 4));
+      }
+    }
+    for (int done = 0; done < nr; done += kDownBoxRows) {
+      uint32_t slot;
+      if (!stage_full(slot)) return false;
+      if (TR && tid == 0 && done == 0) S.t_mark[0] = gtime_ns();
+      const uint8_t* base = S.stage[slot];
+      float c[4][4];
+#pragma unroll
+      for (int q = 0; q < 4; q++) c[q][0] = c[q][1] = c[q][2] = c[q][3] = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; s++) {
+        if (s >= ks) break;
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(a0, a1, a2, a3, base + aoff[s]);
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+          if (q < nq) mma_bf16(c[q], a0, a1, a2, a3, xb[q][s][0], xb[q][s][1]);
+      }
+      stage_release(slot);
+#pragma unroll
+      for (int q = 0; q < 4; q++) {
+        const int tk = 4 * q + cq;
+        if (q < nq && tk < nt) {
+          if (done + gl < nr) part[((done + gl) * kConsumerWarps + warp) * nt + tk] = c[q][0] + c[q][1];
+          if (done + gl + 8 < nr) part[((done + gl + 8) * kConsumerWarps + warp) * nt + tk] = c[q][2] + c[q][3];
+        }
+      }
+    }
+    if (TR && tid == 0) S.t_mark[1] = gtime_ns();
+    return true;
+  }
+
   // ------------------------------------------------ one-token GEMV chunk
   // Row r of the chunk (rows numbered across its groups) belongs to warp
   // r % 8, which computes the whole row: lane l multiplies the 8-column
@@ -1609,10 +1802,9 @@ struct Cons {
   }
 
   // reduction + epilogue of a GEMV chunk (after the barrier)
-  __device__ __forceinline__ void epilogue(const float* part) {
+  __device__ __forceinline__ void epilogue(const float* part, int nseg) {
     const int l = t[R_LAYER], kind = t[R_KIND];
     const int nt = t[R_NT], nrows = t[R_NROWS], row0 = t[R_ROW0];
-    const int nseg = gemv_nseg(t[R_K]);
     const size_t Bm = (size_t)p.Bmax;
     for (int i = tid; i < nrows * nt; i += 256) {
       const int n = i / nrows, r = i % nrows;
@@ -2183,15 +2375,22 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
     if (ok && run) ok = c.wait_counter(bar_index(p, l, p.bl.down), p.n_down_sms);
     if (ok && run) c.moe_sum();
   } else {
+    // an expert's gate / up rows (up to 8 tokens) and down rows on the tensor
+    // cores: one partial per warp instead of one per 256-column segment
+    const int nt = t[R_NT];
+    const int K = t[R_K];
+    const bool mma = run && ((kind != K_DOWN && p.w_maps && mma_multi_rows(K, nt)) ||
+                             (kind == K_DOWN && p.wd_maps));
     if (ok && run) {
       // tokens per pass matched to the chunk (an expert's few routed tokens do
       // not pay for eight)
-      const int nt = t[R_NT];
-      ok = (nt <= 1 ? c.template gemv<1>(part) : c.template gemv<8>(part)) &&
+      ok = (mma ? (kind == K_DOWN ? c.gemv_mma_down(part)
+                  : K == 2048 ? c.template gemv_mma_multi<1>(part) : c.template gemv_mma_multi<2>(part))
+                : nt <= 1 ? c.template gemv<1>(part) : c.template gemv<8>(part)) &&
            c.csync();
     }
     if (ok && run) {
-      c.epilogue(part);
+      c.epilogue(part, mma ? kConsumerWarps : gemv_nseg(t[R_K]));
       if (TR && c.tid == 0) S.t_mark[2] = gtime_ns();
       if (c.lane == 0) S.cchunk[c.warp]++;
     }

@@ -100,6 +100,17 @@ MK_HD inline int rows_per_stage(int K) {
 // use.
 MK_HD inline bool rotated_rows(int K) { return K == 2048 || K == 4096; }
 constexpr int kMmaRows = 128;           // rows of one tensor-core GEMV chunk (one partial buffer)
+// Several tokens: rows of 2048 columns with at most 8 tokens, or of 4096
+// columns with at most 4 (dense rows, an expert's gate / up rows) go to the
+// tensor cores through the same maps; an expert's down rows (I columns, I a
+// multiple of 128 up to 1024) through maps of W_down viewed as [E H rows][I]
+// with boxes of 16 rows x all of I, 128-byte swizzle (row r of column block
+// cb is the 128-byte line 16 cb + r).
+MK_HD inline bool mma_multi_rows(int K, int nt) {
+  return nt >= 1 && ((K == 2048 && nt <= 8) || (K == 4096 && nt <= 4));
+}
+MK_HD inline bool mma_multi_down(int K) { return K % 128 == 0 && K <= 1024; }
+constexpr int kDownBoxRows = 16;
 // tensor maps of the one-token weight matrices, per layer (W_MAP_* + 5 l), then the LM head
 enum : int { W_MAP_ROUTER = 0, W_MAP_QKV = 1, W_MAP_O = 2, W_MAP_GATE = 3, W_MAP_UP = 4, W_MAPS_PER_LAYER = 5 };
 
@@ -152,6 +163,7 @@ struct Params {
   int max_pages, num_pages, Bmax, n_sm;
   int n_comb_sms, n_up_sms;    // SMs that signal the COMBINE / UP counters of a layer
   int n_down_sms, n_rtr_sms;   // SMs with a DOWN task / with router rows in their P1 share
+  int moe_depth;               // one token: stages an SM without attention items keeps in flight
   float rms_eps, attn_scale_log2;
   // caller weights (device pointers; per-layer arrays are device arrays of L pointers)
   const uint16_t* embed;
@@ -170,6 +182,8 @@ struct Params {
                                // of an expert one contiguous [H][8] block (one token: the
                                // UP pieces' column slices stream as whole blocks)
   const uint8_t* mp_map;       // tensor map of mpart: 2-D [groups][H] fp32, boxes 24 x 256
+  const uint8_t* wd_maps;      // several tokens: [L] tensor maps of W_down (16-row boxes;
+                               // nullptr when not used)
   const uint8_t* w_maps;       // one token, rows of 2048 / 4096 columns: [5 L + 1] tensor maps
                                // (W_MAP_*; the last the LM head), 3-D views described above
                                // (nullptr when the model's rows take the other GEMV path)

@@ -50,6 +50,7 @@ int validate_config(const mk_config& c) {
       c.timeout_ms < 0 || c.trace_records < 0)
     return MK_ERR_BAD_CONFIG;
   if (c.kv_split_tokens < 0 || c.kv_split_tokens % 16) return MK_ERR_BAD_CONFIG;
+  if (c.moe_stage_depth < 0 || c.moe_stage_depth > kStages) return MK_ERR_BAD_CONFIG;
   if (c.wave_order < MK_WAVES_DEFAULT || c.wave_order > MK_WAVES_INTERLEAVED) return MK_ERR_BAD_CONFIG;
   return MK_OK;
 }

@@ -44,13 +44,26 @@ def test_strerror_and_version(lib):
     assert mk.mk_strerror(-99) == "unknown error"
 
 
-def test_struct_layout_matches_header(lib):
-    # offsets the C compiler uses must equal the ctypes mirror (x86-64 / aarch64 LP64)
-    assert C.sizeof(mk.mk_config) == 96
-    assert mk.mk_config.rope_theta.offset == 40
-    assert mk.mk_config.rms_eps.offset == 48
-    assert C.sizeof(mk.mk_weights) == 12 * 8
-    assert C.sizeof(mk.mk_error) == 28
+def test_struct_layout_matches_header(lib, tmp_path):
+    """Every field offset and struct size the C compiler gives the header's
+    structs equals the ctypes mirror's."""
+    import subprocess
+    lines = []
+    for st in (mk.mk_config, mk.mk_weights, mk.mk_error):
+        lines.append(f'printf("{st.__name__} %zu\\n", sizeof({st.__name__}));')
+        for name, _ in st._fields_:
+            lines.append(f'printf("{st.__name__}.{name} %zu\\n", offsetof({st.__name__}, {name}));')
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "mk.h"\nint main(void) {\n'
+                   + "\n".join(lines) + "\nreturn 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = dict(line.split() for line in out if line)
+    for st in (mk.mk_config, mk.mk_weights, mk.mk_error):
+        assert int(got[st.__name__]) == C.sizeof(st), st.__name__
+        for name, _ in st._fields_:
+            assert int(got[f"{st.__name__}.{name}"]) == getattr(st, name).offset, (st.__name__, name)
 
 
 def test_create_rejects_bad_configs_before_touching_the_device(lib):

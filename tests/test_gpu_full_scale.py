@@ -11,7 +11,9 @@ teacher-forced trajectories against the whole-model CPU oracle:
 Every step: logits max-abs <= 2e-2 and relative L2 <= 1e-2 over the whole
 vocabulary of every sequence, routed expert sets equal on every (layer,
 sequence) where the oracle's k-th / (k+1)-th router gap exceeds 1e-3, greedy
-tokens equal on >= 99 % of steps.  On the first step the residual entering
+tokens equal on >= 99 % of the (step, sequence) pairs.  Where the GPU decided a near tie (gap <=
+1e-3) the other way, the oracle's step is rerun with the GPU's experts
+imposed there, so the rest of the step is still compared like for like.  On the first step the residual entering
 every layer is also compared with the oracle's (whole-model propagation, no
 teacher forcing inside the step).
 """
@@ -66,8 +68,10 @@ def test_full_size_trajectory_matches_the_oracle(name):
     try:
         exempt, compared, agree = run_trajectory(pair, steps, on_step=residuals)
         assert compared > 0
-        print(f"\n{name}: {steps} steps, argmax agreed on {agree}, routing sets compared {compared}, "
-              f"exempt by the gap rule {exempt}, {time.time() - t0:.0f} s")
+        print(f"\n{name}: {steps} steps, argmax agreed on {agree} (step, sequence) pairs, "
+              f"routing sets compared {compared}, "
+              f"exempt by the gap rule {exempt}, near ties imposed on the oracle {pair.forced}, "
+              f"{time.time() - t0:.0f} s")
     finally:
         pair.close()
         del pair

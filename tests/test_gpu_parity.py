@@ -177,7 +177,7 @@ def test_mid_trajectory_and_split_kv():
         pair.close()
 
 
-@pytest.mark.parametrize("name", ["tiny_b5", "tiny_b12", "mid_b16"])
+@pytest.mark.parametrize("name", ["tiny_b5", "tiny_b12", "mid_b16", "mid_b4", "a3b4_b3"])
 def test_multi_sequence_trajectory_with_churn(name):
     """Several ragged sequences per step (one and two GEMV token passes), one
     sequence retiring and a new one joining every step."""

@@ -27,7 +27,7 @@ import oracle
 from persistent_moe_decode_gb300 import mk
 from persistent_moe_decode_gb300.configs import A3B
 from persistent_moe_decode_gb300.synth import _normal_bf16, make_kv_pools, make_model
-from tests._pair import GAP, MAX_ABS, REL_L2
+from tests._pair import GAP, MAX_ABS, REL_L2, oracle_step_following_ties
 from tests._util import dims_dict, host_pool, host_weights
 
 pytestmark = pytest.mark.gpu
@@ -90,11 +90,11 @@ def test_service_continuous_batching_matches_the_oracle():
             pt = np.full((B, max_pages), -1, dtype=np.int32)
             for i, rid in enumerate(ids):
                 pt[i, :len(pages_of[rid])] = pages_of[rid]
-            ref, tr = orc.decode_step(toks, lens, pt, trace=True)
+            idx, _ = mk.mk_get_routing(dec.h, d.n_layers, B, d.top_k)
+            ref, tr, _ = oracle_step_following_ties(orc, toks, lens, pt, idx)
             err = np.abs(gpu - ref).max()
             rel = np.linalg.norm(gpu - ref) / np.linalg.norm(ref)
             assert err <= MAX_ABS and rel <= REL_L2, f"step {step}: max-abs {err:.3e} rel-L2 {rel:.3e}"
-            idx, _ = mk.mk_get_routing(dec.h, d.n_layers, B, d.top_k)
             ok = tr["gap"] > GAP
             for l in range(d.n_layers):
                 for i in range(B):

@@ -45,9 +45,11 @@ def rope_complex(x: torch.Tensor, pos: int, theta: float) -> torch.Tensor:
     return torch.cat([z.real, z.imag], dim=-1)
 
 
-def torch_layers(m, kp, vp, l0, l1, h, lens, pt):
+def torch_layers(m, kp, vp, l0, l1, h, lens, pt, force=None):
     """Layers [l0, l1) on the residual h [B, H] (fp64); appends K/V to kp, vp
-    (BF16 tensors [L, pages, hkv, P, d]) in place.  Returns the new h."""
+    (BF16 tensors [L, pages, hkv, P, d]) in place.  Returns the new h.
+    ``force`` maps (layer, token) to the experts that token must use (weights
+    renormalised over them)."""
     d_ = m.dims
     hq, hkv, d, P, K = d_.n_q_heads, d_.n_kv_heads, d_.head_dim, d_.page_size, d_.top_k
     B = h.shape[0]
@@ -79,6 +81,11 @@ def torch_layers(m, kp, vp, l0, l1, h, lens, pt):
         p = torch.softmax(r, dim=-1)
         top = torch.topk(p, K, dim=-1)
         mask = torch.zeros_like(p).scatter(1, top.indices, top.values / top.values.sum(1, keepdim=True))
+        for (fl, fb), experts in (force or {}).items():
+            if fl == l:
+                sel = torch.as_tensor(experts)
+                mask[fb] = 0.0
+                mask[fb, sel] = p[fb, sel] / p[fb, sel].sum()
         g = torch.einsum("eih,bh->bei", m.w_gate[l].double(), x)
         u = torch.einsum("eih,bh->bei", m.w_up[l].double(), x)
         y = torch.einsum("ehi,bei->beh", m.w_down[l].double(), F.silu(g) * u)
@@ -87,9 +94,9 @@ def torch_layers(m, kp, vp, l0, l1, h, lens, pt):
     return h
 
 
-def torch_step(m, kp, vp, tokens, lens, pt):
+def torch_step(m, kp, vp, tokens, lens, pt, force=None):
     h = m.embed[torch.as_tensor(tokens, dtype=torch.long)].double()
-    h = torch_layers(m, kp, vp, 0, m.dims.n_layers, h, lens, pt)
+    h = torch_layers(m, kp, vp, 0, m.dims.n_layers, h, lens, pt, force)
     xf = F.rms_norm(h, (m.dims.hidden,), weight=m.final_norm.double(), eps=m.dims.rms_eps)
     return (xf @ m.lm_head.double().T).numpy()
 
@@ -172,3 +179,40 @@ def test_run_layers_composes_over_the_layer_range(oracle_lib):
     np.testing.assert_array_equal(orc.run_layers(1, 1, h1, lens, pt), h1)
     with pytest.raises(RuntimeError):
         orc.run_layers(0, 3, h0, lens, pt)
+
+
+def test_forced_routing_of_its_own_choice_changes_nothing(oracle_lib):
+    m, kp, vp, pt, toks, lens = setup(TINY, 24, [40, 9])
+    orc = new_oracle(m, kp, vp)
+    k0, v0 = orc.k_pool.copy(), orc.v_pool.copy()
+    plain, tr = orc.decode_step(toks, lens, pt, trace=True)
+    orc.k_pool[...] = k0
+    orc.v_pool[...] = v0
+    mask = np.ones(tr["idx"].shape[:2], dtype=bool)
+    forced = orc.decode_step(toks, lens, pt, force=(tr["idx"], mask))
+    np.testing.assert_array_equal(forced, plain)
+
+
+def test_forced_routing_matches_the_torch_restatement(oracle_lib):
+    """Other experts imposed on token 1 at layer 0 and token 0 at layer 1: the
+    oracle equals the restatement that imposes the same sets."""
+    m, kp, vp, pt, toks, lens = setup(TINY, 24, [40, 9])
+    orc = new_oracle(m, kp, vp)
+    k0, v0 = orc.k_pool.copy(), orc.v_pool.copy()
+    _, tr = orc.decode_step(toks, lens, pt, trace=True)
+    orc.k_pool[...] = k0
+    orc.v_pool[...] = v0
+    idx = tr["idx"].copy()
+    mask = np.zeros(idx.shape[:2], dtype=bool)
+    force = {}
+    for (l, b) in ((0, 1), (1, 0)):
+        others = [e for e in range(TINY.n_experts) if e not in idx[l, b]]
+        idx[l, b] = others[:TINY.top_k]
+        mask[l, b] = True
+        force[(l, b)] = others[:TINY.top_k]
+    got, tr2 = orc.decode_step(toks, lens, pt, trace=True, force=(idx, mask))
+    assert tr2["idx"][0, 1].tolist() == force[(0, 1)]
+    ref = torch_step(m, kp.clone(), vp.clone(), toks, lens, pt, force)
+    np.testing.assert_allclose(got, ref, rtol=1e-9, atol=1e-11)
+    plain = torch_step(m, kp.clone(), vp.clone(), toks, lens, pt)
+    assert np.abs(got - plain).max() > 1e-6       # the imposed experts do change the step
