@@ -123,9 +123,10 @@ def run_trajectory(pair, steps, trace_every=1, on_step=None):
     for s in range(steps):
         gpu, ref, tr = pair.step(trace=(s % trace_every == 0))
         try:
-            check_logits(gpu, ref, f"step {s}")
+            err, rel = check_logits(gpu, ref, f"step {s}")
         except AssertionError as e:
             raise AssertionError(f"{e}\n{diagnose(pair, gpu, ref, tr)}") from None
+        pair.worst = max(getattr(pair, "worst", (0.0, 0.0)), (float(err), float(rel)))
         if tr is not None:
             ex = check_routing(pair, tr)
             exempt += ex

@@ -71,6 +71,7 @@ def test_full_size_trajectory_matches_the_oracle(name):
         print(f"\n{name}: {steps} steps, argmax agreed on {agree} (step, sequence) pairs, "
               f"routing sets compared {compared}, "
               f"exempt by the gap rule {exempt}, near ties imposed on the oracle {pair.forced}, "
+              f"worst logits max-abs {pair.worst[0]:.2e} (rel-L2 {pair.worst[1]:.2e}), "
               f"{time.time() - t0:.0f} s")
     finally:
         pair.close()
