@@ -358,6 +358,9 @@ def main():
     wl = WORKLOADS[args.workload]
     if args.layers:
         wl = wl.with_(dims=type(wl.dims)(**{**wl.dims.__dict__, "n_layers": args.layers}))
+    # the page pool covers every step this run takes: warm-up, the device-timed
+    # steps, and the end-to-end leg (3 warm-up steps and K timed ones)
+    wl = wl.with_(steps=max(wl.steps, args.warmup + 2 * args.steps + 3))
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -1153,6 +1153,17 @@ struct Cons {
       const int H4 = p.H / 4;
       return H4 <= 256 ? norm1<1>(l, final_norm) : H4 <= 512 ? norm1<2>(l, final_norm) : norm1<4>(l, final_norm);
     }
+    const int H4 = p.H / 4;
+    return H4 <= 256 ? norm_multi<1>(l, final_norm) : H4 <= 512 ? norm_multi<2>(l, final_norm)
+                     : norm_multi<4>(l, final_norm);
+  }
+
+  // several tokens: the same per token, with the loads of TB = 8 / NI tokens
+  // in flight together (each thread holds columns 4 t + 1024 k, NI float4s of a
+  // token), so a layer's norm waits for a few L2 round trips, not one per token
+  template <int NI>
+  __device__ __forceinline__ bool norm_multi(int l, bool final_norm) {
+    constexpr int TB = 8 / NI;
     const int H = p.H, B = p.B, H4 = H / 4;
     const size_t Bm = (size_t)p.Bmax;
     if (l > 0 && !wait_counter(bar_index(p, l - 1, p.bl.out), out_target() + t[R_BUMP])) return false;
@@ -1160,38 +1171,44 @@ struct Cons {
     float* xl = p.xloc + (size_t)blockIdx.x * Bm * H;
     const bool keep = blockIdx.x == 0;
     const uint16_t* gain = final_norm ? p.final_norm : p.attn_norm[l];
-    constexpr int NI = 4;                       // H <= 4096: at most 4 float4 per thread
-    for (int n = 0; n < B; n++) {
-      // every load of this token first, then the arithmetic and the stores
-      float4 h[NI];
+    // h = the residual + the previous layer's update (the embedding row at l = 0)
+    for (int n0 = 0; n0 < B; n0 += TB) {
+      float4 h[TB][NI];
 #pragma unroll
-      for (int k = 0; k < NI; k++) {
-        const int i4 = tid + 256 * k;
-        h[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i4 < H4) {
-          if (l == 0) {
-            const uint2 e = *(const uint2*)(p.embed + (size_t)p.tokens[n] * H + i4 * 4);
-            h[k] = make_float4(bf16lo(e.x), bf16hi(e.x), bf16lo(e.y), bf16hi(e.y));
-          } else {
-            const float4 a = __ldcg((const float4*)(hl + n * H) + i4);
-            const float4 d = delta4(l - 1, n, i4);
-            h[k] = make_float4(a.x + d.x, a.y + d.y, a.z + d.z, a.w + d.w);
+      for (int b = 0; b < TB; b++)
+#pragma unroll
+        for (int k = 0; k < NI; k++) {
+          const int n = n0 + b, i4 = tid + 256 * k;
+          h[b][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (n < B && i4 < H4) {
+            if (l == 0) {
+              const uint2 e = *(const uint2*)(p.embed + (size_t)p.tokens[n] * H + i4 * 4);
+              h[b][k] = make_float4(bf16lo(e.x), bf16hi(e.x), bf16lo(e.y), bf16hi(e.y));
+            } else {
+              const float4 a = __ldcg((const float4*)(hl + n * H) + i4);
+              const float4 d = delta4(l - 1, n, i4);
+              h[b][k] = make_float4(a.x + d.x, a.y + d.y, a.z + d.z, a.w + d.w);
+            }
           }
         }
-      }
-      float ssl = 0.f;
 #pragma unroll
-      for (int k = 0; k < NI; k++) {
-        const int i4 = tid + 256 * k;
-        if (i4 < H4) {
-          if (!final_norm) __stcg((float4*)(hl + n * H) + i4, h[k]);
-          if (keep) __stcg((float4*)(p.hdbg + ((size_t)l * Bm + n) * H) + i4, h[k]);
-          ssl += h[k].x * h[k].x + h[k].y * h[k].y + h[k].z * h[k].z + h[k].w * h[k].w;
+      for (int b = 0; b < TB; b++) {
+        const int n = n0 + b;
+        if (n >= B) break;
+        float ssl = 0.f;
+#pragma unroll
+        for (int k = 0; k < NI; k++) {
+          const int i4 = tid + 256 * k;
+          if (i4 < H4) {
+            if (!final_norm) __stcg((float4*)(hl + n * H) + i4, h[b][k]);
+            if (keep) __stcg((float4*)(p.hdbg + ((size_t)l * Bm + n) * H) + i4, h[b][k]);
+            ssl += h[b][k].x * h[b][k].x + h[b][k].y * h[b][k].y + h[b][k].z * h[b][k].z + h[b][k].w * h[b][k].w;
+          }
         }
-      }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ssl += __shfl_xor_sync(0xffffffffu, ssl, o);
-      if (lane == 0) S.nred[warp][n] = ssl;
+        for (int o = 16; o > 0; o >>= 1) ssl += __shfl_xor_sync(0xffffffffu, ssl, o);
+        if (lane == 0) S.nred[warp][n] = ssl;
+      }
     }
     if (!csync()) return false;
     if (tid < B) {
@@ -1200,22 +1217,50 @@ struct Cons {
       S.rinv[tid] = 1.0f / sqrtf(sum / (float)H + p.rms_eps);
     }
     if (!csync()) return false;
-    for (int i4 = tid; i4 < H4; i4 += 256) {
-      const uint2 gv = *(const uint2*)(gain + i4 * 4);
-      const float g0 = bf16lo(gv.x), g1 = bf16hi(gv.x), g2 = bf16lo(gv.y), g3 = bf16hi(gv.y);
-      for (int n = 0; n < B; n++) {
-        float4 h;
-        if (final_norm) {
-          const float4 a = __ldcg((const float4*)(hl + n * H) + i4);
-          const float4 d = delta4(l - 1, n, i4);
-          h = make_float4(a.x + d.x, a.y + d.y, a.z + d.z, a.w + d.w);
-        } else {
-          h = __ldcg((const float4*)(hl + n * H) + i4);
+    // x = h / rms * gain (the final norm has not stored its h: it adds the update again)
+    float4 g[NI];
+#pragma unroll
+    for (int k = 0; k < NI; k++) {
+      const int i4 = tid + 256 * k;
+      g[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i4 < H4) {
+        const uint2 gv = *(const uint2*)(gain + i4 * 4);
+        g[k] = make_float4(bf16lo(gv.x), bf16hi(gv.x), bf16lo(gv.y), bf16hi(gv.y));
+      }
+    }
+    for (int n0 = 0; n0 < B; n0 += TB) {
+      float4 h[TB][NI];
+#pragma unroll
+      for (int b = 0; b < TB; b++)
+#pragma unroll
+        for (int k = 0; k < NI; k++) {
+          const int n = n0 + b, i4 = tid + 256 * k;
+          h[b][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (n < B && i4 < H4) {
+            if (final_norm) {
+              const float4 a = __ldcg((const float4*)(hl + n * H) + i4);
+              const float4 d = delta4(l - 1, n, i4);
+              h[b][k] = make_float4(a.x + d.x, a.y + d.y, a.z + d.z, a.w + d.w);
+            } else {
+              h[b][k] = __ldcg((const float4*)(hl + n * H) + i4);
+            }
+          }
         }
+#pragma unroll
+      for (int b = 0; b < TB; b++) {
+        const int n = n0 + b;
+        if (n >= B) break;
         const float r = S.rinv[n];
-        const float4 x = make_float4(h.x * r * g0, h.y * r * g1, h.z * r * g2, h.w * r * g3);
-        __stcg((float4*)(xl + n * H) + i4, x);
-        if (keep) __stcg((float4*)(p.xdbg + ((size_t)l * Bm + n) * H) + i4, x);
+#pragma unroll
+        for (int k = 0; k < NI; k++) {
+          const int i4 = tid + 256 * k;
+          if (i4 < H4) {
+            const float4 x = make_float4(h[b][k].x * r * g[k].x, h[b][k].y * r * g[k].y, h[b][k].z * r * g[k].z,
+                                         h[b][k].w * r * g[k].w);
+            __stcg((float4*)(xl + n * H) + i4, x);
+            if (keep) __stcg((float4*)(p.xdbg + ((size_t)l * Bm + n) * H) + i4, x);
+          }
+        }
       }
     }
     return csync();

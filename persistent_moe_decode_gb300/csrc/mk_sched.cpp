@@ -14,6 +14,8 @@
 // of the same layer, or at the previous layer).
 #include "mk_sched.h"
 
+#include <math.h>
+
 #include <algorithm>
 #include <array>
 
@@ -74,16 +76,33 @@ Desc task(int op, int layer, int a0, int a1) {
 int attention_sms(const mk_config& c, int n_sm, int batch, const int32_t* seq_lens) {
   if (n_sm < 2) return n_sm;
   if (c.n_attn_claimers > 0) return c.n_attn_claimers < n_sm ? c.n_attn_claimers : n_sm;
-  double kv = 0.0;
-  for (int b = 0; b < batch; b++) kv += (double)(seq_lens[b] + 1);
-  kv *= 2.0 * c.n_kv_heads * c.head_dim * 2.0;
+  double keys = 0.0;
+  for (int b = 0; b < batch; b++) keys += (double)(seq_lens[b] + 1);
+  const double kv = keys * 2.0 * c.n_kv_heads * c.head_dim * 2.0;
   const double experts = (double)std::min(c.n_experts, batch * c.top_k);
   const double moe = experts * 3.0 * c.moe_inter * c.hidden * 2.0;   // gate, up and down
-  // a KV byte costs the attention branch about 1.6 times what an expert byte
-  // costs the expert branch (query staging, the merges and the combine come
-  // on top of the stream; measured on the 30B/3.3B model, 8K context)
-  constexpr double kKvWeight = 1.6;
-  int na = (int)(n_sm * kKvWeight * kv / (kKvWeight * kv + moe) + 0.5);
+  // The branches split the SMs in proportion to their bytes, a KV byte
+  // weighted by w against an expert byte.  w folds in what the bytes do not
+  // say: at short contexts the attention's fixed work per layer (query
+  // staging, the merges, the combine) weighs more, and with several tokens
+  // the expert GEMVs cost more per byte.  Fitted to the measured best splits
+  // on the 30B/3.3B model: 40 attention SMs at batch 1 with 8K context
+  // (w = 1.6), 128 at 256K, 20-24 at batch 4 with 8K, 22-26 at batch 16 with
+  // contexts of 1K-32K.
+  const double mean_ctx = keys / batch;
+  const double w = 1.6 * pow(8192.0 / mean_ctx, 0.22) / pow((double)batch, 0.45);
+  double ideal = n_sm * w * kv / (w * kv + moe);
+  // several tokens: at least 16 % of the SMs on the attention branch.  As the
+  // contexts of a continuous batch shrink (short sequences joining), the
+  // byte share would drop to 8 % and the expert branch's per-byte cost (its
+  // multi-token GEMVs) does not follow; 16 % was the best fixed split over
+  // whole batch-16 and batch-4 runs.
+  if (batch > 1) ideal = std::max(ideal, 0.16 * n_sm);
+  // in steps of 4 SMs on a large GPU: each split has its own task lists,
+  // built and uploaded the first time it is used, and the contexts of a
+  // continuous batch move the ideal split by a few SMs every step
+  const int q = n_sm >= 64 ? 4 : 1;
+  const int na = q * (int)(ideal / q + 0.5);
   return std::max(1, std::min(n_sm - 1, na));
 }
 

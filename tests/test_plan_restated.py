@@ -184,15 +184,24 @@ def restated_split(dims, n_sm, na, lens):
 @pytest.mark.parametrize("batch", [1, 5, 16])
 @pytest.mark.parametrize("n_sm", [152, 7])
 def test_attention_split_and_items_equal_the_restated_rules(n_sm, batch):
+    """(The attention-branch size is a float expression: the restatement
+    computes it in the same double precision as the host.)"""
     dims = A3B
     cfg = mk.make_config(dims, 16, 4096, 1 << 20)
     rng = np.random.default_rng(batch * 7 + n_sm)
     lens = rng.integers(1, 40000, size=batch).astype(np.int32)
     plan = mk.mk_plan_step(cfg, n_sm, batch, lens)
-    # attention SMs: KV bytes weighted 1.6 against the routed experts' bytes
-    kv = 1.6 * float(np.sum(lens + 1)) * 2 * dims.n_kv_heads * dims.head_dim * 2
+    # attention SMs: KV bytes weighted by 1.6 (8192 / mean context)^0.22 / batch^0.45
+    # against the routed experts' bytes
+    keys = float(np.sum(lens.astype(np.float64) + 1))
+    w = 1.6 * (8192.0 / (keys / batch)) ** 0.22 / batch ** 0.45
+    kv = w * keys * 2 * dims.n_kv_heads * dims.head_dim * 2
     moe = min(dims.n_experts, batch * dims.top_k) * 3.0 * dims.moe_inter * dims.hidden * 2
-    na = max(1, min(n_sm - 1, int(n_sm * kv / (kv + moe) + 0.5)))
+    q = 4 if n_sm >= 64 else 1                    # in steps of 4 SMs on a large GPU
+    ideal = n_sm * kv / (kv + moe)
+    if batch > 1:                                 # at least 16 % of the SMs with several tokens
+        ideal = max(ideal, 0.16 * n_sm)
+    na = max(1, min(n_sm - 1, q * int(ideal / q + 0.5)))
     assert plan["n_attn"] == na
     items, off = restated_split(dims, n_sm, na, lens)
     got = plan["items"]
