@@ -50,11 +50,15 @@ class _Dims(C.Structure):
 _PP = C.POINTER(C.c_void_p)
 
 
+class _Fp8(C.Structure):
+    _fields_ = [(n, _PP) for n in ("q_gate", "q_up", "q_down", "s_gate", "s_up", "s_down")]
+
+
 class _Model(C.Structure):
     _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p), ("final_norm", C.c_void_p),
                 ("attn_norm", _PP), ("w_qkv", _PP), ("w_o", _PP), ("w_router", _PP),
                 ("w_gate", _PP), ("w_up", _PP), ("w_down", _PP),
-                ("k_pool", _PP), ("v_pool", _PP)]
+                ("k_pool", _PP), ("v_pool", _PP), ("fp8", C.POINTER(_Fp8))]
 
 
 class _Trace(C.Structure):
@@ -78,6 +82,9 @@ def lib():
             L.orc_rmsnorm.argtypes = [i32, vp, vp, dbl, vp]
             L.orc_rope.argtypes = [i32, vp, C.c_long, dbl]
             L.orc_matvec.argtypes = [i32, i32, vp, i32, vp, vp]
+            L.orc_e4m3_to_double.restype = dbl
+            L.orc_e4m3_to_double.argtypes = [C.c_uint8]
+            L.orc_matvec_e4m3.argtypes = [i32, i32, vp, vp, vp, vp]
             L.orc_paged_attention.argtypes = [C.POINTER(_Dims), vp, vp, vp, i32, i32, vp, vp]
             L.orc_paged_attention.restype = i32
             L.orc_route.argtypes = [i32, i32, vp, vp, vp, vp]
@@ -165,6 +172,25 @@ def matvec(w_bits, x) -> np.ndarray:
     return y[0] if x.ndim == 1 else y
 
 
+def e4m3_to_f64(codes) -> np.ndarray:
+    """OCP E4M3 byte -> value (orc_e4m3_to_double), elementwise."""
+    c = np.asarray(codes, dtype=np.uint8)
+    f = lib().orc_e4m3_to_double
+    return np.array([f(int(v)) for v in c.reshape(-1)], dtype=np.float64).reshape(c.shape)
+
+
+def matvec_e4m3(q, scale, x) -> np.ndarray:
+    """y[r] = sum_c (scale[r] * e4m3(q[r][c])) * x[c] (orc_matvec_e4m3)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    sc = np.ascontiguousarray(scale, dtype=np.float32)
+    x = _f64(x)
+    rows, cols = q.shape
+    assert sc.shape == (rows,) and x.shape == (cols,)
+    y = np.empty(rows, dtype=np.float64)
+    lib().orc_matvec_e4m3(rows, cols, _p(q), _p(sc), _p(x), _p(y))
+    return y
+
+
 def _dims(d: dict, num_pages: int) -> _Dims:
     return _Dims(n_layers=d["n_layers"], hidden=d["hidden"], n_q_heads=d["n_q_heads"],
                  n_kv_heads=d["n_kv_heads"], head_dim=d["head_dim"], n_experts=d["n_experts"],
@@ -208,12 +234,23 @@ class Oracle:
     oracle.h (stacked over a leading layer axis where per-layer).  ``k_pool`` /
     ``v_pool`` are [L, pages, hkv, P, d] uint16 arrays that the oracle appends
     the new K/V to (the caller keeps ownership).
+
+    ``fp8``, if given, maps q_gate, q_up, q_down (uint8 E4M3 codes, [L, E, I,
+    H] / [L, E, H, I]) and s_gate, s_up, s_down (float32 per-row scales, [L,
+    E, I] / [L, E, H]) to arrays: the routed experts then use those weights
+    (orc_fp8_experts) and w_gate / w_up / w_down may be omitted.
     """
 
     PER_LAYER = ("attn_norm", "w_qkv", "w_o", "w_router", "w_gate", "w_up", "w_down")
+    FP8 = ("q_gate", "q_up", "q_down", "s_gate", "s_up", "s_down")
 
-    def __init__(self, dims: dict, weights: dict, k_pool: np.ndarray, v_pool: np.ndarray):
+    def __init__(self, dims: dict, weights: dict, k_pool: np.ndarray, v_pool: np.ndarray,
+                 fp8: dict | None = None):
         self.dims = dict(dims)
+        weights = dict(weights)
+        if fp8 is not None:
+            for n in ("w_gate", "w_up", "w_down"):
+                weights.setdefault(n, np.zeros((self.dims["n_layers"], 1), dtype=np.uint16))
         self.w = {n: _u16(a) for n, a in weights.items()}
         self.k_pool = _u16(k_pool)
         self.v_pool = _u16(v_pool)
@@ -234,6 +271,19 @@ class Oracle:
                          final_norm=self.w["final_norm"].ctypes.data,
                          **{n: ptrs(self.w[n]) for n in self.PER_LAYER},
                          k_pool=ptrs(self.k_pool), v_pool=ptrs(self.v_pool))
+        self.fp8 = None
+        if fp8 is not None:
+            E, I, H = self.dims["n_experts"], self.dims["moe_inter"], self.dims["hidden"]
+            shapes = {"q_gate": (E, I, H), "q_up": (E, I, H), "q_down": (E, H, I),
+                      "s_gate": (E, I), "s_up": (E, I), "s_down": (E, H)}
+            self.fp8 = {}
+            for n in self.FP8:
+                a = np.asarray(fp8[n])
+                assert a.dtype == (np.uint8 if n[0] == "q" else np.float32) and a.flags.c_contiguous, n
+                assert a.shape[1:] == shapes[n] and a.shape[0] >= L, n
+                self.fp8[n] = a
+            self._f8 = _Fp8(**{n: ptrs(self.fp8[n]) for n in self.FP8})
+            self._m.fp8 = C.pointer(self._f8)
 
     def moe(self, layer: int, x, idx, w, flags: int = 0) -> np.ndarray:
         x = _f64(x)

@@ -114,6 +114,32 @@ void orc_matvec(int rows, int cols, const uint16_t* w, int nvec, const double* x
   }
 }
 
+/* ------------------------------------------------------------- E4M3
+ * The OCP 8-bit floating point specification, E4M3: sign bit 7, exponent
+ * bits 6..3 with bias 7, mantissa bits 2..0.  Exponent field 0 holds the
+ * subnormals (m / 8) * 2^-6; the encoding has no infinities and uses
+ * S.1111.111 for NaN, so the largest finite magnitude is 1.75 * 2^8 = 448. */
+double orc_e4m3_to_double(uint8_t b) {
+  const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+/* The dequantised row w[c] = scale[r] * e4m3(q[r][c]) (exact in fp64), then
+ * the same sum as orc_matvec. */
+void orc_matvec_e4m3(int rows, int cols, const uint8_t* q, const float* scale, const double* x,
+                     double* y) {
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; r++) {
+    const uint8_t* qr = q + (size_t)r * cols;
+    const double s = (double)scale[r];
+    double acc = 0.0;
+    for (int c = 0; c < cols; c++) acc += (s * orc_e4m3_to_double(qr[c])) * x[c];
+    y[r] = acc;
+  }
+}
+
 /* --------------------------------------------------- paged attention
  * §Tasks, ATTN_DECODE / Fig 2 (paged attention): one query head against the
  * n_keys cached keys of its KV head, key p read at physical page
@@ -199,17 +225,21 @@ void orc_moe(const orc_dims* dm, const orc_model* m, int layer, const double* x,
   for (int i = 0; i < H; i++) out[i] = 0.0;
   for (int j = 0; j < n_sel; j++) {
     int e = idx[j];
-    const uint16_t* wg = m->w_gate[layer] + (size_t)e * I * H;
-    const uint16_t* wu = m->w_up[layer] + (size_t)e * I * H;
-    const uint16_t* wd = m->w_down[layer] + (size_t)e * H * I;
-    orc_matvec(I, H, wg, 1, x, g);
-    orc_matvec(I, H, wu, 1, x, u);
+    const orc_fp8_experts* f = m->fp8;
+    if (f) {
+      orc_matvec_e4m3(I, H, f->q_gate[layer] + (size_t)e * I * H, f->s_gate[layer] + (size_t)e * I, x, g);
+      orc_matvec_e4m3(I, H, f->q_up[layer] + (size_t)e * I * H, f->s_up[layer] + (size_t)e * I, x, u);
+    } else {
+      orc_matvec(I, H, m->w_gate[layer] + (size_t)e * I * H, 1, x, g);
+      orc_matvec(I, H, m->w_up[layer] + (size_t)e * I * H, 1, x, u);
+    }
     for (int i = 0; i < I; i++) {
       double silu = g[i] / (1.0 + exp(-g[i]));
       g[i] = silu * u[i];
       if (flags & ORC_BF16_A) g[i] = orc_round_bf16(g[i]);
     }
-    orc_matvec(H, I, wd, 1, g, y);
+    if (f) orc_matvec_e4m3(H, I, f->q_down[layer] + (size_t)e * H * I, f->s_down[layer] + (size_t)e * H, g, y);
+    else orc_matvec(H, I, m->w_down[layer] + (size_t)e * H * I, 1, g, y);
     for (int i = 0; i < H; i++) out[i] += w[j] * y[i];
   }
   free(g); free(u); free(y);

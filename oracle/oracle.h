@@ -38,6 +38,22 @@ typedef struct {
   double rope_theta, rms_eps;
 } orc_dims;
 
+/* Optional 8-bit routed-expert weights.  Format: the OCP 8-bit floating
+ * point specification's E4M3 (1 sign bit, 4 exponent bits with bias 7,
+ * 3 mantissa bits; exponent field 0 = subnormal m/8 * 2^-6; no infinities,
+ * S.1111.111 is NaN), one fp32 scale per output row: the weight is
+ * scale[row] * e4m3(q[row][col]).  Layouts: q_gate, q_up [E][I][H] and
+ * q_down [E][H][I] bytes; s_gate, s_up [E][I] and s_down [E][H] fp32; each a
+ * per-layer pointer array. */
+typedef struct {
+  const uint8_t* const* q_gate;
+  const uint8_t* const* q_up;
+  const uint8_t* const* q_down;
+  const float* const* s_gate;
+  const float* const* s_up;
+  const float* const* s_down;
+} orc_fp8_experts;
+
 /* BF16 weights as raw uint16 bit patterns, row-major.
  * Per-layer pointers: attn_norm [H]; w_qkv [(hq+2hkv)*d][H] (q heads, k heads,
  * v heads); w_o [H][hq*d]; w_router [E][H]; w_gate, w_up [E][I][H];
@@ -55,6 +71,7 @@ typedef struct {
   const uint16_t* const* w_down;
   uint16_t* const* k_pool;
   uint16_t* const* v_pool;
+  const orc_fp8_experts* fp8;  /* NULL: the experts use w_gate / w_up / w_down   */
 } orc_model;
 
 /* Optional per-layer record of intermediate values; any pointer may be NULL. */
@@ -82,6 +99,10 @@ void orc_rmsnorm(int n, const double* h, const uint16_t* gain, double eps, doubl
 void orc_rope(int d, double* v, long pos, double theta);
 void orc_matvec(int rows, int cols, const uint16_t* w, int nvec, const double* x,
                 double* y);
+double orc_e4m3_to_double(uint8_t b);
+/* y[r] = sum_c (scale[r] * e4m3(q[r][c])) * x[c], summed as orc_matvec sums */
+void orc_matvec_e4m3(int rows, int cols, const uint8_t* q, const float* scale, const double* x,
+                     double* y);
 int orc_paged_attention(const orc_dims* dm, const uint16_t* k_pool, const uint16_t* v_pool,
                         const int32_t* page_table, int n_keys, int kv_head,
                         const double* q, double* out);

@@ -43,8 +43,11 @@ class ModelDims:
         return 2 * (self.qkv_rows * H + H * self.n_q_heads * self.head_dim
                     + self.n_experts * H + H)
 
-    def expert_bytes(self) -> int:
-        """BF16 bytes of one expert's gate, up and down matrices."""
+    def expert_bytes(self, expert_format: str = "bf16") -> int:
+        """Bytes of one expert's gate, up and down matrices: BF16, or E4M3
+        bytes plus one fp32 scale per row (2 I + H rows)."""
+        if expert_format == "fp8":
+            return 3 * self.moe_inter * self.hidden + 4 * (2 * self.moe_inter + self.hidden)
         return 2 * 3 * self.moe_inter * self.hidden
 
     def kv_bytes_per_token(self) -> int:
@@ -71,6 +74,7 @@ class Workload:
     join_context: int = 1024
     seed: int = 0
     extra: dict = field(default_factory=dict)
+    expert_format: str = "bf16"   # "bf16", or "fp8": routed experts in E4M3 + per-row scales
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -117,10 +121,16 @@ WORKLOADS = {
                        churn=True, join_context=100),
     "a3b4_b3": Workload("a3b4_b3", replace(A3B, n_layers=4), batch=3, context=0, steps=3,
                         ragged=(200, 1500), churn=True, join_context=100),
+    # 8-bit (E4M3) routed experts with per-row scales, batch 1: the tiny and
+    # mid models for parity, the 30B/3.3B shape at 8K for throughput
+    "tiny_fp8": Workload("tiny_fp8", TINY, batch=1, context=64, steps=8, expert_format="fp8"),
+    "mid_fp8": Workload("mid_fp8", MID, batch=1, context=8192, steps=32, expert_format="fp8"),
+    "a3b_8k_fp8": Workload("a3b_8k_fp8", A3B, batch=1, context=8192, steps=128, expert_format="fp8"),
 }
 
 
-def algorithmic_bytes(dims: ModelDims, n_distinct_experts_per_layer, keys_per_seq) -> int:
+def algorithmic_bytes(dims: ModelDims, n_distinct_experts_per_layer, keys_per_seq,
+                      expert_format: str = "bf16") -> int:
     """Bytes one decode step must move (the Speed-of-Light numerator).
 
     Dense weights of every layer, the distinct routed experts of every layer,
@@ -129,7 +139,7 @@ def algorithmic_bytes(dims: ModelDims, n_distinct_experts_per_layer, keys_per_se
     ``n_distinct_experts_per_layer`` is a list of per-layer counts.
     """
     dense = dims.n_layers * dims.layer_dense_bytes() + 2 * dims.hidden
-    experts = sum(int(n) for n in n_distinct_experts_per_layer) * dims.expert_bytes()
+    experts = sum(int(n) for n in n_distinct_experts_per_layer) * dims.expert_bytes(expert_format)
     per_tok = dims.n_layers * 2 * dims.n_kv_heads * dims.head_dim * 2
     kv = sum(int(n) for n in keys_per_seq) * per_tok
     lm = 2 * dims.vocab * dims.hidden

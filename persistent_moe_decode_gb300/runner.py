@@ -21,7 +21,8 @@ class StepRunner:
         self.dims = wl.dims
         self.seed = wl.seed if seed is None else seed
         self.device = torch.device(device)
-        self.model = model if model is not None else make_model(wl.dims, self.seed, self.device)
+        self.model = model if model is not None else make_model(wl.dims, self.seed, self.device,
+                                                                 wl.expert_format)
         self.batch = DecodeBatch(wl, self.seed)
         self.k_pool, self.v_pool = make_kv_pools(wl.dims, self.batch.num_pages, wl.kv_std,
                                                  self.seed, self.device)

@@ -14,7 +14,12 @@ synthetic KV cache with random weights):
   activations vanish; the offset keeps a wrong gain index visible);
 * KV pools: BF16 of N(0, kv_std^2) in 16-token pages, physical pages taken from
   a seeded random permutation of the pool;
-* tokens: uniform over the vocabulary.
+* tokens: uniform over the vocabulary;
+* 8-bit experts (``expert_format="fp8"``): the same BF16 expert matrices,
+  quantised per output row to the OCP E4M3 encoding with scale
+  max|row| / 448 (fp32; 448 is E4M3's largest finite value): byte =
+  E4M3(w / scale), round to nearest even.  Both implementations take the
+  bytes and scales as their inputs.
 """
 from __future__ import annotations
 
@@ -80,19 +85,41 @@ class SynthModel:
     w_gate: torch.Tensor
     w_up: torch.Tensor
     w_down: torch.Tensor
+    # 8-bit experts: q_gate, q_up [L, E, I, H] and q_down [L, E, H, I] uint8
+    # (E4M3 codes), s_gate, s_up [L, E, I] and s_down [L, E, H] fp32; the BF16
+    # w_gate / w_up / w_down are then empty ([L, 0])
+    fp8: dict | None = None
 
     NAMES = ("embed", "lm_head", "final_norm", "attn_norm", "w_qkv", "w_o",
              "w_router", "w_gate", "w_up", "w_down")
+    FP8_NAMES = ("q_gate", "q_up", "q_down", "s_gate", "s_up", "s_down")
 
     def to(self, device) -> "SynthModel":
         kw = {n: getattr(self, n).to(device) for n in self.NAMES}
-        return SynthModel(self.dims, **kw)
+        f8 = None if self.fp8 is None else {n: t.to(device) for n, t in self.fp8.items()}
+        return SynthModel(self.dims, **kw, fp8=f8)
 
     def nbytes(self) -> int:
-        return sum(getattr(self, n).numel() * 2 for n in self.NAMES)
+        n = sum(getattr(self, n).numel() * 2 for n in self.NAMES)
+        if self.fp8 is not None:
+            n += sum(t.numel() * t.element_size() for t in self.fp8.values())
+        return n
 
 
-def make_model(dims: ModelDims, seed: int = 0, device="cpu") -> SynthModel:
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3_rows(w: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
+    """Per-row E4M3 quantisation of a [..., rows, cols] BF16 tensor: (codes
+    uint8 [..., rows, cols], scales fp32 [..., rows]), scale = max|row| / 448."""
+    wf = w.float()
+    amax = wf.abs().amax(dim=-1)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    q = (wf / scale.unsqueeze(-1)).clamp_(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8), scale
+
+
+def make_model(dims: ModelDims, seed: int = 0, device="cpu", expert_format: str = "bf16") -> SynthModel:
     L, H, E, I = dims.n_layers, dims.hidden, dims.n_experts, dims.moe_inter
     V = dims.vocab
     qd = dims.n_q_heads * dims.head_dim
@@ -102,6 +129,31 @@ def make_model(dims: ModelDims, seed: int = 0, device="cpu") -> SynthModel:
         for l in range(L):
             out[l] = _normal_bf16(shape, _seed_for(seed, name, l), device, std, mean)
         return out
+
+    fp8 = None
+    if expert_format == "fp8":
+        fp8 = {}
+        for name, shape in (("w_gate", (E, I, H)), ("w_up", (E, I, H)), ("w_down", (E, H, I))):
+            q = torch.empty((L,) + shape, dtype=torch.uint8, device=device)
+            sc = torch.empty((L,) + shape[:2], dtype=torch.float32, device=device)
+            for l in range(L):
+                q[l], sc[l] = quantize_e4m3_rows(_normal_bf16(shape, _seed_for(seed, name, l), device,
+                                                              WEIGHT_STD))
+            fp8["q" + name[1:]] = q
+            fp8["s" + name[1:]] = sc
+        empty = torch.empty((L, 0), dtype=torch.bfloat16, device=device)
+        return SynthModel(
+            dims=dims,
+            embed=_normal_bf16((V, H), _seed_for(seed, "embed"), device, WEIGHT_STD),
+            lm_head=_normal_bf16((V, H), _seed_for(seed, "lm_head"), device, WEIGHT_STD),
+            final_norm=_normal_bf16((H,), _seed_for(seed, "final_norm"), device, WEIGHT_STD, 1.0),
+            attn_norm=stack("attn_norm", (H,), WEIGHT_STD, 1.0),
+            w_qkv=stack("w_qkv", (dims.qkv_rows, H)),
+            w_o=stack("w_o", (H, qd)),
+            w_router=stack("w_router", (E, H)),
+            w_gate=empty, w_up=empty, w_down=empty, fp8=fp8)
+    if expert_format != "bf16":
+        raise ValueError(f"unknown expert format {expert_format!r}")
 
     return SynthModel(
         dims=dims,

@@ -16,7 +16,7 @@ import numpy as np
 import torch
 
 import oracle
-from tests._util import dims_dict, host_pool, host_weights
+from tests._util import dims_dict, host_fp8, host_pool, host_weights
 
 MAX_ABS, REL_L2, GAP = 2e-2, 1e-2, 1e-3
 
@@ -54,7 +54,8 @@ class Pair:
         self.wl = wl
         self.run = StepRunner(wl, device="cuda", **cfg_kw)
         self.orc = oracle.Oracle(dims_dict(wl.dims), host_weights(self.run.model),
-                                 host_pool(self.run.k_pool), host_pool(self.run.v_pool))
+                                 host_pool(self.run.k_pool), host_pool(self.run.v_pool),
+                                 fp8=host_fp8(self.run.model))
 
     def step(self, trace=False):
         b = self.run.batch

@@ -39,7 +39,14 @@ def host_pool(t: torch.Tensor) -> np.ndarray:
     return bf16_bits(t.contiguous()).copy()
 
 
+def host_fp8(model: SynthModel) -> dict | None:
+    """Host numpy copies of the 8-bit experts (codes uint8, scales float32), or None."""
+    if model.fp8 is None:
+        return None
+    return {n: t.cpu().contiguous().numpy() for n, t in model.fp8.items()}
+
+
 def make_oracle(model: SynthModel, k_pool: torch.Tensor, v_pool: torch.Tensor):
     import oracle
     return oracle.Oracle(dims_dict(model.dims), host_weights(model), host_pool(k_pool),
-                         host_pool(v_pool))
+                         host_pool(v_pool), fp8=host_fp8(model))
