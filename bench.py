@@ -125,10 +125,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def step_bytes(dims, routing_idx, keys_per_seq):
+def step_bytes(dims, routing_idx, keys_per_seq, expert_format="bf16"):
     from persistent_moe_decode_gb300.configs import algorithmic_bytes
     distinct = [len(set(routing_idx[l].reshape(-1).tolist())) for l in range(dims.n_layers)]
-    return algorithmic_bytes(dims, distinct, keys_per_seq)
+    return algorithmic_bytes(dims, distinct, keys_per_seq, expert_format)
 
 
 class CpuSample:
@@ -152,8 +152,10 @@ class CpuSample:
             w[name] = bf16_bits(t.cpu().contiguous())
         kp = bf16_bits(k_pool[:n].cpu().contiguous()).copy()
         vp = bf16_bits(v_pool[:n].cpu().contiguous()).copy()
+        fp8 = None if model.fp8 is None else \
+            {name: t[:n].cpu().contiguous().numpy() for name, t in model.fp8.items()}
         self.oracle = oracle
-        self.orc = oracle.Oracle({**dataclasses.asdict(d), "n_layers": n}, w, kp, vp)
+        self.orc = oracle.Oracle({**dataclasses.asdict(d), "n_layers": n}, w, kp, vp, fp8=fp8)
         self.d, self.n, self.lm_frac, self.wl = d, n, lm_frac, wl
         tokens, lens, pt = state
         self.B = len(tokens)
@@ -208,7 +210,7 @@ def run_reference(args, wl):
     d = wl.dims
     n = min(args.ref_layers, d.n_layers)
     small = type(d)(**{**d.__dict__, "n_layers": n})
-    model = make_model(small, wl.seed, "cpu")
+    model = make_model(small, wl.seed, "cpu", wl.expert_format)
     batch = DecodeBatch(wl)
     kp, vp = make_kv_pools(small, batch.num_pages, wl.kv_std, wl.seed, "cpu")
     model.dims = d
@@ -289,7 +291,7 @@ def device_timed(run, wl, args, stream, tok_seq, dist=None, clocks=None):
 
 def roofline_of(run, wl, kern_ms, keys, traffic_key):
     idx, _ = run.dec.routing()
-    bytes_step = step_bytes(wl.dims, idx, keys)
+    bytes_step = step_bytes(wl.dims, idx, keys, wl.expert_format)
     peak, peak_kind = load_peaks()
     achieved = bytes_step / (kern_ms / 1000.0) / 1e9
     return bytes_step, {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -442,7 +444,9 @@ def main():
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.expert_format == "bf16" else "bf16 (routed experts e4m3 + fp32 row scales)",
+        "data": "synthetic",
         "config": {"workload": wl.name + (f" (first {args.layers} layers)" if args.layers else ""),
                    "batch": B, "context": context_of(state[1]),
                    "context_note": "cached tokens at the first timed step",

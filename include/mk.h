@@ -108,7 +108,24 @@ typedef struct {
                              branch (its streams would otherwise take HBM
                              bandwidth from the attention branch, which is on
                              the critical path), else 5                      */
+  int expert_format;      /* enum mk_expert_format: how w_gate / w_up / w_down
+                             hold the routed experts' weights                 */
 } mk_config;
+
+/* Weight format of the routed experts (mk_config.expert_format).
+ *   MK_EXPERTS_BF16     w_gate / w_up / w_down are BF16 (below).
+ *   MK_EXPERTS_FP8_E4M3 they hold bytes in the OCP 8-bit floating point
+ *                       E4M3 encoding (bias 7, no infinities), one fp32
+ *                       scale per output row in s_gate / s_up / s_down:
+ *                       weight = scale[row] * e4m3(byte).  Supported with
+ *                       max_batch == 1, hidden 256, 512, 1024 or 2048 and
+ *                       moe_inter a multiple of 16 (else
+ *                       MK_ERR_BAD_CONFIG).  Halves the experts' bytes, the
+ *                       largest share of a decode step (the pages name 8-bit
+ *                       weights as the next step on Blackwell: "Inside the
+ *                       megakernel serving engine for North Mini Code",
+ *                       §Next steps). */
+enum mk_expert_format { MK_EXPERTS_BF16 = 0, MK_EXPERTS_FP8_E4M3 = 1 };
 
 /*
  * Weights and KV pools, all owned by the caller, all device pointers, all
@@ -122,6 +139,10 @@ typedef struct {
  *   w_router[l]      [E][H]
  *   w_gate[l], w_up[l]  [E][I][H]
  *   w_down[l]        [E][H][I]          (read once, at mk_create: see there)
+ *   s_gate[l], s_up[l]  [E][I] fp32,  s_down[l]  [E][H] fp32: the per-row
+ *                    scales of 8-bit experts (MK_EXPERTS_FP8_E4M3; the three
+ *                    matrices above then hold E4M3 bytes in the same
+ *                    layouts); NULL with BF16 experts
  *   k_pool[l], v_pool[l]  [num_kv_pages][hkv][page_size][d]  (written: the
  *                    step stores its new K/V, post-RoPE, at position seq_len)
  * Every pointer must be 16-byte aligned.
@@ -139,6 +160,9 @@ typedef struct {
   const void* const* w_down;
   void* const* k_pool;
   void* const* v_pool;
+  const void* const* s_gate;
+  const void* const* s_up;
+  const void* const* s_down;
 } mk_weights;
 
 /* Device error word, read by mk_step_status. */
@@ -160,10 +184,11 @@ typedef struct mk_handle mk_handle;
  * queues, task lists: MK_ERR_OOM on failure) and builds the per-layer waves.
  *
  * Weight snapshot: mk_create also copies every layer's w_down into a
- * library-owned device array in a blocked layout, [L][E][I / 8][H][8] BF16
- * (each 8-column group of an expert's down projection contiguous), and the
- * decode step reads that copy, not w_down.  It costs L * E * I * H * 2 bytes
- * of device memory (19.3 GB for L = 48, E = 128, I = 768, H = 2048), counted
+ * library-owned device array in a blocked layout, [L][E][I / 8][H][8]
+ * elements (each 8-column group of an expert's down projection contiguous;
+ * BF16, or E4M3 bytes with 8-bit experts), and the decode step reads that
+ * copy, not w_down.  It costs L * E * I * H * 2 bytes (BF16; half with 8-bit
+ * experts) of device memory (19.3 GB for L = 48, E = 128, I = 768, H = 2048), counted
  * in mk_device_bytes, and is made with a device-wide synchronize before
  * mk_create returns.  Changes the caller makes to w_down after mk_create are
  * therefore NOT seen by later steps: destroy and re-create the handle to pick

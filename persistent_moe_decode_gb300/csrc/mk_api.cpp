@@ -25,6 +25,7 @@
 namespace mk {
 cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream);
 cudaError_t relayout_down(const uint16_t* src, uint16_t* dst, int E, int H, int I);
+cudaError_t relayout_down_e4m3(const uint8_t* src, uint8_t* dst, int E, int H, int I);
 size_t step_smem_bytes();
 int step_kernel_regs();
 int static_counters(int device, uint32_t** out);
@@ -224,8 +225,11 @@ int make_weight_maps(mk_handle* h, const mk_weights* w, const uint8_t** out) {
     int rc = make_row_map(&m[W_MAP_ROUTER], w->w_router[l], (uint64_t)c.n_experts, H);
     if (!rc) rc = make_row_map(&m[W_MAP_QKV], w->w_qkv[l], qrows, H);
     if (!rc) rc = make_row_map(&m[W_MAP_O], w->w_o[l], (uint64_t)H, KO);
-    if (!rc) rc = make_row_map(&m[W_MAP_GATE], w->w_gate[l], erows, H);
-    if (!rc) rc = make_row_map(&m[W_MAP_UP], w->w_up[l], erows, H);
+    // 8-bit experts: rows of H bytes, mapped as H / 2 two-byte columns (16
+    // rows per box instead of 8; the copy moves bytes, the kernel reads E4M3)
+    const int KE = c.expert_format == MK_EXPERTS_FP8_E4M3 ? H / 2 : H;
+    if (!rc) rc = make_row_map(&m[W_MAP_GATE], w->w_gate[l], erows, KE);
+    if (!rc) rc = make_row_map(&m[W_MAP_UP], w->w_up[l], erows, KE);
     if (rc) return rc;
   }
   int rc = make_row_map(&maps.back(), w->lm_head, (uint64_t)c.vocab, H);
@@ -279,13 +283,18 @@ int make_moe_map(mk_handle* h, float* mpart, const uint8_t** mp) {
 int make_down_blocks(mk_handle* h, const mk_weights* w, const uint16_t** out) {
   const mk_config& c = h->cfg;
   const size_t per_layer = (size_t)c.n_experts * c.moe_inter * c.hidden;
+  const bool fp8 = c.expert_format == MK_EXPERTS_FP8_E4M3;
   uint16_t* d = nullptr;
-  int rc = dalloc(h, &d, per_layer * c.n_layers);
+  // elements of 2 bytes (BF16), or bytes (E4M3: half as many 2-byte words)
+  int rc = dalloc(h, &d, fp8 ? per_layer * c.n_layers / 2 : per_layer * c.n_layers);
   if (rc) return rc;
-  for (int l = 0; l < c.n_layers; l++)
-    if (relayout_down((const uint16_t*)w->w_down[l], d + per_layer * l, c.n_experts, c.hidden, c.moe_inter) !=
-        cudaSuccess)
-      return MK_ERR_CUDA;
+  for (int l = 0; l < c.n_layers; l++) {
+    const cudaError_t e =
+        fp8 ? relayout_down_e4m3((const uint8_t*)w->w_down[l], (uint8_t*)d + per_layer * l, c.n_experts, c.hidden,
+                                 c.moe_inter)
+            : relayout_down((const uint16_t*)w->w_down[l], d + per_layer * l, c.n_experts, c.hidden, c.moe_inter);
+    if (e != cudaSuccess) return MK_ERR_CUDA;
+  }
   if (cudaDeviceSynchronize() != cudaSuccess) return MK_ERR_CUDA;
   *out = d;
   return MK_OK;
@@ -471,6 +480,13 @@ int mk_create(const mk_config* cfg, const mk_weights* w, mk_handle** out) {
   TRY(upload_ptrs(h, (const void* const*)w->w_gate, L, (const void* const**)&p.w_gate));
   TRY(upload_ptrs(h, (const void* const*)w->w_up, L, (const void* const**)&p.w_up));
   TRY(upload_ptrs(h, (const void* const*)w->w_down, L, (const void* const**)&p.w_down));
+  p.fp8 = c.expert_format == MK_EXPERTS_FP8_E4M3;
+  if (p.fp8) {
+    if (!w->s_gate || !w->s_up || !w->s_down) { mk_destroy(h); return MK_ERR_BAD_ARG; }
+    TRY(upload_ptrs(h, (const void* const*)w->s_gate, L, (const void* const**)&p.s_gate));
+    TRY(upload_ptrs(h, (const void* const*)w->s_up, L, (const void* const**)&p.s_up));
+    TRY(upload_ptrs(h, (const void* const*)w->s_down, L, (const void* const**)&p.s_down));
+  }
   TRY(upload_ptrs(h, (const void* const*)w->k_pool, L, (const void* const**)&p.k_pool));
   TRY(upload_ptrs(h, (const void* const*)w->v_pool, L, (const void* const**)&p.v_pool));
   TRY(make_kv_maps(h, w, &p.kv_maps));

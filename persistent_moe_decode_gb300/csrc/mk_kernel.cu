@@ -98,6 +98,8 @@ struct __align__(128) Smem {
   unsigned long long t_mark[4];             // timeline: first stage, stages done, reduced
   unsigned long long t_swait;               // timeline: time warp 0 waited for stages
   volatile int32_t abort_flag;
+  int32_t xq_layer;                         // 8-bit experts: layer whose x terms are staged (-1: none)
+  float xq_s0, aq_s0;                       // first-term scales of the staged x / hidden terms
 };
 // the dynamic shared memory is rounded up to a 1024-byte boundary (the
 // swizzled tensor copies of KV pages need it), hence the extra 1 KB
@@ -701,15 +703,38 @@ struct Prod {
       // the piece's gate rows, its up rows, then each of its groups of the
       // down projection (an [H][8] block, streamed as H rows of 8): one
       // stream loop for all of them keeps the code short
-      const size_t eo = (size_t)e * p.I * H;
-      const uint16_t* blk = p.wd_blk + (((size_t)l * p.E + e) * G + i0 / 8) * H * 8;
-      for (int sg = 0; sg < 2 + ncb; sg++) {
+      // (8-bit experts: the same rows and blocks in bytes, streamed as rows
+      // of half as many two-byte words)
+      const int es = p.fp8 ? 2 : 1;
+      const size_t eo = (size_t)e * p.I * H / es;
+      const uint16_t* blk = p.wd_blk + (((size_t)l * p.E + e) * G + i0 / 8) * H * 8 / es;
+      for (int sg = 0; sg < 2 + (p.fp8 ? 0 : ncb); sg++) {
         const bool dn = sg >= 2;
         const uint16_t* src = dn ? blk + (size_t)(sg - 2) * H * 8 : wptr(3 + sg) + eo;
         // gate / up rows through their maps: rows of the [E I][H] matrix
-        if (!stream_rows(src, dn ? 0 : (rotated_rows(H) ? e * p.I : 0) + i0, dn ? H : i1 - i0, dn ? 8 : H,
+        if (!stream_rows(src, dn ? 0 : (rotated_rows(H) ? e * p.I : 0) + i0, dn ? H : i1 - i0,
+                         (dn ? 8 : H) / es,
                          dn || !rotated_rows(H) ? nullptr : wmap(sg == 0 ? W_MAP_GATE : W_MAP_UP)))
           return false;
+      }
+      // 8-bit down projection: quads of up to four groups, a stage holding
+      // the quad's rows [h0, h0 + rd) (one 1-D copy per group)
+      if (p.fp8) {
+        const int rd = min(H, 1024);
+        const uint8_t* b8 = (const uint8_t*)blk;
+        for (int q0 = 0; q0 < ncb; q0 += 4) {
+          const int nq = min(4, ncb - q0);
+          for (int h0 = 0; h0 < H; h0 += rd) {
+            uint32_t slot;
+            if (!acquire_stage(slot)) return false;
+            if (lane == 0) mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(nq * rd * 8));
+            __syncwarp();
+            if (lane < nq)
+              bulk_g2s_hint(&S.stage[slot][lane * rd * 8], b8 + ((size_t)(q0 + lane) * H + h0) * 8,
+                            (uint32_t)(rd * 8), &S.full[slot], policy_evict_first());
+            stage_seq++;
+          }
+        }
       }
       g = ge;
     }
@@ -1735,8 +1760,204 @@ struct Cons {
     return true;
   }
 
+  // 8-bit experts: a vector v as four E4M3 terms, v ~ sum_t s_t q_t with
+  // s_t = s_0 16^-t and s_0 the power of two with max|v| / s_0 <= 448: term t
+  // rounds the remainder r_t / s_t to nearest (r_0 = v, r_{t+1} = r_t -
+  // s_t q_t), so each term adds about four bits (the remainder of a term
+  // is at most half its largest step, 16 s_t) and four terms keep x to about
+  // 16 bits of its largest element, as BF16 high + low halves would.  The
+  // terms are the N columns of E4M3 tensor-core products.
+  __device__ __forceinline__ static float e4m3_scale0(float mx) {
+    const float y = mx / 448.f;
+    if (!(y > 0.f)) return 1.f;
+    int e = ((__float_as_int(y) >> 23) & 0xff) - 127;
+    if (__float_as_int(y) & 0x7fffff) e++;           // round the exponent up unless a power of two
+    e = max(-126, min(127, e));
+    return __int_as_float((e + 127) << 23);
+  }
+  __device__ __forceinline__ static void e4m3_terms(float v, float s0, uint8_t (&q)[4]) {
+#pragma unroll
+    for (int t = 0; t < 4; t++) {
+      const float st = s0 * __int_as_float((127 - 4 * t) << 23);     // s_0 16^-t
+      const float inv = 1.f / st;                                     // a power of two: exact
+      q[t] = f2e4m3(v * inv);
+      v -= st * e4m3f(q[t]);
+    }
+  }
+
+  // the layer's x / rms as E4M3 terms in the top quarter of xs ([4][H] bytes),
+  // once per layer on this SM (every UP piece of the layer reads them); s0:
+  // their first scale (every thread computes it from the same maximum; a
+  // later piece reads the copy the first one left, ordered by the barriers
+  // between the tasks)
+  __device__ __forceinline__ bool stage_xq(float& s0) {
+    const int l = t[R_LAYER], H = p.H;
+    if (S.xq_layer == l) {
+      s0 = S.xq_s0;
+      return true;
+    }
+    const float rinv = S.rinv[0];
+    float mx = 0.f;
+    for (int k = tid; k < H; k += 256) mx = fmaxf(mx, fabsf(S.xs[k] * rinv));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) S.nred[warp][0] = mx;
+    if (!csync()) return false;
+    mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; w++) mx = fmaxf(mx, S.nred[w][0]);
+    s0 = e4m3_scale0(mx);
+    uint8_t* xq = (uint8_t*)(S.xs + kXsFloats * 3 / 4);
+    for (int k = tid; k < H; k += 256) {
+      uint8_t q[4];
+      e4m3_terms(S.xs[k] * rinv, s0, q);
+#pragma unroll
+      for (int tt = 0; tt < 4; tt++) xq[tt * H + k] = q[tt];
+    }
+    if (!csync()) return false;
+    if (tid == 0) {
+      S.xq_s0 = s0;
+      S.xq_layer = l;
+    }
+    return true;
+  }
+
+  // one token, 8-bit expert rows (E4M3) of K = 2048 columns on the tensor
+  // cores: mma.sync m16n8k32 with both operands E4M3 and fp32 accumulation.
+  // A stage holds 16 rows, copied as rows of 1024 two-byte words: column
+  // block cb (128 bytes) of row r is the 128-byte line 16 cb + r, its 16-byte
+  // chunk c stored at chunk c ^ (r & 7).  Warp w takes blocks 2 w and 2 w + 1
+  // (columns [256 w, 256 w + 256)): eight k-steps of 32 columns, each one
+  // ldmatrix of four 8 x 16-byte tiles (rows 0-7 / 8-15 x two chunks), which
+  // are exactly the A fragment, and one MMA.  N side: column t < 4 holds the
+  // x term t (stage_xq), so C[m][t] s_t summed over t is row m's dot product
+  // with x / rms.  The eight warps' sums of a row meet in shared memory
+  // (spart) and are added in warp order; the row scales are applied by the
+  // epilogue.
+  __device__ __forceinline__ bool gemv_mma_e4m3(float* res) {
+    const int ngrp = row_groups(), H = p.H;
+    float s0;
+    if (!stage_xq(s0)) return false;
+    const uint8_t* xq = (const uint8_t*)(S.xs + kXsFloats * 3 / 4);
+    // this lane's term scales (columns 2 cq, 2 cq + 1; terms 4.. are absent)
+    const float sa = cq < 2 ? s0 * __int_as_float((127 - 8 * cq) << 23) : 0.f;
+    const float sb = cq < 2 ? s0 * __int_as_float((127 - 8 * cq - 4) << 23) : 0.f;
+    uint32_t xb[8][2];
+#pragma unroll
+    for (int st = 0; st < 8; st++) {
+      const int k0 = 256 * warp + 32 * st + 4 * cq;
+      xb[st][0] = gl < 4 ? *(const uint32_t*)(xq + gl * H + k0) : 0u;
+      xb[st][1] = gl < 4 ? *(const uint32_t*)(xq + gl * H + k0 + 16) : 0u;
+    }
+    uint32_t aoff[8];
+    {
+      const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int st = 0; st < 8; st++) {
+        const int ch = 2 * st + (lane >> 4);
+        const int line = (2 * warp + (ch >> 3)) * 16 + r;
+        aoff[st] = (uint32_t)(line * 128 + (((ch & 7) ^ (r & 7)) << 4));
+      }
+    }
+    float* part = &S.spart[0][0];
+    int rbase = 0;
+    for (int g = 0; g < ngrp; g++) {
+      const int nr = group_rows(g);
+      for (int done = 0; done < nr; done += 16) {
+        const int rows = min(16, nr - done);
+        uint32_t slot;
+        if (!stage_full(slot)) return false;
+        if (TR && tid == 0 && rbase + done == 0) S.t_mark[0] = gtime_ns();
+        const uint8_t* base = S.stage[slot];
+        float ca[4] = {0.f, 0.f, 0.f, 0.f}, cc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int st = 0; st < 8; st++) {
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(r0, r1, r2, r3, base + aoff[st]);
+          mma_e4m3((st & 1) ? cc : ca, r0, r1, r2, r3, xb[st][0], xb[st][1]);
+        }
+        stage_release(slot);
+        float v0 = sa * (ca[0] + cc[0]) + sb * (ca[1] + cc[1]);      // row gl
+        float v8 = sa * (ca[2] + cc[2]) + sb * (ca[3] + cc[3]);      // row gl + 8
+        v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+        v8 += __shfl_xor_sync(0xffffffffu, v8, 1);
+        if (cq == 0) {
+          if (gl < rows) part[(rbase + done + gl) * kConsumerWarps + warp] = v0;
+          if (gl + 8 < rows) part[(rbase + done + gl + 8) * kConsumerWarps + warp] = v8;
+        }
+      }
+      rbase += nr;
+    }
+    if (TR && tid == 0) S.t_mark[1] = gtime_ns();
+    if (!csync()) return false;
+    if (tid < rbase) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; w++) v += part[tid * kConsumerWarps + w];
+      res[tid] = v;
+    }
+    return true;
+  }
+
+  // one token, 8-bit expert rows of K <= 1024 columns on the CUDA cores: row r
+  // of the chunk belongs to warp r % 8; lane l multiplies the 16-column chunks
+  // l, l + 32, ... (16 bytes each) against x / rms in registers, then one warp
+  // reduction.  NCK: 16-byte chunks per lane (K <= 512 NCK).
+  template <int NCK>
+  __device__ __forceinline__ bool gemv_row_e4m3(float* res) {
+    const int K = t[R_K];
+    const int ngrp = row_groups();
+    const int rps = rows_per_stage(K / 2);
+    const float rinv = S.rinv[0];
+    float xa[NCK][16];
+#pragma unroll
+    for (int c = 0; c < NCK; c++) {
+      const int col = (lane + 32 * c) * 16;
+#pragma unroll
+      for (int j = 0; j < 16; j++) xa[c][j] = col < K ? S.xs[col + j] * rinv : 0.f;
+    }
+    int rbase = 0;
+    for (int g = 0; g < ngrp; g++) {
+      const int nr = group_rows(g);
+      for (int done = 0; done < nr; done += rps) {
+        const int rows = min(rps, nr - done);
+        uint32_t slot;
+        if (!stage_full(slot)) return false;
+        if (TR && tid == 0 && rbase + done == 0) S.t_mark[0] = gtime_ns();
+        const uint8_t* base = S.stage[slot];
+        for (int rr = (warp - (rbase + done) % 8 + 8) % 8; rr < rows; rr += 8) {
+          const uint8_t* wrow = base + (size_t)rr * K;
+          float2 a = make_float2(0.f, 0.f);     // even / odd columns
+#pragma unroll
+          for (int c = 0; c < NCK; c++) {
+            if ((lane + 32 * c) * 16 < K) {
+              const uint4 w = lds128(wrow + (lane + 32 * c) * 16);
+              const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int q = 0; q < 4; q++) {
+                const float2 f0 = f16x2_to_float2(e4m3x2_to_f16x2(wd[q]));
+                const float2 f1 = f16x2_to_float2(e4m3x2_to_f16x2(wd[q] >> 16));
+                a = __ffma2_rn(f0, make_float2(xa[c][4 * q], xa[c][4 * q + 1]), a);
+                a = __ffma2_rn(f1, make_float2(xa[c][4 * q + 2], xa[c][4 * q + 3]), a);
+              }
+            }
+          }
+          float v = a.x + a.y;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) res[rbase + done + rr] = v;
+        }
+        stage_release(slot);
+      }
+      rbase += nr;
+    }
+    if (TR && tid == 0) S.t_mark[1] = gtime_ns();
+    return true;
+  }
+
   // epilogue of a one-token chunk (after the barrier); token 0 throughout
-  __device__ __forceinline__ void epilogue_row(const float* res) {
+  // (8-bit experts, K_UP: sg_t, su_t = the gate / up scales of row tid)
+  __device__ __forceinline__ void epilogue_row(const float* res, float sg_t = 0.f, float su_t = 0.f) {
     const int l = t[R_LAYER], kind = t[R_KIND];
     const int nr = t[R_NROWS], row0 = t[R_ROW0];
     const size_t Bm = (size_t)p.Bmax;
@@ -1756,8 +1977,11 @@ struct Cons {
         const int slot = S.rt.off[t[R_A]];
         const float wa = S.rt.w[0][S.rt.ent[slot] % p.topk];
         const float r = S.rinv[0];   // GEMV of h * gain: scale by 1 / rms
+        // 8-bit experts: the GEMV took x / rms; each row times its scale
+        // (a piece has at most 64 rows: row i is thread i's)
         for (int i = tid; i < nr; i += 256) {
-          const float a = silu_mul(res[i] * r, res[nr + i] * r);
+          const float a = p.fp8 ? silu_mul(res[i] * sg_t, res[nr + i] * su_t)
+                                : silu_mul(res[i] * r, res[nr + i] * r);
           __stcg(p.abuf + ((size_t)l * Bm * p.topk + slot) * p.I + row0 + i, a);
           S.actp[i] = wa * a;
         }
@@ -1802,6 +2026,96 @@ struct Cons {
         stage_release(slot);
       }
     }
+    return true;
+  }
+
+  // The 8-bit down projection of an UP piece on the tensor cores (mma.sync
+  // m16n8k32, E4M3 x E4M3, fp32 accumulate).  The piece's weighted hidden
+  // values (S.actp, 8 per group) are first cut into four E4M3 terms (as x is
+  // by stage_xq; kept in spart).  Its groups arrive as quads of up to four
+  // groups, a stage holding the quad's rows [hb, hb + rd) (group slot j at
+  // j rd 8 bytes, 8 bytes a row).  One MMA takes 16 rows (M) and the quad's 32
+  // columns (K): lane (gl, cq) gives the 4 bytes of columns 4 (cq & 1) .. + 3
+  // of group slot cq >> 1 (k 4 cq .. 4 cq + 3) and of slot 2 + (cq >> 1) (k 16
+  // + 4 cq ..) in rows h0 + gl and h0 + gl + 8; the B fragment holds the
+  // hidden terms of the same columns (N column t = term t).  (Each pair of
+  // row loads swaps rows between the two groups' lanes, so the 32 lanes'
+  // words fall in distinct banks.)  Warp w keeps its 16-row blocks h0 =
+  // 16 (w + 8 i) over the piece's stages; the piece's total, times the row's
+  // scale s_down[e][h] (staged in xs by op_row), goes to its first group's
+  // partial row, zeros to its other groups' rows.
+  __device__ __forceinline__ bool down_mma_e4m3() {
+    constexpr int kMaxBlk = 16;                   // 16-row blocks a warp (H <= 2048)
+    const int H = p.H, ncb = t[R_NROWS] / 8, g0 = t[R_REL0], nr = t[R_NROWS];
+    const int nb = H / 128, rd = min(H, 1024);
+    const float* scl = S.xs + kXsFloats / 2;
+    uint8_t* aq = (uint8_t*)&S.spart[0][0];       // [4][64] hidden terms
+    // the hidden values' terms (threads < nr: one value each)
+    {
+      const float v = tid < nr ? S.actp[tid] : 0.f;
+      float mx = fabsf(v);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0 && warp < 2) S.nred[warp][1] = mx;
+      if (!csync()) return false;
+      const float s0 = e4m3_scale0(fmaxf(S.nred[0][1], S.nred[1][1]));
+      if (tid < 64) {
+        uint8_t q[4];
+        e4m3_terms(v, s0, q);                     // v = 0 past nr: zero terms
+#pragma unroll
+        for (int tt = 0; tt < 4; tt++) aq[tt * 64 + tid] = q[tt];
+      }
+      if (tid == 0) S.aq_s0 = s0;
+      if (!csync()) return false;
+    }
+    const float s0 = S.aq_s0;
+    const float sa = cq < 2 ? s0 * __int_as_float((127 - 8 * cq) << 23) : 0.f;
+    const float sb = cq < 2 ? s0 * __int_as_float((127 - 8 * cq - 4) << 23) : 0.f;
+    const int g1 = cq >> 1, wsel = 4 * (cq & 1);
+    float acc[kMaxBlk][4];
+#pragma unroll
+    for (int i = 0; i < kMaxBlk; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int q0 = 0; q0 < ncb; q0 += 4) {
+      const int nq = min(4, ncb - q0);
+      const bool onl = g1 < nq, onh = 2 + g1 < nq;    // this lane's two group slots are present
+      // B: hidden terms of columns (slot g1, 4 (cq & 1) ..) and (slot 2 + g1, ..)
+      const uint32_t b0 = gl < 4 && onl ? *(const uint32_t*)(aq + gl * 64 + (q0 + g1) * 8 + wsel) : 0u;
+      const uint32_t b1 = gl < 4 && onh ? *(const uint32_t*)(aq + gl * 64 + (q0 + 2 + g1) * 8 + wsel) : 0u;
+      for (int hb = 0; hb < H; hb += rd) {
+        uint32_t slot;
+        if (!stage_full(slot)) return false;
+        const uint8_t* sl = S.stage[slot] + (size_t)g1 * rd * 8 + wsel;          // slot g1
+        const uint8_t* sh = sl + (size_t)2 * rd * 8;                              // slot 2 + g1
+#pragma unroll
+        for (int i = 0; i < kMaxBlk; i++) {
+          const int h0 = 16 * (warp + 8 * i);
+          if (i < nb && h0 >= hb && h0 < hb + rd) {
+            const int ra = 8 * (h0 - hb + gl + 8 * g1), rb = 8 * (h0 - hb + gl + 8 - 8 * g1);
+            const uint32_t la = onl ? *(const uint32_t*)(sl + ra) : 0u, lb = onl ? *(const uint32_t*)(sl + rb) : 0u;
+            const uint32_t ha = onh ? *(const uint32_t*)(sh + ra) : 0u, hb2 = onh ? *(const uint32_t*)(sh + rb) : 0u;
+            // rows h0 + gl (a0, a2) and h0 + gl + 8 (a1, a3)
+            mma_e4m3(acc[i], g1 ? lb : la, g1 ? la : lb, g1 ? hb2 : ha, g1 ? ha : hb2, b0, b1);
+          }
+        }
+        stage_release(slot);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxBlk; i++) {
+      if (i < nb) {
+        float v0 = sa * acc[i][0] + sb * acc[i][1], v8 = sa * acc[i][2] + sb * acc[i][3];
+        v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+        v8 += __shfl_xor_sync(0xffffffffu, v8, 1);
+        if (cq == 0) {
+          const int h = 16 * (warp + 8 * i) + gl;
+          __stcg(p.mpart + (size_t)g0 * H + h, v0 * scl[h]);
+          __stcg(p.mpart + (size_t)g0 * H + h + 8, v8 * scl[h + 8]);
+        }
+      }
+    }
+    // the other groups' rows: one contiguous run of (ncb - 1) H floats
+    float4* z = (float4*)(p.mpart + (size_t)(g0 + 1) * H);
+    for (int k = tid; k < (ncb - 1) * H / 4; k += 256) __stcg(z + k, make_float4(0.f, 0.f, 0.f, 0.f));
     return true;
   }
 
@@ -2461,13 +2775,29 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
     if (ok && run) ok = c.moe_reduce(res);
   } else {
     if (ok && run && kind == K_OPROJ) ok = c.wait_counter(bar_index(p, l, p.bl.comb), p.n_comb_sms) && c.stage_x();
+    // 8-bit expert piece: its row scales, loaded now so that they arrive
+    // while the gate / up rows stream (gate / up: row tid; down: rows
+    // h = tid + 256 j, staged in shared memory before the down projection)
+    float sg_t = 0.f, su_t = 0.f, sdv[8];
+    if (p.fp8 && kind == K_UP && run) {
+      const size_t eo = (size_t)t[R_E];
+      if (c.tid < t[R_NROWS]) {
+        sg_t = __ldg(p.s_gate[l] + eo * p.I + t[R_ROW0] + c.tid);
+        su_t = __ldg(p.s_up[l] + eo * p.I + t[R_ROW0] + c.tid);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; j++) sdv[j] = c.tid + 256 * j < p.H ? __ldg(p.s_down[l] + eo * p.H + c.tid + 256 * j) : 0.f;
+    }
     if (ok && run) {
       const int K = t[R_K];
       // rows of 2048 or 4096 columns (every chunk kind: P1, O-proj, an UP
       // piece's gate and up rows, LM head) on the tensor cores: one code path
       // for the layer's GEMVs
       const bool split = rotated_rows(K);
-      if (split) ok = K == 2048 ? c.template gemv_mma<1>(res) : c.template gemv_mma<2>(res);
+      if (p.fp8 && kind == K_UP)   // 8-bit expert rows (K = 2048, or <= 1024)
+        ok = split ? c.gemv_mma_e4m3(res)
+                   : K <= 512 ? c.template gemv_row_e4m3<1>(res) : c.template gemv_row_e4m3<2>(res);
+      else if (split) ok = K == 2048 ? c.template gemv_mma<1>(res) : c.template gemv_mma<2>(res);
       else ok = K <= 256 ? c.template gemv_row<1>(res) : K <= 768 ? c.template gemv_row<3>(res)
               : K <= 2048 ? c.template gemv_row<8>(res) : c.template gemv_row<16>(res);
       // the tensor-core path's sums are written by the threads that run the
@@ -2477,11 +2807,17 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
       if (ok && !(split && (flags & FL_LAST) && kind != K_UP)) ok = c.csync();
     }
     if (ok && run) {
-      c.epilogue_row(res);
+      c.epilogue_row(res, sg_t, su_t);
       if (TR && c.tid == 0) S.t_mark[2] = gtime_ns();
     }
-    // an UP piece goes on with its columns of the down projection
-    if (ok && run && kind == K_UP) ok = c.csync() && c.down_part();
+    // an UP piece goes on with its columns of the down projection (8-bit:
+    // the rows' scales staged in the upper half of xs first)
+    if (ok && run && kind == K_UP && p.fp8) {
+#pragma unroll
+      for (int j = 0; j < 8; j++)
+        if (c.tid + 256 * j < p.H) S.xs[kXsFloats / 2 + c.tid + 256 * j] = sdv[j];
+    }
+    if (ok && run && kind == K_UP) ok = c.csync() && (p.fp8 ? c.down_mma_e4m3() : c.down_part());
   }
   if (ok && run && c.lane == 0) S.cchunk[c.warp]++;
   if (ok && (flags & (FL_RTR | FL_LAST))) ok = c.finish(flags);
@@ -2615,6 +2951,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
       S.seen_tgt[w] = 0;
     }
     S.abort_flag = 0;
+    S.xq_layer = -1;
     mbar_fence_init();
   }
   __syncthreads();
@@ -2677,6 +3014,24 @@ __global__ void __launch_bounds__(256) relayout_down_kernel(const uint16_t* __re
     if (h0 + r < H && g0 + q < G)
       *(uint4*)(dst + (((size_t)e * G + g0 + q) * H + h0 + r) * 8) = tile[r][q];
   }
+}
+
+// the same blocking for 8-bit (E4M3) down projections: one thread per
+// (expert, group, row) moves the row's 8 bytes of the group
+__global__ void __launch_bounds__(256) relayout_down_e4m3_kernel(const uint8_t* __restrict__ src,
+                                                                 uint8_t* __restrict__ dst, int E, int H, int I) {
+  const size_t G = (size_t)I / 8, total = (size_t)E * G * H;
+  for (size_t k = (size_t)blockIdx.x * 256 + threadIdx.x; k < total; k += (size_t)gridDim.x * 256) {
+    const size_t h = k % H, g = (k / H) % G, e = k / ((size_t)H * G);
+    *(uint2*)(dst + k * 8) = *(const uint2*)(src + (e * H + h) * I + g * 8);
+  }
+}
+
+cudaError_t relayout_down_e4m3(const uint8_t* src, uint8_t* dst, int E, int H, int I) {
+  if (I % 8 || (reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) % 8)
+    return cudaErrorInvalidValue;
+  relayout_down_e4m3_kernel<<<1216, 256>>>(src, dst, E, H, I);
+  return cudaGetLastError();
 }
 
 cudaError_t relayout_down(const uint16_t* src, uint16_t* dst, int E, int H, int I) {

@@ -178,6 +178,12 @@ struct Params {
   const uint16_t* const* w_down;
   uint16_t* const* k_pool;
   uint16_t* const* v_pool;
+  // 8-bit experts (E4M3): w_gate / w_up / w_down hold bytes (same layouts),
+  // weight = scale[row] * e4m3(byte); fp32 per-row scales [E][I], [E][I], [E][H]
+  int fp8;
+  const float* const* s_gate;
+  const float* const* s_up;
+  const float* const* s_down;
   const uint16_t* wd_blk;      // w_down re-laid out as [L][E][I / 8][H][8]: each 8-column group
                                // of an expert one contiguous [H][8] block (one token: the
                                // UP pieces' column slices stream as whole blocks)

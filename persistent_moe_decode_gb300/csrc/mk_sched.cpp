@@ -54,6 +54,14 @@ int validate_config(const mk_config& c) {
   if (c.kv_split_tokens < 0 || c.kv_split_tokens % 16) return MK_ERR_BAD_CONFIG;
   if (c.moe_stage_depth < 0 || c.moe_stage_depth > kStages) return MK_ERR_BAD_CONFIG;
   if (c.wave_order < MK_WAVES_DEFAULT || c.wave_order > MK_WAVES_INTERLEAVED) return MK_ERR_BAD_CONFIG;
+  if (c.expert_format != MK_EXPERTS_BF16 && c.expert_format != MK_EXPERTS_FP8_E4M3) return MK_ERR_BAD_CONFIG;
+  // 8-bit experts: the one-token path (tensor-core rows of 2048 bytes, or
+  // CUDA-core rows of 256, 512 or 1024 bytes in 16-byte lane chunks; a whole
+  // number of hidden rows in every 4096-row stage of the down projection)
+  if (c.expert_format == MK_EXPERTS_FP8_E4M3 &&
+      (c.max_batch != 1 || !(c.hidden == 2048 || c.hidden == 1024 || c.hidden == 512 || c.hidden == 256) ||
+       c.moe_inter % 16))
+    return MK_ERR_BAD_CONFIG;
   return MK_OK;
 }
 
@@ -80,7 +88,11 @@ int attention_sms(const mk_config& c, int n_sm, int batch, const int32_t* seq_le
   for (int b = 0; b < batch; b++) keys += (double)(seq_lens[b] + 1);
   const double kv = keys * 2.0 * c.n_kv_heads * c.head_dim * 2.0;
   const double experts = (double)std::min(c.n_experts, batch * c.top_k);
-  const double moe = experts * 3.0 * c.moe_inter * c.hidden * 2.0;   // gate, up and down
+  // gate, up and down: 2 bytes a weight.  8-bit experts move 1 byte a
+  // weight but their pieces cost more than their bytes (the activations' term
+  // split, the partial rows): weighted as 1.5 (48 attention SMs at 8K, the
+  // measured best of 40 / 44 / 48 / 56 / 64 / 72)
+  const double moe = experts * 3.0 * c.moe_inter * c.hidden * (c.expert_format == MK_EXPERTS_FP8_E4M3 ? 1.5 : 2.0);
   // The branches split the SMs in proportion to their bytes, a KV byte
   // weighted by w against an expert byte.  w folds in what the bytes do not
   // say: at short contexts the attention's fixed work per layer (query

@@ -29,6 +29,7 @@ MK_ERR_BAD_ARG = -8
 MK_ERR_DEVICE = -9
 
 MK_WAVES_DEFAULT, MK_WAVES_ATTN_FIRST, MK_WAVES_INTERLEAVED = 0, 1, 2
+MK_EXPERTS_BF16, MK_EXPERTS_FP8_E4M3 = 0, 1
 (MK_SCRATCH_H, MK_SCRATCH_X, MK_SCRATCH_QKV, MK_SCRATCH_ATTN, MK_SCRATCH_ROUTER,
  MK_SCRATCH_OPROJ, MK_SCRATCH_MOE) = range(7)
 MK_DEBUG_ROUTE_GROUPS, MK_DEBUG_PAGE_GATHER, MK_DEBUG_NEW_SLOT = range(3)
@@ -50,7 +51,8 @@ class mk_config(C.Structure):
                 ("max_batch", C.c_int), ("max_pages_per_seq", C.c_int), ("num_kv_pages", C.c_int),
                 ("max_attn_items", C.c_int), ("wave_order", C.c_int), ("n_attn_claimers", C.c_int),
                 ("n_moe_claimers", C.c_int), ("kv_split_tokens", C.c_int), ("sm_cap", C.c_int),
-                ("timeout_ms", C.c_int), ("trace_records", C.c_int), ("moe_stage_depth", C.c_int)]
+                ("timeout_ms", C.c_int), ("trace_records", C.c_int), ("moe_stage_depth", C.c_int),
+                ("expert_format", C.c_int)]
 
 
 _VPP = C.POINTER(C.c_void_p)
@@ -60,7 +62,7 @@ class mk_weights(C.Structure):
     _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p), ("final_norm", C.c_void_p),
                 ("attn_norm", _VPP), ("w_qkv", _VPP), ("w_o", _VPP), ("w_router", _VPP),
                 ("w_gate", _VPP), ("w_up", _VPP), ("w_down", _VPP), ("k_pool", _VPP),
-                ("v_pool", _VPP)]
+                ("v_pool", _VPP), ("s_gate", _VPP), ("s_up", _VPP), ("s_down", _VPP)]
 
 
 class mk_error(C.Structure):
@@ -337,6 +339,9 @@ class Decoder:
         self.dims = model.dims
         self.model, self.k_pool, self.v_pool = model, k_pool, v_pool
         L = self.dims.n_layers
+        fp8 = getattr(model, "fp8", None)
+        if fp8 is not None:
+            cfg_kw = {**cfg_kw, "expert_format": MK_EXPERTS_FP8_E4M3}
         self.cfg = make_config(self.dims, max_batch, max_pages_per_seq, k_pool.shape[1], **cfg_kw)
         self._keep = []
 
@@ -345,12 +350,17 @@ class Decoder:
             self._keep.append(a)
             return C.cast(a, _VPP)
 
+        ex = fp8 if fp8 is not None else {"q_gate": model.w_gate, "q_up": model.w_up, "q_down": model.w_down}
         self.weights = mk_weights(embed=model.embed.data_ptr(), lm_head=model.lm_head.data_ptr(),
                                   final_norm=model.final_norm.data_ptr(),
                                   attn_norm=arr(model.attn_norm), w_qkv=arr(model.w_qkv),
                                   w_o=arr(model.w_o), w_router=arr(model.w_router),
-                                  w_gate=arr(model.w_gate), w_up=arr(model.w_up),
-                                  w_down=arr(model.w_down), k_pool=arr(k_pool), v_pool=arr(v_pool))
+                                  w_gate=arr(ex["q_gate"]), w_up=arr(ex["q_up"]),
+                                  w_down=arr(ex["q_down"]), k_pool=arr(k_pool), v_pool=arr(v_pool))
+        if fp8 is not None:
+            self.weights.s_gate = arr(fp8["s_gate"])
+            self.weights.s_up = arr(fp8["s_up"])
+            self.weights.s_down = arr(fp8["s_down"])
         self.h = mk_create(self.cfg, self.weights)
         self.batch = 0
 

@@ -70,7 +70,11 @@ def test_create_rejects_bad_configs_before_touching_the_device(lib):
     w = mk.mk_weights()
     for bad in (dict(head_dim=96), dict(n_q_heads=5), dict(max_batch=17), dict(page_size=8),
                 dict(n_experts=300), dict(kv_split_tokens=100), dict(hidden=1000),
-                dict(n_q_heads=64, n_kv_heads=8, head_dim=128)):
+                dict(n_q_heads=64, n_kv_heads=8, head_dim=128), dict(expert_format=2),
+                # 8-bit experts: batch 1 only, hidden 2048 or <= 1024, moe_inter % 16
+                dict(expert_format=mk.MK_EXPERTS_FP8_E4M3, max_batch=2),
+                dict(expert_format=mk.MK_EXPERTS_FP8_E4M3, hidden=1536),
+                dict(expert_format=mk.MK_EXPERTS_FP8_E4M3, moe_inter=136)):
         cfg = mk.make_config(TINY, 1, 8, 16)
         for k, v in bad.items():
             setattr(cfg, k, v)

@@ -6,7 +6,9 @@ teacher-forced trajectories against the whole-model CPU oracle:
   a3b_8k    30B-total / 3.3B-active, batch 1, 8K context: 16 steps;
   a3b_b16   the same model, 16 ragged sequences, one retiring and one joining
             on fresh random pages every step: 8 steps;
-  a3b_256k  the same model, batch 1, 256K context: 2 steps.
+  a3b_256k  the same model, batch 1, 256K context: 2 steps;
+  a3b_8k_fp8  the same model with 8-bit (E4M3) routed experts, batch 1, 8K
+            context: 8 steps.
 
 Every step: logits max-abs <= 2e-2 and relative L2 <= 1e-2 over the whole
 vocabulary of every sequence, routed expert sets equal on every (layer,
@@ -33,7 +35,7 @@ from tests._pair import Pair, run_trajectory
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-STEPS = {"mid_8k": 32, "a3b_8k": 16, "a3b_b16": 8, "a3b_256k": 2}
+STEPS = {"mid_8k": 32, "a3b_8k": 16, "a3b_b16": 8, "a3b_256k": 2, "a3b_8k_fp8": 8}
 
 
 @pytest.fixture(scope="module", autouse=True)

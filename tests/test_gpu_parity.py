@@ -189,6 +189,47 @@ def test_multi_sequence_trajectory_with_churn(name):
         pair.close()
 
 
+def test_fp8_experts_tiny_moe_output_and_trajectory():
+    """8-bit routed experts (E4M3 bytes, one fp32 scale per row; CUDA-core rows
+    of 256 columns): every layer's MoE output on the first step against the
+    oracle's, then the whole teacher-forced trajectory."""
+    wl = WORKLOADS["tiny_fp8"]
+    pair = Pair(wl)
+    try:
+        gpu, ref, tr = pair.step(trace=True)
+        d = wl.dims
+        for l in range(d.n_layers):
+            y = np.frombuffer(pair.run.dec.scratch(mk.MK_SCRATCH_MOE, l), dtype=np.float32)
+            np.testing.assert_allclose(y.reshape(1, d.hidden), tr["moe"][l], atol=1e-4, rtol=1e-3,
+                                       err_msg=f"moe layer {l}")
+        check_logits(gpu, ref)
+        check_routing(pair, tr)
+    finally:
+        pair.close()
+    pair = Pair(wl)
+    try:
+        run_trajectory(pair, wl.steps)
+    finally:
+        pair.close()
+
+
+def test_fp8_experts_mid_trajectory():
+    """8-bit experts on the tensor cores (rows of 2048 E4M3 bytes, 16 per
+    stage), mid model at 8K context."""
+    wl = WORKLOADS["mid_fp8"].with_(steps=4)
+    pair = Pair(wl)
+    try:
+        gpu, ref, tr = pair.step(trace=True)
+        for l in range(wl.dims.n_layers):
+            y = np.frombuffer(pair.run.dec.scratch(mk.MK_SCRATCH_MOE, l), dtype=np.float32)
+            np.testing.assert_allclose(y.reshape(1, -1), tr["moe"][l], atol=1e-4, rtol=1e-3,
+                                       err_msg=f"moe layer {l}")
+        check_logits(gpu, ref)
+        run_trajectory(pair, wl.steps - 1)
+    finally:
+        pair.close()
+
+
 def test_tiny_b12_intermediates():
     pair = Pair(WORKLOADS["tiny_b12"])
     try:

@@ -183,11 +183,15 @@ def restated_split(dims, n_sm, na, lens):
 
 @pytest.mark.parametrize("batch", [1, 5, 16])
 @pytest.mark.parametrize("n_sm", [152, 7])
-def test_attention_split_and_items_equal_the_restated_rules(n_sm, batch):
+@pytest.mark.parametrize("fp8", [False, True])
+def test_attention_split_and_items_equal_the_restated_rules(n_sm, batch, fp8):
     """(The attention-branch size is a float expression: the restatement
     computes it in the same double precision as the host.)"""
     dims = A3B
-    cfg = mk.make_config(dims, 16, 4096, 1 << 20)
+    if fp8 and batch > 1:
+        pytest.skip("8-bit experts are a batch-1 format")
+    cfg = mk.make_config(dims, 1 if fp8 else 16, 4096, 1 << 20,
+                         expert_format=mk.MK_EXPERTS_FP8_E4M3 if fp8 else mk.MK_EXPERTS_BF16)
     rng = np.random.default_rng(batch * 7 + n_sm)
     lens = rng.integers(1, 40000, size=batch).astype(np.int32)
     plan = mk.mk_plan_step(cfg, n_sm, batch, lens)
@@ -196,7 +200,8 @@ def test_attention_split_and_items_equal_the_restated_rules(n_sm, batch):
     keys = float(np.sum(lens.astype(np.float64) + 1))
     w = 1.6 * (8192.0 / (keys / batch)) ** 0.22 / batch ** 0.45
     kv = w * keys * 2 * dims.n_kv_heads * dims.head_dim * 2
-    moe = min(dims.n_experts, batch * dims.top_k) * 3.0 * dims.moe_inter * dims.hidden * 2
+    # 2 bytes a weight; 8-bit experts weighted as 1.5
+    moe = min(dims.n_experts, batch * dims.top_k) * 3.0 * dims.moe_inter * dims.hidden * (1.5 if fp8 else 2)
     q = 4 if n_sm >= 64 else 1                    # in steps of 4 SMs on a large GPU
     ideal = n_sm * kv / (kv + moe)
     if batch > 1:                                 # at least 16 % of the SMs with several tokens
