@@ -1,6 +1,7 @@
 // Thin inline-PTX helpers for the persistent decode kernel (sm_103a):
 // mbarriers, 1-D bulk and 2-D tensor async copies (TMA, global -> shared), acquire/release
-// counter access, the warp-level BF16 tensor-core MMA and the global timer.
+// counter access, the warp-level BF16 and E4M3 tensor-core MMAs, E4M3
+// conversions and the global timer.
 #pragma once
 #include <stdint.h>
 #include <cuda_bf16.h>
@@ -209,16 +210,6 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// D += A * B, m16n8k16, A row-major FP16, B column-major FP16, fp32 accumulate
-__device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
-                                        uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // D += A * B, m16n8k32, A row-major E4M3, B column-major E4M3, fp32 accumulate
 // (four E4M3 values per register, the lowest byte first)
 __device__ __forceinline__ void mma_e4m3(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
@@ -250,11 +241,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
 
 __device__ __forceinline__ float2 f16x2_to_float2(uint32_t v) {
   return __half22float2(*reinterpret_cast<const __half2*>(&v));
-}
-
-// fp32 pair -> FP16 pair bits (first element in the low half), round to nearest even
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-  return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
 }
 
 }  // namespace mk
