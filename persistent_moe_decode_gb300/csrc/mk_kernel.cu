@@ -296,8 +296,9 @@ __device__ __forceinline__ void route_one(const Params& p, RouteTab& rt, int l, 
 // writes them straight into the task ring (lane 0 writes the words; no
 // per-thread arrays, which would live in local memory) and streams their
 // weight / KV stages.
-// ONE: the batch has one token; TR: the task timeline is recorded (kernel instance)
-template <bool ONE, bool TR>
+// ONE: the batch has one token; TR: the task timeline is recorded (kernel
+// instance); F8: the routed experts are 8-bit (E4M3)
+template <bool ONE, bool TR, bool F8 = false>
 struct Prod {
   const Params& p;
   Smem& S;
@@ -705,10 +706,10 @@ struct Prod {
       // stream loop for all of them keeps the code short
       // (8-bit experts: the same rows and blocks in bytes, streamed as rows
       // of half as many two-byte words)
-      const int es = p.fp8 ? 2 : 1;
+      const int es = F8 ? 2 : 1;
       const size_t eo = (size_t)e * p.I * H / es;
       const uint16_t* blk = p.wd_blk + (((size_t)l * p.E + e) * G + i0 / 8) * H * 8 / es;
-      for (int sg = 0; sg < 2 + (p.fp8 ? 0 : ncb); sg++) {
+      for (int sg = 0; sg < 2 + (F8 ? 0 : ncb); sg++) {
         const bool dn = sg >= 2;
         const uint16_t* src = dn ? blk + (size_t)(sg - 2) * H * 8 : wptr(3 + sg) + eo;
         // gate / up rows through their maps: rows of the [E I][H] matrix
@@ -719,7 +720,7 @@ struct Prod {
       }
       // 8-bit down projection: quads of up to four groups, a stage holding
       // the quad's rows [h0, h0 + rd) (one 1-D copy per group)
-      if (p.fp8) {
+      if constexpr (F8) {
         const int rd = min(H, 1024);
         const uint8_t* b8 = (const uint8_t*)blk;
         for (int q0 = 0; q0 < ncb; q0 += 4) {
@@ -1957,6 +1958,7 @@ struct Cons {
 
   // epilogue of a one-token chunk (after the barrier); token 0 throughout
   // (8-bit experts, K_UP: sg_t, su_t = the gate / up scales of row tid)
+  template <bool F8 = false>
   __device__ __forceinline__ void epilogue_row(const float* res, float sg_t = 0.f, float su_t = 0.f) {
     const int l = t[R_LAYER], kind = t[R_KIND];
     const int nr = t[R_NROWS], row0 = t[R_ROW0];
@@ -1980,7 +1982,7 @@ struct Cons {
         // 8-bit experts: the GEMV took x / rms; each row times its scale
         // (a piece has at most 64 rows: row i is thread i's)
         for (int i = tid; i < nr; i += 256) {
-          const float a = p.fp8 ? silu_mul(res[i] * sg_t, res[nr + i] * su_t)
+          const float a = F8 ? silu_mul(res[i] * sg_t, res[nr + i] * su_t)
                                 : silu_mul(res[i] * r, res[nr + i] * r);
           __stcg(p.abuf + ((size_t)l * Bm * p.topk + slot) * p.I + row0 + i, a);
           S.actp[i] = wa * a;
@@ -2761,7 +2763,7 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
 
 // one-token chunk: one copy of the wrapper (norm, waits, epilogue,
 // completion) around the GEMV shape for the row length
-template <bool ONE, bool TR>
+template <bool ONE, bool TR, bool F8>
 __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* t) {
   Cons<ONE, TR> c(p, S, t);
   const int op = t[R_OP], kind = t[R_KIND], flags = t[R_FLAGS], l = t[R_LAYER];
@@ -2779,7 +2781,7 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
     // while the gate / up rows stream (gate / up: row tid; down: rows
     // h = tid + 256 j, staged in shared memory before the down projection)
     float sg_t = 0.f, su_t = 0.f, sdv[8];
-    if (p.fp8 && kind == K_UP && run) {
+    if (F8 && kind == K_UP && run) {
       const size_t eo = (size_t)t[R_E];
       if (c.tid < t[R_NROWS]) {
         sg_t = __ldg(p.s_gate[l] + eo * p.I + t[R_ROW0] + c.tid);
@@ -2794,10 +2796,16 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
       // piece's gate and up rows, LM head) on the tensor cores: one code path
       // for the layer's GEMVs
       const bool split = rotated_rows(K);
-      if (p.fp8 && kind == K_UP)   // 8-bit expert rows (K = 2048, or <= 1024)
-        ok = split ? c.gemv_mma_e4m3(res)
-                   : K <= 512 ? c.template gemv_row_e4m3<1>(res) : c.template gemv_row_e4m3<2>(res);
-      else if (split) ok = K == 2048 ? c.template gemv_mma<1>(res) : c.template gemv_mma<2>(res);
+      bool done8 = false;
+      if constexpr (F8) {
+        if (kind == K_UP) {        // 8-bit expert rows (K = 2048, or <= 1024)
+          ok = split ? c.gemv_mma_e4m3(res)
+                     : K <= 512 ? c.template gemv_row_e4m3<1>(res) : c.template gemv_row_e4m3<2>(res);
+          done8 = true;
+        }
+      }
+      if (done8) {
+      } else if (split) ok = K == 2048 ? c.template gemv_mma<1>(res) : c.template gemv_mma<2>(res);
       else ok = K <= 256 ? c.template gemv_row<1>(res) : K <= 768 ? c.template gemv_row<3>(res)
               : K <= 2048 ? c.template gemv_row<8>(res) : c.template gemv_row<16>(res);
       // the tensor-core path's sums are written by the threads that run the
@@ -2807,17 +2815,20 @@ __device__ __forceinline__ bool op_row(const Params& p, Smem& S, const int32_t* 
       if (ok && !(split && (flags & FL_LAST) && kind != K_UP)) ok = c.csync();
     }
     if (ok && run) {
-      c.epilogue_row(res, sg_t, su_t);
+      c.template epilogue_row<F8>(res, sg_t, su_t);
       if (TR && c.tid == 0) S.t_mark[2] = gtime_ns();
     }
     // an UP piece goes on with its columns of the down projection (8-bit:
     // the rows' scales staged in the upper half of xs first)
-    if (ok && run && kind == K_UP && p.fp8) {
+    if (F8 && ok && run && kind == K_UP) {
 #pragma unroll
       for (int j = 0; j < 8; j++)
         if (c.tid + 256 * j < p.H) S.xs[kXsFloats / 2 + c.tid + 256 * j] = sdv[j];
     }
-    if (ok && run && kind == K_UP) ok = c.csync() && (p.fp8 ? c.down_mma_e4m3() : c.down_part());
+    if (ok && run && kind == K_UP) {
+      if constexpr (F8) ok = c.csync() && c.down_mma_e4m3();
+      else ok = c.csync() && c.down_part();
+    }
   }
   if (ok && run && c.lane == 0) S.cchunk[c.warp]++;
   if (ok && (flags & (FL_RTR | FL_LAST))) ok = c.finish(flags);
@@ -2854,7 +2865,7 @@ __device__ __forceinline__ bool op_combine(const Params& p, Smem& S, const int32
 // instance keeps each instance's union of inlined paths within registers).
 // TR: the timeline is recorded (an instance of its own, so the timed
 // instances carry no clock reads).
-template <bool ONE, bool TR>
+template <bool ONE, bool TR, bool F8>
 __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
   const int tid = threadIdx.x, lane = tid & 31;
   uint32_t task_seq = 0;
@@ -2886,7 +2897,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
         // one token: whole rows per warp, by the row's length; more tokens:
         // up to eight per pass
         if constexpr (ONE) {
-          ok = op_row<true, TR>(p, S, t);
+          ok = op_row<true, TR, F8>(p, S, t);
         } else {
           ok = op_chunk<false, TR>(p, S, t);
         }
@@ -2928,7 +2939,7 @@ __device__ __forceinline__ void consumer_loop(const Params& p, Smem& S) {
   }
 }
 
-template <bool ONE, bool TR>
+template <bool ONE, bool TR, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_constant__ Params p) {
   static_assert(kThreads == 384 && kLaunchRegs == 168, "register split assumes 384 threads x 168");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -2961,25 +2972,29 @@ __global__ void __launch_bounds__(kThreads, 1) mk_step_kernel(const __grid_const
     // registers back
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs) : "memory");
     if (wid == kConsumerWarps) {
-      Prod<ONE, TR> pr(p, S);
+      Prod<ONE, TR, F8> pr(p, S);
       pr.run();
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs) : "memory");
-    consumer_loop<ONE, TR>(p, S);
+    consumer_loop<ONE, TR, F8>(p, S);
   }
 }
 
 // the four kernel instances: (one token, several) x (timeline off, on)
-static const void* const kStepKernels[4] = {
+// and, for one token with 8-bit experts, two more (timeline off, on), so that
+// the BF16 instances carry none of the 8-bit paths
+constexpr int kNumStepKernels = 6;
+static const void* const kStepKernels[kNumStepKernels] = {
     (const void*)mk_step_kernel<false, false>, (const void*)mk_step_kernel<true, false>,
-    (const void*)mk_step_kernel<false, true>, (const void*)mk_step_kernel<true, true>};
+    (const void*)mk_step_kernel<false, true>, (const void*)mk_step_kernel<true, true>,
+    (const void*)mk_step_kernel<true, false, true>, (const void*)mk_step_kernel<true, true, true>};
 
 // registers per thread every kernel instance was built with (the split above
 // needs kLaunchRegs); -1 if they differ or cannot be read
 int step_kernel_regs() {
   int regs = -1;
-  for (int i = 0; i < 4; i++) {
+  for (int i = 0; i < kNumStepKernels; i++) {
     cudaFuncAttributes a;
     if (cudaFuncGetAttributes(&a, kStepKernels[i]) != cudaSuccess) {
       cudaGetLastError();
@@ -3051,7 +3066,7 @@ cudaError_t configure_step_kernels() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < kMaxDev && configured[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  for (int i = 0; i < 4; i++) {
+  for (int i = 0; i < kNumStepKernels; i++) {
     e = cudaFuncSetAttribute(kStepKernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
   }
@@ -3072,7 +3087,8 @@ cudaError_t launch_step(const Params& p, int n_sm, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const void* k = kStepKernels[(p.B == 1 ? 1 : 0) + (p.trace != nullptr ? 2 : 0)];
+  const void* k = p.fp8 ? kStepKernels[4 + (p.trace != nullptr ? 1 : 0)]
+                        : kStepKernels[(p.B == 1 ? 1 : 0) + (p.trace != nullptr ? 2 : 0)];
   void* args[1] = {(void*)&p};
   return cudaLaunchKernelExC(&cfg, k, args);
 }
