@@ -92,6 +92,12 @@ MID = ModelDims(n_layers=8, hidden=2048, n_q_heads=16, n_kv_heads=4, head_dim=12
 A3B = ModelDims(n_layers=48, hidden=2048, n_q_heads=32, n_kv_heads=4, head_dim=128,
                 n_experts=128, top_k=8, moe_inter=768, vocab=151936, rope_theta=1e6)
 
+# dense feed-forward layers: one expert that every token selects (E = k = 1;
+# a softmax over one router logit is exactly 1, so the layer's MoE branch is
+# the dense SwiGLU FFN W_d (SiLU(W_g x) * W_u x))
+TINY_DENSE = replace(TINY, n_experts=1, top_k=1, moe_inter=512)
+MID_DENSE = replace(MID, n_experts=1, top_k=1, moe_inter=4096)
+
 WORKLOADS = {
     # tiny parallel-layer MoE, batch 1, 64 cached tokens, 8 greedy steps
     "tiny": Workload("tiny", TINY, batch=1, context=64, steps=8),
@@ -126,6 +132,12 @@ WORKLOADS = {
     "tiny_fp8": Workload("tiny_fp8", TINY, batch=1, context=64, steps=8, expert_format="fp8"),
     "mid_fp8": Workload("mid_fp8", MID, batch=1, context=8192, steps=32, expert_format="fp8"),
     "a3b_8k_fp8": Workload("a3b_8k_fp8", A3B, batch=1, context=8192, steps=128, expert_format="fp8"),
+    # dense-FFN models (one always-selected expert): tiny at batch 1 and 5 with
+    # churn, mid (intermediate 4096) at 8K
+    "tiny_dense": Workload("tiny_dense", TINY_DENSE, batch=1, context=64, steps=8),
+    "tiny_dense_b5": Workload("tiny_dense_b5", TINY_DENSE, batch=5, context=0, steps=6, ragged=(10, 300),
+                              churn=True, join_context=40),
+    "mid_dense": Workload("mid_dense", MID_DENSE, batch=1, context=8192, steps=32),
 }
 
 

@@ -230,6 +230,19 @@ def test_fp8_experts_mid_trajectory():
         pair.close()
 
 
+@pytest.mark.parametrize("name,steps", [("tiny_dense", 8), ("tiny_dense_b5", 6), ("mid_dense", 4)])
+def test_dense_ffn_models(name, steps):
+    """Dense feed-forward layers as one always-selected expert (E = k = 1):
+    batch 1, several sequences with churn, and the mid shape with an
+    intermediate size of 4096."""
+    wl = WORKLOADS[name].with_(steps=steps)
+    pair = Pair(wl)
+    try:
+        run_trajectory(pair, steps)
+    finally:
+        pair.close()
+
+
 def test_tiny_b12_intermediates():
     pair = Pair(WORKLOADS["tiny_b12"])
     try:

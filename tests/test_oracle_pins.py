@@ -446,3 +446,23 @@ def test_step_rejects_bad_pages():
     bad[0, 0] = orc.num_pages + 3
     with pytest.raises(RuntimeError):
         orc.decode_step(toks, lens, bad)
+
+
+# ------------------------------------------------------- dense FFN layers
+
+def test_one_expert_is_the_dense_ffn():
+    """With E = k = 1 the routing is exactly (0, 1.0) whatever the logit, and
+    the MoE branch is the dense SwiGLU FFN W_d (SiLU(W_g x) * W_u x)."""
+    from persistent_moe_decode_gb300.configs import TINY_DENSE
+    for logit in (-3.5, 0.0, 7.25):
+        idx, w, _ = oracle.route(np.array([logit]), 1)
+        assert idx.tolist() == [0] and w.tolist() == [1.0]
+    m = make_model(TINY_DENSE, seed=4)
+    k, v = make_kv_pools(TINY_DENSE, 8, 1.0, seed=4)
+    orc = make_oracle(m, k, v)
+    x = RNG.standard_normal(TINY_DENSE.hidden)
+    wg, wu, wd = (m.w_gate[1, 0].double(), m.w_up[1, 0].double(), m.w_down[1, 0].double())
+    xt = torch.tensor(x)
+    dense = (wd @ (F.silu(wg @ xt) * (wu @ xt))).numpy()
+    np.testing.assert_allclose(orc.moe(1, x, np.array([0], dtype=np.int32), np.array([1.0])), dense,
+                               rtol=1e-10, atol=1e-13)
