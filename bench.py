@@ -47,7 +47,7 @@ def load_peaks():
 
 
 def load_traffic(workload: str):
-    """dram bytes per step from a committed ncu summary, if one matches this build."""
+    """dram bytes per step from a committed ncu summary measured with the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
