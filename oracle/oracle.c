@@ -15,7 +15,7 @@
  * top-k per token, expert gate/up with SiLU-and-multiply, expert down, the
  * router-weighted sum of each token's expert outputs, LM head).
  *
- * Readings where the pages are silent (each listed in the design notes):
+ * Readings where the pages are silent:
  *   pre-norm parallel layer  h' = h + Attn(x) + MoE(x),  x = RMSNorm(h; g_l);
  *   a final RMSNorm with its own gain before the LM head;
  *   RMSNorm(h) = h / sqrt(mean(h^2) + eps) * g;
