@@ -351,6 +351,9 @@ def main():
                     help="schedule ablation: split-KV chunk in tokens (0 = one run per attention SM)")
     ap.add_argument("--moe-depth", type=int, default=0,
                     help="schedule ablation: stages an expert-branch SM keeps in flight (0 = per step)")
+    ap.add_argument("--claim-rows", type=int, default=0,
+                    help="several tokens: rows per expert tile claimed from per-layer counters "
+                         "(0 = the default, 128; -1 = static equal shares)")
     ap.add_argument("--ref-layers", type=int, default=2)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
@@ -397,6 +400,8 @@ def main():
         sched["kv_split_tokens"] = args.kv_split
     if args.moe_depth:
         sched["moe_stage_depth"] = args.moe_depth
+    if args.claim_rows:
+        sched["moe_claim_rows"] = args.claim_rows
     run = StepRunner(wl.with_(seed=wl.seed + rank), device=f"cuda:{local}", **sched)
     stream = torch.cuda.current_stream()
     B = wl.batch
@@ -456,7 +461,8 @@ def main():
                    "schedule": ({"waves": args.waves} if args.waves else
                                 {"attention_sms": args.attn_sms or "per step"})
                                | ({"kv_split_tokens": args.kv_split} if args.kv_split else {})
-                               | ({"moe_stage_depth": args.moe_depth} if args.moe_depth else {})},
+                               | ({"moe_stage_depth": args.moe_depth} if args.moe_depth else {})
+                               | ({"moe_claim_rows": args.claim_rows} if args.claim_rows else {})},
         "sol_frac": {"of_measured_hbm": roof["frac"], "of_nominal_8tbs": roof["achieved"] / 8000.0},
         "roofline": roof,
         "cpu_baseline": cpu,

@@ -110,6 +110,17 @@ typedef struct {
                              the critical path), else 5                      */
   int expert_format;      /* enum mk_expert_format: how w_gate / w_up / w_down
                              hold the routed experts' weights                 */
+  int moe_claim_rows;     /* several tokens: > 0 (a multiple of 16) = the
+                             expert-branch SMs claim tiles of this many rows
+                             (gate/up pairs, or down rows) one at a time from
+                             a per-layer counter, so an SM whose tiles cost
+                             more takes fewer (the pages' shared work queue:
+                             "Inside the megakernel serving engine for North
+                             Mini Code", §The task scheduler); 0 = chosen per
+                             step: 128-row tiles from 4 tokens up, static
+                             shares below; -1 = each expert-branch SM takes an
+                             equal share of the routed experts' rows.
+                             Results are identical either way.              */
 } mk_config;
 
 /* Weight format of the routed experts (mk_config.expert_format).
@@ -331,7 +342,7 @@ int mk_read_debug(mk_handle* h, int which, void* dst, size_t bytes, size_t* size
  * handle's own error block, so mk_step_status reports the step as usual.
  * The results are the same as those of mk_decode_step for the same batch.
  *
- * Limit: a handle needs 32 + n_layers * round_up(6 + max_batch, 32) words;
+ * Limit: a handle needs 32 + n_layers * round_up(8 + max_batch, 32) words;
  * with max_batch <= 16 that is 32 words per layer, so up to 2,047 layers fit.
  * A larger need returns MK_ERR_BAD_CONFIG.  Other errors: MK_ERR_NOT_SCHEDULED, MK_ERR_BAD_ARG
  * (NULL logits, or the current device is not the handle's), MK_ERR_CUDA.

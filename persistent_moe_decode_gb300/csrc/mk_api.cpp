@@ -651,6 +651,13 @@ Params step_params(const mk_handle* h, const DevPlan& plan, float* logits) {
   // shortest step) and at 256K (12 expert SMs: the full ring)
   const int n_moe = h->n_attn < h->n_sm ? h->n_sm - h->n_attn : 0;
   p.moe_depth = h->cfg.moe_stage_depth > 0 ? h->cfg.moe_stage_depth : (n_moe > h->n_attn ? 3 : kStages);
+  // expert tiles: claimed, 128 rows, from 4 tokens up, unless the config
+  // fixes them (measured on the 30B/3.3B model: at batch 16 128-row tiles
+  // ahead of 64, 192 and 256 and of static shares by 14 % at the same role
+  // split; at batch 4 ahead of static shares by 4 %; at batch 2 behind by 5 %,
+  // its few tiles cost about the same)
+  p.claim_rows = h->cfg.moe_claim_rows > 0 ? h->cfg.moe_claim_rows
+                 : h->cfg.moe_claim_rows == 0 && h->batch >= 4 ? 128 : 0;
   return p;
 }
 

@@ -742,36 +742,60 @@ struct Prod {
     return true;
   }
 
+  // several tokens, claimed tiles: the next tile index of claim counter
+  // `off` of this layer (lane 0's atomic add, broadcast).  The claim orders
+  // nothing: a tile's inputs are ordered by the routing wait and the UP
+  // counter, as with static shares.
+  __device__ __forceinline__ int claim(int off) {
+    int c = 0;
+    if (lane == 0) c = (int)atomicAdd(p.bars + bar_index(p, l, off), 1u);
+    return __shfl_sync(0xffffffffu, c, 0);
+  }
+
+  // several tokens: the chunks of an expert's gate / up pair rows [i0, i1)
+  __device__ __forceinline__ bool up_rows(int a, int i0, int i1, bool last) {
+    const int H = p.H;
+    const int e = S.rt.act[a];
+    const int cnt = S.rt.off[a + 1] - S.rt.off[a];
+    const int cp = max(1, gemv_chunk_rows(H, cnt) / 2);
+    const size_t eo = (size_t)e * p.I * H;
+    const bool mma = p.w_maps && mma_multi_rows(H, cnt);
+    const uint8_t* mg = mma ? wmap(W_MAP_GATE) : nullptr;
+    const uint8_t* mu = mma ? wmap(W_MAP_UP) : nullptr;
+    for (int c0 = i0; c0 < i1; c0 += cp)
+      if (!chunk(K_UP, (last && c0 + cp >= i1) ? FL_LAST : 0, c0, min(cp, i1 - c0), 2, H, cnt, a, e, 0,
+                 wptr(3) + eo, wptr(4) + eo, mg, mu, e * p.I + c0))
+        return false;
+    return true;
+  }
+
   __device__ __forceinline__ bool do_up(int a0, int a1) {
     const int H = p.H;
     if (!wait_route()) return false;
     if (ONE) return do_up1(a0, a1);
     const int n_act = S.rt.n_act;
+    // claimed tiles of claim_rows / 2 pair rows; the next tile is claimed
+    // before this one streams, so the SM knows which chunk is its last
+    if (p.claim_rows > 0) {
+      const int T = max(1, p.claim_rows / 2), tpe = (p.I + T - 1) / T, ntiles = n_act * tpe;
+      int c = a0 >= 0 ? claim(p.bl.claim_up) : ntiles;
+      if (c >= ntiles) return chunk(K_UP, FL_LAST, 0, 0, 2, H, 0, 0, 0, 0, nullptr, nullptr);
+      while (c < ntiles) {
+        const int nx = claim(p.bl.claim_up);
+        const int a = c / tpe, i0 = (c % tpe) * T;
+        if (!up_rows(a, i0, min(i0 + T, p.I), nx >= ntiles)) return false;
+        c = nx;
+      }
+      return true;
+    }
+    // static share: slice a0 of a1 over the routed experts' pair rows, as
+    // (active expert, pair range) pieces of [p0, p1)
     int p0 = 0, p1 = 0;
     if (a0 >= 0) dshare(n_act * p.I, a1, a0, p0, p1);
-    // chunks: (active expert, pair range) pieces of [p0, p1)
-    int n_chunks = 0;
+    if (p1 <= p0) return chunk(K_UP, FL_LAST, 0, 0, 2, H, 0, 0, 0, 0, nullptr, nullptr);
     for (int a = p0 / p.I; a < n_act && a * p.I < p1; a++) {
       const int i0 = max(p0 - a * p.I, 0), i1 = min(p1 - a * p.I, p.I);
-      const int cp = max(1, gemv_chunk_rows(H, S.rt.off[a + 1] - S.rt.off[a]) / 2);
-      n_chunks += (i1 - i0 + cp - 1) / cp;
-    }
-    if (n_chunks == 0) return chunk(K_UP, FL_LAST, 0, 0, 2, H, 0, 0, 0, 0, nullptr, nullptr);
-    for (int a = p0 / p.I; a < n_act && a * p.I < p1; a++) {
-      const int i0 = max(p0 - a * p.I, 0), i1 = min(p1 - a * p.I, p.I);
-      const int e = S.rt.act[a];
-      const int cnt = S.rt.off[a + 1] - S.rt.off[a];
-      const int cp = max(1, gemv_chunk_rows(H, cnt) / 2);
-      const size_t eo = (size_t)e * p.I * H;
-      const bool mma = p.w_maps && mma_multi_rows(H, cnt);
-      const uint8_t* mg = mma ? wmap(W_MAP_GATE) : nullptr;
-      const uint8_t* mu = mma ? wmap(W_MAP_UP) : nullptr;
-      for (int c0 = i0; c0 < i1; c0 += cp) {
-        n_chunks--;
-        if (!chunk(K_UP, n_chunks == 0 ? FL_LAST : 0, c0, min(cp, i1 - c0), 2, H, cnt, a, e, 0,
-                   wptr(3) + eo, wptr(4) + eo, mg, mu, e * p.I + c0))
-          return false;
-      }
+      if (!up_rows(a, i0, i1, a * p.I + i1 == p1)) return false;
     }
     return true;
   }
@@ -852,25 +876,45 @@ struct Prod {
     // weighted output, summed by OUT
     if (!wait_route()) return false;
     const int n_act = S.rt.n_act;
+    // claimed tiles of claim_rows down rows (expert-major), as in do_up
+    if (p.claim_rows > 0) {
+      const int T = p.claim_rows, tpe = (H + T - 1) / T, ntiles = n_act * tpe;
+      int c = a0 >= 0 ? claim(p.bl.claim_down) : ntiles;
+      if (c >= ntiles) return chunk(K_DOWN, FL_LAST, 0, 0, 1, p.I, 0, 0, 0, 0, nullptr, nullptr);
+      while (c < ntiles) {
+        const int nx = claim(p.bl.claim_down);
+        const int a = c / tpe, h0 = (c % tpe) * T;
+        if (!down_rows(a, h0, min(h0 + T, H), nx >= ntiles)) return false;
+        c = nx;
+      }
+      return true;
+    }
     int r0 = 0, r1 = 0;
     if (a0 >= 0) dshare(n_act * H, a1, a0, r0, r1);
     if (r1 <= r0) return chunk(K_DOWN, FL_LAST, 0, 0, 1, p.I, 0, 0, 0, 0, nullptr, nullptr);
     for (int a = r0 / H; a < n_act && a * H < r1; a++) {
       const int h0 = max(r0 - a * H, 0), h1 = min(r1 - a * H, H);
-      const int e = S.rt.act[a];
-      const int cnt = S.rt.off[a + 1] - S.rt.off[a];
-      // tensor cores: one fp32 partial per (row, warp, token) in the chunk's buffer
-      const bool mma = p.wd_maps != nullptr;
-      const int cd = mma ? max(kDownBoxRows, min(512, kPartFloats / (kConsumerWarps * cnt)) / kDownBoxRows *
-                                                 kDownBoxRows)
-                         : gemv_chunk_rows(p.I, cnt);
-      const uint16_t* wd = wptr(5) + (size_t)e * H * p.I;
-      const uint8_t* md = mma ? p.wd_maps + (size_t)l * 128 : nullptr;
-      for (int c0 = h0; c0 < h1; c0 += cd)
-        if (!chunk(K_DOWN, (c0 + cd >= h1 && a * H + h1 == r1) ? FL_LAST : 0, c0, min(cd, h1 - c0), 1, p.I,
-                   cnt, a, e, 0, wd, nullptr, md, nullptr, e * H + c0, kDownBoxRows))
-          return false;
+      if (!down_rows(a, h0, h1, a * H + h1 == r1)) return false;
     }
+    return true;
+  }
+
+  // several tokens: the chunks of an expert's down rows [h0, h1)
+  __device__ __forceinline__ bool down_rows(int a, int h0, int h1, bool last) {
+    const int H = p.H;
+    const int e = S.rt.act[a];
+    const int cnt = S.rt.off[a + 1] - S.rt.off[a];
+    // tensor cores: one fp32 partial per (row, warp, token) in the chunk's buffer
+    const bool mma = p.wd_maps != nullptr;
+    const int cd = mma ? max(kDownBoxRows, min(512, kPartFloats / (kConsumerWarps * cnt)) / kDownBoxRows *
+                                               kDownBoxRows)
+                       : gemv_chunk_rows(p.I, cnt);
+    const uint16_t* wd = wptr(5) + (size_t)e * H * p.I;
+    const uint8_t* md = mma ? p.wd_maps + (size_t)l * 128 : nullptr;
+    for (int c0 = h0; c0 < h1; c0 += cd)
+      if (!chunk(K_DOWN, (last && c0 + cd >= h1) ? FL_LAST : 0, c0, min(cd, h1 - c0), 1, p.I, cnt, a, e, 0, wd,
+                 nullptr, md, nullptr, e * H + c0, kDownBoxRows))
+        return false;
     return true;
   }
 

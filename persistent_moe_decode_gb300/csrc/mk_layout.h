@@ -134,6 +134,8 @@ struct BarLayout {
   int rtr;     // P1 tasks holding router rows done               (target n_rtr_sms)
   int down;    // several tokens: DOWN tasks done                 (target n_down_sms)
   int items;   // + b: split-KV items of sequence b done          (target: its split count)
+  int claim_up;    // several tokens, claimed tiles: next UP tile of the layer (not waited on)
+  int claim_down;  // several tokens, claimed tiles: next DOWN tile of the layer
 };
 
 inline BarLayout bar_layout(int max_batch) {
@@ -145,7 +147,9 @@ inline BarLayout bar_layout(int max_batch) {
   b.rtr = 4;
   b.down = 5;
   b.items = 6;
-  b.per_layer = (6 + max_batch + 31) & ~31;
+  b.claim_up = 6 + max_batch;
+  b.claim_down = 7 + max_batch;
+  b.per_layer = (8 + max_batch + 31) & ~31;
   return b;
 }
 
@@ -164,6 +168,8 @@ struct Params {
   int n_comb_sms, n_up_sms;    // SMs that signal the COMBINE / UP counters of a layer
   int n_down_sms, n_rtr_sms;   // SMs with a DOWN task / with router rows in their P1 share
   int moe_depth;               // one token: stages an SM without attention items keeps in flight
+  int claim_rows;              // several tokens: 0 = static expert shares; > 0 = the expert
+                               // branch claims tiles of this many rows from per-layer counters
   float rms_eps, attn_scale_log2;
   // caller weights (device pointers; per-layer arrays are device arrays of L pointers)
   const uint16_t* embed;

@@ -55,6 +55,7 @@ int validate_config(const mk_config& c) {
   if (c.moe_stage_depth < 0 || c.moe_stage_depth > kStages) return MK_ERR_BAD_CONFIG;
   if (c.wave_order < MK_WAVES_DEFAULT || c.wave_order > MK_WAVES_INTERLEAVED) return MK_ERR_BAD_CONFIG;
   if (c.expert_format != MK_EXPERTS_BF16 && c.expert_format != MK_EXPERTS_FP8_E4M3) return MK_ERR_BAD_CONFIG;
+  if (c.moe_claim_rows < -1 || (c.moe_claim_rows > 0 && c.moe_claim_rows % 16)) return MK_ERR_BAD_CONFIG;
   // 8-bit experts: the one-token path (tensor-core rows of 2048 bytes, or
   // CUDA-core rows of 256, 512 or 1024 bytes in 16-byte lane chunks; a whole
   // number of hidden rows in every 4096-row stage of the down projection)
@@ -104,12 +105,13 @@ int attention_sms(const mk_config& c, int n_sm, int batch, const int32_t* seq_le
   const double mean_ctx = keys / batch;
   const double w = 1.6 * pow(8192.0 / mean_ctx, 0.22) / pow((double)batch, 0.45);
   double ideal = n_sm * w * kv / (w * kv + moe);
-  // several tokens: at least 16 % of the SMs on the attention branch.  As the
-  // contexts of a continuous batch shrink (short sequences joining), the
-  // byte share would drop to 8 % and the expert branch's per-byte cost (its
-  // multi-token GEMVs) does not follow; 16 % was the best fixed split over
-  // whole batch-16 and batch-4 runs.
-  if (batch > 1) ideal = std::max(ideal, 0.16 * n_sm);
+  // several tokens: at least 16 % of the SMs on the attention branch, 23 %
+  // from 8 tokens up.  As the contexts of a continuous batch shrink (short
+  // sequences joining), the byte share would drop to 8 % and the expert
+  // branch's per-byte cost (its multi-token GEMVs) does not follow; with the
+  // expert tiles claimed, 36 of 152 SMs (32 within 0.5 %) were the best
+  // fixed split over whole batch-16 runs and 24 over batch-4 runs.
+  if (batch > 1) ideal = std::max(ideal, (batch >= 8 ? 0.23 : 0.16) * n_sm);
   // in steps of 4 SMs on a large GPU: each split has its own task lists,
   // built and uploaded the first time it is used, and the contexts of a
   // continuous batch move the ideal split by a few SMs every step

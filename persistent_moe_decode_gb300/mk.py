@@ -52,7 +52,7 @@ class mk_config(C.Structure):
                 ("max_attn_items", C.c_int), ("wave_order", C.c_int), ("n_attn_claimers", C.c_int),
                 ("n_moe_claimers", C.c_int), ("kv_split_tokens", C.c_int), ("sm_cap", C.c_int),
                 ("timeout_ms", C.c_int), ("trace_records", C.c_int), ("moe_stage_depth", C.c_int),
-                ("expert_format", C.c_int)]
+                ("expert_format", C.c_int), ("moe_claim_rows", C.c_int)]
 
 
 _VPP = C.POINTER(C.c_void_p)

@@ -243,6 +243,24 @@ def test_dense_ffn_models(name, steps):
         pair.close()
 
 
+@pytest.mark.parametrize("name,rows", [("tiny_b12", 16), ("mid_b16", 64), ("mid_b16", 256), ("a3b4_b3", 128)])
+def test_claimed_expert_tiles_give_identical_logits(name, rows):
+    """Several tokens: the expert branch claiming tiles of its rows from
+    per-layer counters computes every row as the static shares do, so a step
+    gives bit-identical logits whichever SM took which tile."""
+    wl = WORKLOADS[name]
+    from persistent_moe_decode_gb300.runner import StepRunner
+    out = []
+    for kw in ({"moe_claim_rows": -1}, {"moe_claim_rows": rows}):
+        run = StepRunner(wl, device="cuda", **kw)
+        run.step()
+        torch.cuda.synchronize()
+        run.check_status()
+        out.append(run.logits.clone())
+        run.close()
+    assert torch.equal(out[0], out[1])
+
+
 def test_tiny_b12_intermediates():
     pair = Pair(WORKLOADS["tiny_b12"])
     try:

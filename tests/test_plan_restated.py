@@ -204,8 +204,8 @@ def test_attention_split_and_items_equal_the_restated_rules(n_sm, batch, fp8):
     moe = min(dims.n_experts, batch * dims.top_k) * 3.0 * dims.moe_inter * dims.hidden * (1.5 if fp8 else 2)
     q = 4 if n_sm >= 64 else 1                    # in steps of 4 SMs on a large GPU
     ideal = n_sm * kv / (kv + moe)
-    if batch > 1:                                 # at least 16 % of the SMs with several tokens
-        ideal = max(ideal, 0.16 * n_sm)
+    if batch > 1:                                 # at least 16 % of the SMs (23 % from 8 tokens)
+        ideal = max(ideal, (0.23 if batch >= 8 else 0.16) * n_sm)
     na = max(1, min(n_sm - 1, q * int(ideal / q + 0.5)))
     assert plan["n_attn"] == na
     items, off = restated_split(dims, n_sm, na, lens)
