@@ -90,9 +90,13 @@ class StepSim:
     """One step of the plan from mk_plan_step for `dims`, batch and lengths;
     ``routing[l]`` = [batch][top_k] experts of layer l (drawn by the caller)."""
 
-    def __init__(self, dims, plan, batch, routing, n_sm):
+    def __init__(self, dims, plan, batch, routing, n_sm, claim_rows=0):
         self.d, self.plan, self.B, self.routing, self.n_sm = dims, plan, batch, routing, n_sm
         self.one = batch == 1
+        # several tokens, claim_rows > 0: the expert tiles come from the
+        # per-layer claim counters (taken in the interleaving's order)
+        self.claim_rows = 0 if self.one else claim_rows
+        self.claims = {}
         self.counters = {}
         self.route_done = [0] * n_sm
         self.coverage = {"up": {}, "down": {}}      # (layer) -> list of resolved ranges
@@ -296,12 +300,69 @@ class StepSim:
         raise ValueError(f"unknown op {op}")
 
     # ------------------------------------------------------ agents
+    def claimed(self, s, t):
+        """Several tokens, claimed tiles: the producer claims the next tile
+        before it hands over the current one's chunks (so the last claimed
+        tile's last chunk carries the arrival); an SM that claims nothing
+        hands over one empty chunk that arrives."""
+        d, H = self.d, self.d.hidden
+        op, l, a0 = int(t[F_OP]), int(t[F_LAYER]), int(t[F_A0])
+        n_act, cnt = self.active(l)
+        up = op == OP_UP
+        kind = "up" if up else "down"
+        per, T = (d.moe_inter, max(1, self.claim_rows // 2)) if up else (H, self.claim_rows)
+        tpe = cdiv(per, T)
+        ntiles = n_act * tpe
+
+        def claim():
+            v = self.claims.get((kind, l), 0)
+            self.claims[(kind, l)] = v + 1
+            return v
+
+        c = claim() if a0 >= 0 else ntiles
+        if c >= ntiles:
+            yield from self.hand_over(s, [Chunk(arrives=[(kind, l)])])
+            return
+        while c < ntiles:
+            nx = claim()
+            a, lo = c // tpe, (c % tpe) * T
+            hi = min(lo + T, per)
+            self.coverage[kind].setdefault(l, []).append((a * per + lo, a * per + hi))
+            chunks = []
+            step = max(1, chunk_rows(H, cnt[a]) // 2) if up else chunk_rows(d.moe_inter, cnt[a])
+            c0 = lo
+            while c0 < hi:
+                n = min(step, hi - c0)
+                if up:
+                    chunks.append(Chunk(stages=2 * cdiv(n, rows_per_stage(H))))
+                else:
+                    chunks.append(Chunk(waits=[(("up", l), self.target("up"))],
+                                        stages=cdiv(n, rows_per_stage(d.moe_inter))))
+                c0 += step
+            if nx >= ntiles:
+                chunks[-1].arrives.append((kind, l))
+            yield from self.hand_over(s, chunks)
+            c = nx
+
+    def hand_over(self, s, chunks):
+        for ch in chunks:
+            yield ("slot", s)
+            self.handed[s] += 1
+            self.queue[s].append(ch)
+            for _ in range(ch.stages):
+                yield ("stage", s)
+                self.issued[s] += 1
+                ch.issued += 1
+
     def producer(self, s):
         tasks = self.plan["tasks"][self.plan["task_off"][s]:self.plan["task_off"][s + 1]]
         for t in tasks:
             op, l = int(t[F_OP]), int(t[F_LAYER])
             if not self.one and op in (OP_UP, OP_DOWN):
                 yield ("route", s, l)                   # the consumer has routed layer l
+            if self.claim_rows and op in (OP_UP, OP_DOWN):
+                yield from self.claimed(s, t)
+                continue
             chunks, pw = self.resolve(s, t)
             if pw is not None and pw[0] != "after":
                 yield ("ctr",) + pw                     # producer-side wait before the hand-over

@@ -7,7 +7,8 @@ scheduler: any wave order must be free of circular waits).
 
 For every wave order and role split, SM counts 1, 2, 7 and 152, batch 1 and
 16: the step ends; every counter ends exactly at the target the kernel waits
-for; the device-resolved expert shares tile their ranges exactly once.  A
+for; the device-resolved expert shares, or the expert tiles claimed from the
+per-layer counters (several tokens), tile their ranges exactly once.  A
 target raised by one (the bump word the kernel's time-out test uses, or any
 SM count the kernel takes as a target) leaves a wait stuck, which the
 interpreter reports.
@@ -62,8 +63,8 @@ def tiles_once(ranges, total):
     return bool(np.all(hits == 1))
 
 
-def check_step(dims, n_sm, batch, plan, routing, seed):
-    sim = StepSim(dims, plan, batch, routing, n_sm)
+def check_step(dims, n_sm, batch, plan, routing, seed, claim_rows=0):
+    sim = StepSim(dims, plan, batch, routing, n_sm, claim_rows)
     ctr = sim.run(seed=seed)
     one = batch == 1
     L = dims.n_layers
@@ -99,6 +100,22 @@ def test_step_ends_with_every_counter_at_its_target(dims, n_sm, batch, sched):
     plan, routing, _ = make_step(dims, n_sm, batch, sched, seed=n_sm * 31 + batch)
     for seed in (0, 1):
         check_step(dims, n_sm, batch, plan, routing, seed)
+
+
+CLAIM_CASES = [(dims, n_sm, sched, rows) for dims in (TINY, A3B2) for n_sm in (2, 7, 152)
+               for sched in (("roles", 0), ("waves", mk.MK_WAVES_DEFAULT)) for rows in (16, 128)]
+
+
+@pytest.mark.parametrize("dims,n_sm,sched,rows", CLAIM_CASES,
+                         ids=lambda v: f"H{v.hidden}" if hasattr(v, "hidden") else str(v))
+def test_claimed_expert_tiles_end_with_every_counter_at_its_target(dims, n_sm, sched, rows):
+    """Several tokens with the expert tiles claimed from per-layer counters in
+    the order the random interleaving gives: every tile is taken exactly once
+    and every UP / DOWN counter still ends at its target (one arrival per
+    expert-branch SM, whatever it claimed)."""
+    plan, routing, _ = make_step(dims, n_sm, 16, sched, seed=n_sm * 7 + rows)
+    for seed in (0, 1, 2):
+        check_step(dims, n_sm, 16, plan, routing, seed, claim_rows=rows)
 
 
 @pytest.mark.parametrize("batch", [1, 16])
