@@ -132,6 +132,10 @@ WORKLOADS = {
     "tiny_fp8": Workload("tiny_fp8", TINY, batch=1, context=64, steps=8, expert_format="fp8"),
     "mid_fp8": Workload("mid_fp8", MID, batch=1, context=8192, steps=32, expert_format="fp8"),
     "a3b_8k_fp8": Workload("a3b_8k_fp8", A3B, batch=1, context=8192, steps=128, expert_format="fp8"),
+    # attention-heavy several-token case on the mid model (16 sequences at
+    # 4K-16K, churn): about 4 GB on the device, for full profiler captures
+    "mid_b16_16k": Workload("mid_b16_16k", MID, batch=16, context=0, steps=8, ragged=(4096, 16384),
+                            churn=True, join_context=2048),
     # dense-FFN models (one always-selected expert): tiny at batch 1 and 5 with
     # churn, mid (intermediate 4096) at 8K
     "tiny_dense": Workload("tiny_dense", TINY_DENSE, batch=1, context=64, steps=8),
