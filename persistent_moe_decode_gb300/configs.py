@@ -142,6 +142,8 @@ WORKLOADS = {
     "tiny_dense_b5": Workload("tiny_dense_b5", TINY_DENSE, batch=5, context=0, steps=6, ragged=(10, 300),
                               churn=True, join_context=40),
     "mid_dense": Workload("mid_dense", MID_DENSE, batch=1, context=8192, steps=32),
+    # a dense FFN model whose one expert is 8-bit
+    "tiny_dense_fp8": Workload("tiny_dense_fp8", TINY_DENSE, batch=1, context=64, steps=8, expert_format="fp8"),
 }
 
 

@@ -74,7 +74,9 @@ def test_create_rejects_bad_configs_before_touching_the_device(lib):
                 # 8-bit experts: batch 1 only, hidden 2048 or <= 1024, moe_inter % 16
                 dict(expert_format=mk.MK_EXPERTS_FP8_E4M3, max_batch=2),
                 dict(expert_format=mk.MK_EXPERTS_FP8_E4M3, hidden=1536),
-                dict(expert_format=mk.MK_EXPERTS_FP8_E4M3, moe_inter=136)):
+                dict(expert_format=mk.MK_EXPERTS_FP8_E4M3, moe_inter=136),
+                # claimed expert tiles: a multiple of 16 rows, or 0 / -1
+                dict(moe_claim_rows=24), dict(moe_claim_rows=-2)):
         cfg = mk.make_config(TINY, 1, 8, 16)
         for k, v in bad.items():
             setattr(cfg, k, v)

@@ -213,6 +213,17 @@ def test_fp8_experts_tiny_moe_output_and_trajectory():
         pair.close()
 
 
+def test_fp8_experts_mid_with_forced_split_kv():
+    """8-bit experts with 256-token split-KV items (many items, several
+    combines per head): two steps of the trajectory."""
+    wl = WORKLOADS["mid_fp8"].with_(steps=2)
+    pair = Pair(wl, kv_split_tokens=256)
+    try:
+        run_trajectory(pair, wl.steps)
+    finally:
+        pair.close()
+
+
 def test_fp8_experts_mid_trajectory():
     """8-bit experts on the tensor cores (rows of 2048 E4M3 bytes, 16 per
     stage), mid model at 8K context."""
@@ -230,7 +241,8 @@ def test_fp8_experts_mid_trajectory():
         pair.close()
 
 
-@pytest.mark.parametrize("name,steps", [("tiny_dense", 8), ("tiny_dense_b5", 6), ("mid_dense", 4)])
+@pytest.mark.parametrize("name,steps", [("tiny_dense", 8), ("tiny_dense_b5", 6), ("mid_dense", 4),
+                                        ("tiny_dense_fp8", 8)])
 def test_dense_ffn_models(name, steps):
     """Dense feed-forward layers as one always-selected expert (E = k = 1):
     batch 1, several sequences with churn, and the mid shape with an
