@@ -42,3 +42,18 @@ def test_cpu_sample_after_advance_on_a_page_boundary(tiny_inputs):
 def test_context_reported_the_same_way_in_both_arms():
     assert bench.context_of(np.array([8197])) == 8197
     assert bench.context_of(np.array([1, 2])) == "ragged"
+
+
+def test_algorithmic_bytes_count_the_expert_format():
+    """Per distinct routed expert: 2 bytes a weight (BF16), or 1 byte a weight
+    plus one fp32 scale per row of its gate, up and down matrices (E4M3)."""
+    from persistent_moe_decode_gb300.configs import A3B, algorithmic_bytes
+    d = A3B
+    per_bf16 = 3 * d.moe_inter * d.hidden * 2
+    per_fp8 = 3 * d.moe_inter * d.hidden + 4 * (2 * d.moe_inter + d.hidden)
+    distinct = [8] * d.n_layers
+    keys = [8197]
+    b16 = algorithmic_bytes(d, distinct, keys)
+    b8 = algorithmic_bytes(d, distinct, keys, "fp8")
+    assert b16 - b8 == sum(distinct) * (per_bf16 - per_fp8)
+    assert b16 == 6889312256                     # the 8K batch-1 step the benchmark reports (8197 keys)
