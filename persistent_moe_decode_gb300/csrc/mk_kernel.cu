@@ -2127,23 +2127,38 @@ struct Cons {
       // B: hidden terms of columns (slot g1, 4 (cq & 1) ..) and (slot 2 + g1, ..)
       const uint32_t b0 = gl < 4 && onl ? *(const uint32_t*)(aq + gl * 64 + (q0 + g1) * 8 + wsel) : 0u;
       const uint32_t b1 = gl < 4 && onh ? *(const uint32_t*)(aq + gl * 64 + (q0 + 2 + g1) * 8 + wsel) : 0u;
-      for (int hb = 0; hb < H; hb += rd) {
-        uint32_t slot;
-        if (!stage_full(slot)) return false;
-        const uint8_t* sl = S.stage[slot] + (size_t)g1 * rd * 8 + wsel;          // slot g1
-        const uint8_t* sh = sl + (size_t)2 * rd * 8;                              // slot 2 + g1
+      // one 16-row block: its four row words and the MMA
+      auto block = [&](const uint8_t* sl, const uint8_t* sh, int r, float* a) {
+        const int ra = 8 * (r + gl + 8 * g1), rb = 8 * (r + gl + 8 - 8 * g1);
+        const uint32_t la = onl ? *(const uint32_t*)(sl + ra) : 0u, lb = onl ? *(const uint32_t*)(sl + rb) : 0u;
+        const uint32_t ha = onh ? *(const uint32_t*)(sh + ra) : 0u, hb2 = onh ? *(const uint32_t*)(sh + rb) : 0u;
+        // rows r + gl (a0, a2) and r + gl + 8 (a1, a3) of the stage
+        mma_e4m3(a, g1 ? lb : la, g1 ? la : lb, g1 ? hb2 : ha, g1 ? ha : hb2, b0, b1);
+      };
+      if (H == 2048) {
+        // two stages of 1024 rows: blocks 0-7 of the warp in the first, 8-15
+        // in the second (h0 = 16 w + 128 i), every index known at compile time
 #pragma unroll
-        for (int i = 0; i < kMaxBlk; i++) {
-          const int h0 = 16 * (warp + 8 * i);
-          if (i < nb && h0 >= hb && h0 < hb + rd) {
-            const int ra = 8 * (h0 - hb + gl + 8 * g1), rb = 8 * (h0 - hb + gl + 8 - 8 * g1);
-            const uint32_t la = onl ? *(const uint32_t*)(sl + ra) : 0u, lb = onl ? *(const uint32_t*)(sl + rb) : 0u;
-            const uint32_t ha = onh ? *(const uint32_t*)(sh + ra) : 0u, hb2 = onh ? *(const uint32_t*)(sh + rb) : 0u;
-            // rows h0 + gl (a0, a2) and h0 + gl + 8 (a1, a3)
-            mma_e4m3(acc[i], g1 ? lb : la, g1 ? la : lb, g1 ? hb2 : ha, g1 ? ha : hb2, b0, b1);
-          }
+        for (int half = 0; half < 2; half++) {
+          uint32_t slot;
+          if (!stage_full(slot)) return false;
+          const uint8_t* sl = S.stage[slot] + (size_t)g1 * 1024 * 8 + wsel;
+#pragma unroll
+          for (int j = 0; j < 8; j++) block(sl, sl + 2 * 1024 * 8, 16 * warp + 128 * j, acc[8 * half + j]);
+          stage_release(slot);
         }
-        stage_release(slot);
+      } else {
+        for (int hb = 0; hb < H; hb += rd) {
+          uint32_t slot;
+          if (!stage_full(slot)) return false;
+          const uint8_t* sl = S.stage[slot] + (size_t)g1 * rd * 8 + wsel;          // slot g1
+#pragma unroll
+          for (int i = 0; i < kMaxBlk; i++) {
+            const int h0 = 16 * (warp + 8 * i);
+            if (i < nb && h0 >= hb && h0 < hb + rd) block(sl, sl + (size_t)2 * rd * 8, h0 - hb, acc[i]);
+          }
+          stage_release(slot);
+        }
       }
     }
 #pragma unroll
