@@ -1501,11 +1501,13 @@ struct Cons {
   // + g / (4 NH), part (g / 2) % P, high or low half g % 2 of x.  C[m][n] is
   // kept where the parts match; the lanes holding a token's parts of a row
   // are added (quad shuffles; with R = 4 also the two quads of a row).
-  template <int NH>
+  // (NQ: n-tiles in use, 1..4, fixed at compile time so that the unrolled
+  // loops carry no per-tile predicates)
+  template <int NH, int NQ>
   __device__ __forceinline__ bool gemv_mma_multi(float* part) {
     constexpr int R = 8 / NH, TPT = 2 / NH;       // rows per stage, tokens per n-tile
     const int nt = t[R_NT], nr = t[R_NROWS], nblk = t[R_NBLK];
-    const int nq = (nt + TPT - 1) / TPT;          // n-tiles in use (<= 4)
+    constexpr int nq = NQ;
     uint32_t xb[4][8][2];
 #pragma unroll
     for (int q = 0; q < 4; q++) {
@@ -1579,10 +1581,11 @@ struct Cons {
   // rows x every column block (swizzled, line 16 cb + r): the M side is the 16
   // rows, the K side the warp's I / 8 columns, the N side column n = 8 q + g
   // holds token 4 q + g / 2, high or low half g % 2 of its hidden vector.
+  template <int NQ>
   __device__ __forceinline__ bool gemv_mma_down(float* part) {
     const int K = t[R_K], nt = t[R_NT], nr = t[R_NROWS];
     const int ks = K >> 7;                        // k-steps per warp (<= 8)
-    const int nq = (nt + 3) >> 2;                 // n-tiles: four tokens each
+    constexpr int nq = NQ;                        // n-tiles: four tokens each
     const int col0 = warp * (K >> 3);
     uint32_t xb[4][8][2];
 #pragma unroll
@@ -2804,10 +2807,21 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
     if (ok && run) {
       // tokens per pass matched to the chunk (an expert's few routed tokens do
       // not pay for eight)
-      ok = (mma ? (kind == K_DOWN ? c.gemv_mma_down(part)
-                  : K == 2048 ? c.template gemv_mma_multi<1>(part) : c.template gemv_mma_multi<2>(part))
-                : nt <= 1 ? c.template gemv<1>(part) : c.template gemv<8>(part)) &&
-           c.csync();
+      if (mma && kind == K_DOWN) {
+        const int nq = (nt + 3) >> 2;
+        ok = nq <= 1 ? c.template gemv_mma_down<1>(part) : nq == 2 ? c.template gemv_mma_down<2>(part)
+           : nq == 3 ? c.template gemv_mma_down<3>(part) : c.template gemv_mma_down<4>(part);
+      } else if (mma && K == 2048) {
+        const int nq = (nt + 1) >> 1;
+        ok = nq <= 1 ? c.template gemv_mma_multi<1, 1>(part) : nq == 2 ? c.template gemv_mma_multi<1, 2>(part)
+           : nq == 3 ? c.template gemv_mma_multi<1, 3>(part) : c.template gemv_mma_multi<1, 4>(part);
+      } else if (mma) {
+        ok = nt <= 1 ? c.template gemv_mma_multi<2, 1>(part) : nt == 2 ? c.template gemv_mma_multi<2, 2>(part)
+           : nt == 3 ? c.template gemv_mma_multi<2, 3>(part) : c.template gemv_mma_multi<2, 4>(part);
+      } else {
+        ok = nt <= 1 ? c.template gemv<1>(part) : c.template gemv<8>(part);
+      }
+      ok = ok && c.csync();
     }
     if (ok && run) {
       c.epilogue(part, mma ? kConsumerWarps : gemv_nseg(t[R_K]));
