@@ -330,7 +330,7 @@ int mk_read_debug(mk_handle* h, int which, void* dst, size_t bytes, size_t* size
  * run a step: a real-time serving loop that must not take the allocator's
  * locks or meet an out-of-memory failure between steps, or a host runtime
  * that owns every device allocation itself and forbids its plug-ins to call
- * cudaMalloc.  The paper has no counterpart of this call.
+ * cudaMalloc.  The megakernel serving engine it follows has no such call.
  *
  * mk_decode_step keeps the step's counters, queue claim heads and error words
  * in device memory the handle allocated; this call keeps them instead in one
