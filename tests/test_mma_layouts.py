@@ -269,3 +269,216 @@ def test_partial_slots_stay_in_the_buffer(nt):
             assert top * nt + nt - 1 < PART_FLOATS, (K, nt, nblk, nr)
     cd = max(16, min(512, PART_FLOATS // (WARPS * nt)) // 16 * 16)
     assert ((cd - 1) * WARPS + WARPS - 1) * nt + nt - 1 < PART_FLOATS
+
+
+# ---------------------------------------------------------------- 8-bit experts
+# mma.sync m16n8k32 with E4M3 operands (PTX fragment layout of the 8-bit
+# types): lane (g, c) holds A[g][4c..4c+3] (a0), A[g+8][4c..] (a1),
+# A[g][16+4c..] (a2), A[g+8][16+4c..] (a3), B[4c..4c+3][g] (b0) and
+# B[16+4c..][g] (b1); C as above.  ldmatrix.x4 of b16 tiles hands lane l the
+# 4 bytes 4 (l % 4) .. + 3 of row l / 4 of each tile.
+
+def ldmatrix_x4_bytes(stage: np.ndarray, addr: np.ndarray):
+    """Per lane, the four 4-byte registers ldmatrix.x4 returns."""
+    regs = np.zeros((32, 4, 4))
+    for i in range(4):
+        a = addr[8 * i:8 * i + 8]
+        assert len(set(((a // 16) % 8).tolist())) == 8, "bank conflict"
+        for lane in range(32):
+            row = a[lane >> 2]
+            regs[lane, i] = stage[row + 4 * (lane & 3):row + 4 * (lane & 3) + 4]
+    return regs
+
+
+def a_from_regs(regs) -> np.ndarray:
+    A = np.full((16, 32), np.nan)
+    for lane in range(32):
+        g, c = lane >> 2, lane & 3
+        A[g, 4 * c:4 * c + 4] = regs[lane][0]
+        A[g + 8, 4 * c:4 * c + 4] = regs[lane][1]
+        A[g, 16 + 4 * c:20 + 4 * c] = regs[lane][2]
+        A[g + 8, 16 + 4 * c:20 + 4 * c] = regs[lane][3]
+    return A
+
+
+def b_from_words(b0, b1) -> np.ndarray:
+    B = np.zeros((32, 8))
+    for lane in range(32):
+        g, c = lane >> 2, lane & 3
+        B[4 * c:4 * c + 4, g] = b0[lane]
+        B[16 + 4 * c:20 + 4 * c, g] = b1[lane]
+    return B
+
+
+def term_scales(s0: float, c: int):
+    """The lane's scales of its C columns 2 c and 2 c + 1 (terms 2 c, 2 c + 1;
+    columns past the four terms carry nothing)."""
+    return (s0 * 16.0 ** (-2 * c), s0 * 16.0 ** (-2 * c - 1)) if c < 2 else (0.0, 0.0)
+
+
+@pytest.mark.parametrize("rows", [16, 11])
+def test_e4m3_gate_up_rows(rows):
+    """gemv_mma_e4m3: 16 rows of 2048 bytes per stage, copied as rows of 1024
+    two-byte words (128-byte block cb of row r is line 16 cb + r, chunk c at
+    c ^ (line & 7)); warp w takes columns [256 w, 256 w + 256) in 8 k-steps;
+    N column t < 4 is x's term t.  Byte values are stand-ins (the index
+    arithmetic does not depend on them)."""
+    rng = np.random.default_rng(rows)
+    K, s0 = 2048, 0.375
+    W = rng.standard_normal((16, K))
+    xq = rng.standard_normal((4, K))
+    r, k = np.meshgrid(np.arange(16), np.arange(K), indexing="ij")
+    line = (k // 128) * 16 + r
+    byte = line * 128 + (((k % 128) // 16) ^ (line & 7)) * 16 + k % 16
+    assert len(np.unique(byte)) == byte.size and byte.max() < STAGE_BYTES
+    st = np.full(STAGE_BYTES, np.nan)
+    st[byte.ravel()] = W[r, k].ravel()
+    part = np.full((16, WARPS), np.nan)
+    for warp in range(WARPS):
+        C = np.zeros((16, 8))
+        for s in range(8):
+            addr = np.zeros(32, dtype=np.int64)
+            for lane in range(32):
+                rr, ch = ((lane >> 3) & 1) * 8 + (lane & 7), 2 * s + (lane >> 4)
+                ln = (2 * warp + (ch >> 3)) * 16 + rr
+                addr[lane] = ln * 128 + (((ch & 7) ^ (rr & 7)) << 4)
+            b0, b1 = np.zeros((32, 4)), np.zeros((32, 4))
+            for lane in range(32):
+                g, c = lane >> 2, lane & 3
+                k0 = 256 * warp + 32 * s + 4 * c
+                if g < 4:
+                    b0[lane], b1[lane] = xq[g, k0:k0 + 4], xq[g, k0 + 16:k0 + 20]
+            C += a_from_regs(ldmatrix_x4_bytes(st, addr)) @ b_from_words(b0, b1)
+        v0, v8 = np.zeros(32), np.zeros(32)
+        for lane in range(32):
+            sa, sb = term_scales(s0, lane & 3)
+            c0, c1, c2, c3 = c_lane(C, lane)
+            v0[lane], v8[lane] = sa * c0 + sb * c1, sa * c2 + sb * c3
+        v0, v8 = v0 + shfl_xor(v0, 1), v8 + shfl_xor(v8, 1)
+        for lane in range(32):
+            g, c = lane >> 2, lane & 3
+            if c == 0:
+                if g < rows:
+                    part[g, warp] = v0[lane]
+                if g + 8 < rows:
+                    part[g + 8, warp] = v8[lane]
+    x = sum(s0 * 16.0 ** -t * xq[t] for t in range(4))
+    assert np.isnan(part[rows:]).all()
+    np.testing.assert_allclose(part[:rows].sum(1), (W @ x)[:rows], rtol=1e-12, atol=1e-9)
+
+
+@pytest.mark.parametrize("H,ncb", [(256, 1), (256, 5), (512, 8), (1024, 3), (2048, 1), (2048, 6), (2048, 8)])
+def test_e4m3_down_quads(H, ncb):
+    """down_mma_e4m3: a piece's ncb groups of 8 columns arrive as quads; a
+    stage holds the quad's rows [hb, hb + rd) (rd = min(H, 1024); group slot j
+    at j rd 8 bytes, 8 bytes a row); lane (g, c) takes columns 4 (c & 1) ..
+    + 3 of slots c >> 1 and 2 + (c >> 1) in rows h0 + g and h0 + g + 8, the
+    two loads of a pair swapped between the slots' lanes; the B words are the
+    hidden terms of the same columns.  The 32 lanes' words must fall in
+    distinct banks."""
+    rng = np.random.default_rng(H + ncb)
+    s0, rd, nb = 0.0625, min(H, 1024), H // 128
+    Wd = rng.standard_normal((ncb, H, 8))          # group c: [H][8]
+    aq = np.zeros((4, 64))
+    aq[:, :8 * ncb] = rng.standard_normal((4, 8 * ncb))
+    scl = rng.standard_normal(H)
+    out = np.full(H, np.nan)
+    for warp in range(WARPS):
+        acc = np.zeros((16, 16, 8))                  # [block][C]
+        for q0 in range(0, ncb, 4):
+            nq = min(4, ncb - q0)
+            b0, b1 = np.zeros((32, 4)), np.zeros((32, 4))
+            for lane in range(32):
+                g, c = lane >> 2, lane & 3
+                g1, wsel = c >> 1, 4 * (c & 1)
+                if g < 4 and g1 < nq:
+                    b0[lane] = aq[g, (q0 + g1) * 8 + wsel:(q0 + g1) * 8 + wsel + 4]
+                if g < 4 and 2 + g1 < nq:
+                    b1[lane] = aq[g, (q0 + 2 + g1) * 8 + wsel:(q0 + 2 + g1) * 8 + wsel + 4]
+            B = b_from_words(b0, b1)
+            for hb in range(0, H, rd):
+                st = np.full(STAGE_BYTES, np.nan)
+                for j in range(nq):
+                    st[j * rd * 8:(j + 1) * rd * 8] = Wd[q0 + j, hb:hb + rd].ravel()
+                blocks = ([(8 * (hb // 1024) + j, 16 * warp + 128 * j) for j in range(8)] if H == 2048 else
+                          [(i, 16 * (warp + 8 * i) - hb) for i in range(nb) if hb <= 16 * (warp + 8 * i) < hb + rd])
+                for i, r in blocks:
+                    regs = np.zeros((32, 4, 4))
+                    banks = []
+                    for lane in range(32):
+                        g, c = lane >> 2, lane & 3
+                        g1, wsel = c >> 1, 4 * (c & 1)
+                        sl, sh = g1 * rd * 8 + wsel, (2 + g1) * rd * 8 + wsel
+                        ra, rb = 8 * (r + g + 8 * g1), 8 * (r + g + 8 - 8 * g1)
+                        onl, onh = g1 < nq, 2 + g1 < nq
+                        la = st[sl + ra:sl + ra + 4] if onl else np.zeros(4)
+                        lb = st[sl + rb:sl + rb + 4] if onl else np.zeros(4)
+                        ha = st[sh + ra:sh + ra + 4] if onh else np.zeros(4)
+                        hb2 = st[sh + rb:sh + rb + 4] if onh else np.zeros(4)
+                        regs[lane] = (lb, la, hb2, ha) if g1 else (la, lb, ha, hb2)
+                        banks.append(((sl + ra) // 4) % 32)
+                    assert sorted(banks) == list(range(32)), "bank conflict"
+                    A = a_from_regs(regs)
+                    assert not np.isnan(A).any()
+                    acc[i] += A @ B
+        for i in range(nb):
+            v0, v8 = np.zeros(32), np.zeros(32)
+            for lane in range(32):
+                sa, sb = term_scales(s0, lane & 3)
+                c0, c1, c2, c3 = c_lane(acc[i], lane)
+                v0[lane], v8[lane] = sa * c0 + sb * c1, sa * c2 + sb * c3
+            v0, v8 = v0 + shfl_xor(v0, 1), v8 + shfl_xor(v8, 1)
+            for lane in range(32):
+                g, c = lane >> 2, lane & 3
+                if c == 0:
+                    h = 16 * (warp + 8 * i) + g
+                    assert np.isnan(out[h]) and np.isnan(out[h + 8])
+                    out[h], out[h + 8] = v0[lane] * scl[h], v8[lane] * scl[h + 8]
+    a = sum(s0 * 16.0 ** -t * aq[t] for t in range(4))
+    ref = sum(Wd[c] @ a[8 * c:8 * c + 8] for c in range(ncb)) * scl
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-9)
+
+
+def _e4m3(v: np.ndarray) -> np.ndarray:
+    """Round to the nearest E4M3 value (ties to even), saturating at 448."""
+    import torch
+    t = torch.from_numpy(np.clip(v, -448.0, 448.0).astype(np.float32)).to(torch.float8_e4m3fn)
+    return t.to(torch.float32).numpy()
+
+
+def _scale0(mx: float) -> float:
+    """The smallest power of two s with mx / s <= 448 (1 for mx = 0)."""
+    y = np.float32(mx) / np.float32(448.0)
+    if not y > 0:
+        return 1.0
+    m, e = np.frexp(np.float64(y))               # y = m 2^e, m in [0.5, 1)
+    return float(2.0 ** (e - 1) if m == 0.5 else 2.0 ** e)
+
+
+@pytest.mark.parametrize("kind", ["normal", "outliers", "tiny", "zero"])
+def test_four_e4m3_terms_keep_x_to_about_16_bits(kind):
+    """The activations' cut into E4M3 terms: s_0 the smallest power of two
+    with max|x| / s_0 <= 448, s_t = s_0 16^-t, term t the nearest E4M3 value
+    of the remainder / s_t.  No term saturates (|remainder / s_t| <= 448) and
+    the four terms give x back to within 2^-16 of max|x| (each term's
+    remainder is at most half its largest step)."""
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal(4096).astype(np.float32)
+    if kind == "outliers":
+        x[rng.integers(0, 4096, 5)] *= 300.0
+    elif kind == "tiny":
+        x *= np.float32(1e-30)
+    elif kind == "zero":
+        x[:] = 0.0
+    s0 = _scale0(float(np.abs(x).max()))
+    r = x.copy()
+    rec = np.zeros(4096)
+    for t in range(4):
+        st = np.float32(s0 * 16.0 ** -t)
+        y = r / st
+        assert np.abs(y).max() <= 448.0
+        q = _e4m3(y)
+        rec += np.float64(st) * q
+        r = (r - st * q).astype(np.float32)
+    bound = 2.0 ** -16 * float(np.abs(x).max())
+    assert np.abs(rec - x).max() <= bound
