@@ -23,7 +23,8 @@ epilogue adds them, equal W (x_hi + x_lo) for every row and token.  The high
 and low halves of x are drawn independently, so a dropped, doubled or swapped
 half fails.  A dropped term, a wrong part or token index, or a transposed
 operand fails the equality; the partial-slot bound is checked for every chunk
-the producer can hand over.
+the producer can hand over.  The 8-bit expert paths (m16n8k32 with E4M3
+operands, x as four E4M3 terms) are checked the same way further down.
 """
 from __future__ import annotations
 
