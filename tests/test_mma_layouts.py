@@ -24,7 +24,9 @@ and low halves of x are drawn independently, so a dropped, doubled or swapped
 half fails.  A dropped term, a wrong part or token index, or a transposed
 operand fails the equality; the partial-slot bound is checked for every chunk
 the producer can hand over.  The 8-bit expert paths (m16n8k32 with E4M3
-operands, x as four E4M3 terms) are checked the same way further down.
+operands, x as four E4M3 terms) and the attention's two products on a staged
+page (ldmatrix .trans for V, movmatrix for P^T) are checked the same way
+further down.
 """
 from __future__ import annotations
 
@@ -483,3 +485,141 @@ def test_four_e4m3_terms_keep_x_to_about_16_bits(kind):
         r = (r - st * q).astype(np.float32)
     bound = 2.0 ** -16 * float(np.abs(x).max())
     assert np.abs(rec - x).max() <= bound
+
+
+# ------------------------------------------------------------------ attention
+# One page of one KV group g, as a warp of the attention item sees it.  The
+# page image holds rows = hkv x 16 rows (head-major: row g P + token) of D
+# dims as boxes of 64 dims, 128-byte swizzled; the query is staged as [head][D]
+# with 16-byte chunk c of row h at c ^ (h & 7).  ldmatrix .trans hands lane l
+# the pair (2 (l % 4), l / 4), (2 (l % 4) + 1, l / 4) of each tile as stored;
+# movmatrix .trans turns lane l's pair of row l / 4 into the same pair of the
+# transposed 8 x 8 block.
+
+PAGE = 16
+
+
+def kv_off(r: int, c: int, rows: int) -> int:
+    return (c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4)
+
+
+def page_image(KV: np.ndarray) -> np.ndarray:
+    """KV [hkv][16][D] as the staged page image, in 2-byte slots."""
+    hkv, P, D = KV.shape
+    rows = hkv * P
+    img = np.full(rows * D, np.nan)
+    for g in range(hkv):
+        for t in range(P):
+            for k in range(D):
+                o = kv_off(g * P + t, k >> 3, rows) + (k & 7) * 2
+                assert np.isnan(img[o // 2])
+                img[o // 2] = KV[g, t, k]
+    assert not np.isnan(img).any()
+    return img
+
+
+def ldmatrix_x4_trans(stage: np.ndarray, addr: np.ndarray) -> np.ndarray:
+    A = np.full((16, 16), np.nan)
+    for i in range(4):
+        a = addr[8 * i:8 * i + 8]
+        assert len(set(((a // 16) % 8).tolist())) == 8, "bank conflict"
+        tile = np.array([stage[a[g] // 2:a[g] // 2 + 8] for g in range(8)])
+        A[8 * (i & 1):8 * (i & 1) + 8, 8 * (i >> 1):8 * (i >> 1) + 8] = tile.T
+    return A
+
+
+def movmatrix_trans(pairs: np.ndarray) -> np.ndarray:
+    """pairs[lane] = (X[l / 4][2 (l % 4)], X[l / 4][2 (l % 4) + 1]) of an 8 x 8
+    block X; returns the same pairs of X^T."""
+    X = np.zeros((8, 8))
+    for lane in range(32):
+        X[lane >> 2, 2 * (lane & 3):2 * (lane & 3) + 2] = pairs[lane]
+    out = np.zeros((32, 2))
+    for lane in range(32):
+        out[lane] = X.T[lane >> 2, 2 * (lane & 3):2 * (lane & 3) + 2]
+    return out
+
+
+def b_from_pairs(b0: np.ndarray, b1: np.ndarray) -> np.ndarray:
+    """m16n8k16 B from each lane's two registers (pairs of rows 2c, 2c + 1 and
+    2c + 8, 2c + 9 of column g)."""
+    B = np.zeros((16, 8))
+    for lane in range(32):
+        g, c = lane >> 2, lane & 3
+        B[2 * c:2 * c + 2, g] = b0[lane]
+        B[8 + 2 * c:8 + 2 * c + 2, g] = b1[lane]
+    return B
+
+
+@pytest.mark.parametrize("D,hkv,grp,lo_t,hi_t", [(128, 4, 8, 0, 16), (128, 4, 8, 3, 11), (64, 2, 2, 0, 16),
+                                                 (128, 8, 4, 5, 16), (64, 4, 3, 0, 7)])
+def test_attention_page_fragments(D, hkv, grp, lo_t, hi_t):
+    """S^T = K Q^T (A: the group's K rows by ldmatrix, B: Q^T from the swizzled
+    query staging, high and low halves) and O^T = V^T P^T (A: ldmatrix .trans
+    of the V rows, B: the score fragments' probabilities transposed by
+    movmatrix, high and low halves): every group g, every valid token and
+    every head of the group, for both D."""
+    rng = np.random.default_rng(D + hkv + grp + lo_t)
+    KS, rows, hq = D // 16, hkv * PAGE, hkv * grp
+    Kp, Vp = rng.standard_normal((hkv, PAGE, D)), rng.standard_normal((hkv, PAGE, D))
+    kimg, vimg = page_image(Kp), page_image(Vp)
+    qh, ql = rng.standard_normal((hq, D)), rng.standard_normal((hq, D))
+    qhi, qlo = np.full(hq * D, np.nan), np.full(hq * D, np.nan)
+    for h in range(hq):
+        for k in range(D):
+            o = h * D * 2 + (((k >> 3) ^ (h & 7)) << 4) + (k & 7) * 2
+            qhi[o // 2], qlo[o // 2] = qh[h, k], ql[h, k]
+    ph, pl = rng.standard_normal((PAGE, 8)), rng.standard_normal((PAGE, 8))   # [token][head]
+    for g in range(hkv):
+        # B fragments of Q^T
+        qb = {}
+        for s in range(KS):
+            for which, img in (("h", qhi), ("l", qlo)):
+                regs = np.zeros((2, 32, 2))
+                for lane in range(32):
+                    gl, cq = lane >> 2, lane & 3
+                    qrow = g * grp + gl
+                    for hf in range(2):
+                        off = qrow * D * 2 + (((2 * s + hf) ^ (qrow & 7)) << 4) + 4 * cq
+                        regs[hf, lane] = img[off // 2:off // 2 + 2] if gl < grp else 0.0
+                qb[s, which] = b_from_pairs(regs[0], regs[1])
+        # S^T = K Q^T
+        C = np.zeros((16, 8))
+        for s in range(KS):
+            addr = np.array([kv_off(g * PAGE + ((lane >> 3) & 1) * 8 + (lane & 7), 2 * s + (lane >> 4), rows)
+                             for lane in range(32)])
+            A = ldmatrix_x4(kimg, addr)
+            C += A @ qb[s, "h"] + A @ qb[s, "l"]
+        ref = Kp[g] @ (qh + ql)[g * grp:g * grp + grp].T          # [token][head]
+        for lane in range(32):
+            gl, cq = lane >> 2, lane & 3
+            c0, c1, c2, c3 = c_lane(C, lane)
+            for tok, hd, v in ((gl, 2 * cq, c0), (gl, 2 * cq + 1, c1), (gl + 8, 2 * cq, c2), (gl + 8, 2 * cq + 1, c3)):
+                if hd < grp:
+                    assert abs(v - ref[tok, hd]) < 1e-9, (g, tok, hd)
+                else:
+                    assert v == 0.0                                  # no padded head carries a score
+        # O^T += V^T P^T with the lanes' probabilities (invalid rows give 0)
+        pv = {}
+        for which, src in (("h", ph), ("l", pl)):
+            p01, p23 = np.zeros((32, 2)), np.zeros((32, 2))
+            for lane in range(32):
+                gl, cq = lane >> 2, lane & 3
+                ok0, ok1 = lo_t <= gl < hi_t, lo_t <= gl + 8 < hi_t
+                p01[lane] = src[gl, 2 * cq:2 * cq + 2] if ok0 else 0.0
+                p23[lane] = src[gl + 8, 2 * cq:2 * cq + 2] if ok1 else 0.0
+            pv[which] = b_from_pairs(movmatrix_trans(p01), movmatrix_trans(p23))
+        P = np.zeros((PAGE, 8))
+        P[lo_t:hi_t] = (ph + pl)[lo_t:hi_t]
+        oref = Vp[g].T @ P                                           # [dim][head]
+        for s in range(KS):
+            addr = np.array([kv_off(g * PAGE + (lane >> 4) * 8 + (lane & 7), 2 * s + ((lane >> 3) & 1), rows)
+                             for lane in range(32)])
+            A = ldmatrix_x4_trans(vimg, addr)
+            O = A @ pv["h"] + A @ pv["l"]
+            for lane in range(32):
+                gl, cq = lane >> 2, lane & 3
+                o0, o1, o2, o3 = c_lane(O, lane)
+                for dim, hd, v in ((16 * s + gl, 2 * cq, o0), (16 * s + gl, 2 * cq + 1, o1),
+                                   (16 * s + 8 + gl, 2 * cq, o2), (16 * s + 8 + gl, 2 * cq + 1, o3)):
+                    assert abs(v - oref[dim, hd]) < 1e-9, (g, s, dim, hd)
