@@ -71,6 +71,23 @@ def kernel_sha() -> str:
     return h.hexdigest()[:16]
 
 
+def slowest(seconds: float, dist=None) -> float:
+    """The slowest rank's time, on every rank (one rank: its own time).  The
+    whole-job rate divides all ranks' units by it."""
+    if dist is None:
+        return seconds
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: int, world: int, seconds: float) -> float:
+    """Units all ranks processed per second of the slowest rank's time."""
+    return units_per_rank * world / seconds
+
+
 class ClockSampler:
     """nvidia-smi sampling during the timed region (SM clock, throttle reasons)."""
 
@@ -301,7 +318,7 @@ def roofline_of(run, wl, kern_ms, keys, traffic_key):
                         "kernel": "mk_step_kernel (persistent, one block per SM)"}
 
 
-def e2e_timed(run, wl, args, stream, world):
+def e2e_timed(run, wl, args, stream, world, dist=None):
     """The same metric end to end through the C ABI: per step the host arrays
     go up (schedule), the step runs, the logits come back to pinned host
     memory and the host picks the next tokens (greedy)."""
@@ -315,6 +332,8 @@ def e2e_timed(run, wl, args, stream, world):
         torch.cuda.synchronize()
         run.advance(host_logits.numpy().argmax(1).astype(np.int32), refill=False)
     torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
     h2d = d2h = 0
     ts = time.perf_counter()
     for i in range(args.steps):
@@ -326,7 +345,7 @@ def e2e_timed(run, wl, args, stream, world):
         run.advance(host_logits.numpy().argmax(1).astype(np.int32), refill=False)
     te = time.perf_counter()
     run.check_status()
-    return {"value": B * args.steps * world / (te - ts), "unit": "tok/s",
+    return {"value": job_rate(B * args.steps, world, slowest(te - ts, dist)), "unit": "tok/s",
             "h2d_bytes_per_step": int(h2d // args.steps), "d2h_bytes_per_step": int(d2h // args.steps)}
 
 
@@ -410,15 +429,12 @@ def main():
 
     elapsed_ms, kern_ms, state, keys, clk = device_timed(run, wl, args, stream, tok_seq, dist,
                                                          ClockSampler(local))
-    if dist:
-        tt = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
-    tok_s = B * args.steps * world / (elapsed_ms / 1000.0)
+    elapsed_ms = slowest(elapsed_ms, dist)
+    tok_s = job_rate(B * args.steps, world, elapsed_ms / 1000.0)
     traffic_key = wl.name if not args.layers else f"{wl.name}:L{args.layers}"
     bytes_step, roof = roofline_of(run, wl, kern_ms, keys, traffic_key)
 
-    e2e = None if args.no_e2e else e2e_timed(run, wl, args, stream, world)
+    e2e = None if args.no_e2e else e2e_timed(run, wl, args, stream, world, dist)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -439,8 +455,9 @@ def main():
         el16, kern16, st16, keys16, clk16 = device_timed(run16, wl16, a16, stream, tok16, dist,
                                                          ClockSampler(local))
         bytes16, roof16 = roofline_of(run16, wl16, kern16, keys16, wl16.name)
+        el16 = slowest(el16, dist)
         b16 = {"workload": wl16.name, "batch": 16, "steps": a16.steps,
-               "value": 16 * a16.steps * world / (el16 / 1000.0), "unit": "tok/s",
+               "value": job_rate(16 * a16.steps, world, el16 / 1000.0), "unit": "tok/s",
                "ms_per_step": el16 / a16.steps,
                "contexts": f"{int(st16[1].min())}..{int(st16[1].max())} at the first timed step",
                "roofline": roof16, "clocks": clk16}
