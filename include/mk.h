@@ -7,10 +7,11 @@
  * engine for North Mini Code", §What is a Megakernel, Fig 2).  Dependencies
  * between tiles are global-memory counters that producers increment and
  * consumers spin on (§Barriers, Listing 2).  Work whose size depends on the
- * live sequence lengths or on the routing is cut into equal shares: the
- * split-KV items on the host, the routed experts' rows on the device once the
- * routing is known (the pages drain such tiles from shared queues; §The task
- * scheduler, the dynamic part).
+ * live sequence lengths or on the routing is cut at run time: the split-KV
+ * items on the host; the routed experts' rows on the device once the routing
+ * is known, into equal shares with one token and, with several tokens, into
+ * fixed-size tiles that the expert-branch SMs claim from per-layer counters
+ * (the pages' shared queues; §The task scheduler, the dynamic part).
  *
  * The host side mirrors the pages' decode service loop (§The serving engine
  * around the kernel: update_kv_page_tables, clear_scratch_and_barriers,
