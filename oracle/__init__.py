@@ -19,6 +19,9 @@ import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "liboracle.so")
+# a prebuilt copy of the same source to load instead (the sanitizer test
+# builds one with AddressSanitizer); it is used as it is, never rebuilt
+LIB_OVERRIDE = os.environ.get("ORACLE_LIB")
 
 BF16_X, BF16_Q, BF16_ATTN, BF16_A = 1, 2, 4, 8
 ALL_BF16 = BF16_X | BF16_Q | BF16_ATTN | BF16_A
@@ -70,8 +73,11 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            L = C.CDLL(LIB_PATH)
+            if LIB_OVERRIDE:
+                L = C.CDLL(LIB_OVERRIDE)
+            else:
+                build()
+                L = C.CDLL(LIB_PATH)
             vp, i32, dbl = C.c_void_p, C.c_int, C.c_double
             L.orc_bf16_to_double.restype = dbl
             L.orc_bf16_to_double.argtypes = [C.c_uint16]
