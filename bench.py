@@ -47,7 +47,7 @@ def load_peaks():
 
 
 def load_traffic(workload: str):
-    """dram bytes per step from a committed ncu summary measured with the current kernel sources."""
+    """dram bytes per step from a committed ncu summary measured with the current kernel code."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -60,14 +60,25 @@ def load_traffic(workload: str):
     return None
 
 
+def kernel_code(text: str) -> str:
+    """A CUDA / C++ source without its comments, trailing blanks and blank
+    lines: what the compiler turns into code."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
 def kernel_sha() -> str:
+    """Key of the traffic record: a hash of the kernel sources' code (comments
+    excluded, so an edit to the documentation keeps the record)."""
     import hashlib
     h = hashlib.sha256()
     cs = os.path.join(ROOT, "persistent_moe_decode_gb300", "csrc")
     for fn in sorted(os.listdir(cs)):
         if fn.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(cs, fn), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(cs, fn), encoding="utf-8") as f:
+                h.update(fn.encode() + b"\0" + kernel_code(f.read()).encode() + b"\0")
     return h.hexdigest()[:16]
 
 

@@ -16,23 +16,32 @@
 //  - block = 8 consumer warps + 1 producer warp (setmaxnreg 216 / 72).  The
 //    producer resolves the task list (attention items, the routed experts'
 //    rows) and streams every weight / KV byte HBM -> shared memory into a
-//    5-stage ring of 32 KB stages guarded by mbarriers: 1-D bulk copies of
-//    whole weight rows, 2-D tensor copies (128-byte swizzle) of KV pages, all
-//    with an evict-first L2 policy (each of those bytes is read once a step;
-//    the kernel's code and activations stay in L2).  The ring runs ahead
-//    across task boundaries, so a task that waits for its activations
-//    already has its weights in flight.
+//    5-stage ring of 32 KB stages guarded by mbarriers: 3-D tensor copies of
+//    whole weight rows laid out with the 128-byte swizzle (rows of 2048 or
+//    4096 columns; 1-D bulk copies where no tensor map applies), 2-D tensor
+//    copies of KV pages, all with an evict-first L2 policy (each of those
+//    bytes is read once a step; the kernel's code and activations stay in
+//    L2).  The ring runs ahead across task boundaries, so a task that waits
+//    for its activations already has its weights in flight.
 //  - roles: per step the SMs split into an attention branch (P1, ATTN,
 //    COMBINE, OUT) and an expert branch (P1, ROUTE, UP, DOWN, OUT) of the
 //    parallel layer; every SM of a branch takes an equal share of each of
 //    its waves (one token: an attention SM takes 4 times an expert SM's
-//    O-proj rows).
-//  - GEMV, one token: P1, O-proj and UP chunks split the contraction over the
-//    warps (x in registers, a transposed butterfly per stage, the warps' sums
-//    in a fixed order); an UP piece also multiplies its columns of the down
-//    projection, one fp32 partial per 8-column group, summed by the DOWN
-//    wave.  Several tokens: 256-column segments per warp, up to eight tokens
-//    per pass, fixed-order segment sums.  CUDA cores, fp32 (packed FMAs).
+//    O-proj rows), except the routed experts' rows with 4 tokens or more,
+//    which the expert SMs claim as 128-row tiles from per-layer counters.
+//  - GEMV: mma.sync m16n8k16 on the tensor cores, BF16 weights against the
+//    fp32 activations split into BF16 high and low halves, fp32 accumulate;
+//    the stage's rows and column parts on the M side, the tokens (and the
+//    halves) on the N side; one token for rows of 2048 / 4096 columns, up to
+//    8 / 4 tokens for several, and an expert's down rows for up to 16 tokens.
+//    The other shapes (the 16-token dense rows among them) run on the CUDA
+//    cores with fp32 FMAs, 256-column segments per warp.  Every reduction
+//    adds the warps' partial sums in a fixed order.  One token: an UP piece
+//    also multiplies its columns of the down projection, one fp32 partial per
+//    8-column group, summed by the DOWN wave.
+//  - 8-bit experts (OCP E4M3, one fp32 scale per output row; batch 1): the
+//    activations as four E4M3 terms against the E4M3 weights in mma.sync
+//    m16n8k32, fp32 accumulate, in kernel instances of their own.
 //  - the residual add + RMSNorm is computed by every SM for itself at the
 //    start of each layer (its own copy of the residual stream), so no SM waits
 //    for a norm task; the routing likewise (one token: by each expert SM's
