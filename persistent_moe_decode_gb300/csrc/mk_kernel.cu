@@ -392,8 +392,8 @@ struct Prod {
   }
 
   // rows [row0, row0 + nrows) of a row-major [*, K] matrix, whole rows, one
-  // copy per stage: a 1-D bulk copy, or (one token, rows of 2048 or 4096
-  // columns) a 3-D tensor copy through the matrix's map, which lands the
+  // copy per stage: a 1-D bulk copy, or (rows of 2048 or 4096 columns bound
+  // for the tensor cores) a 3-D tensor copy through the matrix's map, which lands the
   // stage swizzled for the tensor-core GEMV (a whole box: rows past a short
   // last stage are copied too, or zero-filled past the matrix)
   // (map_row0: the first row's index in the map, when it differs from row0;
@@ -2807,8 +2807,9 @@ __device__ __forceinline__ bool op_chunk(const Params& p, Smem& S, const int32_t
     if (ok && run) ok = c.wait_counter(bar_index(p, l, p.bl.down), p.n_down_sms);
     if (ok && run) c.moe_sum();
   } else {
-    // an expert's gate / up rows (up to 8 tokens) and down rows on the tensor
-    // cores: one partial per warp instead of one per 256-column segment
+    // dense rows and an expert's gate / up rows (up to 8 tokens at 2048
+    // columns, 4 at 4096) and an expert's down rows on the tensor cores: one
+    // partial per warp instead of one per 256-column segment
     const int nt = t[R_NT];
     const int K = t[R_K];
     const bool mma = run && ((kind != K_DOWN && p.w_maps && mma_multi_rows(K, nt)) ||
