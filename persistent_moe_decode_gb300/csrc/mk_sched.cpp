@@ -7,7 +7,10 @@
 // that run it: all of them, or the SMs of one branch of the parallel layer.
 // An SM's list holds one task per wave and layer; the shares whose size
 // depends on routing (the experts' rows) are fixed as "slice s of n" and
-// resolved on the device once the routing is known.  Any order of the waves
+// resolved on the device once the routing is known; with several tokens the
+// SMs that hold such a slice claim fixed-size tiles of those rows from
+// per-layer counters instead (the slice then only says that the SM takes
+// part).  Any order of the waves
 // in which ROUTE precedes UP precedes DOWN and ATTN precedes COMBINE precedes
 // OUT (and, with several tokens, DOWN precedes OUT, whose expert sums wait for
 // every DOWN task) has no circular wait (every wait points at an earlier wave
