@@ -208,7 +208,7 @@ int make_row_map(CUtensorMap* m, const void* base, uint64_t rows, int K, int box
   return MK_OK;
 }
 
-// the one-token tensor maps of every layer's router, W_qkv, W_o, gate and up
+// the tensor maps of every layer's router, W_qkv, W_o, gate and up
 // matrices and of the LM head (W_MAP_* order); none when the hidden size does
 // not take the tensor-core path
 int make_weight_maps(mk_handle* h, const mk_weights* w, const uint8_t** out) {

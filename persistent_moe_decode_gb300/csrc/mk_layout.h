@@ -111,7 +111,7 @@ MK_HD inline bool mma_multi_rows(int K, int nt) {
 }
 MK_HD inline bool mma_multi_down(int K) { return K % 128 == 0 && K <= 1024; }
 constexpr int kDownBoxRows = 16;
-// tensor maps of the one-token weight matrices, per layer (W_MAP_* + 5 l), then the LM head
+// tensor maps of the weight matrices bound for the tensor cores, per layer (W_MAP_* + 5 l), then the LM head
 enum : int { W_MAP_ROUTER = 0, W_MAP_QKV = 1, W_MAP_O = 2, W_MAP_GATE = 3, W_MAP_UP = 4, W_MAPS_PER_LAYER = 5 };
 
 // GEMV contraction segments: 256 columns (32 lanes x 8), or all of K below that
@@ -196,7 +196,7 @@ struct Params {
   const uint8_t* mp_map;       // tensor map of mpart: 2-D [groups][H] fp32, boxes 24 x 256
   const uint8_t* wd_maps;      // several tokens: [L] tensor maps of W_down (16-row boxes;
                                // nullptr when not used)
-  const uint8_t* w_maps;       // one token, rows of 2048 / 4096 columns: [5 L + 1] tensor maps
+  const uint8_t* w_maps;       // rows of 2048 / 4096 columns: [5 L + 1] tensor maps
                                // (W_MAP_*; the last the LM head), 3-D views described above
                                // (nullptr when the model's rows take the other GEMV path)
   const uint8_t* kv_maps;      // [L][2] tensor maps (128 bytes each) of the K and V pools:
