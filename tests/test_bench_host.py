@@ -57,3 +57,13 @@ def test_algorithmic_bytes_count_the_expert_format():
     b8 = algorithmic_bytes(d, distinct, keys, "fp8")
     assert b16 - b8 == sum(distinct) * (per_bf16 - per_fp8)
     assert b16 == 6889312256                     # the 8K batch-1 step the benchmark reports (8197 keys)
+
+
+def test_traffic_key_ignores_comments_but_not_code():
+    """The traffic record's key hashes the kernel code without comments and
+    blank lines: a documentation edit keeps it, a code edit changes it."""
+    import bench
+    src = "int a; // count\n/* the\n   block */ int b;\n\n  float c;   \n"
+    assert bench.kernel_code(src) == "int a;\n int b;\n  float c;"
+    assert bench.kernel_code(src.replace("// count", "// the number of things")) == bench.kernel_code(src)
+    assert bench.kernel_code(src.replace("int b;", "int b = 1;")) != bench.kernel_code(src)
