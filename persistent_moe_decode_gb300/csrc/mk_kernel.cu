@@ -425,7 +425,7 @@ struct Prod {
     return true;
   }
 
-  // one token: the tensor map of matrix `which` (W_MAP_*) of the current layer
+  // the tensor map of matrix `which` (W_MAP_*) of the current layer
   __device__ __forceinline__ const uint8_t* wmap(int which) const {
     return p.w_maps + ((size_t)W_MAPS_PER_LAYER * l + which) * 128;
   }
